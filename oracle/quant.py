@@ -1,0 +1,168 @@
+"""Q4_0 weight quantiser and per-block int4 activation quantiser -- oracle side.
+
+Sources (engine docs "The lean option: ROCmFP4, ROCmI4 and Hadamard Q4_0"):
+
+* section "Hadamard-rotated Q4_0: W4A4 prompt processing": weights are plain
+  Q4_0, read bit for bit; a Q4_0 code q stands for q - 8, and q ^ 8 read as a
+  signed 4-bit number is exactly q - 8; only the activations are rounded to 4
+  bits, after the same per-32-block rotation as the weights;
+* section "MoE: W4A4 on the experts": Q4_0 has one scale per 32 values.
+
+Readings where the pages are silent (all listed in the design doc):
+
+* weight block: m = the rotated value of largest magnitude, the lowest index
+  on ties; d = m / -8 in fp32; id = 1/d (0 when d == 0); code
+  q = clamp(round_half_away(fl(y * id)) + 8, 0, 15); the stored scale is d
+  rounded to fp16 (nearest even); the codes use the fp32 d;
+* activation block: a = max |y|; d_a = a / 7 in fp32, stored as fp32;
+  id = 1/d_a (0 when d_a == 0); q = clamp(round_half_away(fl(y * id)), -8, 7);
+* nibble order inside a block's 16 bytes: byte i holds element i in its low
+  nibble and element i + 16 in its high nibble (the Q4_0 block layout); the
+  activations use the same order, each code as a 4-bit two's complement nibble.
+
+All rounding decisions are taken on fp32 values computed with one IEEE
+operation per step, exactly as written; round_half_away is evaluated in fp64,
+where |v| + 0.5 is exact for every fp32 v.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from .hadamard import rotate_h32
+
+
+def round_half_away(v: np.ndarray) -> np.ndarray:
+    """Round to the nearest integer, ties away from zero (returns float64)."""
+    v64 = np.asarray(v, dtype=np.float64)
+    return np.copysign(np.floor(np.abs(v64) + 0.5), v64)
+
+
+def _blocks(y: np.ndarray) -> np.ndarray:
+    K = y.shape[-1]
+    assert K % 32 == 0, "K must be a multiple of 32"
+    return y.reshape(y.shape[:-1] + (K // 32, 32))
+
+
+def _safe_recip(d: np.ndarray) -> np.ndarray:
+    out = np.zeros_like(d)
+    nz = d != 0
+    out[nz] = np.float32(1.0) / d[nz]
+    return out
+
+
+def quantize_weights_q4_0(y: np.ndarray) -> dict:
+    """Q4_0-quantise fp32 values y [..., K] per 32-block.
+
+    Returns codes (uint8 0..15, [..., K]), d32 (fp32 scale, [..., K/32]) and d16
+    (the stored fp16 scale).
+    """
+    y = np.asarray(y, dtype=np.float32)
+    blk = _blocks(y)
+    idx = np.argmax(np.abs(blk), axis=-1)  # first index of the largest magnitude
+    m = np.take_along_axis(blk, idx[..., None], axis=-1)[..., 0]
+    d = (m / np.float32(-8.0)).astype(np.float32)
+    inv = _safe_recip(d)
+    v = (blk * inv[..., None]).astype(np.float32)
+    q = np.clip(round_half_away(v) + 8.0, 0.0, 15.0).astype(np.uint8)
+    return {"codes": q.reshape(y.shape), "d32": d, "d16": d.astype(np.float16)}
+
+
+def quantize_act_int4(y: np.ndarray) -> dict:
+    """int4-quantise fp32 values y [..., K] per 32-block.
+
+    Returns q (int8 in -8..7, [..., K]) and d_a (fp32, [..., K/32]).
+    """
+    y = np.asarray(y, dtype=np.float32)
+    blk = _blocks(y)
+    a = np.max(np.abs(blk), axis=-1)
+    d_a = (a / np.float32(7.0)).astype(np.float32)
+    inv = _safe_recip(d_a)
+    v = (blk * inv[..., None]).astype(np.float32)
+    q = np.clip(round_half_away(v), -8.0, 7.0).astype(np.int8)
+    return {"q": q.reshape(y.shape), "d_a": d_a}
+
+
+def pack_nibbles(nib: np.ndarray) -> np.ndarray:
+    """Pack 4-bit values (uint8 0..15, [..., K]) into [..., K/2] bytes, Q4_0 order."""
+    blk = _blocks(np.asarray(nib, dtype=np.uint8))
+    lo = blk[..., :16]
+    hi = blk[..., 16:]
+    packed = (lo | (hi << 4)).astype(np.uint8)
+    return packed.reshape(nib.shape[:-1] + (nib.shape[-1] // 2,))
+
+
+def unpack_nibbles(packed: np.ndarray) -> np.ndarray:
+    """Inverse of ``pack_nibbles``: [..., K/2] bytes -> [..., K] values 0..15."""
+    p = np.asarray(packed, dtype=np.uint8)
+    Kh = p.shape[-1]
+    assert Kh % 16 == 0
+    blk = p.reshape(p.shape[:-1] + (Kh // 16, 16))
+    out = np.concatenate([blk & 0x0F, blk >> 4], axis=-1)
+    return out.reshape(p.shape[:-1] + (Kh * 2,))
+
+
+def weight_codes_from_nibbles(nib: np.ndarray) -> np.ndarray:
+    """Q4_0 code q -> the integer it stands for, q - 8 (int64)."""
+    return np.asarray(nib, dtype=np.int64) - 8
+
+
+def act_codes_from_nibbles(nib: np.ndarray) -> np.ndarray:
+    """4-bit two's complement nibble -> signed integer in -8..7 (int64)."""
+    n = np.asarray(nib, dtype=np.int64)
+    return np.where(n >= 8, n - 16, n)
+
+
+def q4_0_to_aos(codes_packed: np.ndarray, d16: np.ndarray) -> np.ndarray:
+    """SoA (codes [N][K/2], fp16 scales [N][K/32]) -> canonical 18-byte blocks.
+
+    Each block is the little-endian fp16 scale followed by its 16 code bytes;
+    returns uint8 [N][K/32][18].
+    """
+    N, Kh = codes_packed.shape
+    B = Kh // 16
+    out = np.empty((N, B, 18), dtype=np.uint8)
+    out[..., 0:2] = np.ascontiguousarray(d16, dtype="<f2").view(np.uint8).reshape(N, B, 2)
+    out[..., 2:] = codes_packed.reshape(N, B, 16)
+    return out
+
+
+def q4_0_from_aos(blocks: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    """Canonical 18-byte blocks [N][B][18] -> (codes [N][16B], fp16 scales [N][B])."""
+    blocks = np.asarray(blocks, dtype=np.uint8)
+    N, B, _ = blocks.shape
+    d16 = np.ascontiguousarray(blocks[..., 0:2]).view("<f2").reshape(N, B).astype(np.float16)
+    codes = np.ascontiguousarray(blocks[..., 2:]).reshape(N, B * 16)
+    return codes, d16
+
+
+def _weights_fp32(w: np.ndarray) -> np.ndarray:
+    w = np.asarray(w)
+    if w.dtype == np.uint16:  # bf16 bit patterns: exact widening to fp32
+        return (w.astype(np.uint32) << 16).view(np.float32)
+    return w.astype(np.float32)
+
+
+def pack_weights(w: np.ndarray, rotate: bool = True) -> dict:
+    """Weights [N][K] (fp32 values or bf16 bits as uint16) -> rotated Q4_0.
+
+    Returns codes (packed bytes [N][K/2]), d16 [N][K/32] (stored scales), d32
+    and q (unpacked codes [N][K]).
+    """
+    wf = _weights_fp32(w)
+    y = rotate_h32(wf) if rotate else wf
+    qz = quantize_weights_q4_0(y)
+    return {"codes": pack_nibbles(qz["codes"]), "d16": qz["d16"], "d32": qz["d32"],
+            "q": qz["codes"], "rotated": bool(rotate)}
+
+
+def quantize_activations(x: np.ndarray, rotate: bool = True) -> dict:
+    """Activations [M][K] fp32 -> rotated int4 codes + fp32 per-block scales.
+
+    Returns codes (packed bytes [M][K/2], two's complement nibbles), d_a
+    [M][K/32] fp32 and q (int8 [M][K]).
+    """
+    xf = np.asarray(x, dtype=np.float32)
+    y = rotate_h32(xf) if rotate else xf
+    qa = quantize_act_int4(y)
+    nib = (qa["q"].astype(np.int16) & 0x0F).astype(np.uint8)
+    return {"codes": pack_nibbles(nib), "d_a": qa["d_a"], "q": qa["q"], "rotated": bool(rotate)}

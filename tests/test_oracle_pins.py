@@ -1,0 +1,344 @@
+"""Pins for the CPU oracle: each test ties it to something other than itself --
+exact rational arithmetic, an independent construction, a closed form worked out
+from the method's definition, hand-worked values (tests/golden/), or brute-force
+Python loops on tiny inputs.
+
+Method: engine docs "The lean option: ROCmFP4, ROCmI4 and Hadamard Q4_0",
+sections "Hadamard-rotated Q4_0: W4A4 prompt processing" and "MoE: W4A4 on the
+experts".
+"""
+import math
+import os
+import struct
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+import synth_inputs as si
+
+
+# ---------------------------------------------------------------- helpers (independent)
+def hadamard_recursive(n: int) -> np.ndarray:
+    """Sylvester construction H_{2n} = [[H, H], [H, -H]], built without popcounts."""
+    H = np.array([[1]], dtype=np.int64)
+    while H.shape[0] < n:
+        H = np.block([[H, H], [H, -H]])
+    return H
+
+
+H32 = hadamard_recursive(32)
+
+
+def read_golden(path):
+    cases = []
+    with open(path) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            name, d, vals, codes = [x.strip() for x in line.split("|")]
+            cases.append((name, float(d), np.array([float(v) for v in vals.split()], dtype=np.float32),
+                          np.array([int(c) for c in codes.split()])))
+    return cases
+
+
+# ---------------------------------------------------------------- the rotation
+def test_c_is_nearest_fp32_to_inv_sqrt32():
+    c = Fraction(float(oracle.C_H32))
+    bits = int(np.float32(oracle.C_H32).view(np.uint32))
+    ulp = Fraction(2) ** (((bits >> 23) & 0xFF) - 127 - 23)
+    # c - ulp/2 < 1/sqrt(32) < c + ulp/2  <=>  squares bracket 1/32
+    assert (c - ulp / 2) ** 2 < Fraction(1, 32) < (c + ulp / 2) ** 2
+    assert bits == 0x3E3504F3
+
+
+def test_sylvester_matches_recursive_construction_and_is_orthogonal():
+    H = oracle.sylvester_h32()
+    assert np.array_equal(H, H32)
+    assert np.array_equal(H @ H.T, 32 * np.eye(32, dtype=np.int64))
+    assert np.array_equal(H, H.T)
+
+
+def test_butterfly_equals_dense_product_on_integers():
+    rng = np.random.default_rng(1)
+    x = rng.integers(-1000, 1001, size=(50, 32))
+    got = oracle.fwht32(x.astype(np.float32))
+    want = x @ H32.T  # |sums| <= 32000: exact in fp32
+    assert np.array_equal(got.astype(np.int64), want)
+    assert np.array_equal(oracle.fwht32(x.astype(np.int64)), want)
+
+
+def test_butterfly_of_ones_is_32_e0():
+    u = oracle.fwht32(np.ones(32, dtype=np.float32))
+    e = np.zeros(32, dtype=np.float32)
+    e[0] = 32
+    assert np.array_equal(u, e)
+
+
+def test_rotation_preserves_dot_products_fp64():
+    rng = np.random.default_rng(2)
+    x = rng.standard_normal((8, 256))
+    w = rng.standard_normal((8, 256))
+    rx = oracle.rotate_h32(x, dtype=np.float64)
+    rw = oracle.rotate_h32(w, dtype=np.float64)
+    lhs = (rx * rw).sum(axis=1)
+    rhs = (x * w).sum(axis=1)
+    assert np.allclose(lhs, rhs, rtol=1e-12, atol=1e-12)
+    # orthogonal and symmetric: rotating twice is the identity
+    assert np.allclose(oracle.rotate_h32(rx, dtype=np.float64), x, atol=1e-13)
+
+
+def test_rotation_fp32_within_rounding_bound_of_exact():
+    rng = np.random.default_rng(3)
+    x = (rng.standard_normal((64, 128)) * 3).astype(np.float32)
+    y32 = oracle.rotate_h32(x).astype(np.float64)
+    exact = (x.astype(np.float64).reshape(64, 4, 32) @ H32.T.astype(np.float64)) / math.sqrt(32)
+    l1 = np.abs(x.astype(np.float64)).reshape(64, 4, 32).sum(-1, keepdims=True)
+    bound = 8 * 2.0 ** -24 * l1  # five rounded adds plus one rounded multiply per element
+    assert np.all(np.abs(y32.reshape(64, 4, 32) - exact) <= bound)
+
+
+# ---------------------------------------------------------------- quantisers, hand-worked
+def test_q4_0_hand_worked_blocks(golden_dir):
+    cases = read_golden(os.path.join(golden_dir, "q4_0_hand_blocks.txt"))
+    assert len(cases) == 4
+    for name, d, vals, codes in cases:
+        qz = oracle.quantize_weights_q4_0(vals[None, :])
+        assert float(qz["d32"][0, 0]) == d, name
+        assert np.array_equal(qz["codes"][0].astype(np.int64), codes), name
+
+
+def test_int4_hand_worked_blocks(golden_dir):
+    cases = read_golden(os.path.join(golden_dir, "int4_act_hand_blocks.txt"))
+    assert len(cases) == 3
+    for name, d, vals, codes in cases:
+        qa = oracle.quantize_act_int4(vals[None, :])
+        assert float(qa["d_a"][0, 0]) == d, name
+        assert np.array_equal(qa["q"][0].astype(np.int64), codes), name
+
+
+def test_round_half_away_against_exact_rationals():
+    vals = [0.5, -0.5, 1.5, -1.5, 2.5, -2.5, 0.49999997, -0.49999997, 7.4999995, 3.0000002,
+            -6.5, 1e-8, -0.0, 0.0, 7.5, -7.5]
+    got = oracle.round_half_away(np.array(vals, dtype=np.float32))
+    for v, g in zip(vals, got):
+        f = Fraction(float(np.float32(v)))
+        r = math.floor(abs(f) + Fraction(1, 2))
+        assert g == (r if f >= 0 else -r), v
+
+
+# ---------------------------------------------------------------- quantisers, closed forms
+def test_unit_vectors_closed_form():
+    """x = e_j in one block: rotated y_i = c * H[i][j]; all magnitudes tie, the
+    lowest index (i = 0, H[0][j] = +1) is m, so d = -c/8 and the weight codes are
+    0 where H[i][j] = +1 and 16 -> 15 (clamped) where H[i][j] = -1; the int4
+    codes are 7 * H[i][j].  Writing the weight values q - 8 as -1/2 - 15/2 H[i][k],
+    P[activation e_j][weight e_k] = -1680 [j == k] - 112 [j == 0]."""
+    E = np.eye(32, dtype=np.float32)
+    wp = oracle.pack_weights(E)  # rows are weight vectors e_j
+    ap = oracle.quantize_activations(E)
+    c = np.float32(oracle.C_H32)
+    for j in range(32):
+        want_w = np.where(H32[:, j] == 1, 0, 15)
+        assert np.array_equal(wp["q"][j].astype(np.int64), want_w)
+        assert wp["d32"][j, 0] == np.float32(-c / np.float32(8))
+        assert np.array_equal(ap["q"][j].astype(np.int64), 7 * H32[:, j])
+    P = oracle.block_partials(wp, ap)[:, :, 0]  # P[m = activation e_j][n = weight e_k]
+    for ja in range(32):
+        for kw in range(32):
+            assert P[ja, kw] == -1680 * (ja == kw) - 112 * (ja == 0)
+            # and by brute force on the sign patterns
+            wv = np.where(H32[:, kw] == 1, -8, 7)
+            assert P[ja, kw] == int((wv * 7 * H32[:, ja]).sum())
+
+
+def test_constant_blocks_closed_form():
+    """Weight block constant alpha, activation block constant beta: y = 32 alpha c e0,
+    weight codes (0, 8, 8, ...), int4 codes (+-7, 0, ...), P = -56 sign(beta), and
+    d_w d_a P = (y_w / -8)(|y_a| / 7)(-56 sign beta) = 32 alpha beta (up to the
+    fp16 scale), the exact product."""
+    rng = np.random.default_rng(4)
+    B = 8
+    alpha = rng.uniform(0.1, 2.0, B) * rng.choice([-1, 1], B)
+    beta = rng.uniform(0.1, 2.0, B) * rng.choice([-1, 1], B)
+    w = np.repeat(alpha, 32).astype(np.float32)[None, :]
+    x = np.repeat(beta, 32).astype(np.float32)[None, :]
+    wp = oracle.pack_weights(w)
+    ap = oracle.quantize_activations(x)
+    for b in range(B):
+        qw = wp["q"][0, 32 * b:32 * b + 32].astype(np.int64)
+        qa = ap["q"][0, 32 * b:32 * b + 32].astype(np.int64)
+        assert qw[0] == 0 and np.all(qw[1:] == 8)
+        assert qa[0] == 7 * np.sign(beta[b]) and np.all(qa[1:] == 0)
+    P = oracle.block_partials(wp, ap)[0, 0]
+    assert np.array_equal(P, -56 * np.sign(beta).astype(np.int64))
+    Y = oracle.w4a4_matmul(wp, ap)[0, 0]
+    exact = float(np.sum(32 * np.float32(alpha).astype(np.float64) * np.float32(beta).astype(np.float64)))
+    scale = float(np.sum(np.abs(32 * alpha * beta)))
+    assert abs(Y - exact) <= 2.0 ** -10 * scale
+
+
+def test_q4_0_round_trip_bounds_random():
+    rng = np.random.default_rng(5)
+    y = (rng.standard_normal((200, 256)) * rng.uniform(1e-3, 10, (200, 1))).astype(np.float32)
+    qz = oracle.quantize_weights_q4_0(y)
+    q = qz["codes"].reshape(200, 8, 32).astype(np.float64)
+    d = qz["d32"].astype(np.float64)[..., None]
+    yb = y.reshape(200, 8, 32).astype(np.float64)
+    err = np.abs(yb - d * (q - 8))
+    v = yb / d
+    dd = np.broadcast_to(np.abs(d), err.shape)
+    inside = np.abs(v) <= 7.49  # not clamped: error at most half a step
+    assert np.all(err[inside] <= 0.5 * dd[inside] * (1 + 2.0 ** -20))
+    assert np.all(err <= dd * (1 + 2.0 ** -20))  # clamped (+8 -> 15): at most one step
+    # the signed-max element maps to code 0
+    idx = np.argmax(np.abs(yb), axis=-1)
+    assert np.all(np.take_along_axis(q, idx[..., None], -1) == 0)
+    # fp16 stored scale within 2^-11 relative (normal fp16 range)
+    d16 = qz["d16"].astype(np.float64)
+    rel = np.abs(d16 - qz["d32"]) / np.abs(qz["d32"])
+    assert np.all(rel <= 2.0 ** -11)
+
+
+def test_int4_round_trip_bounds_random():
+    rng = np.random.default_rng(6)
+    y = (rng.standard_normal((200, 256)) * rng.uniform(1e-3, 10, (200, 1))).astype(np.float32)
+    qa = oracle.quantize_act_int4(y)
+    q = qa["q"].reshape(200, 8, 32).astype(np.float64)
+    d = qa["d_a"].astype(np.float64)[..., None]
+    yb = y.reshape(200, 8, 32).astype(np.float64)
+    assert np.all(np.abs(yb - d * q) <= 0.5 * d * (1 + 2.0 ** -20))
+    idx = np.argmax(np.abs(yb), axis=-1)
+    assert np.all(np.abs(np.take_along_axis(q, idx[..., None], -1)) == 7)
+    assert q.min() >= -7  # -8 is never produced (|y / d_a| <= 7 up to rounding)
+
+
+def test_activation_scale_invariance_powers_of_two():
+    rng = np.random.default_rng(7)
+    x = rng.standard_normal((16, 128)).astype(np.float32)
+    base = oracle.quantize_activations(x)
+    for k in (-3, 5):
+        s = np.float32(2.0 ** k)
+        sc = oracle.quantize_activations(x * s)
+        assert np.array_equal(sc["codes"], base["codes"])
+        assert np.array_equal(sc["d_a"], base["d_a"] * s)
+
+
+# ---------------------------------------------------------------- nibble formats
+def test_q_xor_8_is_q_minus_8_exhaustive():
+    for q in range(16):
+        n = q ^ 8
+        signed = n - 16 if n >= 8 else n
+        assert signed == q - 8
+        assert int(oracle.weight_codes_from_nibbles(np.array([q]))[0]) == q - 8
+    for v in range(-8, 8):
+        assert int(oracle.act_codes_from_nibbles(np.array([v & 0xF]))[0]) == v
+
+
+def test_nibble_packing_brute_force():
+    rng = np.random.default_rng(8)
+    nib = rng.integers(0, 16, size=(3, 96)).astype(np.uint8)
+    packed = oracle.pack_nibbles(nib)
+    for r in range(3):
+        for b in range(3):
+            for i in range(16):
+                byte = int(nib[r, 32 * b + i]) | (int(nib[r, 32 * b + i + 16]) << 4)
+                assert packed[r, 16 * b + i] == byte
+    assert np.array_equal(oracle.unpack_nibbles(packed), nib)
+
+
+def test_q4_0_aos_brute_force():
+    rng = np.random.default_rng(9)
+    codes = rng.integers(0, 256, size=(2, 48)).astype(np.uint8)  # N=2, K=96
+    d16 = rng.standard_normal((2, 3)).astype(np.float16)
+    aos = oracle.q4_0_to_aos(codes, d16)
+    for n in range(2):
+        for b in range(3):
+            want = struct.pack("<e", float(d16[n, b])) + bytes(codes[n, 16 * b:16 * b + 16].tolist())
+            assert bytes(aos[n, b].tolist()) == want
+    c2, d2 = oracle.q4_0_from_aos(aos)
+    assert np.array_equal(c2, codes) and np.array_equal(d2.view(np.uint16), d16.view(np.uint16))
+
+
+# ---------------------------------------------------------------- products, brute force
+def _tiny(seed, M=3, N=4, K=64):
+    d = si.random_dense(M, K, N, seed=seed)
+    return d, oracle.pack_weights(d["w_bf16"]), oracle.quantize_activations(d["x"])
+
+
+def test_partials_brute_force():
+    d, wp, ap = _tiny(10)
+    P = oracle.block_partials(wp, ap)
+    wq, aq = wp["q"], ap["q"]
+    for m in range(3):
+        for n in range(4):
+            for b in range(2):
+                s = 0
+                for j in range(32):
+                    s += (int(wq[n, 32 * b + j]) - 8) * int(aq[m, 32 * b + j])
+                assert P[m, n, b] == s
+
+
+def test_w4a4_matmul_brute_force():
+    d, wp, ap = _tiny(11)
+    Y = oracle.w4a4_matmul(wp, ap)
+    wq, aq = wp["q"], ap["q"]
+    for m in range(3):
+        for n in range(4):
+            acc = Fraction(0)
+            for b in range(2):
+                s = sum((int(wq[n, 32 * b + j]) - 8) * int(aq[m, 32 * b + j]) for j in range(32))
+                acc += Fraction(float(wp["d16"][n, b])) * Fraction(float(ap["d_a"][m, b])) * s
+            assert abs(Y[m, n] - float(acc)) <= 1e-15 * max(1.0, abs(float(acc)))
+    # selected rows / columns agree with the full product
+    Ys = oracle.w4a4_matmul(wp, ap, m_idx=[2, 0], n_idx=[3, 1])
+    assert np.array_equal(Ys, Y[np.ix_([2, 0], [3, 1])])
+
+
+def test_exact_matmul_brute_force():
+    d, _, _ = _tiny(12)
+    R = oracle.exact_matmul(d["x"], d["w_bf16"])
+    for m in range(3):
+        for n in range(4):
+            s = math.fsum(float(d["x"][m, k]) * float(d["w"][n, k]) for k in range(64))
+            assert abs(R[m, n] - s) <= 1e-12 * max(1.0, abs(s))
+
+
+@pytest.mark.parametrize("act_per_slot", [False, True])
+def test_matmul_id_reduces_to_dense_per_token_slot(act_per_slot):
+    mi = si.moe_inputs("moe_tiny", seed=3)
+    s = mi["shape"]
+    if act_per_slot:
+        w, x, N = mi["wd_bf16"], mi["x_down"], s.N_down
+    else:
+        w, x, N = mi["wg_bf16"], mi["x_gate"], s.N_gate
+    wp = oracle.pack_weights(w.reshape(s.E * N, -1))
+    ap = oracle.quantize_activations(x)
+    Y = oracle.w4a4_matmul_id(wp, s.E, ap, mi["ids"], act_per_slot)
+    wq, aq = wp["q"], ap["q"]
+    K = x.shape[1]
+    for t in range(s.M):
+        for slot in range(s.top_k):
+            e = int(mi["ids"][t, slot])
+            r = t * s.top_k + slot if act_per_slot else t
+            for n in (0, N // 2, N - 1):
+                acc = 0.0
+                for b in range(K // 32):
+                    p = sum((int(wq[e * N + n, 32 * b + j]) - 8) * int(aq[r, 32 * b + j]) for j in range(32))
+                    acc += float(wp["d16"][e * N + n, b]) * float(ap["d_a"][r, b]) * p
+                assert abs(Y[t, slot, n] - acc) <= 1e-12 * max(1.0, abs(acc))
+
+
+# ---------------------------------------------------------------- the pages' accuracy claim
+def test_rotation_reduces_w4a4_error_on_outlier_activations():
+    """The rotation spreads a block's few large values before 4-bit rounding, so on
+    activations with outlier channels the rotated product is closer to the exact one."""
+    d = si.dense_inputs("c0")
+    R = oracle.exact_matmul(d["x"], d["w_bf16"])
+    Yr = oracle.w4a4_matmul(oracle.pack_weights(d["w_bf16"]), oracle.quantize_activations(d["x"]))
+    Yu = oracle.w4a4_matmul(oracle.pack_weights(d["w_bf16"], rotate=False),
+                            oracle.quantize_activations(d["x"], rotate=False))
+    err_r = np.linalg.norm(Yr - R) / np.linalg.norm(R)
+    err_u = np.linalg.norm(Yu - R) / np.linalg.norm(R)
+    assert err_r < err_u
