@@ -1,0 +1,372 @@
+#!/usr/bin/env python3
+"""Benchmark of the W4A4 prefill matmul on GB300 (one JSON line on stdout).
+
+Workload (the dense attention-projection GEMM the headline metric is quoted on):
+M = 512 tokens (one micro-batch), K = 5120, N = 5120; H32-rotated Q4_0 weights
+(bf16 N(0, 0.02) source), fp32 activations N(0, 1) with 1% outlier channels x20.
+One step = the whole hot path on one batch: rotate + int4-quantise the
+activations, then the block-scaled W4A4 GEMM (fp32 output).  Weight packing runs
+once per model and is timed separately.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+``--impl reference`` times the CPU oracle (``oracle/``) on the host cores on a
+bounded row sample of the same workload.  Under torchrun (N > 1) every rank
+runs an independent replica (the path has no exchange step), the step time is
+the max over ranks and ``value`` counts the work of all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth_inputs as si  # noqa: E402
+
+METRIC = "W4A4 GEMM effective TOPS and prefill tok/s at M=512; % of int8 tensor peak"
+UNIT = "TOPS"  # effective: 2*M*N*K integer ops per second
+L2_BYTES = 129 * 2 ** 20
+
+
+def env_rank():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+        self._t = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self) -> dict:
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- oracle arm
+def oracle_sample_step(d: dict, wp: dict, rows: np.ndarray) -> float:
+    """One oracle pass (activation rotate + quantise, block-scaled product) over `rows`."""
+    import oracle
+    t0 = time.perf_counter()
+    ap = oracle.quantize_activations(d["x"][rows])
+    oracle.w4a4_matmul(wp, ap)
+    return time.perf_counter() - t0
+
+
+def cpu_rows_for_budget(d, wp, budget_s: float) -> tuple[np.ndarray, float]:
+    """Pick a row sample whose oracle pass takes about budget_s seconds."""
+    M = d["x"].shape[0]
+    t1 = oracle_sample_step(d, wp, np.arange(1))
+    t4 = oracle_sample_step(d, wp, np.arange(4))
+    per_row = max((t4 - t1) / 3.0, 1e-4)
+    n = int(min(M, max(1, budget_s / per_row)))
+    return np.arange(n), per_row
+
+
+def run_reference(args, shape) -> dict:
+    rank, world, _ = env_rank()
+    if rank != 0:
+        sys.exit(0)
+    import oracle
+    d = si.dense_inputs(shape.name)
+    wp = oracle.pack_weights(d["w_bf16"])
+    rows, _ = cpu_rows_for_budget(d, wp, budget_s=6.0)
+    for _ in range(args.warmup):
+        oracle_sample_step(d, wp, rows)
+    times = [oracle_sample_step(d, wp, rows) for _ in range(args.steps)]
+    t = sum(times) / len(times)
+    ops = 2.0 * len(rows) * shape.N * shape.K
+    value = ops / t / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int4 codes, f64 block-scaled sum", "data": "synthetic",
+        "config": {"workload": shape.what, "M": shape.M, "K": shape.K, "N": shape.N,
+                   "sample_rows": int(len(rows))},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": f"{len(rows)} of {shape.M} activation rows x all {shape.N} weight rows per step "
+                                   f"(numpy; BLAS matmuls threaded over the host cores, elementwise work on one)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    return line
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def read_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f)
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "sm_max_mhz": 2070.0, "fallback": True}
+
+
+def run_probes() -> dict:
+    """int8 / fp8 tensor and fp32 FMA throughput on this GPU (ops/s), via libw4a4_probes.so."""
+    import ctypes
+    from hadamard_rotated_w4a4_gb300 import build as b
+    try:
+        b.build(probes=True)
+        lib = ctypes.CDLL(b.PROBE_LIB)
+    except Exception as e:  # noqa: BLE001
+        return {"error": str(e)}
+    lib.w4a4_probe_mma_sync.argtypes, lib.w4a4_probe_mma_sync.restype = [ctypes.c_int, ctypes.c_int], ctypes.c_double
+    lib.w4a4_probe_ffma.argtypes, lib.w4a4_probe_ffma.restype = [ctypes.c_int, ctypes.c_int], ctypes.c_double
+    lib.w4a4_probe_tcgen05_f8.argtypes, lib.w4a4_probe_tcgen05_f8.restype = [ctypes.c_int], ctypes.c_double
+    out = {
+        "int8_mma_sync_tops": lib.w4a4_probe_mma_sync(0, 4096) / 1e12,
+        "fp8_mma_sync_tflops": lib.w4a4_probe_mma_sync(1, 4096) / 1e12,
+        "int4_mma_sync_tops": lib.w4a4_probe_mma_sync(2, 4096) / 1e12,
+        "fp32_ffma_tflops": lib.w4a4_probe_ffma(0, 20000) / 1e12,
+        "fp32_ffma2_tflops": lib.w4a4_probe_ffma(1, 20000) / 1e12,
+        "fp8_tcgen05_tflops": lib.w4a4_probe_tcgen05_f8(20000) / 1e12,
+    }
+    return out
+
+
+def run_ours(args, shape) -> dict | None:
+    import torch
+    import hadamard_rotated_w4a4_gb300 as w4
+
+    rank, world, local = env_rank()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device() if world == 1 else local)
+    w4.load_library(build_if_missing=True)
+    stream = torch.cuda.current_stream()
+    M, K, N = shape.M, shape.K, shape.N
+
+    # ---- inputs: one seeded draw, copied into enough sets that a step never finds its inputs in L2
+    d = si.dense_inputs(shape.name)
+    w_dev = torch.from_numpy(d["w_bf16"].view(np.int16)).to(dev).view(torch.bfloat16)
+    x0 = torch.from_numpy(d["x"]).to(dev)
+    set_bytes = M * K * 4 + N * K // 2 + N * K // 16 + M * K // 2 + M * K // 8 + M * N * 4
+    nsets = max(2, int(np.ceil(2.2 * L2_BYTES / set_bytes)))
+    e_pack0, e_pack1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_pack0.record(stream)
+    wq0 = w4.h32_q4_0_pack_weights(w_dev)
+    e_pack1.record(stream)
+    torch.cuda.synchronize()
+    pack_ms = e_pack0.elapsed_time(e_pack1)
+    sets = []
+    for i in range(nsets):
+        wq = w4.alloc_q4_0(N, K, dev)
+        wq.codes.copy_(wq0.codes)
+        wq.scales_buf.copy_(wq0.scales_buf)
+        xs = x0.clone()
+        aq = w4.alloc_act4(M, K, dev)
+        y = torch.empty(M, N, dtype=torch.float32, device=dev)
+        sets.append((wq, xs, aq, y))
+    del w_dev
+    torch.cuda.synchronize()
+
+    def step(i, ev=None):
+        wq, xs, aq, y = sets[i % nsets]
+        if ev is not None:
+            ev[0].record(stream)
+        w4.w4a4_rotate_quantize_act(xs, out=aq)
+        if ev is not None:
+            ev[1].record(stream)
+        w4.w4a4_gemm(wq, aq, y=y)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index or 0) as clk:
+        t0.record(stream)
+        for i in range(args.steps):
+            step(args.warmup + i, evs[i])
+        t1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = t0.elapsed_time(t1)
+    act_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    gemm_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    if world > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_per_step = total_ms / args.steps
+    ops = 2.0 * M * N * K
+    value = world * ops / (ms_per_step * 1e-3) / 1e12
+
+    # ---- end to end through the public API: host activations in, host output back, every step
+    x_host = torch.from_numpy(d["x"]).pin_memory()
+    y_host = torch.empty(M, N, dtype=torch.float32).pin_memory()
+    wq_e, xs_e, aq_e, y_e = sets[0]
+
+    def e2e_step():
+        xs_e.copy_(x_host, non_blocking=True)
+        w4.w4a4_rotate_quantize_act(xs_e, out=aq_e)
+        w4.w4a4_gemm(wq_e, aq_e, y=y_e)
+        y_host.copy_(y_e, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    a1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = a0.elapsed_time(a1) / args.steps
+    e2e_value = world * ops / (e2e_ms * 1e-3) / 1e12
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return None
+
+    peaks = read_peaks()
+    probes = run_probes() if not args.no_probes else {}
+    B = K // 32
+    gemm_avg = sum(gemm_ms) / len(gemm_ms)
+    act_avg = sum(act_ms) / len(act_ms)
+    # GEMM roofline: the per-block scale fold on the fp32 pipe (2 flops per (m, n, block))
+    fold_flops = 2.0 * M * N * B
+    sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
+    fp32_peak = sm_count * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+    gemm_roof = {"bound": "alu", "achieved": fold_flops / (gemm_avg * 1e-3) / 1e12, "peak": fp32_peak,
+                 "unit": "TFLOP/s", "frac": None, "traffic": args.gemm_traffic,
+                 "kernel": "w4a4_gemm_mma_kernel",
+                 "peak_source": f"derived: {sm_count} SMs x 128 fp32 lanes x 2 flops x {peaks.get('sm_max_mhz', 2070.0)} MHz"}
+    gemm_roof["frac"] = gemm_roof["achieved"] / gemm_roof["peak"]
+    act_bytes = M * K * 4 + M * K // 2 + M * B * 4
+    act_roof = {"bound": "hbm", "achieved": act_bytes / (act_avg * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "kernel": "act_rotate_quantize_kernel",
+                "peak_source": "MEASURED_PEAKS.json hbm_gbs (measured)" if not peaks.get("fallback") else "fallback"}
+    act_roof["frac"] = act_roof["achieved"] / act_roof["peak"]
+    eff_tops_gemm = ops / (gemm_avg * 1e-3) / 1e12
+    int8_peak = probes.get("int8_mma_sync_tops") if probes else None
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        wp = oracle.pack_weights(d["w_bf16"])
+        rows, _ = cpu_rows_for_budget(d, wp, budget_s=args.cpu_budget)
+        tc = oracle_sample_step(d, wp, rows)
+        cpu = {"value": 2.0 * len(rows) * N * K / tc / 1e12, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"{len(rows)} of {M} activation rows x all {N} weight rows, one pass "
+                         f"(numpy; BLAS matmuls threaded, elementwise single-threaded)", "seconds": tc}
+
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int4 x int4 (exact fp8 tensor-core MMA) -> f32 fold", "data": "synthetic",
+        "config": {"workload": shape.what, "M": M, "K": K, "N": N,
+                   "l2": f"inputs larger than L2: {nsets} input sets ({nsets * set_bytes / 2**20:.0f} MiB) "
+                         f"rotated across steps", "parallelism": "replicas" if world > 1 else "single"},
+        "roofline": gemm_roof,
+        "roofline_act": act_roof,
+        "gemm_effective_tops": eff_tops_gemm,
+        "pct_int8_peak": (eff_tops_gemm / int8_peak) if int8_peak else None,
+        "prefill_tok_s_proxy": None,
+        "kernel_ms": {"act_rotate_quantize": act_avg, "gemm": gemm_avg},
+        "pack_weights_ms": pack_ms,
+        "probes": probes,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(M * K * 4),
+                "d2h_bytes_per_step": int(M * N * 4), "ms_per_step": e2e_ms},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+    }
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return line
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="c1", choices=["c1", "c2", "c3"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-probes", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--gemm-traffic", type=float, default=None,
+                    help="dram bytes per GEMM launch from an ncu capture of the current kernel")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    shape = si.DENSE[args.config]
+    line = run_reference(args, shape) if args.impl == "reference" else run_ours(args, shape)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

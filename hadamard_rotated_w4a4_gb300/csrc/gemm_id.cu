@@ -1,0 +1,106 @@
+// Expert-routed W4A4 product (MUL_MAT_ID), engine docs "The lean option:
+// ROCmFP4, ROCmI4 and Hadamard Q4_0", section "MoE: W4A4 on the experts": the
+// W4A4 kernel runs the expert matmuls too, where an MoE spends nearly all of its
+// prompt work.
+//
+// Two launches on the caller's stream:
+//   1. route_prep (one CTA): histogram of ids per expert, exclusive scans of the
+//      pair counts and of the 128-row tiles per expert, the pair list grouped by
+//      expert, zeroed output rows and a device flag for ids outside [0, E);
+//   2. the grouped GEMM over (expert row tile, weight tile), gathering each
+//      tile's activation rows through the pair list and scattering its outputs.
+#include "w4a4_kernels.cuh"
+
+namespace w4a4 {
+
+namespace {
+
+constexpr int kPrepThreads = 1024;
+
+__global__ void __launch_bounds__(kPrepThreads) route_prep_kernel(const int32_t* __restrict__ ids, int64_t npairs,
+                                                                   int E, int64_t N, float* __restrict__ y,
+                                                                   Routing r) {
+  extern __shared__ int32_t sh[];  // cnt[E], cursor[E]
+  int32_t* cnt = sh;
+  int32_t* cur = sh + E;
+  __shared__ int bad;
+  const int tid = threadIdx.x;
+  for (int e = tid; e < E; e += blockDim.x) cnt[e] = 0;
+  if (tid == 0) bad = 0;
+  __syncthreads();
+  for (int64_t i = tid; i < npairs; i += blockDim.x) {
+    const int e = ids[i];
+    if (e >= 0 && e < E) {
+      atomicAdd(&cnt[e], 1);
+    } else {
+      bad = 1;
+      float* yr = y + i * N;  // an unused slot's output row is zero
+      for (int64_t n = 0; n < N; ++n) yr[n] = 0.f;
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int32_t off = 0, toff = 0;
+    for (int e = 0; e < E; ++e) {
+      r.offsets[e] = off;
+      r.tile_off[e] = toff;
+      r.counts[e] = cnt[e];
+      cur[e] = off;
+      off += cnt[e];
+      toff += (cnt[e] + kGemmBM - 1) / kGemmBM;
+    }
+    r.offsets[E] = off;
+    r.tile_off[E] = toff;
+    r.flag[0] = bad;
+  }
+  __syncthreads();
+  for (int64_t i = tid; i < npairs; i += blockDim.x) {
+    const int e = ids[i];
+    if (e >= 0 && e < E) {
+      const int pos = atomicAdd(&cur[e], 1);
+      r.perm[pos] = static_cast<int32_t>(i);
+    }
+  }
+}
+
+size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
+
+}  // namespace
+
+RoutingLayout routing_layout(int64_t npairs, int E) {
+  RoutingLayout L{};
+  size_t off = 0;
+  L.flag = off;     off += 16;  // first, so that a status query needs only the pointer
+  L.counts = off;   off += align16(sizeof(int32_t) * static_cast<size_t>(E));
+  L.offsets = off;  off += align16(sizeof(int32_t) * static_cast<size_t>(E + 1));
+  L.tile_off = off; off += align16(sizeof(int32_t) * static_cast<size_t>(E + 1));
+  L.perm = off;     off += align16(sizeof(int32_t) * static_cast<size_t>(npairs));
+  L.total = off;
+  return L;
+}
+
+Routing routing_in(void* ws, int64_t npairs, int E) {
+  const RoutingLayout L = routing_layout(npairs, E);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  Routing r;
+  r.counts = reinterpret_cast<int32_t*>(base + L.counts);
+  r.offsets = reinterpret_cast<int32_t*>(base + L.offsets);
+  r.tile_off = reinterpret_cast<int32_t*>(base + L.tile_off);
+  r.perm = reinterpret_cast<int32_t*>(base + L.perm);
+  r.flag = reinterpret_cast<int32_t*>(base + L.flag);
+  return r;
+}
+
+cudaError_t launch_gemm_id(const uint8_t* w_codes, const uint16_t* w_scales, int E, int64_t N,
+                           const uint8_t* a_codes, const float* a_scales, int64_t K, const int32_t* ids, int64_t M,
+                           int top_k, int act_per_slot, float* y, const Routing& r, cudaStream_t stream) {
+  const int64_t npairs = M * top_k;
+  const size_t sh = sizeof(int32_t) * 2 * static_cast<size_t>(E);
+  route_prep_kernel<<<1, kPrepThreads, sh, stream>>>(ids, npairs, E, N, y, r);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_gemm_routed(w_codes, w_scales, E, N, a_codes, a_scales, K, npairs, top_k, act_per_slot, y, r,
+                            stream);
+}
+
+}  // namespace w4a4

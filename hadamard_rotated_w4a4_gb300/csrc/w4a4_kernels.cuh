@@ -1,0 +1,51 @@
+// Internal declarations shared by the CUDA translation units of libw4a4.so.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "w4a4_device.cuh"
+
+namespace w4a4 {
+
+// Number of SMs of the current device (cached per device).
+int num_sms();
+
+// Routing tables of one MUL_MAT_ID call, carved out of the caller's workspace.
+struct Routing {
+  int32_t* counts;    // [E]     (token, slot) pairs per expert
+  int32_t* offsets;   // [E + 1] exclusive prefix of counts
+  int32_t* tile_off;  // [E + 1] exclusive prefix of row tiles per expert
+  int32_t* perm;      // [M * top_k] pair indices p = t * top_k + s, grouped by expert
+  int32_t* flag;      // [1]     nonzero: some id was outside [0, E)
+};
+
+struct RoutingLayout {
+  size_t counts, offsets, tile_off, perm, flag, total;
+};
+RoutingLayout routing_layout(int64_t npairs, int E);
+Routing routing_in(void* ws, int64_t npairs, int E);
+
+// Row tile of the GEMM main loop (activation rows per CTA tile).
+constexpr int kGemmBM = 128;
+constexpr int kGemmBN = 128;
+
+cudaError_t launch_act_rotate_quantize(const float* x, int64_t M, int64_t K, int64_t ldx, int rotate,
+                                       uint8_t* codes, float* scales, cudaStream_t stream);
+cudaError_t launch_pack_q4_0(const void* w, int w_dtype, int64_t N, int64_t K, int64_t ldw, int rotate,
+                             uint8_t* codes, uint16_t* scales, cudaStream_t stream);
+cudaError_t launch_import_q4_0(const void* blocks, int64_t N, int64_t K, uint8_t* codes, uint16_t* scales,
+                               cudaStream_t stream);
+cudaError_t launch_gemm(const uint8_t* w_codes, const uint16_t* w_scales, int64_t N, const uint8_t* a_codes,
+                        const float* a_scales, int64_t M, int64_t K, float* y, int64_t ldy, cudaStream_t stream);
+cudaError_t launch_gemm_partials(const uint8_t* w_codes, const uint16_t* w_scales, int64_t N,
+                                 const uint8_t* a_codes, const float* a_scales, int64_t M, int64_t K, int32_t* P,
+                                 cudaStream_t stream);
+cudaError_t launch_gemm_routed(const uint8_t* w_codes, const uint16_t* w_scales, int E, int64_t N,
+                               const uint8_t* a_codes, const float* a_scales, int64_t K, int64_t npairs, int top_k,
+                               int act_per_slot, float* y, const Routing& r, cudaStream_t stream);
+cudaError_t launch_gemm_id(const uint8_t* w_codes, const uint16_t* w_scales, int E, int64_t N,
+                           const uint8_t* a_codes, const float* a_scales, int64_t K, const int32_t* ids, int64_t M,
+                           int top_k, int act_per_slot, float* y, const Routing& r, cudaStream_t stream);
+
+}  // namespace w4a4

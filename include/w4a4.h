@@ -1,0 +1,220 @@
+/*
+ * w4a4.h -- C ABI of libw4a4.so: the prompt-processing (prefill) matmul of a
+ * Hadamard-rotated Q4_0 model run as W4A4, on one NVIDIA GB300 (sm_103a).
+ *
+ * The method is the one described on the engine docs page "The lean option:
+ * ROCmFP4, ROCmI4 and Hadamard Q4_0", section "Hadamard-rotated Q4_0: W4A4
+ * prompt processing":
+ *   - weights are plain Q4_0 (one fp16 scale per 32 values along K, 4-bit codes
+ *     q standing for q - 8), made once from weights rotated per 32-element block
+ *     along K by a normalised 32-point Walsh-Hadamard transform H32;
+ *   - activations get the same per-block rotation at run time and are rounded
+ *     to 4 bits per block (int4 codes, one scale per block);
+ *   - each output is  Y[m][n] = sum_b d_w[n][b] * d_a[m][b] * P[m][n][b],
+ *     P[m][n][b] = sum_{j<32} (q_w - 8) * q_a  (an exact integer, |P| <= 2048).
+ * Section "MoE: W4A4 on the experts" applies the same product to the routed
+ * expert matmuls (MUL_MAT_ID).  The engine's per-tensor rotation flag (engine
+ * PR #262, "Pin ROCmFPX fc664ba: Hadamard rotation per tensor ...") is kept as
+ * a per-operand tag: a rotated operand is never multiplied with an unrotated
+ * one (the silently-wrong mixed case the PR's review warns about is refused).
+ *
+ * Conventions for every entry point:
+ *   - Ownership: the caller allocates every buffer.  Pointers named "device"
+ *     are CUDA device (or managed) memory of the current device; nothing is
+ *     retained after the call returns.  The library allocates no memory and
+ *     keeps no per-call global state.
+ *   - Streams: all GPU work is enqueued on `stream` (a cudaStream_t; 0 is the
+ *     legacy default stream) and is asynchronous with respect to the host;
+ *     outputs are valid once the stream reaches that point.
+ *   - Errors: arguments are checked before anything is launched; a failed
+ *     check returns a status (never aborts, never throws) and records a message
+ *     for w4a4_last_error() (thread-local).  A launch failure returns
+ *     W4A4_ERR_CUDA with the CUDA error text.  Data errors found on the device
+ *     (expert ids out of range) are reported through a device flag, see
+ *     w4a4_gemm_id / w4a4_gemm_id_status.
+ *   - Sizes: K is a positive multiple of 32 (the block size); B = K / 32.
+ *     Row counts may be 0 (nothing is launched, W4A4_OK).
+ *   - Alignment: every device pointer must be 16-byte aligned and every row
+ *     stride must keep rows 16-byte aligned, else W4A4_ERR_ALIGNMENT.
+ *   - Domain: inputs are finite; a nonzero block whose largest magnitude is
+ *     below 2^-100 is outside the domain (its reciprocal scale overflows).
+ */
+#ifndef W4A4_H
+#define W4A4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t, declared without the CUDA headers. */
+typedef struct CUstream_st* w4a4_stream_t;
+
+typedef enum {
+  W4A4_OK = 0,
+  W4A4_ERR_INVALID_ARG = 1,  /* bad size, null pointer, bad enum value          */
+  W4A4_ERR_ALIGNMENT = 2,    /* pointer or row stride not 16-byte aligned        */
+  W4A4_ERR_MISMATCH = 3,     /* operand tags disagree (rotated vs unrotated, K)  */
+  W4A4_ERR_UNSUPPORTED = 4,  /* valid request this build does not handle         */
+  W4A4_ERR_CUDA = 5,         /* a CUDA call or kernel launch failed              */
+  W4A4_ERR_DEVICE_FLAG = 6,  /* the device reported bad data (see gemm_id)       */
+  W4A4_ERR_WORKSPACE = 7     /* workspace missing or smaller than required       */
+} w4a4_status;
+
+/* Operand tags: a magic in the high half, flags in the low half. */
+#define W4A4_TAG_Q4_0 0x51340000u    /* Q4_0 weights                          */
+#define W4A4_TAG_ACT4 0x41340000u    /* int4 activations                      */
+#define W4A4_TAG_MAGIC_MASK 0xFFFF0000u
+#define W4A4_TAG_ROTATED 0x00000001u /* values were rotated by H32 per block  */
+
+/* Weight input element types for h32_q4_0_pack_weights. */
+#define W4A4_DTYPE_BF16 0
+#define W4A4_DTYPE_F32 1
+
+/*
+ * Q4_0 weights, structure of arrays (rows = output features N, or E*N for
+ * stacked experts):
+ *   codes : device, [rows][K/2] bytes.  Block b of row r is the 16 bytes at
+ *           codes + r*K/2 + 16*b; byte i holds code q_i in its low nibble and
+ *           q_{i+16} in its high nibble (the Q4_0 block order); code q stands
+ *           for the integer q - 8.
+ *   scales: device, [rows][K/32] IEEE fp16 (binary16 bits), the block scale d.
+ */
+typedef struct {
+  uint8_t* codes;
+  uint16_t* scales;
+  int64_t rows;
+  int64_t K;
+  uint32_t tag; /* W4A4_TAG_Q4_0 | (W4A4_TAG_ROTATED if rotated) */
+} w4a4_q4_0;
+
+/*
+ * int4 activations, structure of arrays:
+ *   codes : device, [rows][K/2] bytes, same nibble order as Q4_0; each nibble is
+ *           a 4-bit two's complement integer in -8..7.
+ *   scales: device, [rows][K/32] fp32, the block scale d_a.
+ */
+typedef struct {
+  uint8_t* codes;
+  float* scales;
+  int64_t rows;
+  int64_t K;
+  uint32_t tag; /* W4A4_TAG_ACT4 | (W4A4_TAG_ROTATED if rotated) */
+} w4a4_act4;
+
+/* Bytes needed for the two arrays of a Q4_0 / int4 operand (0 if K is invalid). */
+size_t w4a4_q4_0_codes_bytes(int64_t rows, int64_t K);
+size_t w4a4_q4_0_scales_bytes(int64_t rows, int64_t K);
+size_t w4a4_act4_codes_bytes(int64_t rows, int64_t K);
+size_t w4a4_act4_scales_bytes(int64_t rows, int64_t K);
+
+/*
+ * h32_q4_0_pack_weights -- rotate weights per 32-block along K and quantise to
+ * Q4_0 (engine docs "The lean option ...", section "Hadamard-rotated Q4_0: W4A4
+ * prompt processing": the same rotation applied to the weights once, then plain
+ * Q4_0; section "MoE: W4A4 on the experts": one scale per 32 values).
+ *   w      : device, [N][ldw] elements of type w_dtype (row n holds W[n][0..K-1]).
+ *   rotate : 1 = apply H32 (normalised) before quantising; 0 = plain Q4_0.
+ *   out    : host struct; out->codes and out->scales must point to caller
+ *            buffers of w4a4_q4_0_codes_bytes / _scales_bytes; rows, K and tag
+ *            are written by this call.
+ * Per block: y = H32 w / sqrt(32) (fp32 butterfly, stages 1,2,4,8,16, then one
+ * multiply by fl32(1/sqrt 32)); m = the y of largest magnitude (lowest index on
+ * ties); d = m / -8; q = clamp(round_half_away(y * (1/d)) + 8, 0, 15) (q = 8
+ * when d = 0); stored scale = fp16(d), round to nearest even.
+ */
+w4a4_status h32_q4_0_pack_weights(const void* w, int w_dtype, int64_t N, int64_t K, int64_t ldw,
+                                  int rotate, w4a4_q4_0* out, w4a4_stream_t stream);
+
+/*
+ * q4_0_import -- take existing Q4_0 weights bit for bit (section "Hadamard-
+ * rotated Q4_0: W4A4 prompt processing": the kernel reads plain Q4_0 weights
+ * bit for bit).
+ *   blocks : device, [N][K/32] canonical 18-byte Q4_0 blocks (little-endian fp16
+ *            scale, then 16 code bytes), 2-byte aligned.
+ *   rotated: 1 if the file's weights were rotated by H32 (the stamped files of
+ *            the page), 0 for plain Q4_0.
+ *   out    : as for h32_q4_0_pack_weights.
+ */
+w4a4_status q4_0_import(const void* blocks, int64_t N, int64_t K, int rotated, w4a4_q4_0* out,
+                        w4a4_stream_t stream);
+
+/*
+ * w4a4_rotate_quantize_act -- rotate activations per 32-block along K and
+ * round them to int4 per block (section "Hadamard-rotated Q4_0: W4A4 prompt
+ * processing": only the activations are rounded to 4 bits, after the same
+ * rotation).
+ *   x      : device, fp32 [M][ldx] (row m holds X[m][0..K-1]).
+ *   rotate : 1 = rotate (for rotated weights); 0 = quantise unrotated values.
+ *   out    : host struct; out->codes / out->scales point to caller buffers of
+ *            w4a4_act4_codes_bytes / _scales_bytes; rows, K, tag are written.
+ * Per block: y as for the weights; a = max |y|; d_a = a / 7 (fp32, stored);
+ * q = clamp(round_half_away(y * (1/d_a)), -8, 7) (q = 0 when d_a = 0).
+ */
+w4a4_status w4a4_rotate_quantize_act(const float* x, int64_t M, int64_t K, int64_t ldx, int rotate,
+                                     w4a4_act4* out, w4a4_stream_t stream);
+
+/*
+ * w4a4_gemm -- Y = the block-scaled W4A4 product (MUL_MAT), section
+ * "Hadamard-rotated Q4_0: W4A4 prompt processing".
+ *   w   : Q4_0 weights, rows = N.       a : int4 activations, rows = M.
+ *   y   : device, fp32 [M][ldy], ldy >= N; Y[m][n] = sum_b d_w d_a P (fp32).
+ * w->K must equal a->K and both tags must agree on rotation, else
+ * W4A4_ERR_MISMATCH.  The per-block integer partials are exact on the tensor
+ * cores; the scale fold is fp32.
+ */
+w4a4_status w4a4_gemm(const w4a4_q4_0* w, const w4a4_act4* a, float* y, int64_t ldy,
+                      w4a4_stream_t stream);
+
+/*
+ * w4a4_gemm_partials -- the exact per-block integer dot products
+ * P[m][n][b] = sum_j (q_w - 8) q_a (int32, device [M][N][K/32]), computed by the
+ * same tensor-core main loop as w4a4_gemm.  For verification.
+ */
+w4a4_status w4a4_gemm_partials(const w4a4_q4_0* w, const w4a4_act4* a, int32_t* P,
+                               w4a4_stream_t stream);
+
+/*
+ * w4a4_gemm_id -- the expert-routed product (MUL_MAT_ID), section "MoE: W4A4 on
+ * the experts": token t's slot s uses expert e = ids[t][s].
+ *   experts : Q4_0 weights of all experts stacked along rows, rows = E * N;
+ *             expert e owns rows e*N .. e*N+N-1.
+ *   a       : int4 activations; rows = M (act_per_slot = 0: one row per token,
+ *             the gate/up projections) or M * top_k (act_per_slot = 1: row
+ *             t*top_k + s per token-slot, the down projection).
+ *   ids     : device, int32 [M][top_k].
+ *   y       : device, fp32 [M][top_k][N] (row t*top_k + s), contiguous.
+ *   ws      : device workspace of at least w4a4_gemm_id_workspace_bytes(M,
+ *             top_k, E) bytes, 16-byte aligned; its contents on entry do not
+ *             matter.  It holds the routing (counts, offsets, gather list) and a
+ *             device error flag.
+ * An id outside [0, E) is not used: its output row is zeroed, the device flag in
+ * ws is set, and w4a4_gemm_id_status() on the same ws returns
+ * W4A4_ERR_DEVICE_FLAG.  Each call clears the flag first.
+ */
+w4a4_status w4a4_gemm_id(const w4a4_q4_0* experts, int E, int64_t N, const w4a4_act4* a,
+                         const int32_t* ids, int64_t M, int top_k, int act_per_slot, float* y,
+                         void* ws, size_t ws_bytes, w4a4_stream_t stream);
+
+size_t w4a4_gemm_id_workspace_bytes(int64_t M, int top_k, int E);
+
+/*
+ * w4a4_gemm_id_status -- synchronise `stream`, then read the device flag that
+ * the last w4a4_gemm_id on `ws` left: W4A4_OK, or W4A4_ERR_DEVICE_FLAG if some
+ * id was out of range (or W4A4_ERR_CUDA).
+ */
+w4a4_status w4a4_gemm_id_status(const void* ws, w4a4_stream_t stream);
+
+/* The message of the last failed call on this thread ("" if none). */
+const char* w4a4_last_error(void);
+/* A fixed name for a status value. */
+const char* w4a4_status_name(w4a4_status s);
+/* ABI version of this library (major * 100 + minor). */
+int w4a4_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* W4A4_H */
