@@ -203,7 +203,8 @@ def h32_q4_0_pack_weights(w: torch.Tensor, rotate: bool = True, out: Q4_0Weights
     N, K = w.shape
     out = out or alloc_q4_0(N, K, w.device, rotate)
     d = out.desc()
-    _check(load_library().h32_q4_0_pack_weights(w.data_ptr(), dtype, N, K, w.stride(0), int(rotate),
+    ldw = w.stride(0) if N > 1 else K  # a single row's stride is meaningless (may be 0)
+    _check(load_library().h32_q4_0_pack_weights(w.data_ptr(), dtype, N, K, ldw, int(rotate),
                                                  ctypes.byref(d), _stream(stream)))
     out.rotated = bool(d.tag & TAG_ROTATED)
     return out
@@ -234,7 +235,8 @@ def w4a4_rotate_quantize_act(x: torch.Tensor, rotate: bool = True, out: Act4 | N
     M, K = x.shape
     out = out or alloc_act4(M, K, x.device, rotate)
     d = out.desc()
-    _check(load_library().w4a4_rotate_quantize_act(x.data_ptr(), M, K, x.stride(0), int(rotate),
+    ldx = x.stride(0) if M > 1 else K
+    _check(load_library().w4a4_rotate_quantize_act(x.data_ptr(), M, K, ldx, int(rotate),
                                                     ctypes.byref(d), _stream(stream)))
     out.rotated = bool(rotate)
     return out
@@ -247,7 +249,8 @@ def w4a4_gemm(w: Q4_0Weights, a: Act4, y: torch.Tensor | None = None, stream=Non
     _cuda(y, "y")
     if y.dtype != torch.float32 or y.dim() != 2 or y.stride(1) != 1:
         raise ValueError("y must be a 2-D fp32 tensor with unit stride along N")
-    _check(load_library().w4a4_gemm(ctypes.byref(w.desc()), ctypes.byref(a.desc()), y.data_ptr(), y.stride(0),
+    ldy = y.stride(0) if y.shape[0] > 1 else max(w.rows, 1)
+    _check(load_library().w4a4_gemm(ctypes.byref(w.desc()), ctypes.byref(a.desc()), y.data_ptr(), ldy,
                                     _stream(stream)))
     return y
 

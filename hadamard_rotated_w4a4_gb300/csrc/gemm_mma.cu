@@ -271,6 +271,8 @@ __global__ void __launch_bounds__(THREADS) w4a4_gemm_mma_kernel(Args p) {
   cp_async_wait<0>();
 
   if constexpr (MODE == Mode::kFold) {
+    // paired stores need 8-byte aligned rows
+    const bool vec2 = ((reinterpret_cast<uintptr_t>(p.y) & 7u) == 0) && ((p.ldy & 1) == 0);
     if (!warp_active) {
       // rows of a partial tile still get written below (zeros are correct only for
       // rows that exist; inactive warps own no existing rows)
@@ -293,8 +295,11 @@ __global__ void __launch_bounds__(THREADS) w4a4_gemm_mma_kernel(Args p) {
         for (int ni = 0; ni < 4; ++ni) {
           const int64_t col = n0 + wn * 32 + ni * 8 + 2 * t;
           const float v0 = acc[mi][ni][2 * h], v1 = acc[mi][ni][2 * h + 1];
-          if (col + 1 < p.N) {
+          if (col + 1 < p.N && vec2) {
             *reinterpret_cast<float2*>(yr + col) = make_float2(v0, v1);
+          } else if (col + 1 < p.N) {
+            yr[col] = v0;
+            yr[col + 1] = v1;
           } else if (col < p.N) {
             yr[col] = v0;
           }

@@ -160,7 +160,8 @@ w4a4_status w4a4_rotate_quantize_act(const float* x, int64_t M, int64_t K, int64
  * w4a4_gemm -- Y = the block-scaled W4A4 product (MUL_MAT), section
  * "Hadamard-rotated Q4_0: W4A4 prompt processing".
  *   w   : Q4_0 weights, rows = N.       a : int4 activations, rows = M.
- *   y   : device, fp32 [M][ldy], ldy >= N; Y[m][n] = sum_b d_w d_a P (fp32).
+ *   y   : device, fp32 [M][ldy], ldy >= N, 4-byte aligned (the one exception to
+ *         the 16-byte rule); Y[m][n] = sum_b d_w d_a P (fp32).
  * w->K must equal a->K and both tags must agree on rotation, else
  * W4A4_ERR_MISMATCH.  The per-block integer partials are exact on the tensor
  * cores; the scale fold is fp32.
@@ -185,7 +186,8 @@ w4a4_status w4a4_gemm_partials(const w4a4_q4_0* w, const w4a4_act4* a, int32_t* 
  *             the gate/up projections) or M * top_k (act_per_slot = 1: row
  *             t*top_k + s per token-slot, the down projection).
  *   ids     : device, int32 [M][top_k].
- *   y       : device, fp32 [M][top_k][N] (row t*top_k + s), contiguous.
+ *   y       : device, fp32 [M][top_k][N] (row t*top_k + s), contiguous,
+ *             4-byte aligned.
  *   ws      : device workspace of at least w4a4_gemm_id_workspace_bytes(M,
  *             top_k, E) bytes, 16-byte aligned; its contents on entry do not
  *             matter.  It holds the routing (counts, offsets, gather list) and a
