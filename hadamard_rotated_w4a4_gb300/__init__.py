@@ -32,12 +32,13 @@ __all__ = [
     "W4A4Error", "Q4_0Weights", "Act4", "load_library", "library_path",
     "h32_q4_0_pack_weights", "q4_0_import", "w4a4_rotate_quantize_act",
     "w4a4_gemm", "w4a4_gemm_partials", "w4a4_gemm_id", "w4a4_gemm_id_status",
-    "w4a4_gemm_id_workspace_bytes", "STATUS",
+    "w4a4_gemm_id_workspace_bytes", "w4a4_check", "STATUS",
 ]
 
 STATUS = {
     0: "W4A4_OK", 1: "W4A4_ERR_INVALID_ARG", 2: "W4A4_ERR_ALIGNMENT", 3: "W4A4_ERR_MISMATCH",
     4: "W4A4_ERR_UNSUPPORTED", 5: "W4A4_ERR_CUDA", 6: "W4A4_ERR_DEVICE_FLAG", 7: "W4A4_ERR_WORKSPACE",
+    8: "W4A4_ERR_TIMEOUT",
 }
 TAG_Q4_0 = 0x51340000
 TAG_ACT4 = 0x41340000
@@ -47,7 +48,7 @@ TAG_ROTATED = 0x1
 EXPORTS = [
     "w4a4_q4_0_codes_bytes", "w4a4_q4_0_scales_bytes", "w4a4_act4_codes_bytes", "w4a4_act4_scales_bytes",
     "h32_q4_0_pack_weights", "q4_0_import", "w4a4_rotate_quantize_act", "w4a4_gemm", "w4a4_gemm_partials",
-    "w4a4_gemm_id", "w4a4_gemm_id_workspace_bytes", "w4a4_gemm_id_status", "w4a4_last_error",
+    "w4a4_gemm_id", "w4a4_gemm_id_workspace_bytes", "w4a4_gemm_id_status", "w4a4_check", "w4a4_last_error",
     "w4a4_status_name", "w4a4_abi_version",
 ]
 
@@ -100,8 +101,9 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
                                  vp, vp, u, vp]
     lib.w4a4_gemm_id_workspace_bytes.argtypes, lib.w4a4_gemm_id_workspace_bytes.restype = [i64, i32, i32], u
     lib.w4a4_gemm_id_status.argtypes = [vp, vp]
+    lib.w4a4_check.argtypes = [vp]
     for name in ("h32_q4_0_pack_weights", "q4_0_import", "w4a4_rotate_quantize_act", "w4a4_gemm",
-                 "w4a4_gemm_partials", "w4a4_gemm_id", "w4a4_gemm_id_status"):
+                 "w4a4_gemm_partials", "w4a4_gemm_id", "w4a4_gemm_id_status", "w4a4_check"):
         getattr(lib, name).restype = ctypes.c_int
     lib.w4a4_last_error.argtypes, lib.w4a4_last_error.restype = [], ctypes.c_char_p
     lib.w4a4_status_name.argtypes, lib.w4a4_status_name.restype = [ctypes.c_int], ctypes.c_char_p
@@ -286,6 +288,11 @@ def w4a4_gemm_id(experts: Q4_0Weights, E: int, a: Act4, ids: torch.Tensor, top_k
                                        M, top_k, int(act_per_slot), y.data_ptr(), ws.data_ptr(),
                                        ws.numel() * ws.element_size(), _stream(stream)))
     return y
+
+
+def w4a4_check(stream=None) -> None:
+    """Synchronise and raise W4A4Error(W4A4_ERR_TIMEOUT) if a GEMM kernel gave up on a bounded wait."""
+    _check(load_library().w4a4_check(_stream(stream)))
 
 
 def w4a4_gemm_id_status(ws: torch.Tensor, stream=None) -> None:

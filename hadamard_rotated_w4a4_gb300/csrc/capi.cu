@@ -181,8 +181,8 @@ w4a4_status w4a4_gemm(const w4a4_q4_0* w, const w4a4_act4* a, float* y, int64_t 
   if (M == 0 || N == 0) return ok();
   if (!y) return fail(W4A4_ERR_INVALID_ARG, "%s: y is NULL", fn);
   if ((reinterpret_cast<uintptr_t>(y) & 3u) != 0) return fail(W4A4_ERR_ALIGNMENT, "%s: y must be 4-byte aligned", fn);
-  return cuda_status(w4a4::launch_gemm(w->codes, w->scales, N, a->codes, a->scales, M, a->K, y, ldy,
-                                       reinterpret_cast<cudaStream_t>(stream)), fn);
+  return cuda_status(w4a4::launch_gemm_tc(w->codes, w->scales, N, a->codes, a->scales, M, a->K, y, ldy, nullptr,
+                                          reinterpret_cast<cudaStream_t>(stream)), fn);
 }
 
 w4a4_status w4a4_gemm_partials(const w4a4_q4_0* w, const w4a4_act4* a, int32_t* P, w4a4_stream_t stream) {
@@ -194,8 +194,8 @@ w4a4_status w4a4_gemm_partials(const w4a4_q4_0* w, const w4a4_act4* a, int32_t* 
   if (a->rows == 0 || w->rows == 0) return ok();
   if (!P) return fail(W4A4_ERR_INVALID_ARG, "%s: P is NULL", fn);
   if (!aligned16(P)) return fail(W4A4_ERR_ALIGNMENT, "%s: P must be 16-byte aligned", fn);
-  return cuda_status(w4a4::launch_gemm_partials(w->codes, w->scales, w->rows, a->codes, a->scales, a->rows, a->K, P,
-                                                reinterpret_cast<cudaStream_t>(stream)), fn);
+  return cuda_status(w4a4::launch_gemm_tc(w->codes, w->scales, w->rows, a->codes, a->scales, a->rows, a->K, nullptr,
+                                          0, P, reinterpret_cast<cudaStream_t>(stream)), fn);
 }
 
 size_t w4a4_gemm_id_workspace_bytes(int64_t M, int top_k, int E) {
@@ -246,6 +246,18 @@ w4a4_status w4a4_gemm_id_status(const void* ws, w4a4_stream_t stream) {
   return ok();
 }
 
+w4a4_status w4a4_check(w4a4_stream_t stream) {
+  const char* fn = "w4a4_check";
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_status(e, fn);
+  int flag = 0;
+  e = w4a4::read_and_clear_device_error(&flag);
+  if (e != cudaSuccess) return cuda_status(e, fn);
+  if (flag != 0)
+    return fail(W4A4_ERR_TIMEOUT, "%s: a bounded wait inside a GEMM kernel gave up; its output is incomplete", fn);
+  return ok();
+}
+
 const char* w4a4_last_error(void) { return g_err; }
 
 const char* w4a4_status_name(w4a4_status s) {
@@ -258,6 +270,7 @@ const char* w4a4_status_name(w4a4_status s) {
     case W4A4_ERR_CUDA: return "W4A4_ERR_CUDA";
     case W4A4_ERR_DEVICE_FLAG: return "W4A4_ERR_DEVICE_FLAG";
     case W4A4_ERR_WORKSPACE: return "W4A4_ERR_WORKSPACE";
+    case W4A4_ERR_TIMEOUT: return "W4A4_ERR_TIMEOUT";
   }
   return "W4A4_ERR_UNKNOWN";
 }

@@ -18,8 +18,8 @@ namespace {
 constexpr int kPrepThreads = 1024;
 
 __global__ void __launch_bounds__(kPrepThreads) route_prep_kernel(const int32_t* __restrict__ ids, int64_t npairs,
-                                                                   int E, int64_t N, float* __restrict__ y,
-                                                                   Routing r) {
+                                                                   int E, int64_t N, int tile_tokens,
+                                                                   float* __restrict__ y, Routing r) {
   extern __shared__ int32_t sh[];  // cnt[E], cursor[E]
   int32_t* cnt = sh;
   int32_t* cur = sh + E;
@@ -47,7 +47,7 @@ __global__ void __launch_bounds__(kPrepThreads) route_prep_kernel(const int32_t*
       r.counts[e] = cnt[e];
       cur[e] = off;
       off += cnt[e];
-      toff += (cnt[e] + kGemmBM - 1) / kGemmBM;
+      toff += (cnt[e] + tile_tokens - 1) / tile_tokens;
     }
     r.offsets[E] = off;
     r.tile_off[E] = toff;
@@ -66,6 +66,15 @@ __global__ void __launch_bounds__(kPrepThreads) route_prep_kernel(const int32_t*
 size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
 }  // namespace
+
+int routed_tile_tokens(int64_t npairs, int E) {
+  // about one tile per expert: the mean number of rows an expert receives, in 32s
+  const int64_t mean = (npairs + E - 1) / E;
+  int64_t t = (mean + 31) & ~int64_t(31);
+  if (t < 32) t = 32;
+  if (t > 256) t = 256;
+  return static_cast<int>(t);
+}
 
 RoutingLayout routing_layout(int64_t npairs, int E) {
   RoutingLayout L{};
@@ -96,11 +105,12 @@ cudaError_t launch_gemm_id(const uint8_t* w_codes, const uint16_t* w_scales, int
                            int top_k, int act_per_slot, float* y, const Routing& r, cudaStream_t stream) {
   const int64_t npairs = M * top_k;
   const size_t sh = sizeof(int32_t) * 2 * static_cast<size_t>(E);
-  route_prep_kernel<<<1, kPrepThreads, sh, stream>>>(ids, npairs, E, N, y, r);
+  const int tile = routed_tile_tokens(npairs, E);
+  route_prep_kernel<<<1, kPrepThreads, sh, stream>>>(ids, npairs, E, N, tile, y, r);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return launch_gemm_routed(w_codes, w_scales, E, N, a_codes, a_scales, K, npairs, top_k, act_per_slot, y, r,
-                            stream);
+  return launch_gemm_tc_routed(w_codes, w_scales, E, N, a_codes, a_scales, K, npairs, top_k, act_per_slot, tile,
+                               y, r, stream);
 }
 
 }  // namespace w4a4

@@ -60,7 +60,8 @@ typedef enum {
   W4A4_ERR_UNSUPPORTED = 4,  /* valid request this build does not handle         */
   W4A4_ERR_CUDA = 5,         /* a CUDA call or kernel launch failed              */
   W4A4_ERR_DEVICE_FLAG = 6,  /* the device reported bad data (see gemm_id)       */
-  W4A4_ERR_WORKSPACE = 7     /* workspace missing or smaller than required       */
+  W4A4_ERR_WORKSPACE = 7,    /* workspace missing or smaller than required       */
+  W4A4_ERR_TIMEOUT = 8       /* a bounded wait inside a kernel gave up           */
 } w4a4_status;
 
 /* Operand tags: a magic in the high half, flags in the low half. */
@@ -208,6 +209,15 @@ size_t w4a4_gemm_id_workspace_bytes(int64_t M, int top_k, int E);
  * id was out of range (or W4A4_ERR_CUDA).
  */
 w4a4_status w4a4_gemm_id_status(const void* ws, w4a4_stream_t stream);
+
+/*
+ * w4a4_check -- synchronise `stream`, then report whether any GEMM kernel run
+ * since the last check gave up on one of its bounded internal waits (a pipeline
+ * that stopped making progress for a second).  Such a kernel stops early, so
+ * its output is incomplete: W4A4_ERR_TIMEOUT.  Clears the condition.  Returns
+ * W4A4_ERR_CUDA for an error already pending on the stream.
+ */
+w4a4_status w4a4_check(w4a4_stream_t stream);
 
 /* The message of the last failed call on this thread ("" if none). */
 const char* w4a4_last_error(void);
