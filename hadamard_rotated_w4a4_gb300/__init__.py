@@ -99,7 +99,7 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.w4a4_gemm_partials.argtypes = [ctypes.POINTER(_Q4_0Desc), ctypes.POINTER(_Act4Desc), vp, vp]
     lib.w4a4_gemm_id.argtypes = [ctypes.POINTER(_Q4_0Desc), i32, i64, ctypes.POINTER(_Act4Desc), vp, i64, i32, i32,
                                  vp, vp, u, vp]
-    lib.w4a4_gemm_id_workspace_bytes.argtypes, lib.w4a4_gemm_id_workspace_bytes.restype = [i64, i32, i32], u
+    lib.w4a4_gemm_id_workspace_bytes.argtypes, lib.w4a4_gemm_id_workspace_bytes.restype = [i64, i32, i32, i64], u
     lib.w4a4_gemm_id_status.argtypes = [vp, vp]
     lib.w4a4_check.argtypes = [vp]
     for name in ("h32_q4_0_pack_weights", "q4_0_import", "w4a4_rotate_quantize_act", "w4a4_gemm",
@@ -267,8 +267,8 @@ def w4a4_gemm_partials(w: Q4_0Weights, a: Act4, P: torch.Tensor | None = None, s
     return P
 
 
-def w4a4_gemm_id_workspace_bytes(M: int, top_k: int, E: int) -> int:
-    return int(load_library().w4a4_gemm_id_workspace_bytes(M, top_k, E))
+def w4a4_gemm_id_workspace_bytes(M: int, top_k: int, E: int, K: int) -> int:
+    return int(load_library().w4a4_gemm_id_workspace_bytes(M, top_k, E, K))
 
 
 def w4a4_gemm_id(experts: Q4_0Weights, E: int, a: Act4, ids: torch.Tensor, top_k: int, act_per_slot: bool,
@@ -281,7 +281,7 @@ def w4a4_gemm_id(experts: Q4_0Weights, E: int, a: Act4, ids: torch.Tensor, top_k
     N = experts.rows // E
     if y is None:
         y = torch.empty(M, top_k, N, dtype=torch.float32, device=ids.device)
-    need = w4a4_gemm_id_workspace_bytes(M, top_k, E)
+    need = w4a4_gemm_id_workspace_bytes(M, top_k, E, a.K)
     if ws is None:
         ws = torch.empty(max(need, 16), dtype=torch.uint8, device=ids.device)
     _check(load_library().w4a4_gemm_id(ctypes.byref(experts.desc()), E, N, ctypes.byref(a.desc()), ids.data_ptr(),

@@ -198,9 +198,9 @@ w4a4_status w4a4_gemm_partials(const w4a4_q4_0* w, const w4a4_act4* a, int32_t* 
                                           0, P, reinterpret_cast<cudaStream_t>(stream)), fn);
 }
 
-size_t w4a4_gemm_id_workspace_bytes(int64_t M, int top_k, int E) {
-  if (M < 0 || top_k <= 0 || E <= 0) return 0;
-  return w4a4::routing_layout(M * top_k, E).total;
+size_t w4a4_gemm_id_workspace_bytes(int64_t M, int top_k, int E, int64_t K) {
+  if (M < 0 || top_k <= 0 || E <= 0 || !valid_k(K)) return 0;
+  return w4a4::routing_layout(M * top_k, E, K).total;
 }
 
 w4a4_status w4a4_gemm_id(const w4a4_q4_0* experts, int E, int64_t N, const w4a4_act4* a, const int32_t* ids,
@@ -225,11 +225,11 @@ w4a4_status w4a4_gemm_id(const w4a4_q4_0* experts, int E, int64_t N, const w4a4_
                 (long long)want_rows);
   if (M == 0) return ok();
   if (!ids || !y || !ws) return fail(W4A4_ERR_INVALID_ARG, "%s: NULL pointer", fn);
-  const size_t need = w4a4_gemm_id_workspace_bytes(M, top_k, E);
+  const size_t need = w4a4_gemm_id_workspace_bytes(M, top_k, E, a->K);
   if (ws_bytes < need) return fail(W4A4_ERR_WORKSPACE, "%s: workspace %zu bytes < %zu needed", fn, ws_bytes, need);
   if (!aligned16(ws) || (reinterpret_cast<uintptr_t>(y) & 3u) != 0)
     return fail(W4A4_ERR_ALIGNMENT, "%s: ws must be 16-byte aligned and y 4-byte aligned", fn);
-  const w4a4::Routing r = w4a4::routing_in(ws, M * top_k, E);
+  const w4a4::Routing r = w4a4::routing_in(ws, M * top_k, E, a->K);
   return cuda_status(w4a4::launch_gemm_id(experts->codes, experts->scales, E, N, a->codes, a->scales, a->K, ids, M,
                                           top_k, act_per_slot, y, r, reinterpret_cast<cudaStream_t>(stream)), fn);
 }

@@ -3,12 +3,14 @@
 // W4A4 kernel runs the expert matmuls too, where an MoE spends nearly all of its
 // prompt work.
 //
-// Two launches on the caller's stream:
+// Three launches on the caller's stream:
 //   1. route_prep (one CTA): histogram of ids per expert, exclusive scans of the
-//      pair counts and of the 128-row tiles per expert, the pair list grouped by
+//      pair counts and of the row tiles per expert, the pair list grouped by
 //      expert, zeroed output rows and a device flag for ids outside [0, E);
-//   2. the grouped GEMM over (expert row tile, weight tile), gathering each
-//      tile's activation rows through the pair list and scattering its outputs.
+//   2. gather: each routed row's activation codes and scales, copied in expert
+//      order into the workspace, so that every expert's rows are contiguous;
+//   3. the grouped GEMM over (expert row tile, weight tile), loading both
+//      operands with 2D TMA and scattering each output row to (token, slot).
 #include "w4a4_kernels.cuh"
 
 namespace w4a4 {
@@ -65,6 +67,28 @@ __global__ void __launch_bounds__(kPrepThreads) route_prep_kernel(const int32_t*
 
 size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
+// One warp per gathered row: 16-byte code chunks and the row's scales.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint8_t* __restrict__ codes,
+                                                          const float* __restrict__ scales, int64_t K,
+                                                          int top_k, int act_per_slot, Routing r, int E,
+                                                          uint8_t* __restrict__ gcodes, float* __restrict__ gscales) {
+  const int64_t rows = r.offsets[E];
+  const int64_t B = K / 32;
+  const int lane = threadIdx.x & 31;
+  const int64_t w0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t i = w0; i < rows; i += nw) {
+    const int64_t pr = r.perm[i];
+    const int64_t src = act_per_slot ? pr : pr / top_k;
+    const uint4* s = reinterpret_cast<const uint4*>(codes + src * (K / 2));
+    uint4* d = reinterpret_cast<uint4*>(gcodes + i * (K / 2));
+    for (int64_t c = lane; c < B; c += 32) d[c] = s[c];
+    const float* ss = scales + src * B;
+    float* ds = gscales + i * B;
+    for (int64_t c = lane; c < B; c += 32) ds[c] = ss[c];
+  }
+}
+
 }  // namespace
 
 int routed_tile_tokens(int64_t npairs, int E) {
@@ -76,7 +100,7 @@ int routed_tile_tokens(int64_t npairs, int E) {
   return static_cast<int>(t);
 }
 
-RoutingLayout routing_layout(int64_t npairs, int E) {
+RoutingLayout routing_layout(int64_t npairs, int E, int64_t K) {
   RoutingLayout L{};
   size_t off = 0;
   L.flag = off;     off += 16;  // first, so that a status query needs only the pointer
@@ -84,12 +108,14 @@ RoutingLayout routing_layout(int64_t npairs, int E) {
   L.offsets = off;  off += align16(sizeof(int32_t) * static_cast<size_t>(E + 1));
   L.tile_off = off; off += align16(sizeof(int32_t) * static_cast<size_t>(E + 1));
   L.perm = off;     off += align16(sizeof(int32_t) * static_cast<size_t>(npairs));
+  L.gcodes = off;   off += align16(static_cast<size_t>(npairs) * static_cast<size_t>(K / 2));
+  L.gscales = off;  off += align16(static_cast<size_t>(npairs) * static_cast<size_t>(K / 32) * sizeof(float));
   L.total = off;
   return L;
 }
 
-Routing routing_in(void* ws, int64_t npairs, int E) {
-  const RoutingLayout L = routing_layout(npairs, E);
+Routing routing_in(void* ws, int64_t npairs, int E, int64_t K) {
+  const RoutingLayout L = routing_layout(npairs, E, K);
   uint8_t* base = static_cast<uint8_t*>(ws);
   Routing r;
   r.counts = reinterpret_cast<int32_t*>(base + L.counts);
@@ -97,6 +123,8 @@ Routing routing_in(void* ws, int64_t npairs, int E) {
   r.tile_off = reinterpret_cast<int32_t*>(base + L.tile_off);
   r.perm = reinterpret_cast<int32_t*>(base + L.perm);
   r.flag = reinterpret_cast<int32_t*>(base + L.flag);
+  r.gcodes = base + L.gcodes;
+  r.gscales = reinterpret_cast<float*>(base + L.gscales);
   return r;
 }
 
@@ -109,8 +137,13 @@ cudaError_t launch_gemm_id(const uint8_t* w_codes, const uint16_t* w_scales, int
   route_prep_kernel<<<1, kPrepThreads, sh, stream>>>(ids, npairs, E, N, tile, y, r);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return launch_gemm_tc_routed(w_codes, w_scales, E, N, a_codes, a_scales, K, npairs, top_k, act_per_slot, tile,
-                               y, r, stream);
+  const int64_t gwarps = npairs < 4096 * 8 ? npairs : 4096 * 8;
+  gather_rows_kernel<<<static_cast<unsigned>((gwarps + 7) / 8), 256, 0, stream>>>(a_codes, a_scales, K, top_k,
+                                                                                 act_per_slot, r, E, r.gcodes,
+                                                                                 r.gscales);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_gemm_tc_routed(w_codes, w_scales, E, N, r.gcodes, r.gscales, K, npairs, tile, y, r, stream);
 }
 
 }  // namespace w4a4

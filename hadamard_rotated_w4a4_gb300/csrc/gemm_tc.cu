@@ -1,4 +1,4 @@
-// Block-scaled W4A4 GEMM on the 5th-generation tensor cores (tcgen05, TMEM).
+// Block-scaled W4A4 GEMM on the 5th-generation tensor cores (tcgen05, TMEM, TMA).
 //
 // Engine docs "The lean option: ROCmFP4, ROCmI4 and Hadamard Q4_0", section
 // "Hadamard-rotated Q4_0: W4A4 prompt processing": int4 weights times int4
@@ -11,28 +11,34 @@
 //
 // Exact integer dot on fp8 hardware.  sm_103a has no integer tcgen05 kind, but
 // every 4-bit value v is exactly the e4m3 value v * 2^-9 (bytes 0x00..0x0F are
-// linear, 0x80 adds the sign), so one kind::f8f6f4 MMA with K = 32 yields
-// P * 2^-18 in fp32 without rounding; 2^18 is folded into the weight scale.
-// Weights enter as signed values q - 8 (a q ^ 8 nibble converted to
-// sign-magnitude).  Activations enter as the unsigned offset codes u = a + 8
-// (two's complement nibble with bit 3 flipped, no sign logic), and a second MMA
-// per block against a constant -8 operand adds -8 * sum_j (q_w - 8), so the
-// accumulator holds exactly sum_j (q_w - 8)(u - 8) = P.
+// linear, 0x80 adds the sign), so one kind::f8f6f4 MMA with K = 32 gives a
+// 32-term sum of exact products in fp32, again exact (|sum| <= 3360 * 2^-18).
+// Weights enter as signed values q - 8 (the q ^ 8 nibble in sign-magnitude);
+// activations as their unsigned offset codes u = a + 8 (a two's complement
+// nibble with bit 3 flipped: no sign logic).  The MMA therefore yields
+// D = P + 8 S_w with S_w = sum_j (q_w - 8), and the fold removes 8 S_w inside its
+// first fused multiply-add:
+//   t = fma(D * 2^-18, d_w * 2^18, -d_w * 8 S_w) = round(d_w * P)
+// -- exact operands (d_w * 8 S_w has at most 20 significant bits), one rounding,
+// the same value as multiplying the exact P by d_w -- then acc = fma(t, d_a, acc).
 //
 // Tile: 128 weight rows (MMA M = the 128 TMEM lanes) x up to 256 token columns
 // (MMA N), two TMEM accumulator buffers (512 columns) so that the MMA of block
 // b + 1 overlaps the fold of block b.  Warp roles (384 threads, 1 CTA per SM):
-//   warp 0      producer: cp.async.bulk of each row's packed codes for a stage
-//               of 4 blocks into a 3-deep raw ring (mbarrier complete_tx);
-//   warp 1      TMEM allocator and MMA issuer (one thread);
-//   warps 2-3   converters: unpack int4 -> fp8 into the MMA operand layout
-//               (K-major 8-row x 16-byte core matrices), 4 buffers ahead;
-//   warps 4-11  workers: load each stage's scales and fold each block's
-//               accumulator (tcgen05.ld) into fp32 registers; store Y.
-// Warpgroup 0 releases registers (setmaxnreg.dec) to the two worker
-// warpgroups (setmaxnreg.inc), which hold 128 fp32 accumulators per thread.
-// Every mbarrier wait is bounded (globaltimer); a wait that gives up sets a
-// device error word (read by w4a4_check) and the CTA winds down.
+//   warp 0      producer: two 2D TMA loads per stage of 4 blocks (the weight and
+//               activation code tiles, 64 bytes of each row) into a 3-deep ring;
+//   warp 1      TMEM allocator and MMA issuer (one thread, one MMA per block);
+//   warps 2-3   converters: unpack a stage's int4 codes into four fp8 operand
+//               buffers (K-major 8-row x 16-byte core matrices) and the weight
+//               block sums S_w;
+//   warps 4-11  workers: each stage's scales, the fold of each block's
+//               accumulator (tcgen05.ld) into 128 fp32 registers per thread, Y.
+// Warpgroup 0 releases registers (setmaxnreg.dec) to the two worker warpgroups
+// (setmaxnreg.inc).  Every mbarrier wait is bounded (globaltimer); a wait that
+// gives up sets a device error word (read by w4a4_check) and the CTA winds down.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "w4a4_kernels.cuh"
 
 namespace w4a4 {
@@ -43,32 +49,34 @@ __device__ int g_w4a4_device_error;
 
 namespace {
 
-constexpr int kWorkerWarps = 8;                 // warpgroups 1 and 2: fold
-constexpr int kConvWarps = 2;                   // warps 2-3 of warpgroup 0: int4 -> fp8
+constexpr int kWorkerWarps = 8;
+constexpr int kConvWarps = 2;
 constexpr int kThreads = 128 + 32 * kWorkerWarps;
-constexpr int kRegsLow = 80;    // warpgroup 0 after setmaxnreg.dec
-constexpr int kRegsHigh = 208;  // warpgroups 1-2 after setmaxnreg.inc
-constexpr int TW = 128;             // weight rows per tile
-constexpr int TT = 256;             // token columns per tile (max)
-constexpr int KB = 4;               // 32-blocks per raw stage
-constexpr int RAW = 3;              // raw stages in flight
-constexpr int F8 = 4;               // converted operand buffers
-constexpr int RROW = KB * 16 + 16;  // padded raw row: 8 consecutive rows hit distinct banks
+constexpr int kRegsLow = 64;    // warpgroup 0 after setmaxnreg.dec
+constexpr int kRegsHigh = 216;  // warpgroups 1-2 after setmaxnreg.inc
+constexpr int TW = 128;         // weight rows per tile
+constexpr int TT = 256;         // token columns per tile (max)
+constexpr int KB = 4;           // 32-blocks per stage (64 code bytes per row)
+constexpr int RAW = 3;          // stages of raw codes in flight
+constexpr int F8 = 8;           // fp8 operand buffers (two stages)
+constexpr int WF8 = TW * 32 + 32;  // buffer strides padded by 32 bytes: the converters'
+constexpr int AF8 = TT * 32 + 32;  // 16-byte stores to 4 buffers hit distinct banks
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kTimeoutNs = 1000000000ull;  // 1 s
 
 struct __align__(1024) Smem {
-  uint8_t wf8[F8][TW * 32];
-  uint8_t af8[F8][TT * 32];
-  uint8_t cneg[TT * 32];
-  uint8_t wraw[RAW][TW * RROW];
-  uint8_t araw[RAW][TT * RROW];
+  uint8_t wraw[RAW][TW * KB * 16];  // TMA box: 128 rows x 64 bytes
+  uint8_t araw[RAW][TT * KB * 16];  // TMA box: tt rows x 64 bytes
+  uint8_t wf8[F8][WF8];
+  uint8_t af8[F8][AF8];
+  int32_t sw[F8][TW];               // per weight row and block: sum_j (q_w - 8)
   float sda[2][KB][TT];
   float sdw[2][KB][TW];
   uint64_t full_raw[RAW];
   uint64_t empty_raw[RAW];
   uint64_t f8_full[F8];
-  uint64_t f8_empty[F8];
+  uint64_t f8_empty[F8];   // the MMA has read the operand buffer
+  uint64_t sw_empty[F8];   // the workers have read the block sums
   uint64_t tm_full[2];
   uint64_t tm_empty[2];
   uint64_t sc_ready[2];
@@ -79,23 +87,19 @@ struct __align__(1024) Smem {
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;  // + alignment slack
 
 struct TcArgs {
-  const uint8_t* w_codes;
   const uint16_t* w_scales;
-  const uint8_t* a_codes;
-  const float* a_scales;
-  int64_t M;  // dense: token rows; routed: (token, slot) pairs
-  int64_t N;  // output features (per expert)
+  const float* a_scales;  // dense: [M][B]; routed: gathered [npairs][B]
+  int64_t M;              // dense: token rows; routed: (token, slot) pairs
+  int64_t N;              // output features (per expert)
   int64_t K;
   float* y;
   int64_t ldy;
   int32_t* P;
-  int tt;  // token tile (multiple of 32, <= TT)
-  const int32_t* perm;
+  int tt;                 // token tile (multiple of 32, <= TT): the A box height
+  const int32_t* perm;    // routed: gathered row -> pair index (the Y row)
   const int32_t* offsets;
   const int32_t* tile_off;
   int E;
-  int top_k;
-  int act_per_slot;
 };
 
 // ------------------------------------------------------------------ PTX helpers
@@ -139,10 +143,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, Smem& S)
     }
   }
 }
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+__device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* map, int32_t x, int32_t y, uint64_t* bar) {
   asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(su32(dst)),
-      "l"(src), "r"(bytes), "r"(su32(bar))
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(su32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(su32(bar))
       : "memory");
 }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
@@ -161,11 +165,11 @@ __device__ __forceinline__ uint64_t kmajor_desc(const void* smem) {
 __device__ __forceinline__ uint32_t f8_idesc(int n) {
   return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(128 >> 4) << 24);
 }
-__device__ __forceinline__ void mma_f8(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, int acc) {
+__device__ __forceinline__ void mma_f8(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc) {
   asm volatile(
-      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "{\n.reg .pred p;\nsetp.ne.b32 p, 0, 0;\n"
       "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc));
+      "l"(a), "l"(b), "r"(idesc));
 }
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(bar))
@@ -182,12 +186,17 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
+// sum of the 8 nibbles of a word
+__device__ __forceinline__ int nibble_sum(uint32_t w) {
+  const uint32_t s = (w & 0x0F0F0F0Fu) + ((w >> 4) & 0x0F0F0F0Fu);  // 4 bytes, each <= 30
+  return __dp4a(static_cast<int>(s), 0x01010101, 0);
+}
 
 // ------------------------------------------------------------------ tiles
 struct Tile {
   int64_t n0;     // first weight row of the tile within its expert
-  int64_t wbase;  // first weight row in the stacked weight array
-  int64_t m0;     // dense: first token row; routed: first pair of the segment
+  int64_t wrow0;  // first weight row in the (stacked) weight tensor
+  int64_t m0;     // first token row (dense) or gathered row (routed)
   int rows_w;     // valid weight rows (<= 128)
   int ntok;       // valid token rows (<= tt)
   int nmma;       // MMA N: ntok rounded up to 32
@@ -203,7 +212,7 @@ __device__ __forceinline__ Tile decode_tile(const TcArgs& p, int64_t t) {
   Tile T;
   const int64_t ntw = (p.N + TW - 1) / TW;
   int64_t wt;
-  if (p.tile_off) {
+  if (p.tile_off) {  // expert segments of the gathered rows, tt rows per tile
     const int64_t mt = t / ntw;
     wt = t - mt * ntw;
     int lo = 0, hi = p.E - 1;  // last expert whose first tile is <= mt
@@ -214,82 +223,45 @@ __device__ __forceinline__ Tile decode_tile(const TcArgs& p, int64_t t) {
     T.m0 = p.offsets[lo] + (mt - p.tile_off[lo]) * p.tt;
     const int64_t left = p.offsets[lo + 1] - T.m0;
     T.ntok = static_cast<int>(left < p.tt ? left : p.tt);
-    T.wbase = static_cast<int64_t>(lo) * p.N;
-  } else {
+    T.wrow0 = static_cast<int64_t>(lo) * p.N;
+  } else {  // weight tile major, so consecutive CTAs share a weight tile in L2
     const int64_t ntt = (p.M + p.tt - 1) / p.tt;
     wt = t / ntt;
     const int64_t tt = t - wt * ntt;
     T.m0 = tt * p.tt;
     const int64_t left = p.M - T.m0;
     T.ntok = static_cast<int>(left < p.tt ? left : p.tt);
-    T.wbase = 0;
+    T.wrow0 = 0;
   }
   T.n0 = wt * TW;
+  T.wrow0 += T.n0;
   const int64_t lw = p.N - T.n0;
   T.rows_w = static_cast<int>(lw < TW ? lw : TW);
   T.nmma = (T.ntok + 31) & ~31;
   return T;
 }
 
-__device__ __forceinline__ int64_t act_row(const TcArgs& p, const Tile& T, int r) {
-  if (p.tile_off) {
-    const int64_t pr = p.perm[T.m0 + r];
-    return p.act_per_slot ? pr : pr / p.top_k;
-  }
-  return T.m0 + r;
-}
-__device__ __forceinline__ int64_t out_row(const TcArgs& p, const Tile& T, int r) {
-  return p.tile_off ? static_cast<int64_t>(p.perm[T.m0 + r]) : T.m0 + r;
-}
-
 // ------------------------------------------------------------------ roles
-__device__ void producer_loop(const TcArgs& p, Smem& S, uint32_t& gstage) {
-  const int lane = threadIdx.x & 31;
+__device__ void producer(const TcArgs& p, Smem& S, const CUtensorMap* wmap, const CUtensorMap* amap) {
   const int64_t B = p.K / 32;
   const int64_t nst = (B + KB - 1) / KB;
   const int64_t ntiles = num_tiles(p);
-  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+  const uint32_t bytes = static_cast<uint32_t>(KB * 16 * (TW + p.tt));  // full boxes, zero fill included
+  uint32_t gstage = 0;
+  for (int64_t t = blockIdx.x; t < ntiles && !S.abort; t += gridDim.x) {
     const Tile T = decode_tile(p, t);
-    const uint8_t* wrow[TW / 32];
-    const uint8_t* arow[TT / 32];
-#pragma unroll
-    for (int i = 0; i < TW / 32; ++i) {
-      const int r = lane + 32 * i;
-      wrow[i] = p.w_codes + (T.wbase + T.n0 + (r < T.rows_w ? r : 0)) * (p.K / 2);
-    }
-#pragma unroll
-    for (int i = 0; i < TT / 32; ++i) {
-      const int r = lane + 32 * i;
-      arow[i] = p.a_codes + act_row(p, T, r < T.ntok ? r : 0) * (p.K / 2);
-    }
     for (int64_t s = 0; s < nst; ++s) {
       const int slot = gstage % RAW;
-      if (!mbar_wait(&S.empty_raw[slot], ((gstage / RAW) & 1) ^ 1, S)) return;
-      const int64_t kb0 = s * KB;
-      const uint32_t nbk = static_cast<uint32_t>(B - kb0 < KB ? B - kb0 : KB);
-      const uint32_t rb = nbk * 16;
-      if (lane == 0) mbar_expect_tx(&S.full_raw[slot], rb * static_cast<uint32_t>(T.rows_w + T.ntok));
-      __syncwarp();
-#pragma unroll
-      for (int i = 0; i < TW / 32; ++i) {
-        const int r = lane + 32 * i;
-        if (r < T.rows_w) bulk_g2s(S.wraw[slot] + r * RROW, wrow[i] + kb0 * 16, rb, &S.full_raw[slot]);
-      }
-#pragma unroll
-      for (int i = 0; i < TT / 32; ++i) {
-        const int r = lane + 32 * i;
-        if (r < T.ntok) bulk_g2s(S.araw[slot] + r * RROW, arow[i] + kb0 * 16, rb, &S.full_raw[slot]);
-      }
+      if (!mbar_wait(&S.empty_raw[slot], ((gstage / RAW) & 1) ^ 1, S)) break;
+      mbar_expect_tx(&S.full_raw[slot], bytes);
+      const int32_t x = static_cast<int32_t>(s * KB * 16);
+      tma_2d(S.wraw[slot], wmap, x, static_cast<int32_t>(T.wrow0), &S.full_raw[slot]);
+      tma_2d(S.araw[slot], amap, x, static_cast<int32_t>(T.m0), &S.full_raw[slot]);
       ++gstage;
     }
   }
-}
-
-__device__ void producer(const TcArgs& p, Smem& S) {
-  uint32_t gstage = 0;  // stages whose copies were issued
-  producer_loop(p, S, gstage);
   // Drain: the last RAW stages' copies must have landed before the CTA exits
-  // (normally the workers have already consumed them and this returns at once).
+  // (normally the consumers already waited for them and this returns at once).
   const uint32_t first = gstage > RAW ? gstage - RAW : 0;
   for (uint32_t g = first; g < gstage; ++g) {
     const uint64_t t0 = gtime();
@@ -301,7 +273,6 @@ __device__ void producer(const TcArgs& p, Smem& S) {
 __device__ void mma_issuer(const TcArgs& p, Smem& S, uint32_t tmem) {
   const int64_t B = p.K / 32;
   const int64_t ntiles = num_tiles(p);
-  const uint64_t cdesc = kmajor_desc(S.cneg);
   uint32_t gblk = 0;
   for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
     const Tile T = decode_tile(p, t);
@@ -312,12 +283,7 @@ __device__ void mma_issuer(const TcArgs& p, Smem& S, uint32_t tmem) {
       if (!mbar_wait(&S.f8_full[f], (gblk / F8) & 1, S)) goto done;
       if (!mbar_wait(&S.tm_empty[tb], ((gblk >> 1) & 1) ^ 1, S)) goto done;
       tc_fence_after();
-      {
-        const uint32_t d = tmem + static_cast<uint32_t>(tb * TT);
-        const uint64_t wdesc = kmajor_desc(S.wf8[f]);
-        mma_f8(d, wdesc, kmajor_desc(S.af8[f]), idesc, 0);
-        mma_f8(d, wdesc, cdesc, idesc, 1);
-      }
+      mma_f8(tmem + static_cast<uint32_t>(tb * TT), kmajor_desc(S.wf8[f]), kmajor_desc(S.af8[f]), idesc);
       mma_commit(&S.tm_full[tb]);
       mma_commit(&S.f8_empty[f]);
     }
@@ -332,49 +298,56 @@ done:
   }
 }
 
+// Two warps convert one stage (4 blocks) at a time.  Lane l of a pass takes row
+// (pass base + l / 4) and block l % 4, so 8 lanes read 128 contiguous raw bytes;
+// the destination buffers are padded so that the four blocks' stores of the
+// same 8 lanes land in distinct banks too.
 __device__ void converters(const TcArgs& p, Smem& S) {
   const int ct = threadIdx.x - 64;  // 0..63
   const int lane = threadIdx.x & 31;
   const int64_t B = p.K / 32;
   const int64_t nst = (B + KB - 1) / KB;
   const int64_t ntiles = num_tiles(p);
-  uint32_t gstage = 0, gconv = 0;
+  uint32_t gstage = 0, gblk = 0;
   for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
     const Tile T = decode_tile(p, t);
-    for (int64_t b = 0; b < B; ++b) {
-      const int64_t s = b / KB;
-      const int kb = static_cast<int>(b - s * KB);
-      const uint32_t gs = gstage + static_cast<uint32_t>(s);
-      const int slot = gs % RAW;
-      if (kb == 0 && !mbar_wait(&S.full_raw[slot], (gs / RAW) & 1, S)) return;
-      const int f = gconv % F8;
-      if (!mbar_wait(&S.f8_empty[f], ((gconv / F8) & 1) ^ 1, S)) return;
-      // weights: rows ct and ct + 64, signed q - 8
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const int r = ct + 64 * i;
-        if (r < T.rows_w) {
-          const uint4 raw = *reinterpret_cast<const uint4*>(S.wraw[slot] + r * RROW + kb * 16);
+    for (int64_t s = 0; s < nst; ++s, ++gstage) {
+      const int nbk = static_cast<int>(B - s * KB < KB ? B - s * KB : KB);
+      const int slot = gstage % RAW;
+      if (!mbar_wait(&S.full_raw[slot], (gstage / RAW) & 1, S)) return;
+      for (int k = 0; k < nbk; ++k) {
+        const uint32_t g = gblk + k;
+        if (!mbar_wait(&S.f8_empty[g % F8], ((g / F8) & 1) ^ 1, S)) return;
+        if (!mbar_wait(&S.sw_empty[g % F8], ((g / F8) & 1) ^ 1, S)) return;
+      }
+      // weights: 128 rows x 4 blocks, signed q - 8, and the block sums
+#pragma unroll 2
+      for (int it = 0; it < TW * KB / 64; ++it) {
+        const int rb = it * 64 + ct;
+        const int r = rb >> 2, k = rb & 3;
+        if (k < nbk) {
+          const uint4 raw = *reinterpret_cast<const uint4*>(S.wraw[slot] + r * (KB * 16) + k * 16);
           uint32_t l0, h0, l1, h1, l2, h2, l3, h3;
           q4_0_word_to_e4m3(raw.x, l0, h0);
           q4_0_word_to_e4m3(raw.y, l1, h1);
           q4_0_word_to_e4m3(raw.z, l2, h2);
           q4_0_word_to_e4m3(raw.w, l3, h3);
+          const int f = (gblk + k) % F8;
           uint8_t* dst = S.wf8[f] + (r >> 3) * 256 + (r & 7) * 16;
           *reinterpret_cast<uint4*>(dst) = make_uint4(l0, l1, l2, l3);
           *reinterpret_cast<uint4*>(dst + 128) = make_uint4(h0, h1, h2, h3);
+          S.sw[f][r] = nibble_sum(raw.x) + nibble_sum(raw.y) + nibble_sum(raw.z) + nibble_sum(raw.w) - 256;
         }
       }
-      // activations: rows ct + 64 i; offset codes u = a + 8 are the e4m3 bytes themselves
-#pragma unroll
-      for (int i = 0; i < TT / 64; ++i) {
-        const int r = ct + 64 * i;
-        if (r < T.nmma) {
-          uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-          if (r < T.ntok) raw = *reinterpret_cast<const uint4*>(S.araw[slot] + r * RROW + kb * 16);
+      // activations: nmma rows x 4 blocks; the offset codes u = a + 8 are the e4m3 bytes
+      for (int it = 0; it < T.nmma * KB / 64; ++it) {
+        const int rb = it * 64 + ct;
+        const int r = rb >> 2, k = rb & 3;
+        if (k < nbk) {
+          const uint4 raw = *reinterpret_cast<const uint4*>(S.araw[slot] + r * (KB * 16) + k * 16);
           const uint32_t x0 = raw.x ^ 0x88888888u, x1 = raw.y ^ 0x88888888u;
           const uint32_t x2 = raw.z ^ 0x88888888u, x3 = raw.w ^ 0x88888888u;
-          uint8_t* dst = S.af8[f] + (r >> 3) * 256 + (r & 7) * 16;
+          uint8_t* dst = S.af8[(gblk + k) % F8] + (r >> 3) * 256 + (r & 7) * 16;
           *reinterpret_cast<uint4*>(dst) =
               make_uint4(x0 & 0x0F0F0F0Fu, x1 & 0x0F0F0F0Fu, x2 & 0x0F0F0F0Fu, x3 & 0x0F0F0F0Fu);
           *reinterpret_cast<uint4*>(dst + 128) = make_uint4((x0 >> 4) & 0x0F0F0F0Fu, (x1 >> 4) & 0x0F0F0F0Fu,
@@ -384,12 +357,11 @@ __device__ void converters(const TcArgs& p, Smem& S) {
       fence_async_smem();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&S.f8_full[f]);
-        if (kb == KB - 1 || b == B - 1) mbar_arrive(&S.empty_raw[slot]);
+        for (int k = 0; k < nbk; ++k) mbar_arrive(&S.f8_full[(gblk + k) % F8]);
+        mbar_arrive(&S.empty_raw[slot]);
       }
-      ++gconv;
+      gblk += nbk;
     }
-    gstage += static_cast<uint32_t>(nst);
   }
 }
 
@@ -412,16 +384,18 @@ __device__ void workers(const TcArgs& p, Smem& S, uint32_t tmem) {
     // scale sources of this thread: activation row wt, weight row wt (wt < 128)
     const bool a_ok = wt < T.ntok;
     const bool w_ok = wt < T.rows_w;
-    const float* as_row = p.a_scales + (a_ok ? act_row(p, T, wt) : 0) * B;
-    const uint16_t* ws_row = p.w_scales + (T.wbase + T.n0 + (w_ok ? wt : 0)) * B;
-    float da_r[KB], dw_r[KB];
+    const float* as_row = p.a_scales + (T.m0 + (a_ok ? wt : 0)) * B;
+    const uint16_t* ws_row = p.w_scales + (T.wrow0 + (w_ok ? wt : 0)) * B;
+    float da_r[KB];
+    uint32_t dw_r[KB / 2];  // raw fp16 bits, two per register
     auto load_scales = [&](int s) {
 #pragma unroll
       for (int k = 0; k < KB; ++k) {
         const int b = s * KB + k;
         const bool bok = b < B;
         da_r[k] = (a_ok && bok) ? __ldg(as_row + b) : 0.f;
-        dw_r[k] = (w_ok && bok) ? __half2float(__ushort_as_half(__ldg(ws_row + b))) * fp8_unscale() : 0.f;
+        const uint32_t hbits = (w_ok && bok) ? static_cast<uint32_t>(__ldg(ws_row + b)) : 0u;
+        if (k & 1) dw_r[k >> 1] |= hbits << 16; else dw_r[k >> 1] = hbits;
       }
     };
     // publish the registers' scales for one stage and wait until every worker warp has
@@ -430,7 +404,10 @@ __device__ void workers(const TcArgs& p, Smem& S, uint32_t tmem) {
 #pragma unroll
       for (int k = 0; k < KB; ++k) {
         S.sda[slot][k][wt] = da_r[k];
-        if (wt < TW) S.sdw[slot][k][wt] = dw_r[k];
+        if (wt < TW) {
+          const uint16_t hb = static_cast<uint16_t>((dw_r[k >> 1] >> (16 * (k & 1))) & 0xFFFFu);
+          S.sdw[slot][k][wt] = __half2float(__ushort_as_half(hb)) * fp8_unscale();
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.sc_ready[slot]);
@@ -457,10 +434,16 @@ __device__ void workers(const TcArgs& p, Smem& S, uint32_t tmem) {
       }
       // ---- fold block b
       const int tb = gfold & 1;
+      const int f = gfold % F8;
       if (!mbar_wait(&S.tm_full[tb], (gfold >> 1) & 1, S)) return;
       tc_fence_after();
       const int slot = (gsc - 1) & 1;
       const float dw = S.sdw[slot][kb][n_in];
+      const int sw = S.sw[f][n_in];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.sw_empty[f]);
+      // -d_w * 8 S_w, exact: (d_w 2^18) * (S_w 2^-15)
+      const float corr = -dw * (static_cast<float>(sw) * 3.0517578125e-05f);
       const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(tb * TT);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -477,7 +460,8 @@ __device__ void workers(const TcArgs& p, Smem& S, uint32_t tmem) {
                 const int col = c * 32 + 16 * half + j;
                 if (col < T.ntok && n_in < T.rows_w) {
                   const int64_t m = T.m0 + col;
-                  p.P[(m * p.N + n) * B + b] = static_cast<int32_t>(v[j] * fp8_unscale());
+                  // D = P + 8 S_w, an exact integer times 2^-18
+                  p.P[(m * p.N + n) * B + b] = static_cast<int32_t>(v[j] * fp8_unscale()) - 8 * sw;
                 }
               }
             } else {
@@ -486,10 +470,10 @@ __device__ void workers(const TcArgs& p, Smem& S, uint32_t tmem) {
               for (int j = 0; j < 4; ++j) {
                 const float4 d = da4[j];
                 const int o = 16 * half + 4 * j;
-                acc[i][o + 0] = fmaf(v[4 * j + 0] * dw, d.x, acc[i][o + 0]);
-                acc[i][o + 1] = fmaf(v[4 * j + 1] * dw, d.y, acc[i][o + 1]);
-                acc[i][o + 2] = fmaf(v[4 * j + 2] * dw, d.z, acc[i][o + 2]);
-                acc[i][o + 3] = fmaf(v[4 * j + 3] * dw, d.w, acc[i][o + 3]);
+                acc[i][o + 0] = fmaf(fmaf(v[4 * j + 0], dw, corr), d.x, acc[i][o + 0]);
+                acc[i][o + 1] = fmaf(fmaf(v[4 * j + 1], dw, corr), d.y, acc[i][o + 1]);
+                acc[i][o + 2] = fmaf(fmaf(v[4 * j + 2], dw, corr), d.z, acc[i][o + 2]);
+                acc[i][o + 3] = fmaf(fmaf(v[4 * j + 3], dw, corr), d.w, acc[i][o + 3]);
               }
             }
           }
@@ -511,7 +495,10 @@ __device__ void workers(const TcArgs& p, Smem& S, uint32_t tmem) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
               const int col = c * 32 + j;
-              if (col < T.ntok) p.y[out_row(p, T, col) * p.ldy + n] = acc[i][j];
+              if (col < T.ntok) {
+                const int64_t row = p.perm ? static_cast<int64_t>(p.perm[T.m0 + col]) : T.m0 + col;
+                p.y[row * p.ldy + n] = acc[i][j];
+              }
             }
           }
         }
@@ -521,7 +508,9 @@ __device__ void workers(const TcArgs& p, Smem& S, uint32_t tmem) {
 }
 
 template <bool PARTIALS>
-__global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_tc_kernel(const TcArgs p) {
+__global__ void __launch_bounds__(kThreads, 1)
+    w4a4_gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap amap,
+                        const TcArgs p) {
   extern __shared__ uint8_t smem_dyn[];
   Smem& S = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
@@ -534,6 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_tc_kernel(const TcArgs 
     for (int i = 0; i < F8; ++i) {
       mbar_init(&S.f8_full[i], kConvWarps);
       mbar_init(&S.f8_empty[i], 1);
+      mbar_init(&S.sw_empty[i], kWorkerWarps);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&S.tm_full[i], 1);
@@ -543,10 +533,9 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_tc_kernel(const TcArgs 
     mbar_init(&S.mma_done, 1);
     S.abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&wmap)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&amap)) : "memory");
   }
-  for (int i = threadIdx.x; i < TT * 32 / 4; i += blockDim.x)
-    reinterpret_cast<uint32_t*>(S.cneg)[i] = 0x88888888u;  // e4m3 -8 * 2^-9
-  fence_async_smem();
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&S.tmem_base)),
                  "r"(kTmemCols));
@@ -560,7 +549,8 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_tc_kernel(const TcArgs 
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
     if (warp == 0) {
-      producer(p, S);
+      if ((threadIdx.x & 31) == 0) producer(p, S, &wmap, &amap);
+      __syncwarp();
     } else if (warp == 1) {
       if ((threadIdx.x & 31) == 0) mma_issuer(p, S, tmem);
       __syncwarp();
@@ -581,31 +571,59 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_gemm_tc_kernel(const TcArgs 
   }
 }
 
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2D map over packed codes [rows][K/2] bytes, box = 64 bytes x box_rows rows.
+cudaError_t codes_map(CUtensorMap* m, const uint8_t* codes, int64_t rows, int64_t K, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(KB * 16), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(codes), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <bool PARTIALS>
-cudaError_t launch_tc(const TcArgs& a, int64_t max_tiles, cudaStream_t stream) {
+cudaError_t launch_tc(const CUtensorMap& wmap, const CUtensorMap& amap, const TcArgs& a, int64_t max_tiles,
+                      cudaStream_t stream) {
   auto kern = w4a4_gemm_tc_kernel<PARTIALS>;
   static bool configured[64] = {};
+  static int regs_ok[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
-    configured[dev] = true;
-  }
-  // setmaxnreg.inc waits until the block's launch registers cover the split:
-  // refuse to launch a build whose register count would make it wait forever.
-  static int regs_ok[64] = {};
-  if (dev >= 0 && dev < 64 && regs_ok[dev] == 0) {
+    // setmaxnreg.inc waits until the block's launch registers cover the split:
+    // refuse to launch a build whose register count would make it wait forever.
     cudaFuncAttributes fa{};
-    cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+    e = cudaFuncGetAttributes(&fa, kern);
     if (e != cudaSuccess) return e;
     regs_ok[dev] = (fa.numRegs * kThreads >= 128 * kRegsLow + 256 * kRegsHigh) ? 1 : -1;
+    configured[dev] = true;
   }
-  if (dev >= 0 && dev < 64 && regs_ok[dev] < 0) return cudaErrorInvalidConfiguration;
+  if (regs_ok[dev] < 0) return cudaErrorInvalidConfiguration;
   int64_t grid = max_tiles < num_sms() ? max_tiles : num_sms();
   if (grid < 1) grid = 1;
-  kern<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(a);
+  kern<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(wmap, amap, a);
   return cudaGetLastError();
 }
 
@@ -620,25 +638,31 @@ cudaError_t launch_gemm_tc(const uint8_t* w_codes, const uint16_t* w_scales, int
                            const float* a_scales, int64_t M, int64_t K, float* y, int64_t ldy, int32_t* P,
                            cudaStream_t stream) {
   TcArgs a{};
-  a.w_codes = w_codes; a.w_scales = w_scales; a.a_codes = a_codes; a.a_scales = a_scales;
+  a.w_scales = w_scales; a.a_scales = a_scales;
   a.M = M; a.N = N; a.K = K; a.y = y; a.ldy = ldy; a.P = P;
   a.tt = token_tile(M);
+  CUtensorMap wmap, amap;
+  cudaError_t e = codes_map(&wmap, w_codes, N, K, TW);
+  if (e == cudaSuccess) e = codes_map(&amap, a_codes, M, K, a.tt);
+  if (e != cudaSuccess) return e;
   const int64_t tiles = ((N + TW - 1) / TW) * ((M + a.tt - 1) / a.tt);
-  return P ? launch_tc<true>(a, tiles, stream) : launch_tc<false>(a, tiles, stream);
+  return P ? launch_tc<true>(wmap, amap, a, tiles, stream) : launch_tc<false>(wmap, amap, a, tiles, stream);
 }
 
 cudaError_t launch_gemm_tc_routed(const uint8_t* w_codes, const uint16_t* w_scales, int E, int64_t N,
-                                  const uint8_t* a_codes, const float* a_scales, int64_t K, int64_t npairs,
-                                  int top_k, int act_per_slot, int tile_tokens, float* y, const Routing& r,
-                                  cudaStream_t stream) {
+                                  const uint8_t* g_codes, const float* g_scales, int64_t K, int64_t npairs,
+                                  int tile_tokens, float* y, const Routing& r, cudaStream_t stream) {
   TcArgs a{};
-  a.w_codes = w_codes; a.w_scales = w_scales; a.a_codes = a_codes; a.a_scales = a_scales;
+  a.w_scales = w_scales; a.a_scales = g_scales;
   a.M = npairs; a.N = N; a.K = K; a.y = y; a.ldy = N;
   a.tt = tile_tokens;
-  a.perm = r.perm; a.offsets = r.offsets; a.tile_off = r.tile_off; a.E = E; a.top_k = top_k;
-  a.act_per_slot = act_per_slot;
+  a.perm = r.perm; a.offsets = r.offsets; a.tile_off = r.tile_off; a.E = E;
+  CUtensorMap wmap, amap;
+  cudaError_t e = codes_map(&wmap, w_codes, static_cast<int64_t>(E) * N, K, TW);
+  if (e == cudaSuccess) e = codes_map(&amap, g_codes, npairs, K, a.tt);
+  if (e != cudaSuccess) return e;
   const int64_t max_tiles = (npairs / tile_tokens + E) * ((N + TW - 1) / TW);
-  return launch_tc<false>(a, max_tiles, stream);
+  return launch_tc<false>(wmap, amap, a, max_tiles, stream);
 }
 
 cudaError_t read_and_clear_device_error(int* value) {

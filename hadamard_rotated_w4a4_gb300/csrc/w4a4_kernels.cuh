@@ -18,13 +18,15 @@ struct Routing {
   int32_t* tile_off;  // [E + 1] exclusive prefix of row tiles per expert
   int32_t* perm;      // [M * top_k] pair indices p = t * top_k + s, grouped by expert
   int32_t* flag;      // [1]     nonzero: some id was outside [0, E)
+  uint8_t* gcodes;    // [M * top_k][K/2] activation codes gathered in expert order
+  float* gscales;     // [M * top_k][K/32] their scales
 };
 
 struct RoutingLayout {
-  size_t counts, offsets, tile_off, perm, flag, total;
+  size_t counts, offsets, tile_off, perm, flag, gcodes, gscales, total;
 };
-RoutingLayout routing_layout(int64_t npairs, int E);
-Routing routing_in(void* ws, int64_t npairs, int E);
+RoutingLayout routing_layout(int64_t npairs, int E, int64_t K);
+Routing routing_in(void* ws, int64_t npairs, int E, int64_t K);
 
 cudaError_t launch_act_rotate_quantize(const float* x, int64_t M, int64_t K, int64_t ldx, int rotate,
                                        uint8_t* codes, float* scales, cudaStream_t stream);
@@ -36,9 +38,8 @@ cudaError_t launch_gemm_tc(const uint8_t* w_codes, const uint16_t* w_scales, int
                            const float* a_scales, int64_t M, int64_t K, float* y, int64_t ldy, int32_t* P,
                            cudaStream_t stream);
 cudaError_t launch_gemm_tc_routed(const uint8_t* w_codes, const uint16_t* w_scales, int E, int64_t N,
-                                  const uint8_t* a_codes, const float* a_scales, int64_t K, int64_t npairs,
-                                  int top_k, int act_per_slot, int tile_tokens, float* y, const Routing& r,
-                                  cudaStream_t stream);
+                                  const uint8_t* g_codes, const float* g_scales, int64_t K, int64_t npairs,
+                                  int tile_tokens, float* y, const Routing& r, cudaStream_t stream);
 // Token rows per routed tile for a MUL_MAT_ID problem (multiple of 32, <= 256).
 int routed_tile_tokens(int64_t npairs, int E);
 // Reads the GEMM kernels' device error word (bounded waits that gave up) and clears it.

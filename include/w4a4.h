@@ -190,9 +190,10 @@ w4a4_status w4a4_gemm_partials(const w4a4_q4_0* w, const w4a4_act4* a, int32_t* 
  *   y       : device, fp32 [M][top_k][N] (row t*top_k + s), contiguous,
  *             4-byte aligned.
  *   ws      : device workspace of at least w4a4_gemm_id_workspace_bytes(M,
- *             top_k, E) bytes, 16-byte aligned; its contents on entry do not
- *             matter.  It holds the routing (counts, offsets, gather list) and a
- *             device error flag.
+ *             top_k, E, K) bytes, 16-byte aligned; its contents on entry do not
+ *             matter.  It holds the routing (counts, offsets, pair list), the
+ *             routed activation rows gathered in expert order, and a device
+ *             error flag (its first word).
  * An id outside [0, E) is not used: its output row is zeroed, the device flag in
  * ws is set, and w4a4_gemm_id_status() on the same ws returns
  * W4A4_ERR_DEVICE_FLAG.  Each call clears the flag first.
@@ -201,7 +202,7 @@ w4a4_status w4a4_gemm_id(const w4a4_q4_0* experts, int E, int64_t N, const w4a4_
                          const int32_t* ids, int64_t M, int top_k, int act_per_slot, float* y,
                          void* ws, size_t ws_bytes, w4a4_stream_t stream);
 
-size_t w4a4_gemm_id_workspace_bytes(int64_t M, int top_k, int E);
+size_t w4a4_gemm_id_workspace_bytes(int64_t M, int top_k, int E, int64_t K);
 
 /*
  * w4a4_gemm_id_status -- synchronise `stream`, then read the device flag that

@@ -44,7 +44,7 @@ def test_size_queries(lib):
     assert lib.w4a4_q4_0_scales_bytes(3, 96) == 32  # 3 * 3 * 2 = 18 bytes, padded to 16
     assert lib.w4a4_act4_scales_bytes(2, 64) == 16
     assert lib.w4a4_q4_0_codes_bytes(4, 33) == 0   # K not a multiple of 32
-    assert lib.w4a4_gemm_id_workspace_bytes(1024, 8, 128) >= 4 * (1024 * 8 + 3 * 128)
+    assert lib.w4a4_gemm_id_workspace_bytes(1024, 8, 128, 2048) >= 4 * (1024 * 8 + 3 * 128) + 1024 * 8 * (1024 + 256)
 
 
 FAKE = 0x10000  # aligned, never dereferenced: every call below fails validation first
@@ -121,7 +121,7 @@ def test_act_and_pack_argument_checks(lib):
 def test_gemm_id_argument_checks(lib):
     E, N, M, k = 4, 64, 8, 2
     ex = q4(rows=E * N)
-    need = lib.w4a4_gemm_id_workspace_bytes(M, k, E)
+    need = lib.w4a4_gemm_id_workspace_bytes(M, k, E, 256)
 
     def call(experts=ex, E=E, N=N, a=a4(rows=M), M=M, k=k, aps=0, ws_bytes=need, ws=FAKE):
         return status(lib, "w4a4_gemm_id", ctypes.byref(experts), E, N, ctypes.byref(a), FAKE, M, k, aps,

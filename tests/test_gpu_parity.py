@@ -251,7 +251,7 @@ def _moe_gpu(dev, w_bits, E, N, x, ids, top_k, act_per_slot, ws=None):
     aq = w4.w4a4_rotate_quantize_act(f32_tensor(x, dev))
     idt = torch.from_numpy(np.ascontiguousarray(ids, dtype=np.int32)).to(dev)
     if ws is None:
-        ws = torch.empty(w4.w4a4_gemm_id_workspace_bytes(ids.shape[0], top_k, E), dtype=torch.uint8, device=dev)
+        ws = torch.empty(w4.w4a4_gemm_id_workspace_bytes(ids.shape[0], top_k, E, x.shape[1]), dtype=torch.uint8, device=dev)
     y = w4.w4a4_gemm_id(wq, E, aq, idt, top_k, act_per_slot, ws=ws)
     return y, ws
 
