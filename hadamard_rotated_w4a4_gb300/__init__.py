@@ -46,8 +46,8 @@ TAG_ROTATED = 0x1
 
 #: every symbol include/w4a4.h declares
 EXPORTS = [
-    "w4a4_q4_0_codes_bytes", "w4a4_q4_0_scales_bytes", "w4a4_act4_codes_bytes", "w4a4_act4_scales_bytes",
-    "h32_q4_0_pack_weights", "q4_0_import", "w4a4_rotate_quantize_act", "w4a4_gemm", "w4a4_gemm_partials",
+    "w4a4_q4_0_codes_bytes", "w4a4_q4_0_scales_bytes", "w4a4_q4_0_sums_bytes", "w4a4_act4_codes_bytes",
+    "w4a4_act4_scales_bytes", "h32_q4_0_pack_weights", "q4_0_import", "w4a4_rotate_quantize_act", "w4a4_gemm", "w4a4_gemm_partials",
     "w4a4_gemm_id", "w4a4_gemm_id_workspace_bytes", "w4a4_gemm_id_status", "w4a4_check", "w4a4_last_error",
     "w4a4_status_name", "w4a4_abi_version",
 ]
@@ -61,8 +61,8 @@ class W4A4Error(RuntimeError):
 
 
 class _Q4_0Desc(ctypes.Structure):
-    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("rows", ctypes.c_int64),
-                ("K", ctypes.c_int64), ("tag", ctypes.c_uint32)]
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("sums", ctypes.c_void_p),
+                ("rows", ctypes.c_int64), ("K", ctypes.c_int64), ("tag", ctypes.c_uint32)]
 
 
 class _Act4Desc(ctypes.Structure):
@@ -89,7 +89,8 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         _build.build()
     lib = ctypes.CDLL(path)
     i64, vp, i32, u = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
-    for name in ("w4a4_q4_0_codes_bytes", "w4a4_q4_0_scales_bytes", "w4a4_act4_codes_bytes", "w4a4_act4_scales_bytes"):
+    for name in ("w4a4_q4_0_codes_bytes", "w4a4_q4_0_scales_bytes", "w4a4_q4_0_sums_bytes", "w4a4_act4_codes_bytes",
+                 "w4a4_act4_scales_bytes"):
         f = getattr(lib, name)
         f.argtypes, f.restype = [i64, i64], u
     lib.h32_q4_0_pack_weights.argtypes = [vp, i32, i64, i64, i64, i32, ctypes.POINTER(_Q4_0Desc), vp]
@@ -131,12 +132,19 @@ def _cuda(t: torch.Tensor, name: str) -> None:
 
 @dataclass
 class Q4_0Weights:
-    """Q4_0 weights in the library's layout: codes uint8 [rows][K/2], scales fp16 [rows][K/32]."""
+    """Q4_0 weights in the library's layout: codes uint8 [rows][K/2], scales fp16 [rows][K/32],
+    and the derived per-block code sums int16 [rows][K/32]."""
     codes: torch.Tensor
     scales_buf: torch.Tensor  # uint8 buffer (padded to 16 bytes) holding the fp16 scales
+    sums_buf: torch.Tensor    # uint8 buffer (padded to 16 bytes) holding the int16 block sums
     rows: int
     K: int
     rotated: bool
+
+    @property
+    def sums(self) -> torch.Tensor:
+        n = self.rows * (self.K // 32)
+        return self.sums_buf[: 2 * n].view(torch.int16).view(self.rows, self.K // 32)
 
     @property
     def scales(self) -> torch.Tensor:
@@ -148,7 +156,12 @@ class Q4_0Weights:
         return TAG_Q4_0 | (TAG_ROTATED if self.rotated else 0)
 
     def desc(self) -> _Q4_0Desc:
-        return _Q4_0Desc(self.codes.data_ptr(), self.scales_buf.data_ptr(), self.rows, self.K, self.tag)
+        return _Q4_0Desc(self.codes.data_ptr(), self.scales_buf.data_ptr(), self.sums_buf.data_ptr(), self.rows,
+                         self.K, self.tag)
+
+    def head(self, rows: int) -> "Q4_0Weights":
+        """The first `rows` rows (views of the same buffers)."""
+        return Q4_0Weights(self.codes[:rows], self.scales_buf, self.sums_buf, rows, self.K, self.rotated)
 
 
 @dataclass
@@ -169,6 +182,10 @@ class Act4:
     def tag(self) -> int:
         return TAG_ACT4 | (TAG_ROTATED if self.rotated else 0)
 
+    def head(self, rows: int) -> "Act4":
+        """The first `rows` rows (views of the same buffers)."""
+        return Act4(self.codes[:rows], self.scales_buf, rows, self.K, self.rotated)
+
     def desc(self) -> _Act4Desc:
         return _Act4Desc(self.codes.data_ptr(), self.scales_buf.data_ptr(), self.rows, self.K, self.tag)
 
@@ -180,7 +197,8 @@ def alloc_q4_0(rows: int, K: int, device, rotated: bool = True) -> Q4_0Weights:
         raise W4A4Error(1, f"K={K} must be a positive multiple of 32")
     codes = torch.empty(max(nc, 16), dtype=torch.uint8, device=device)[:nc].view(rows, K // 2)
     sbuf = torch.empty(max(ns, 16), dtype=torch.uint8, device=device)
-    return Q4_0Weights(codes, sbuf, rows, K, rotated)
+    ubuf = torch.empty(max(lib.w4a4_q4_0_sums_bytes(rows, K), 16), dtype=torch.uint8, device=device)
+    return Q4_0Weights(codes, sbuf, ubuf, rows, K, rotated)
 
 
 def alloc_act4(rows: int, K: int, device, rotated: bool = True) -> Act4:

@@ -63,9 +63,10 @@ w4a4_status check_q4_0(const w4a4_q4_0* w, const char* fn) {
     return fail(W4A4_ERR_INVALID_ARG, "%s: weight descriptor tag 0x%08x is not a Q4_0 tag", fn, w->tag);
   w4a4_status s = check_k_rows(w->rows, w->K, fn);
   if (s != W4A4_OK) return s;
-  if (w->rows > 0 && (!w->codes || !w->scales)) return fail(W4A4_ERR_INVALID_ARG, "%s: weight pointers are NULL", fn);
-  if (!aligned16(w->codes) || !aligned16(w->scales))
-    return fail(W4A4_ERR_ALIGNMENT, "%s: weight codes/scales must be 16-byte aligned", fn);
+  if (w->rows > 0 && (!w->codes || !w->scales || !w->sums))
+    return fail(W4A4_ERR_INVALID_ARG, "%s: weight pointers are NULL", fn);
+  if (!aligned16(w->codes) || !aligned16(w->scales) || !aligned16(w->sums))
+    return fail(W4A4_ERR_ALIGNMENT, "%s: weight codes/scales/sums must be 16-byte aligned", fn);
   return W4A4_OK;
 }
 
@@ -105,6 +106,7 @@ size_t w4a4_q4_0_scales_bytes(int64_t rows, int64_t K) {
   // padded to 16 bytes: the GEMM reads each fp16 scale through its aligned 4-byte word
   return round16(static_cast<size_t>(rows) * static_cast<size_t>(K / 32) * 2);
 }
+size_t w4a4_q4_0_sums_bytes(int64_t rows, int64_t K) { return w4a4_q4_0_scales_bytes(rows, K); }
 size_t w4a4_act4_codes_bytes(int64_t rows, int64_t K) { return w4a4_q4_0_codes_bytes(rows, K); }
 size_t w4a4_act4_scales_bytes(int64_t rows, int64_t K) {
   if (!valid_k(K) || rows < 0) return 0;
@@ -122,14 +124,16 @@ w4a4_status h32_q4_0_pack_weights(const void* w, int w_dtype, int64_t N, int64_t
   if (rotate != 0 && rotate != 1) return fail(W4A4_ERR_INVALID_ARG, "%s: rotate must be 0 or 1", fn);
   if (ldw < K) return fail(W4A4_ERR_INVALID_ARG, "%s: ldw=%lld < K=%lld", fn, (long long)ldw, (long long)K);
   const int64_t esz = (w_dtype == W4A4_DTYPE_BF16) ? 2 : 4;
-  if (N > 0 && (!w || !out->codes || !out->scales)) return fail(W4A4_ERR_INVALID_ARG, "%s: NULL pointer", fn);
-  if (!aligned16(w) || !aligned16(out->codes) || !aligned16(out->scales) || (ldw * esz) % 16 != 0)
+  if (N > 0 && (!w || !out->codes || !out->scales || !out->sums))
+    return fail(W4A4_ERR_INVALID_ARG, "%s: NULL pointer", fn);
+  if (!aligned16(w) || !aligned16(out->codes) || !aligned16(out->scales) || !aligned16(out->sums) ||
+      (ldw * esz) % 16 != 0)
     return fail(W4A4_ERR_ALIGNMENT, "%s: pointers and rows (ldw * element size) must be 16-byte aligned", fn);
   out->rows = N;
   out->K = K;
   out->tag = W4A4_TAG_Q4_0 | (rotate ? W4A4_TAG_ROTATED : 0u);
   if (N == 0) return ok();
-  return cuda_status(w4a4::launch_pack_q4_0(w, w_dtype, N, K, ldw, rotate, out->codes, out->scales,
+  return cuda_status(w4a4::launch_pack_q4_0(w, w_dtype, N, K, ldw, rotate, out->codes, out->scales, out->sums,
                                             reinterpret_cast<cudaStream_t>(stream)), fn);
 }
 
@@ -140,14 +144,16 @@ w4a4_status q4_0_import(const void* blocks, int64_t N, int64_t K, int rotated, w
   w4a4_status s = check_k_rows(N, K, fn);
   if (s != W4A4_OK) return s;
   if (rotated != 0 && rotated != 1) return fail(W4A4_ERR_INVALID_ARG, "%s: rotated must be 0 or 1", fn);
-  if (N > 0 && (!blocks || !out->codes || !out->scales)) return fail(W4A4_ERR_INVALID_ARG, "%s: NULL pointer", fn);
-  if ((reinterpret_cast<uintptr_t>(blocks) & 1u) != 0 || !aligned16(out->codes) || !aligned16(out->scales))
+  if (N > 0 && (!blocks || !out->codes || !out->scales || !out->sums))
+    return fail(W4A4_ERR_INVALID_ARG, "%s: NULL pointer", fn);
+  if ((reinterpret_cast<uintptr_t>(blocks) & 1u) != 0 || !aligned16(out->codes) || !aligned16(out->scales) ||
+      !aligned16(out->sums))
     return fail(W4A4_ERR_ALIGNMENT, "%s: blocks must be 2-byte aligned, outputs 16-byte aligned", fn);
   out->rows = N;
   out->K = K;
   out->tag = W4A4_TAG_Q4_0 | (rotated ? W4A4_TAG_ROTATED : 0u);
   if (N == 0) return ok();
-  return cuda_status(w4a4::launch_import_q4_0(blocks, N, K, out->codes, out->scales,
+  return cuda_status(w4a4::launch_import_q4_0(blocks, N, K, out->codes, out->scales, out->sums,
                                               reinterpret_cast<cudaStream_t>(stream)), fn);
 }
 
@@ -181,7 +187,7 @@ w4a4_status w4a4_gemm(const w4a4_q4_0* w, const w4a4_act4* a, float* y, int64_t 
   if (M == 0 || N == 0) return ok();
   if (!y) return fail(W4A4_ERR_INVALID_ARG, "%s: y is NULL", fn);
   if ((reinterpret_cast<uintptr_t>(y) & 3u) != 0) return fail(W4A4_ERR_ALIGNMENT, "%s: y must be 4-byte aligned", fn);
-  return cuda_status(w4a4::launch_gemm_tc(w->codes, w->scales, N, a->codes, a->scales, M, a->K, y, ldy, nullptr,
+  return cuda_status(w4a4::launch_gemm_tc(w->codes, w->scales, w->sums, N, a->codes, a->scales, M, a->K, y, ldy, nullptr,
                                           reinterpret_cast<cudaStream_t>(stream)), fn);
 }
 
@@ -194,7 +200,7 @@ w4a4_status w4a4_gemm_partials(const w4a4_q4_0* w, const w4a4_act4* a, int32_t* 
   if (a->rows == 0 || w->rows == 0) return ok();
   if (!P) return fail(W4A4_ERR_INVALID_ARG, "%s: P is NULL", fn);
   if (!aligned16(P)) return fail(W4A4_ERR_ALIGNMENT, "%s: P must be 16-byte aligned", fn);
-  return cuda_status(w4a4::launch_gemm_tc(w->codes, w->scales, w->rows, a->codes, a->scales, a->rows, a->K, nullptr,
+  return cuda_status(w4a4::launch_gemm_tc(w->codes, w->scales, w->sums, w->rows, a->codes, a->scales, a->rows, a->K, nullptr,
                                           0, P, reinterpret_cast<cudaStream_t>(stream)), fn);
 }
 
@@ -230,7 +236,7 @@ w4a4_status w4a4_gemm_id(const w4a4_q4_0* experts, int E, int64_t N, const w4a4_
   if (!aligned16(ws) || (reinterpret_cast<uintptr_t>(y) & 3u) != 0)
     return fail(W4A4_ERR_ALIGNMENT, "%s: ws must be 16-byte aligned and y 4-byte aligned", fn);
   const w4a4::Routing r = w4a4::routing_in(ws, M * top_k, E, a->K);
-  return cuda_status(w4a4::launch_gemm_id(experts->codes, experts->scales, E, N, a->codes, a->scales, a->K, ids, M,
+  return cuda_status(w4a4::launch_gemm_id(experts->codes, experts->scales, experts->sums, E, N, a->codes, a->scales, a->K, ids, M,
                                           top_k, act_per_slot, y, r, reinterpret_cast<cudaStream_t>(stream)), fn);
 }
 

@@ -128,7 +128,7 @@ Routing routing_in(void* ws, int64_t npairs, int E, int64_t K) {
   return r;
 }
 
-cudaError_t launch_gemm_id(const uint8_t* w_codes, const uint16_t* w_scales, int E, int64_t N,
+cudaError_t launch_gemm_id(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums, int E, int64_t N,
                            const uint8_t* a_codes, const float* a_scales, int64_t K, const int32_t* ids, int64_t M,
                            int top_k, int act_per_slot, float* y, const Routing& r, cudaStream_t stream) {
   const int64_t npairs = M * top_k;
@@ -143,7 +143,7 @@ cudaError_t launch_gemm_id(const uint8_t* w_codes, const uint16_t* w_scales, int
                                                                                  r.gscales);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return launch_gemm_tc_routed(w_codes, w_scales, E, N, r.gcodes, r.gscales, K, npairs, tile, y, r, stream);
+  return launch_gemm_tc_routed(w_codes, w_scales, w_sums, E, N, r.gcodes, r.gscales, K, npairs, tile, y, r, stream);
 }
 
 }  // namespace w4a4

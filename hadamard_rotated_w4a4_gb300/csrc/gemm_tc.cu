@@ -16,8 +16,8 @@
 // Weights enter as signed values q - 8 (the q ^ 8 nibble in sign-magnitude);
 // activations as their unsigned offset codes u = a + 8 (a two's complement
 // nibble with bit 3 flipped: no sign logic).  The MMA therefore yields
-// D = P + 8 S_w with S_w = sum_j (q_w - 8), and the fold removes 8 S_w inside its
-// first fused multiply-add:
+// D = P + 8 S_w with S_w = sum_j (q_w - 8) (stored with the weights), and the
+// fold removes 8 S_w inside its first fused multiply-add:
 //   t = fma(D * 2^-18, d_w * 2^18, -d_w * 8 S_w) = round(d_w * P)
 // -- exact operands (d_w * 8 S_w has at most 20 significant bits), one rounding,
 // the same value as multiplying the exact P by d_w -- then acc = fma(t, d_a, acc).
@@ -29,8 +29,7 @@
 //               activation code tiles, 64 bytes of each row) into a 3-deep ring;
 //   warp 1      TMEM allocator and MMA issuer (one thread, one MMA per block);
 //   warps 2-3   converters: unpack a stage's int4 codes into four fp8 operand
-//               buffers (K-major 8-row x 16-byte core matrices) and the weight
-//               block sums S_w;
+//               buffers (K-major 8-row x 16-byte core matrices);
 //   warps 4-11  workers: each stage's scales, the fold of each block's
 //               accumulator (tcgen05.ld) into 128 fp32 registers per thread, Y.
 // Warpgroup 0 releases registers (setmaxnreg.dec) to the two worker warpgroups
@@ -64,30 +63,32 @@ constexpr int AF8 = TT * 32 + 32;  // 16-byte stores to 4 buffers hit distinct b
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kTimeoutNs = 1000000000ull;  // 1 s
 
-struct __align__(1024) Smem {
+
+struct __align__(128) Smem {
   uint8_t wraw[RAW][TW * KB * 16];  // TMA box: 128 rows x 64 bytes
   uint8_t araw[RAW][TT * KB * 16];  // TMA box: tt rows x 64 bytes
   uint8_t wf8[F8][WF8];
   uint8_t af8[F8][AF8];
-  int32_t sw[F8][TW];               // per weight row and block: sum_j (q_w - 8)
-  float sda[2][KB][TT];
-  float sdw[2][KB][TW];
+  float sda[2][KB][TT];              // d_a per stage, block-major
+  float sdw[2][KB][TW];              // d_w * 2^18
+  float scorr[2][KB][TW];            // -d_w * 8 S_w (exact)
   uint64_t full_raw[RAW];
   uint64_t empty_raw[RAW];
   uint64_t f8_full[F8];
   uint64_t f8_empty[F8];   // the MMA has read the operand buffer
-  uint64_t sw_empty[F8];   // the workers have read the block sums
   uint64_t tm_full[2];
   uint64_t tm_empty[2];
   uint64_t sc_ready[2];
+  uint64_t tile_done;      // every worker warp has finished its previous tile
   uint64_t mma_done;
   uint32_t tmem_base;
   volatile int abort;
 };
-constexpr size_t kSmemBytes = sizeof(Smem) + 1024;  // + alignment slack
+constexpr size_t kSmemBytes = sizeof(Smem);
 
 struct TcArgs {
   const uint16_t* w_scales;
+  const int16_t* w_sums;  // per weight row and block: S_w = sum_j (q_w - 8)
   const float* a_scales;  // dense: [M][B]; routed: gathered [npairs][B]
   int64_t M;              // dense: token rows; routed: (token, slot) pairs
   int64_t N;              // output features (per expert)
@@ -129,12 +130,23 @@ __device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// As mbar_try, but the thread may sleep (up to `ns` nanoseconds) until the phase
+// completes instead of spinning through issue slots.
+__device__ __forceinline__ bool mbar_try_sleep(uint64_t* b, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\nselp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(su32(b)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
 // Bounded wait on phase `parity`; false if it (or another role) gave up.
 __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, Smem& S) {
   if (mbar_try(b, parity)) return true;
   const uint64_t t0 = gtime();
   for (;;) {
-    if (mbar_try(b, parity)) return true;
+    if (mbar_try_sleep(b, parity, 20000u)) return true;
     if (S.abort) return false;
     if (gtime() - t0 > kTimeoutNs) {
       S.abort = 1;
@@ -175,23 +187,24 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(bar))
                : "memory");
 }
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
+// 16 consecutive TMEM columns of this thread's lane; asynchronous until tmem_wait.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
         "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
-// sum of the 8 nibbles of a word
-__device__ __forceinline__ int nibble_sum(uint32_t w) {
-  const uint32_t s = (w & 0x0F0F0F0Fu) + ((w >> 4) & 0x0F0F0F0Fu);  // 4 bytes, each <= 30
-  return __dp4a(static_cast<int>(s), 0x01010101, 0);
+// Wait for this thread's outstanding TMEM loads.  The registers of the load in
+// flight are in/out operands, so no use of them can be scheduled above the wait.
+__device__ __forceinline__ void tmem_wait(uint32_t (&r)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15])
+               :
+               : "memory");
 }
-
 // ------------------------------------------------------------------ tiles
 struct Tile {
   int64_t n0;     // first weight row of the tile within its expert
@@ -318,9 +331,8 @@ __device__ void converters(const TcArgs& p, Smem& S) {
       for (int k = 0; k < nbk; ++k) {
         const uint32_t g = gblk + k;
         if (!mbar_wait(&S.f8_empty[g % F8], ((g / F8) & 1) ^ 1, S)) return;
-        if (!mbar_wait(&S.sw_empty[g % F8], ((g / F8) & 1) ^ 1, S)) return;
       }
-      // weights: 128 rows x 4 blocks, signed q - 8, and the block sums
+      // weights: 128 rows x 4 blocks, signed q - 8
 #pragma unroll 2
       for (int it = 0; it < TW * KB / 64; ++it) {
         const int rb = it * 64 + ct;
@@ -336,7 +348,6 @@ __device__ void converters(const TcArgs& p, Smem& S) {
           uint8_t* dst = S.wf8[f] + (r >> 3) * 256 + (r & 7) * 16;
           *reinterpret_cast<uint4*>(dst) = make_uint4(l0, l1, l2, l3);
           *reinterpret_cast<uint4*>(dst + 128) = make_uint4(h0, h1, h2, h3);
-          S.sw[f][r] = nibble_sum(raw.x) + nibble_sum(raw.y) + nibble_sum(raw.z) + nibble_sum(raw.w) - 256;
         }
       }
       // activations: nmma rows x 4 blocks; the offset codes u = a + 8 are the e4m3 bytes
@@ -376,9 +387,11 @@ __device__ void workers(const TcArgs& p, Smem& S, uint32_t tmem) {
   const int B = static_cast<int>(p.K / 32);
   const int nst = (B + KB - 1) / KB;
   const int64_t ntiles = num_tiles(p);
-  uint32_t gfold = 0, gsc = 0;
+  uint32_t gfold = 0, gsc = 0, gtile = 0;
 
-  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++gtile) {
+    // the scale slots are reused across tiles: start only when every warp is done
+    if (gtile > 0 && !mbar_wait(&S.tile_done, (gtile - 1) & 1, S)) return;
     const Tile T = decode_tile(p, t);
     const int nchunks = T.nmma / 32;
     // scale sources of this thread: activation row wt, weight row wt (wt < 128)
@@ -386,96 +399,148 @@ __device__ void workers(const TcArgs& p, Smem& S, uint32_t tmem) {
     const bool w_ok = wt < T.rows_w;
     const float* as_row = p.a_scales + (T.m0 + (a_ok ? wt : 0)) * B;
     const uint16_t* ws_row = p.w_scales + (T.wrow0 + (w_ok ? wt : 0)) * B;
+    const int16_t* wsum_row = p.w_sums + (T.wrow0 + (w_ok ? wt : 0)) * B;
+    // Scales of the next stage, prefetched into registers one stage ahead and kept
+    // as loaded (no arithmetic on them until they are published, so the warp does
+    // not wait for the loads).
     float da_r[KB];
-    uint32_t dw_r[KB / 2];  // raw fp16 bits, two per register
+    unsigned short dw_r[KB];
+    short sw_r[KB];
+    // Loads are unconditional (clamped to valid addresses); validity is applied
+    // when publishing, so nothing consumes a loaded value early.
     auto load_scales = [&](int s) {
 #pragma unroll
       for (int k = 0; k < KB; ++k) {
-        const int b = s * KB + k;
-        const bool bok = b < B;
-        da_r[k] = (a_ok && bok) ? __ldg(as_row + b) : 0.f;
-        const uint32_t hbits = (w_ok && bok) ? static_cast<uint32_t>(__ldg(ws_row + b)) : 0u;
-        if (k & 1) dw_r[k >> 1] |= hbits << 16; else dw_r[k >> 1] = hbits;
+        const int b = min(s * KB + k, B - 1);
+        da_r[k] = __ldg(as_row + b);
+        dw_r[k] = __ldg(ws_row + b);
+        sw_r[k] = __ldg(wsum_row + b);
       }
     };
-    // publish the registers' scales for one stage and wait until every worker warp has
-    auto publish_scales = [&]() -> bool {
-      const int slot = gsc & 1;
+    // Store the registers' scales into a slot and arrive; waiting is separate.
+    auto publish_scales = [&](int slot, int s) {
 #pragma unroll
       for (int k = 0; k < KB; ++k) {
-        S.sda[slot][k][wt] = da_r[k];
+        const bool bok = s * KB + k < B;
+        S.sda[slot][k][wt] = (a_ok && bok) ? da_r[k] : 0.f;
         if (wt < TW) {
-          const uint16_t hb = static_cast<uint16_t>((dw_r[k >> 1] >> (16 * (k & 1))) & 0xFFFFu);
-          S.sdw[slot][k][wt] = __half2float(__ushort_as_half(hb)) * fp8_unscale();
+          const float dw = (w_ok && bok) ? __half2float(__ushort_as_half(dw_r[k])) * fp8_unscale() : 0.f;
+          S.sdw[slot][k][wt] = dw;
+          // -d_w * 8 S_w, exact: (d_w 2^18) * (S_w 2^-15), at most 20 significant bits
+          S.scorr[slot][k][wt] = (w_ok && bok) ? -dw * (static_cast<float>(sw_r[k]) * 3.0517578125e-05f) : 0.f;
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.sc_ready[slot]);
-      const bool ok = mbar_wait(&S.sc_ready[slot], (gsc >> 1) & 1, S);
-      ++gsc;
-      return ok;
     };
-    float acc[4][32];
+    float2 acc[4][16];  // column pairs (2j, 2j + 1) of chunk h + 2i
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int j = 0; j < 32; ++j) acc[i][j] = 0.f;
+      for (int j = 0; j < 16; ++j) acc[i][j] = make_float2(0.f, 0.f);
 
+    // Stage s's scales live in slot (gsc0 + s) & 1.  During stage s the registers
+    // hold stage s + 1's scales; they are published once block kb = 2 of stage s
+    // has its accumulator (the MMA of block b needs every warp to have released
+    // block b - 2, so every warp is past stage s - 1, the slot's previous user),
+    // then stage s + 2 is prefetched.  A stage's slot is waited for at kb = 0.
+    const uint32_t gsc0 = gsc;
     load_scales(0);
-    if (!publish_scales()) return;
+    publish_scales(gsc0 & 1, 0);
     if (nst > 1) load_scales(1);
 
     for (int b = 0; b < B; ++b) {
       const int s = b / KB;
       const int kb = b - s * KB;
-      if (kb == 0 && b > 0) {
-        if (!publish_scales()) return;
-        if (s + 1 < nst) load_scales(s + 1);
-      }
+      const uint32_t gs = gsc0 + static_cast<uint32_t>(s);
+      if (kb == 0 && !mbar_wait(&S.sc_ready[gs & 1], (gs >> 1) & 1, S)) return;
       // ---- fold block b
       const int tb = gfold & 1;
-      const int f = gfold % F8;
       if (!mbar_wait(&S.tm_full[tb], (gfold >> 1) & 1, S)) return;
       tc_fence_after();
-      const int slot = (gsc - 1) & 1;
+      if (kb == 2 && s + 1 < nst) {
+        publish_scales((gs + 1) & 1, s + 1);
+        if (s + 2 < nst) load_scales(s + 2);
+      }
+      const int slot = gs & 1;
       const float dw = S.sdw[slot][kb][n_in];
-      const int sw = S.sw[f][n_in];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.sw_empty[f]);
-      // -d_w * 8 S_w, exact: (d_w 2^18) * (S_w 2^-15)
-      const float corr = -dw * (static_cast<float>(sw) * 3.0517578125e-05f);
+      const float corr = S.scorr[slot][kb][n_in];
+      const float2 dw2 = make_float2(dw, dw);
+      const float2 corr2 = make_float2(corr, corr);
       const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(tb * TT);
+      if (!PARTIALS && nchunks == TT / 32) {
+        // Full-width tile: straight-line fold, TMEM columns and d_a addresses at
+        // fixed offsets from this warp's base (chunk h + 2i, piece half).
+        const uint32_t tw = tbase + static_cast<uint32_t>(h * 32);
+        const float* dab = &S.sda[slot][kb][h * 32];
+        uint32_t ra[16], rb[16];
+        tmem_ld16(tw, ra);
+        tmem_wait(ra);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int c = h + 2 * i;
-        if (c < nchunks) {
+        for (int k = 0; k < 8; ++k) {
+          uint32_t(&cur)[16] = (k & 1) ? rb : ra;
+          uint32_t(&nxt)[16] = (k & 1) ? ra : rb;
+          if (k < 7) tmem_ld16(tw + static_cast<uint32_t>(64 * ((k + 1) >> 1) + 16 * ((k + 1) & 1)), nxt);
+          const int i = k >> 1, half = k & 1;
+          const float4* da4 = reinterpret_cast<const float4*>(dab + 64 * i + 16 * half);
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            float v[16];
-            tmem_ld16(tbase + static_cast<uint32_t>(c * 32 + 16 * half), v);
+          for (int j = 0; j < 4; ++j) {
+            const float4 d = da4[j];
+            const int o = 8 * half + 2 * j;
+            const float2 t0 = __ffma2_rn(
+                make_float2(__uint_as_float(cur[4 * j + 0]), __uint_as_float(cur[4 * j + 1])), dw2, corr2);
+            const float2 t1 = __ffma2_rn(
+                make_float2(__uint_as_float(cur[4 * j + 2]), __uint_as_float(cur[4 * j + 3])), dw2, corr2);
+            acc[i][o + 0] = __ffma2_rn(t0, make_float2(d.x, d.y), acc[i][o + 0]);
+            acc[i][o + 1] = __ffma2_rn(t1, make_float2(d.z, d.w), acc[i][o + 1]);
+          }
+          if (k < 7) tmem_wait(nxt);
+        }
+      } else {
+        // This warp's 16-column pieces: k = 0..7 -> chunk h + 2 (k / 2), half k % 2.
+        // The load of piece k + 1 is in flight while piece k is folded.
+        const int npieces = 2 * ((nchunks - h + 1) / 2);
+        uint32_t ra[16], rb[16];
+        tmem_ld16(tbase + static_cast<uint32_t>(h * 32), ra);
+        tmem_wait(ra);
+  #pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          if (k < npieces) {
+            uint32_t(&cur)[16] = (k & 1) ? rb : ra;
+            uint32_t(&nxt)[16] = (k & 1) ? ra : rb;
+            const int kn = k + 1;
+            if (kn < npieces) tmem_ld16(tbase + static_cast<uint32_t>((h + 2 * (kn >> 1)) * 32 + 16 * (kn & 1)), nxt);
+            const int i = k >> 1, half = k & 1;
+            const int c0 = (h + 2 * i) * 32 + 16 * half;  // first column of the piece
             if constexpr (PARTIALS) {
               const int64_t n = T.n0 + n_in;
-#pragma unroll 1
+  #pragma unroll 1
               for (int j = 0; j < 16; ++j) {
-                const int col = c * 32 + 16 * half + j;
+                const int col = c0 + j;
                 if (col < T.ntok && n_in < T.rows_w) {
                   const int64_t m = T.m0 + col;
                   // D = P + 8 S_w, an exact integer times 2^-18
-                  p.P[(m * p.N + n) * B + b] = static_cast<int32_t>(v[j] * fp8_unscale()) - 8 * sw;
+                  const int sw = p.w_sums[(T.wrow0 + n_in) * B + b];
+                  p.P[(m * p.N + n) * B + b] =
+                      static_cast<int32_t>(__uint_as_float(cur[j]) * fp8_unscale()) - 8 * sw;
                 }
               }
             } else {
-              const float4* da4 = reinterpret_cast<const float4*>(&S.sda[slot][kb][c * 32 + 16 * half]);
-#pragma unroll
+              const float4* da4 = reinterpret_cast<const float4*>(&S.sda[slot][kb][c0]);
+  #pragma unroll
               for (int j = 0; j < 4; ++j) {
-                const float4 d = da4[j];
-                const int o = 16 * half + 4 * j;
-                acc[i][o + 0] = fmaf(fmaf(v[4 * j + 0], dw, corr), d.x, acc[i][o + 0]);
-                acc[i][o + 1] = fmaf(fmaf(v[4 * j + 1], dw, corr), d.y, acc[i][o + 1]);
-                acc[i][o + 2] = fmaf(fmaf(v[4 * j + 2], dw, corr), d.z, acc[i][o + 2]);
-                acc[i][o + 3] = fmaf(fmaf(v[4 * j + 3], dw, corr), d.w, acc[i][o + 3]);
+                const float4 d = da4[j];  // d_a of columns c0 + 4j .. c0 + 4j + 3
+                const int o = 8 * half + 2 * j;
+                // f32x2 fused multiply-adds: each lane rounds exactly like fmaf
+                const float2 t0 = __ffma2_rn(
+                    make_float2(__uint_as_float(cur[4 * j + 0]), __uint_as_float(cur[4 * j + 1])), dw2, corr2);
+                const float2 t1 = __ffma2_rn(
+                    make_float2(__uint_as_float(cur[4 * j + 2]), __uint_as_float(cur[4 * j + 3])), dw2, corr2);
+                acc[i][o + 0] = __ffma2_rn(t0, make_float2(d.x, d.y), acc[i][o + 0]);
+                acc[i][o + 1] = __ffma2_rn(t1, make_float2(d.z, d.w), acc[i][o + 1]);
               }
             }
+            if (kn < npieces) tmem_wait(nxt);
           }
         }
       }
@@ -484,6 +549,7 @@ __device__ void workers(const TcArgs& p, Smem& S, uint32_t tmem) {
       if (lane == 0) mbar_arrive(&S.tm_empty[tb]);
       ++gfold;
     }
+    gsc = gsc0 + static_cast<uint32_t>(nst);
 
     if constexpr (!PARTIALS) {
       if (n_in < T.rows_w) {
@@ -493,17 +559,24 @@ __device__ void workers(const TcArgs& p, Smem& S, uint32_t tmem) {
           const int c = h + 2 * i;
           if (c < nchunks) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int col = c * 32 + j;
+            for (int j = 0; j < 16; ++j) {
+              const float v0 = acc[i][j].x, v1 = acc[i][j].y;
+              const int col = c * 32 + 2 * j;
               if (col < T.ntok) {
                 const int64_t row = p.perm ? static_cast<int64_t>(p.perm[T.m0 + col]) : T.m0 + col;
-                p.y[row * p.ldy + n] = acc[i][j];
+                p.y[row * p.ldy + n] = v0;
+              }
+              if (col + 1 < T.ntok) {
+                const int64_t row = p.perm ? static_cast<int64_t>(p.perm[T.m0 + col + 1]) : T.m0 + col + 1;
+                p.y[row * p.ldy + n] = v1;
               }
             }
           }
         }
       }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.tile_done);
   }
 }
 
@@ -511,9 +584,16 @@ template <bool PARTIALS>
 __global__ void __launch_bounds__(kThreads, 1)
     w4a4_gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap amap,
                         const TcArgs p) {
-  extern __shared__ uint8_t smem_dyn[];
-  Smem& S = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+  // Smem is taken straight from the __shared__ array (no integer round trip), so
+  // the compiler keeps every access in the shared address space (LDS/STS).  The
+  // operands need 16-byte alignment (no swizzle), the TMA boxes 128 bytes.
+  extern __shared__ __align__(1024) uint8_t smem_dyn[];
+  Smem& S = *reinterpret_cast<Smem*>(smem_dyn);
   const int warp = threadIdx.x >> 5;
+  if ((static_cast<uint32_t>(__cvta_generic_to_shared(smem_dyn)) & 127u) != 0) {  // never expected
+    if (threadIdx.x == 0) atomicOr(&g_w4a4_device_error, 2);
+    return;
+  }
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < RAW; ++i) {
@@ -523,13 +603,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < F8; ++i) {
       mbar_init(&S.f8_full[i], kConvWarps);
       mbar_init(&S.f8_empty[i], 1);
-      mbar_init(&S.sw_empty[i], kWorkerWarps);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&S.tm_full[i], 1);
       mbar_init(&S.tm_empty[i], kWorkerWarps);
       mbar_init(&S.sc_ready[i], kWorkerWarps);
     }
+    mbar_init(&S.tile_done, kWorkerWarps);
     mbar_init(&S.mma_done, 1);
     S.abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -634,11 +714,11 @@ int token_tile(int64_t M) {
 
 }  // namespace
 
-cudaError_t launch_gemm_tc(const uint8_t* w_codes, const uint16_t* w_scales, int64_t N, const uint8_t* a_codes,
-                           const float* a_scales, int64_t M, int64_t K, float* y, int64_t ldy, int32_t* P,
-                           cudaStream_t stream) {
+cudaError_t launch_gemm_tc(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums, int64_t N,
+                           const uint8_t* a_codes, const float* a_scales, int64_t M, int64_t K, float* y, int64_t ldy,
+                           int32_t* P, cudaStream_t stream) {
   TcArgs a{};
-  a.w_scales = w_scales; a.a_scales = a_scales;
+  a.w_scales = w_scales; a.w_sums = w_sums; a.a_scales = a_scales;
   a.M = M; a.N = N; a.K = K; a.y = y; a.ldy = ldy; a.P = P;
   a.tt = token_tile(M);
   CUtensorMap wmap, amap;
@@ -649,11 +729,11 @@ cudaError_t launch_gemm_tc(const uint8_t* w_codes, const uint16_t* w_scales, int
   return P ? launch_tc<true>(wmap, amap, a, tiles, stream) : launch_tc<false>(wmap, amap, a, tiles, stream);
 }
 
-cudaError_t launch_gemm_tc_routed(const uint8_t* w_codes, const uint16_t* w_scales, int E, int64_t N,
-                                  const uint8_t* g_codes, const float* g_scales, int64_t K, int64_t npairs,
+cudaError_t launch_gemm_tc_routed(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums, int E,
+                                  int64_t N, const uint8_t* g_codes, const float* g_scales, int64_t K, int64_t npairs,
                                   int tile_tokens, float* y, const Routing& r, cudaStream_t stream) {
   TcArgs a{};
-  a.w_scales = w_scales; a.a_scales = g_scales;
+  a.w_scales = w_scales; a.w_sums = w_sums; a.a_scales = g_scales;
   a.M = npairs; a.N = N; a.K = K; a.y = y; a.ldy = N;
   a.tt = tile_tokens;
   a.perm = r.perm; a.offsets = r.offsets; a.tile_off = r.tile_off; a.E = E;

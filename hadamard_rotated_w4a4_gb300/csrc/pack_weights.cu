@@ -41,7 +41,8 @@ __device__ __forceinline__ void keep_larger(float& mval, float& mabs, int& midx,
 __global__ void __launch_bounds__(256) pack_q4_0_kernel(const void* __restrict__ w, int w_dtype, int64_t N,
                                                          int64_t K, int64_t ldw, int rotate,
                                                          uint8_t* __restrict__ codes,
-                                                         uint16_t* __restrict__ scales) {
+                                                         uint16_t* __restrict__ scales,
+                                                         int16_t* __restrict__ sums) {
   const int lane = threadIdx.x & 31;
   const int sub = lane >> 3;
   const int t = lane & 7;
@@ -101,24 +102,35 @@ __global__ void __launch_bounds__(256) pack_q4_0_kernel(const void* __restrict__
     const float d = __fdiv_rn(mval, -8.0f);
     const float inv = (d != 0.0f) ? __frcp_rn(d) : 0.0f;
     uint32_t lo = 0;
+    int qsum = 0;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       float r = round_half_away(__fmul_rn(v[j], inv));
       r = fminf(fmaxf(__fadd_rn(r, 8.0f), 0.0f), 15.0f);
-      lo |= static_cast<uint32_t>(static_cast<int>(r)) << (8 * j);
+      const int q = static_cast<int>(r);
+      lo |= static_cast<uint32_t>(q) << (8 * j);
+      qsum += q - 8;
     }
+    qsum += __shfl_xor_sync(0xFFFFFFFFu, qsum, 1);
+    qsum += __shfl_xor_sync(0xFFFFFFFFu, qsum, 2);
+    qsum += __shfl_xor_sync(0xFFFFFFFFu, qsum, 4);
     const uint32_t hi = __shfl_down_sync(0xFFFFFFFFu, lo << 4, 4);
     if (ok) {
       if (t < 4) reinterpret_cast<uint32_t*>(codes + n * (K / 2) + b * 16)[t] = lo | hi;
-      if (t == 0) scales[n * B + b] = __half_as_ushort(__float2half_rn(d));
+      if (t == 0) {
+        scales[n * B + b] = __half_as_ushort(__float2half_rn(d));
+        sums[n * B + b] = static_cast<int16_t>(qsum);
+      }
     }
   }
 }
 
-// One thread per 18-byte block: fp16 scale then 16 code bytes, copied bit for bit.
+// One thread per 18-byte block: fp16 scale then 16 code bytes, copied bit for
+// bit, and the block's code sum sum_j (q_j - 8).
 __global__ void __launch_bounds__(256) import_q4_0_kernel(const uint8_t* __restrict__ blocks, int64_t nblk,
                                                            uint8_t* __restrict__ codes,
-                                                           uint16_t* __restrict__ scales) {
+                                                           uint16_t* __restrict__ scales,
+                                                           int16_t* __restrict__ sums) {
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= nblk) return;
   const uint16_t* src = reinterpret_cast<const uint16_t*>(blocks + i * 18);  // 2-byte aligned
@@ -127,27 +139,35 @@ __global__ void __launch_bounds__(256) import_q4_0_kernel(const uint8_t* __restr
 #pragma unroll
   for (int j = 0; j < 4; ++j) q[j] = static_cast<uint32_t>(src[1 + 2 * j]) | (static_cast<uint32_t>(src[2 + 2 * j]) << 16);
   reinterpret_cast<uint4*>(codes)[i] = make_uint4(q[0], q[1], q[2], q[3]);
+  int total = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t nib = (q[j] & 0x0F0F0F0Fu) + ((q[j] >> 4) & 0x0F0F0F0Fu);  // per byte <= 30
+    total += static_cast<int>((nib & 0xFF) + ((nib >> 8) & 0xFF) + ((nib >> 16) & 0xFF) + (nib >> 24));
+  }
+  sums[i] = static_cast<int16_t>(total - 256);
 }
 
 }  // namespace
 
 cudaError_t launch_pack_q4_0(const void* w, int w_dtype, int64_t N, int64_t K, int64_t ldw, int rotate,
-                             uint8_t* codes, uint16_t* scales, cudaStream_t stream) {
+                             uint8_t* codes, uint16_t* scales, int16_t* sums, cudaStream_t stream) {
   const int64_t ngroups = (N * (K / 32) + 3) / 4;
   int64_t ctas = (ngroups + 7) / 8;
   const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
   if (ctas > cap) ctas = cap;
   if (ctas < 1) ctas = 1;
-  pack_q4_0_kernel<<<static_cast<unsigned>(ctas), 256, 0, stream>>>(w, w_dtype, N, K, ldw, rotate, codes, scales);
+  pack_q4_0_kernel<<<static_cast<unsigned>(ctas), 256, 0, stream>>>(w, w_dtype, N, K, ldw, rotate, codes, scales,
+                                                                     sums);
   return cudaGetLastError();
 }
 
 cudaError_t launch_import_q4_0(const void* blocks, int64_t N, int64_t K, uint8_t* codes, uint16_t* scales,
-                               cudaStream_t stream) {
+                               int16_t* sums, cudaStream_t stream) {
   const int64_t nblk = N * (K / 32);
   const int64_t ctas = (nblk + 255) / 256;
   import_q4_0_kernel<<<static_cast<unsigned>(ctas), 256, 0, stream>>>(static_cast<const uint8_t*>(blocks), nblk,
-                                                                       codes, scales);
+                                                                       codes, scales, sums);
   return cudaGetLastError();
 }
 

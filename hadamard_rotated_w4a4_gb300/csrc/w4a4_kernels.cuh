@@ -31,20 +31,22 @@ Routing routing_in(void* ws, int64_t npairs, int E, int64_t K);
 cudaError_t launch_act_rotate_quantize(const float* x, int64_t M, int64_t K, int64_t ldx, int rotate,
                                        uint8_t* codes, float* scales, cudaStream_t stream);
 cudaError_t launch_pack_q4_0(const void* w, int w_dtype, int64_t N, int64_t K, int64_t ldw, int rotate,
-                             uint8_t* codes, uint16_t* scales, cudaStream_t stream);
+                             uint8_t* codes, uint16_t* scales, int16_t* sums, cudaStream_t stream);
 cudaError_t launch_import_q4_0(const void* blocks, int64_t N, int64_t K, uint8_t* codes, uint16_t* scales,
-                               cudaStream_t stream);
-cudaError_t launch_gemm_tc(const uint8_t* w_codes, const uint16_t* w_scales, int64_t N, const uint8_t* a_codes,
+                               int16_t* sums, cudaStream_t stream);
+cudaError_t launch_gemm_tc(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums, int64_t N,
+                           const uint8_t* a_codes,
                            const float* a_scales, int64_t M, int64_t K, float* y, int64_t ldy, int32_t* P,
                            cudaStream_t stream);
-cudaError_t launch_gemm_tc_routed(const uint8_t* w_codes, const uint16_t* w_scales, int E, int64_t N,
+cudaError_t launch_gemm_tc_routed(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums, int E,
+                                  int64_t N,
                                   const uint8_t* g_codes, const float* g_scales, int64_t K, int64_t npairs,
                                   int tile_tokens, float* y, const Routing& r, cudaStream_t stream);
 // Token rows per routed tile for a MUL_MAT_ID problem (multiple of 32, <= 256).
 int routed_tile_tokens(int64_t npairs, int E);
 // Reads the GEMM kernels' device error word (bounded waits that gave up) and clears it.
 cudaError_t read_and_clear_device_error(int* value);
-cudaError_t launch_gemm_id(const uint8_t* w_codes, const uint16_t* w_scales, int E, int64_t N,
+cudaError_t launch_gemm_id(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums, int E, int64_t N,
                            const uint8_t* a_codes, const float* a_scales, int64_t K, const int32_t* ids, int64_t M,
                            int top_k, int act_per_slot, float* y, const Routing& r, cudaStream_t stream);
 

@@ -82,10 +82,14 @@ typedef enum {
  *           q_{i+16} in its high nibble (the Q4_0 block order); code q stands
  *           for the integer q - 8.
  *   scales: device, [rows][K/32] IEEE fp16 (binary16 bits), the block scale d.
+ *   sums  : device, [rows][K/32] int16, the block's code sum sum_j (q_j - 8).
+ *           Derived data (no extra information): written by h32_q4_0_pack_weights
+ *           and q4_0_import from the codes, read by the GEMMs.
  */
 typedef struct {
   uint8_t* codes;
   uint16_t* scales;
+  int16_t* sums;
   int64_t rows;
   int64_t K;
   uint32_t tag; /* W4A4_TAG_Q4_0 | (W4A4_TAG_ROTATED if rotated) */
@@ -108,6 +112,7 @@ typedef struct {
 /* Bytes needed for the two arrays of a Q4_0 / int4 operand (0 if K is invalid). */
 size_t w4a4_q4_0_codes_bytes(int64_t rows, int64_t K);
 size_t w4a4_q4_0_scales_bytes(int64_t rows, int64_t K);
+size_t w4a4_q4_0_sums_bytes(int64_t rows, int64_t K);
 size_t w4a4_act4_codes_bytes(int64_t rows, int64_t K);
 size_t w4a4_act4_scales_bytes(int64_t rows, int64_t K);
 
@@ -118,9 +123,9 @@ size_t w4a4_act4_scales_bytes(int64_t rows, int64_t K);
  * Q4_0; section "MoE: W4A4 on the experts": one scale per 32 values).
  *   w      : device, [N][ldw] elements of type w_dtype (row n holds W[n][0..K-1]).
  *   rotate : 1 = apply H32 (normalised) before quantising; 0 = plain Q4_0.
- *   out    : host struct; out->codes and out->scales must point to caller
- *            buffers of w4a4_q4_0_codes_bytes / _scales_bytes; rows, K and tag
- *            are written by this call.
+ *   out    : host struct; out->codes, out->scales and out->sums must point to
+ *            caller buffers of w4a4_q4_0_codes_bytes / _scales_bytes /
+ *            _sums_bytes; rows, K and tag are written by this call.
  * Per block: y = H32 w / sqrt(32) (fp32 butterfly, stages 1,2,4,8,16, then one
  * multiply by fl32(1/sqrt 32)); m = the y of largest magnitude (lowest index on
  * ties); d = m / -8; q = clamp(round_half_away(y * (1/d)) + 8, 0, 15) (q = 8

@@ -51,7 +51,7 @@ FAKE = 0x10000  # aligned, never dereferenced: every call below fails validation
 
 
 def q4(rows=64, K=256, rotated=True, tag=None):
-    return _Q4_0Desc(FAKE, FAKE, rows, K, tag if tag is not None else (w4.TAG_Q4_0 | (1 if rotated else 0)))
+    return _Q4_0Desc(FAKE, FAKE, FAKE, rows, K, tag if tag is not None else (w4.TAG_Q4_0 | (1 if rotated else 0)))
 
 
 def a4(rows=64, K=256, rotated=True, tag=None):
@@ -86,7 +86,10 @@ def test_gemm_argument_checks(lib):
     assert s == "W4A4_ERR_INVALID_ARG"
     s, _ = status(lib, "w4a4_gemm", ctypes.byref(q4()), ctypes.byref(a4()), FAKE + 2, 64, None)  # y not 4B aligned
     assert s == "W4A4_ERR_ALIGNMENT"
-    bad = _Q4_0Desc(FAKE + 8, FAKE, 64, 256, w4.TAG_Q4_0 | 1)
+    bad = _Q4_0Desc(FAKE + 8, FAKE, FAKE, 64, 256, w4.TAG_Q4_0 | 1)
+    s, _ = status(lib, "w4a4_gemm", ctypes.byref(bad), ctypes.byref(a4()), FAKE, 64, None)
+    assert s == "W4A4_ERR_ALIGNMENT"
+    bad = _Q4_0Desc(FAKE, FAKE, FAKE + 4, 64, 256, w4.TAG_Q4_0 | 1)  # sums not 16-byte aligned
     s, _ = status(lib, "w4a4_gemm", ctypes.byref(bad), ctypes.byref(a4()), FAKE, 64, None)
     assert s == "W4A4_ERR_ALIGNMENT"
     s, _ = status(lib, "w4a4_gemm", ctypes.byref(q4()), ctypes.byref(a4()), None, 64, None)
@@ -110,7 +113,7 @@ def test_act_and_pack_argument_checks(lib):
     assert status(lib, "w4a4_rotate_quantize_act", FAKE, 4, 64, 66, 1, ctypes.byref(d), None)[0] == "W4A4_ERR_ALIGNMENT"
     assert status(lib, "w4a4_rotate_quantize_act", FAKE, 4, 64, 64, 2, ctypes.byref(d), None)[0] == "W4A4_ERR_INVALID_ARG"
     assert status(lib, "w4a4_rotate_quantize_act", FAKE, 4, 64, 64, 1, None, None)[0] == "W4A4_ERR_INVALID_ARG"
-    w = _Q4_0Desc(FAKE, FAKE, 0, 0, 0)
+    w = _Q4_0Desc(FAKE, FAKE, FAKE, 0, 0, 0)
     assert status(lib, "h32_q4_0_pack_weights", FAKE, 2, 4, 64, 64, 1, ctypes.byref(w), None)[0] == "W4A4_ERR_INVALID_ARG"
     assert status(lib, "h32_q4_0_pack_weights", FAKE, 0, 4, 64, 68, 1, ctypes.byref(w), None)[0] == "W4A4_ERR_ALIGNMENT"
     assert status(lib, "h32_q4_0_pack_weights", FAKE + 2, 0, 4, 64, 64, 1, ctypes.byref(w), None)[0] == "W4A4_ERR_ALIGNMENT"

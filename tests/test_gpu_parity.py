@@ -231,15 +231,14 @@ def test_full_size_dense(dev, cfg):
     wp_rows = oracle.pack_weights(d["w_bf16"][rows])
     assert_weights_bit_exact(weights_np(wq), wp_rows, rows=rows)
     # integer partials on a cropped slice: first 128 activation rows x 256 weight rows, all of K
-    wsub = w4.Q4_0Weights(wq.codes[:256], wq.scales_buf, 256, s.K, True)
-    asub = w4.Act4(aq.codes[:128], aq.scales_buf, 128, s.K, True)
+    wsub = wq.head(256)
+    asub = aq.head(128)
     P = w4.w4a4_gemm_partials(wsub, asub).cpu().numpy()
     wp_head = oracle.pack_weights(d["w_bf16"][:256])
     ap_head = {"q": ap["q"][:128], "d_a": ap["d_a"][:128]}
     assert np.array_equal(P, oracle.block_partials(wp_head, ap_head))
     # outputs: sampled rows, every column
     mrows = np.sort(rng.choice(s.M, 6, replace=False))
-    wp_all = {"q": None}
     wp_all = oracle.pack_weights(d["w_bf16"])
     R = oracle.w4a4_matmul(wp_all, ap, m_idx=mrows)
     assert_close(Y[torch.from_numpy(mrows).to(dev)].cpu().numpy(), R)

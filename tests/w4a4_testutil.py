@@ -28,7 +28,7 @@ def f32_tensor(x: np.ndarray, dev) -> torch.Tensor:
 
 def weights_np(wq: w4.Q4_0Weights) -> dict:
     torch.cuda.synchronize()
-    return {"codes": wq.codes.cpu().numpy(), "d16": wq.scales.cpu().numpy()}
+    return {"codes": wq.codes.cpu().numpy(), "d16": wq.scales.cpu().numpy(), "sums": wq.sums.cpu().numpy()}
 
 
 def act_np(aq: w4.Act4) -> dict:
@@ -44,6 +44,11 @@ def assert_weights_bit_exact(gpu: dict, ref: dict, rows=None) -> None:
     bad = np.argwhere(gc != ref["codes"])
     assert len(bad) == 0, f"{len(bad)} code bytes differ, first at {bad[:5].tolist()}"
     assert np.array_equal(gd.view(np.uint16), np.asarray(ref["d16"], dtype=np.float16).view(np.uint16))
+    # the derived block sums agree with the codes themselves: sum_j (q_j - 8)
+    gs = gpu["sums"] if rows is None else gpu["sums"][rows]
+    q = gc.reshape(gc.shape[0], -1, 16)
+    want = ((q & 0x0F).astype(np.int64) + (q >> 4)).sum(axis=-1) - 256
+    assert np.array_equal(gs.astype(np.int64), want)
 
 
 def assert_act_bit_exact(gpu: dict, ref: dict) -> None:
