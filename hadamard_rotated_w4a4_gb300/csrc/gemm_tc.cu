@@ -56,6 +56,7 @@ constexpr int kRegsHigh = 216;  // warpgroups 1-2 after setmaxnreg.inc
 constexpr int TW = 128;         // weight rows per tile
 constexpr int TT = 256;         // token columns per tile (max)
 constexpr int KB = 4;           // 32-blocks per stage (64 code bytes per row)
+static_assert(KB == 4, "the vector scale loads take 4 blocks per stage");
 constexpr int RAW = 3;          // stages of raw codes in flight
 constexpr int F8 = 8;           // fp8 operand buffers (two stages)
 constexpr int WF8 = TW * 32 + 32;  // buffer strides padded by 32 bytes: the converters'
@@ -408,7 +409,26 @@ __device__ void workers(const TcArgs& p, Smem& S, uint32_t tmem) {
     short sw_r[KB];
     // Loads are unconditional (clamped to valid addresses); validity is applied
     // when publishing, so nothing consumes a loaded value early.
+    // Rows whose KB-block groups are aligned take one vector load per array.
+    const bool vec = (B % KB) == 0 && (reinterpret_cast<uintptr_t>(p.a_scales) & 15) == 0 &&
+                     (reinterpret_cast<uintptr_t>(p.w_scales) & 7) == 0 &&
+                     (reinterpret_cast<uintptr_t>(p.w_sums) & 7) == 0;
     auto load_scales = [&](int s) {
+      if (vec) {
+        const float4 a4 = __ldg(reinterpret_cast<const float4*>(as_row + s * KB));
+        const uint2 w2 = __ldg(reinterpret_cast<const uint2*>(ws_row + s * KB));
+        const uint2 s2 = __ldg(reinterpret_cast<const uint2*>(wsum_row + s * KB));
+        da_r[0] = a4.x; da_r[1] = a4.y; da_r[2] = a4.z; da_r[3] = a4.w;
+        dw_r[0] = static_cast<unsigned short>(w2.x & 0xFFFFu);
+        dw_r[1] = static_cast<unsigned short>(w2.x >> 16);
+        dw_r[2] = static_cast<unsigned short>(w2.y & 0xFFFFu);
+        dw_r[3] = static_cast<unsigned short>(w2.y >> 16);
+        sw_r[0] = static_cast<short>(s2.x & 0xFFFFu);
+        sw_r[1] = static_cast<short>(s2.x >> 16);
+        sw_r[2] = static_cast<short>(s2.y & 0xFFFFu);
+        sw_r[3] = static_cast<short>(s2.y >> 16);
+        return;
+      }
 #pragma unroll
       for (int k = 0; k < KB; ++k) {
         const int b = min(s * KB + k, B - 1);
