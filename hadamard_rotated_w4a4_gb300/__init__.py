@@ -48,7 +48,7 @@ TAG_ROTATED = 0x1
 EXPORTS = [
     "w4a4_q4_0_codes_bytes", "w4a4_q4_0_scales_bytes", "w4a4_q4_0_sums_bytes", "w4a4_act4_codes_bytes",
     "w4a4_act4_scales_bytes", "h32_q4_0_pack_weights", "q4_0_import", "w4a4_rotate_quantize_act", "w4a4_gemm", "w4a4_gemm_partials",
-    "w4a4_gemm_id", "w4a4_gemm_id_workspace_bytes", "w4a4_gemm_id_status", "w4a4_check", "w4a4_last_error",
+    "w4a4_gemm_id", "w4a4_gemm_id_workspace_bytes", "w4a4_gemm_id_status", "w4a4_gemm_id_static", "w4a4_check", "w4a4_last_error",
     "w4a4_status_name", "w4a4_abi_version",
 ]
 
@@ -102,6 +102,8 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
                                  vp, vp, u, vp]
     lib.w4a4_gemm_id_workspace_bytes.argtypes, lib.w4a4_gemm_id_workspace_bytes.restype = [i64, i32, i32, i64], u
     lib.w4a4_gemm_id_status.argtypes = [vp, vp]
+    lib.w4a4_gemm_id_static.argtypes = [ctypes.POINTER(_Q4_0Desc), i32, i64, ctypes.POINTER(_Act4Desc), vp, i64, i32,
+                                         i32, vp, vp]
     lib.w4a4_check.argtypes = [vp]
     for name in ("h32_q4_0_pack_weights", "q4_0_import", "w4a4_rotate_quantize_act", "w4a4_gemm",
                  "w4a4_gemm_partials", "w4a4_gemm_id", "w4a4_gemm_id_status", "w4a4_check"):
@@ -305,6 +307,29 @@ def w4a4_gemm_id(experts: Q4_0Weights, E: int, a: Act4, ids: torch.Tensor, top_k
     _check(load_library().w4a4_gemm_id(ctypes.byref(experts.desc()), E, N, ctypes.byref(a.desc()), ids.data_ptr(),
                                        M, top_k, int(act_per_slot), y.data_ptr(), ws.data_ptr(),
                                        ws.numel() * ws.element_size(), _stream(stream)))
+    return y
+
+
+#: bytes of the library's fixed routing scratch, per device
+GEMM_ID_STATIC_SCRATCH_BYTES = 16 << 20
+
+
+def w4a4_gemm_id_static(experts: Q4_0Weights, E: int, a: Act4, ids: torch.Tensor, top_k: int, act_per_slot: bool,
+                        y: torch.Tensor, stream=None) -> torch.Tensor:
+    """w4a4_gemm_id with the library's fixed routing scratch instead of a workspace.
+
+    Nothing is allocated: the caller passes the output ``y`` [M][top_k][N].
+    Calls that may overlap on the GPU share the scratch and race.
+    """
+    _cuda(ids, "ids")
+    if ids.dtype != torch.int32 or not ids.is_contiguous() or ids.dim() != 2 or ids.shape[1] != top_k:
+        raise ValueError("ids must be a contiguous int32 [M][top_k] tensor")
+    _cuda(y, "y")
+    if y.dtype != torch.float32 or not y.is_contiguous() or tuple(y.shape) != (ids.shape[0], top_k, experts.rows // E):
+        raise ValueError("y must be a contiguous float32 [M][top_k][N] tensor")
+    _check(load_library().w4a4_gemm_id_static(ctypes.byref(experts.desc()), E, experts.rows // E,
+                                              ctypes.byref(a.desc()), ids.data_ptr(), ids.shape[0], top_k,
+                                              int(act_per_slot), y.data_ptr(), _stream(stream)))
     return y
 
 

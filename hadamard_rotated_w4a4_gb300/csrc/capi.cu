@@ -252,6 +252,46 @@ w4a4_status w4a4_gemm_id_status(const void* ws, w4a4_stream_t stream) {
   return ok();
 }
 
+static_assert(W4A4_GEMM_ID_STATIC_SCRATCH_BYTES == w4a4::kIdStaticScratchBytes, "scratch size mismatch");
+
+w4a4_status w4a4_gemm_id_static(const w4a4_q4_0* experts, int E, int64_t N, const w4a4_act4* a, const int32_t* ids,
+                                int64_t M, int top_k, int act_per_slot, float* y, w4a4_stream_t stream) {
+  const char* fn = "w4a4_gemm_id_static";
+  w4a4_status s = check_q4_0(experts, fn);
+  if (s != W4A4_OK) return s;
+  if ((s = check_act4(a, fn)) != W4A4_OK) return s;
+  if ((s = check_pair(experts, a, fn)) != W4A4_OK) return s;
+  if (E < 1 || E > 4096) return fail(W4A4_ERR_INVALID_ARG, "%s: E=%d outside 1..4096", fn, E);
+  if (top_k < 1 || top_k > E) return fail(W4A4_ERR_INVALID_ARG, "%s: top_k=%d outside 1..E", fn, top_k);
+  if (N < 1) return fail(W4A4_ERR_INVALID_ARG, "%s: N=%lld must be positive", fn, (long long)N);
+  if (M < 0 || M * top_k > (int64_t(1) << 31) - 1) return fail(W4A4_ERR_INVALID_ARG, "%s: bad M", fn);
+  if (act_per_slot != 0 && act_per_slot != 1) return fail(W4A4_ERR_INVALID_ARG, "%s: act_per_slot must be 0 or 1", fn);
+  if (experts->rows != static_cast<int64_t>(E) * N)
+    return fail(W4A4_ERR_MISMATCH, "%s: expert weights have %lld rows, expected E*N = %lld", fn,
+                (long long)experts->rows, (long long)(static_cast<int64_t>(E) * N));
+  const int64_t want_rows = act_per_slot ? M * top_k : M;
+  if (a->rows != want_rows)
+    return fail(W4A4_ERR_MISMATCH, "%s: activations have %lld rows, expected %lld", fn, (long long)a->rows,
+                (long long)want_rows);
+  if (M == 0) return ok();
+  if (!ids || !y) return fail(W4A4_ERR_INVALID_ARG, "%s: NULL pointer", fn);
+  const size_t need = w4a4_gemm_id_workspace_bytes(M, top_k, E, a->K);
+  if (need > W4A4_GEMM_ID_STATIC_SCRATCH_BYTES)
+    return fail(W4A4_ERR_WORKSPACE,
+                "%s: this problem needs %zu bytes of routing scratch, more than the fixed %zu; "
+                "call w4a4_gemm_id with a workspace instead",
+                fn, need, static_cast<size_t>(W4A4_GEMM_ID_STATIC_SCRATCH_BYTES));
+  if ((reinterpret_cast<uintptr_t>(y) & 3u) != 0) return fail(W4A4_ERR_ALIGNMENT, "%s: y must be 4-byte aligned", fn);
+  void* ws = nullptr;
+  cudaError_t e = w4a4::id_static_scratch(&ws);
+  if (e != cudaSuccess) return cuda_status(e, fn);
+  const w4a4::Routing r = w4a4::routing_in(ws, M * top_k, E, a->K);
+  return cuda_status(w4a4::launch_gemm_id(experts->codes, experts->scales, experts->sums, E, N, a->codes, a->scales,
+                                          a->K, ids, M, top_k, act_per_slot, y, r,
+                                          reinterpret_cast<cudaStream_t>(stream)),
+                     fn);
+}
+
 w4a4_status w4a4_check(w4a4_stream_t stream) {
   const char* fn = "w4a4_check";
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));

@@ -11,6 +11,8 @@
 //      order into the workspace, so that every expert's rows are contiguous;
 //   3. the grouped GEMM over (expert row tile, weight tile), loading both
 //      operands with 2D TMA and scattering each output row to (token, slot).
+#include <mutex>
+
 #include "w4a4_kernels.cuh"
 
 namespace w4a4 {
@@ -126,6 +128,29 @@ Routing routing_in(void* ws, int64_t npairs, int E, int64_t K) {
   r.gcodes = base + L.gcodes;
   r.gscales = reinterpret_cast<float*>(base + L.gscales);
   return r;
+}
+
+// One routing scratch per device, for callers without a workspace.  The
+// kernels write every word they read, so it is never cleared.
+static __device__ __align__(256) uint8_t g_id_scratch[kIdStaticScratchBytes];
+
+cudaError_t id_static_scratch(void** addr) {
+  static std::mutex mu;
+  static void* cached[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cached[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_id_scratch);  // the current device's copy
+    if (e != cudaSuccess) return e;
+    if (!p) return cudaErrorInvalidSymbol;
+    cached[dev] = p;
+  }
+  *addr = cached[dev];
+  return cudaSuccess;
 }
 
 cudaError_t launch_gemm_id(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums, int E, int64_t N,

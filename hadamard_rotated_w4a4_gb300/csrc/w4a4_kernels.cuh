@@ -28,6 +28,11 @@ struct RoutingLayout {
 RoutingLayout routing_layout(int64_t npairs, int E, int64_t K);
 Routing routing_in(void* ws, int64_t npairs, int E, int64_t K);
 
+// Fixed routing scratch (for the no-workspace variant of the routed product):
+// its size, and the device address of the current device's copy.
+constexpr size_t kIdStaticScratchBytes = size_t(16) << 20;
+cudaError_t id_static_scratch(void** addr);
+
 cudaError_t launch_act_rotate_quantize(const float* x, int64_t M, int64_t K, int64_t ldx, int rotate,
                                        uint8_t* codes, float* scales, cudaStream_t stream);
 cudaError_t launch_pack_q4_0(const void* w, int w_dtype, int64_t N, int64_t K, int64_t ldw, int rotate,

@@ -217,6 +217,44 @@ size_t w4a4_gemm_id_workspace_bytes(int64_t M, int top_k, int E, int64_t K);
 w4a4_status w4a4_gemm_id_status(const void* ws, w4a4_stream_t stream);
 
 /*
+ * w4a4_gemm_id_static -- w4a4_gemm_id without a caller workspace.  The pages
+ * describe no such call: it is an interface convenience of this library.
+ *
+ * Some callers cannot hand device memory to an op at the call site.  One case
+ * is an op plugged into a host engine whose callback passes only its tensors:
+ * the engine owns every buffer, and no allocator is in reach.  Another is a
+ * step loop that must not call cudaMalloc/cudaFree, which can synchronise the
+ * device and whose cost varies from call to call.  For them this entry point
+ * keeps the routing scratch in a fixed device array inside the library,
+ * W4A4_GEMM_ID_STATIC_SCRATCH_BYTES bytes per device.  It makes no allocation
+ * of its own, through CUDA or any other library.
+ *
+ * Arguments, layouts and results are those of w4a4_gemm_id without ws and
+ * ws_bytes.  The output is the same as w4a4_gemm_id's on the same inputs.
+ *   - Size limit: a problem with w4a4_gemm_id_workspace_bytes(M, top_k, E, K)
+ *     greater than W4A4_GEMM_ID_STATIC_SCRATCH_BYTES is refused with
+ *     W4A4_ERR_WORKSPACE before anything runs; use w4a4_gemm_id for it.
+ *   - Set-up: the first call on a device, with that device current, looks up
+ *     the array's device address once (cudaGetSymbolAddress) and keeps it.
+ *     Make that first call before any stream capture.
+ *   - Starting state: nothing in the array needs to be zero on entry.  Each
+ *     call's first kernel writes every count, offset, pair index and flag that
+ *     the later kernels read.
+ *   - Concurrency: one array serves all calls on a device.  Two calls whose
+ *     kernels can overlap on the GPU race on it and give wrong results.  This
+ *     includes calls on different streams, or from different host threads,
+ *     without an ordering between them.  Calls ordered on one stream are safe.
+ *   - Bad ids: an id outside [0, E) zeroes its output row as in w4a4_gemm_id.
+ *     The flag that records it stays inside the library, so no status query
+ *     reports it.  Callers that need the check use w4a4_gemm_id.
+ */
+#define W4A4_GEMM_ID_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+
+w4a4_status w4a4_gemm_id_static(const w4a4_q4_0* experts, int E, int64_t N, const w4a4_act4* a,
+                                const int32_t* ids, int64_t M, int top_k, int act_per_slot, float* y,
+                                w4a4_stream_t stream);
+
+/*
  * w4a4_check -- synchronise `stream`, then report whether any GEMM kernel run
  * since the last check gave up on one of its bounded internal waits (a pipeline
  * that stopped making progress for a second).  Such a kernel stops early, so

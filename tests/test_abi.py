@@ -22,6 +22,7 @@ def lib():
 def declared_functions():
     text = open(os.path.join(ROOT, "include", "w4a4.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"^\s*#.*$", "", text, flags=re.M)  # preprocessor lines (macros are not exports)
     return sorted(set(re.findall(r"\b(\w+)\s*\([^;{]*\)\s*;", text)))
 
 
