@@ -160,6 +160,108 @@ def read_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "sm_max_mhz": 2070.0, "fallback": True}
 
 
+def source_digest(*names: str) -> str:
+    """sha256 over kernel sources, to tie an ncu traffic figure to the kernel it was taken on."""
+    import hashlib
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "hadamard_rotated_w4a4_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(summary: str, sources: tuple[str, ...]) -> tuple[float | None, str]:
+    """DRAM bytes per launch recorded in a profiles/ summary, if its kernel sources are unchanged.
+
+    The summary carries the lines ``traffic_bytes_per_launch: <int>`` and
+    ``kernel_sources_sha256: <digest>``; a digest that no longer matches the
+    sources means the counters describe an older kernel, and the traffic is null.
+    """
+    p = os.path.join(ROOT, "profiles", summary)
+    if not os.path.exists(p):
+        return None, f"profiles/{summary} missing"
+    kv = {}
+    with open(p) as f:
+        for line in f:
+            line = line.strip().strip("`")
+            if ":" in line:
+                k, v = line.split(":", 1)
+                kv[k.strip()] = v.strip()
+    digest = source_digest(*sources)
+    if kv.get("kernel_sources_sha256") != digest:
+        return None, f"profiles/{summary} was taken on other kernel sources"
+    try:
+        return float(kv["traffic_bytes_per_launch"]), f"profiles/{summary} (ncu dram__bytes_read+write)"
+    except (KeyError, ValueError):
+        return None, f"profiles/{summary} has no traffic line"
+
+
+GEMM_SOURCES = ("gemm_tc.cu", "w4a4_device.cuh", "w4a4_kernels.cuh")
+ACT_SOURCES = ("act_quant.cu", "w4a4_device.cuh", "w4a4_kernels.cuh")
+
+
+def prefill_proxy(dev, stream, nrep: int) -> dict:
+    """GEMM-only prefill proxy for one dense layer at 512 tokens.
+
+    A dense layer of the pages' 27B model at hidden 5120 / FFN 17408 runs, per
+    512-token micro-batch: 4 attention projections (taken at K5120 N5120),
+    gate and up (K5120 N17408) and down (K17408 N5120), with 4 activation
+    quantisations (attention input, attention output, FFN input at K5120; FFN
+    hidden at K17408).  tok/s = 512 / (sum of those kernel times).  It leaves
+    out attention, norms and everything else in a layer: not comparable with
+    whole-model prompt rates.
+    """
+    import torch
+    import hadamard_rotated_w4a4_gb300 as w4
+
+    def timed(fn, n):
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for i in range(3):
+            fn(i)
+        torch.cuda.synchronize()
+        a0.record(stream)
+        for i in range(n):
+            fn(i)
+        a1.record(stream)
+        torch.cuda.synchronize()
+        return a0.elapsed_time(a1) / n
+
+    out = {}
+    for name, rows in (("c1", 512), ("c2", 512), ("c3", 512)):
+        d = si.dense_inputs(name)
+        w = torch.from_numpy(d["w_bf16"].view(np.int16)).to(dev).view(torch.bfloat16)
+        x = torch.from_numpy(np.ascontiguousarray(d["x"][:rows])).to(dev)
+        del d
+        N, K = w.shape
+        set_bytes = N * K // 2 + N * K // 8 + rows * K * 4.5 + rows * N * 4
+        nsets = max(2, int(np.ceil(2.2 * L2_BYTES / set_bytes)))
+        wq0 = w4.h32_q4_0_pack_weights(w)
+        del w
+        sets = []
+        for i in range(nsets):
+            wq = w4.alloc_q4_0(N, K, dev)
+            wq.codes.copy_(wq0.codes)
+            wq.scales_buf.copy_(wq0.scales_buf)
+            wq.sums_buf.copy_(wq0.sums_buf)
+            sets.append((wq, x.clone(), w4.alloc_act4(rows, K, dev), torch.empty(rows, N, device=dev)))
+        del wq0
+        for s_ in sets:
+            w4.w4a4_rotate_quantize_act(s_[1], out=s_[2])
+        out[name] = {
+            "act_ms": timed(lambda i: w4.w4a4_rotate_quantize_act(sets[i % nsets][1], out=sets[i % nsets][2]), nrep),
+            "gemm_ms": timed(lambda i: w4.w4a4_gemm(sets[i % nsets][0], sets[i % nsets][2], y=sets[i % nsets][3]),
+                             nrep),
+        }
+        del sets
+        torch.cuda.empty_cache()
+    layer_ms = (4 * out["c1"]["gemm_ms"] + 2 * out["c2"]["gemm_ms"] + out["c3"]["gemm_ms"]
+                + 3 * out["c1"]["act_ms"] + out["c3"]["act_ms"])
+    return {"value": 512.0 / (layer_ms * 1e-3), "unit": "tok/s per layer", "layer_ms": layer_ms,
+            "what": "512 / (4 GEMM K5120xN5120 + 2 GEMM K5120xN17408 + 1 GEMM K17408xN5120 + 3 act K5120 "
+                    "+ 1 act K17408), M=512; GEMM-only, not a whole-model rate",
+            "kernels_ms": out}
+
+
 def run_probes() -> dict:
     """int8 / fp8 tensor and fp32 FMA throughput on this GPU (ops/s), via libw4a4_probes.so."""
     import ctypes
@@ -214,6 +316,7 @@ def run_ours(args, shape) -> dict | None:
         wq = w4.alloc_q4_0(N, K, dev)
         wq.codes.copy_(wq0.codes)
         wq.scales_buf.copy_(wq0.scales_buf)
+        wq.sums_buf.copy_(wq0.sums_buf)
         xs = x0.clone()
         aq = w4.alloc_act4(M, K, dev)
         y = torch.empty(M, N, dtype=torch.float32, device=dev)
@@ -306,18 +409,25 @@ def run_ours(args, shape) -> dict | None:
     fold_flops = 2.0 * M * N * B
     sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
     fp32_peak = sm_count * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+    gemm_traffic, gemm_traffic_src = profiled_traffic(f"gemm_tc_{shape.name}.md", GEMM_SOURCES)
+    act_traffic, act_traffic_src = profiled_traffic(f"act_rotate_quantize_{shape.name}.md", ACT_SOURCES)
     gemm_roof = {"bound": "alu", "achieved": fold_flops / (gemm_avg * 1e-3) / 1e12, "peak": fp32_peak,
-                 "unit": "TFLOP/s", "frac": None, "traffic": args.gemm_traffic,
+                 "unit": "TFLOP/s", "frac": None, "traffic": gemm_traffic, "traffic_source": gemm_traffic_src,
+                 "algorithmic_bytes": float(N * K // 2 + N * B * 4 + M * K // 2 + M * B * 4 + M * N * 4),
                  "kernel": "w4a4_gemm_tc_kernel",
                  "peak_source": f"derived: {sm_count} SMs x 128 fp32 lanes x 2 flops x {peaks.get('sm_max_mhz', 2070.0)} MHz"}
     gemm_roof["frac"] = gemm_roof["achieved"] / gemm_roof["peak"]
     act_bytes = M * K * 4 + M * K // 2 + M * B * 4
     act_roof = {"bound": "hbm", "achieved": act_bytes / (act_avg * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "kernel": "act_rotate_quantize_kernel",
+                "unit": "GB/s", "kernel": "act_rotate_quantize_kernel", "traffic": act_traffic,
+                "traffic_source": act_traffic_src, "algorithmic_bytes": float(act_bytes),
                 "peak_source": "MEASURED_PEAKS.json hbm_gbs (measured)" if not peaks.get("fallback") else "fallback"}
     act_roof["frac"] = act_roof["achieved"] / act_roof["peak"]
     eff_tops_gemm = ops / (gemm_avg * 1e-3) / 1e12
     int8_peak = probes.get("int8_mma_sync_tops") if probes else None
+    proxy = None
+    if not args.no_proxy and world == 1:
+        proxy = prefill_proxy(dev, stream, max(10, args.steps // 2))
 
     cpu = None
     if not args.no_cpu_baseline:
@@ -333,7 +443,7 @@ def run_ours(args, shape) -> dict | None:
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "int4 x int4 (exact fp8 tensor-core MMA) -> f32 fold", "data": "synthetic",
+        "vs_baseline": None, "dtype": "s4", "data": "synthetic",
         "config": {"workload": shape.what, "M": M, "K": K, "N": N,
                    "l2": f"inputs larger than L2: {nsets} input sets ({nsets * set_bytes / 2**20:.0f} MiB) "
                          f"rotated across steps", "parallelism": "replicas" if world > 1 else "single"},
@@ -341,7 +451,7 @@ def run_ours(args, shape) -> dict | None:
         "roofline_act": act_roof,
         "gemm_effective_tops": eff_tops_gemm,
         "pct_int8_peak": (eff_tops_gemm / int8_peak) if int8_peak else None,
-        "prefill_tok_s_proxy": None,
+        "prefill_tok_s_proxy": proxy,
         "kernel_ms": {"act_rotate_quantize": act_avg, "gemm": gemm_avg},
         "pack_weights_ms": pack_ms,
         "probes": probes,
@@ -366,8 +476,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-probes", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
-    ap.add_argument("--gemm-traffic", type=float, default=None,
-                    help="dram bytes per GEMM launch from an ncu capture of the current kernel")
+    ap.add_argument("--no-proxy", action="store_true", help="skip the per-layer prefill proxy")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -31,8 +31,8 @@ from . import build as _build
 __all__ = [
     "W4A4Error", "Q4_0Weights", "Act4", "load_library", "library_path",
     "h32_q4_0_pack_weights", "q4_0_import", "w4a4_rotate_quantize_act",
-    "w4a4_gemm", "w4a4_gemm_partials", "w4a4_gemm_id", "w4a4_gemm_id_status",
-    "w4a4_gemm_id_workspace_bytes", "w4a4_check", "STATUS",
+    "w4a4_gemm", "w4a4_gemm_workspace_bytes", "w4a4_gemm_partials", "w4a4_gemm_id", "w4a4_gemm_id_status",
+    "w4a4_gemm_id_workspace_bytes", "w4a4_gemm_id_static", "w4a4_check", "STATUS",
 ]
 
 STATUS = {
@@ -47,8 +47,8 @@ TAG_ROTATED = 0x1
 #: every symbol include/w4a4.h declares
 EXPORTS = [
     "w4a4_q4_0_codes_bytes", "w4a4_q4_0_scales_bytes", "w4a4_q4_0_sums_bytes", "w4a4_act4_codes_bytes",
-    "w4a4_act4_scales_bytes", "h32_q4_0_pack_weights", "q4_0_import", "w4a4_rotate_quantize_act", "w4a4_gemm", "w4a4_gemm_partials",
-    "w4a4_gemm_id", "w4a4_gemm_id_workspace_bytes", "w4a4_gemm_id_status", "w4a4_gemm_id_static", "w4a4_check", "w4a4_last_error",
+    "w4a4_act4_scales_bytes", "h32_q4_0_pack_weights", "q4_0_import", "w4a4_rotate_quantize_act", "w4a4_gemm", "w4a4_gemm_workspace_bytes",
+    "w4a4_gemm_partials", "w4a4_gemm_id", "w4a4_gemm_id_workspace_bytes", "w4a4_gemm_id_status", "w4a4_gemm_id_static", "w4a4_check", "w4a4_last_error",
     "w4a4_status_name", "w4a4_abi_version",
 ]
 
@@ -96,7 +96,8 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.h32_q4_0_pack_weights.argtypes = [vp, i32, i64, i64, i64, i32, ctypes.POINTER(_Q4_0Desc), vp]
     lib.q4_0_import.argtypes = [vp, i64, i64, i32, ctypes.POINTER(_Q4_0Desc), vp]
     lib.w4a4_rotate_quantize_act.argtypes = [vp, i64, i64, i64, i32, ctypes.POINTER(_Act4Desc), vp]
-    lib.w4a4_gemm.argtypes = [ctypes.POINTER(_Q4_0Desc), ctypes.POINTER(_Act4Desc), vp, i64, vp]
+    lib.w4a4_gemm.argtypes = [ctypes.POINTER(_Q4_0Desc), ctypes.POINTER(_Act4Desc), vp, i64, vp, u, vp]
+    lib.w4a4_gemm_workspace_bytes.argtypes, lib.w4a4_gemm_workspace_bytes.restype = [i64, i64, i64], u
     lib.w4a4_gemm_partials.argtypes = [ctypes.POINTER(_Q4_0Desc), ctypes.POINTER(_Act4Desc), vp, vp]
     lib.w4a4_gemm_id.argtypes = [ctypes.POINTER(_Q4_0Desc), i32, i64, ctypes.POINTER(_Act4Desc), vp, i64, i32, i32,
                                  vp, vp, u, vp]
@@ -264,16 +265,49 @@ def w4a4_rotate_quantize_act(x: torch.Tensor, rotate: bool = True, out: Act4 | N
     return out
 
 
-def w4a4_gemm(w: Q4_0Weights, a: Act4, y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """Y[m][n] = sum_b d_w[n][b] d_a[m][b] P[m][n][b] (fp32 [M][N])."""
+def w4a4_gemm_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(load_library().w4a4_gemm_workspace_bytes(M, N, K))
+
+
+_GEMM_WS: dict = {}
+
+
+def gemm_workspace(M: int, N: int, K: int, device, stream=None) -> torch.Tensor | None:
+    """A zero-initialised GEMM workspace kept per (device, stream), grown on demand.
+
+    One per stream, because calls sharing a workspace must not overlap on the GPU.
+    """
+    need = w4a4_gemm_workspace_bytes(M, N, K)
+    if need == 0:
+        return None
+    key = (torch.device(device).index, _stream(stream))
+    ws = _GEMM_WS.get(key)
+    if ws is None or ws.numel() < need:
+        ws = torch.zeros(need, dtype=torch.uint8, device=device)
+        _GEMM_WS[key] = ws
+    return ws
+
+
+def w4a4_gemm(w: Q4_0Weights, a: Act4, y: torch.Tensor | None = None, ws: torch.Tensor | None | bool = True,
+              stream=None) -> torch.Tensor:
+    """Y[m][n] = sum_b d_w[n][b] d_a[m][b] P[m][n][b] (fp32 [M][N]).
+
+    ws: True = the cached per-stream workspace (stream-K where it pays), a tensor
+    = that workspace (zero before its first use), None/False = whole-tile schedule.
+    """
     if y is None:
         y = torch.empty(a.rows, w.rows, dtype=torch.float32, device=w.codes.device)
     _cuda(y, "y")
     if y.dtype != torch.float32 or y.dim() != 2 or y.stride(1) != 1:
         raise ValueError("y must be a 2-D fp32 tensor with unit stride along N")
     ldy = y.stride(0) if y.shape[0] > 1 else max(w.rows, 1)
-    _check(load_library().w4a4_gemm(ctypes.byref(w.desc()), ctypes.byref(a.desc()), y.data_ptr(), ldy,
-                                    _stream(stream)))
+    if ws is True:
+        ws = gemm_workspace(a.rows, w.rows, w.K, y.device, stream)
+    elif ws is False:
+        ws = None
+    ws_ptr, ws_bytes = (ws.data_ptr(), ws.numel() * ws.element_size()) if ws is not None else (None, 0)
+    _check(load_library().w4a4_gemm(ctypes.byref(w.desc()), ctypes.byref(a.desc()), y.data_ptr(), ldy, ws_ptr,
+                                    ws_bytes, _stream(stream)))
     return y
 
 

@@ -176,7 +176,13 @@ w4a4_status w4a4_rotate_quantize_act(const float* x, int64_t M, int64_t K, int64
                                                       reinterpret_cast<cudaStream_t>(stream)), fn);
 }
 
-w4a4_status w4a4_gemm(const w4a4_q4_0* w, const w4a4_act4* a, float* y, int64_t ldy, w4a4_stream_t stream) {
+size_t w4a4_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  if (M < 0 || N < 0 || !valid_k(K)) return 0;
+  return w4a4::gemm_workspace_bytes(M, N, K);
+}
+
+w4a4_status w4a4_gemm(const w4a4_q4_0* w, const w4a4_act4* a, float* y, int64_t ldy, void* ws, size_t ws_bytes,
+                      w4a4_stream_t stream) {
   const char* fn = "w4a4_gemm";
   w4a4_status s = check_q4_0(w, fn);
   if (s != W4A4_OK) return s;
@@ -187,8 +193,14 @@ w4a4_status w4a4_gemm(const w4a4_q4_0* w, const w4a4_act4* a, float* y, int64_t 
   if (M == 0 || N == 0) return ok();
   if (!y) return fail(W4A4_ERR_INVALID_ARG, "%s: y is NULL", fn);
   if ((reinterpret_cast<uintptr_t>(y) & 3u) != 0) return fail(W4A4_ERR_ALIGNMENT, "%s: y must be 4-byte aligned", fn);
+  if (ws) {
+    const size_t need = w4a4::gemm_workspace_bytes(M, N, a->K);
+    if (ws_bytes < need)
+      return fail(W4A4_ERR_WORKSPACE, "%s: workspace %zu bytes < %zu needed", fn, ws_bytes, need);
+    if (!aligned16(ws)) return fail(W4A4_ERR_ALIGNMENT, "%s: ws must be 16-byte aligned", fn);
+  }
   return cuda_status(w4a4::launch_gemm_tc(w->codes, w->scales, w->sums, N, a->codes, a->scales, M, a->K, y, ldy, nullptr,
-                                          reinterpret_cast<cudaStream_t>(stream)), fn);
+                                          ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream)), fn);
 }
 
 w4a4_status w4a4_gemm_partials(const w4a4_q4_0* w, const w4a4_act4* a, int32_t* P, w4a4_stream_t stream) {
@@ -201,7 +213,7 @@ w4a4_status w4a4_gemm_partials(const w4a4_q4_0* w, const w4a4_act4* a, int32_t* 
   if (!P) return fail(W4A4_ERR_INVALID_ARG, "%s: P is NULL", fn);
   if (!aligned16(P)) return fail(W4A4_ERR_ALIGNMENT, "%s: P must be 16-byte aligned", fn);
   return cuda_status(w4a4::launch_gemm_tc(w->codes, w->scales, w->sums, w->rows, a->codes, a->scales, a->rows, a->K, nullptr,
-                                          0, P, reinterpret_cast<cudaStream_t>(stream)), fn);
+                                          0, P, nullptr, 0, reinterpret_cast<cudaStream_t>(stream)), fn);
 }
 
 size_t w4a4_gemm_id_workspace_bytes(int64_t M, int top_k, int E, int64_t K) {

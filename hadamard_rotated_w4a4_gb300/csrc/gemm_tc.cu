@@ -38,6 +38,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
+
 #include "w4a4_kernels.cuh"
 
 namespace w4a4 {
@@ -102,6 +104,13 @@ struct TcArgs {
   const int32_t* offsets;
   const int32_t* tile_off;
   int E;
+  // Stream-K schedule (dense product only): the tiles' K stages form one list of
+  // sk_units units, cut into gridDim.x equal contiguous ranges.  0 = each CTA
+  // takes whole tiles blockIdx.x, blockIdx.x + gridDim.x, ...
+  int64_t sk_units;
+  unsigned long long* sk_count;  // [tiles][8 worker warps]: (epoch << 32) | arrivals
+  float4* sk_part;               // [2 * gridDim.x][8 warps][32][32 lanes] fp32 partials
+  uint32_t sk_epoch;             // distinct per launch
 };
 
 // ------------------------------------------------------------------ PTX helpers
@@ -255,16 +264,139 @@ __device__ __forceinline__ Tile decode_tile(const TcArgs& p, int64_t t) {
   return T;
 }
 
+// ------------------------------------------------------------------ schedule
+// A segment: stages [s0, s1) of tile t; `first`: the CTA's first segment.
+struct Seg {
+  int64_t t;
+  int s0, s1;
+  bool first;
+};
+// The iteration state is one position (a unit, or a tile); the CTA's range is
+// recomputed from blockIdx at each step, to keep registers free in the workers.
+struct SegIter {
+  int64_t next;
+};
+__device__ __forceinline__ int64_t sk_begin(const TcArgs& p, int64_t c) { return c * p.sk_units / gridDim.x; }
+__device__ __forceinline__ SegIter seg_iter(const TcArgs& p) {
+  SegIter it;
+  it.next = p.sk_units ? sk_begin(p, blockIdx.x) : static_cast<int64_t>(blockIdx.x);
+  return it;
+}
+__device__ __forceinline__ bool seg_next(const TcArgs& p, int nst, SegIter& it, Seg& g) {
+  if (p.sk_units) {
+    const int64_t start = sk_begin(p, blockIdx.x), end = sk_begin(p, blockIdx.x + 1);
+    if (it.next >= end) return false;
+    g.first = it.next == start;
+    g.t = it.next / nst;
+    g.s0 = static_cast<int>(it.next - g.t * nst);
+    const int64_t left = end - it.next;
+    g.s1 = (nst - g.s0 <= left) ? nst : g.s0 + static_cast<int>(left);
+    it.next += g.s1 - g.s0;
+  } else {
+    if (it.next >= num_tiles(p)) return false;
+    g.first = it.next == blockIdx.x;
+    g.t = it.next;
+    g.s0 = 0;
+    g.s1 = nst;
+    it.next += gridDim.x;
+  }
+  return true;
+}
+// The CTA whose unit range holds unit u (ranges are [c U / G, (c + 1) U / G)).
+__device__ __forceinline__ int64_t sk_cta_of_unit(const TcArgs& p, int64_t u) {
+  const int64_t G = gridDim.x;
+  int64_t c = u * G / p.sk_units;
+  if (c >= G) c = G - 1;
+  for (int i = 0; i < 4 && c > 0 && sk_begin(p, c) > u; ++i) --c;
+  for (int i = 0; i < 4 && c + 1 < G && sk_begin(p, c + 1) <= u; ++i) ++c;
+  return c;
+}
+// One arrival on a (tile, warp) ticket; 1 if it was the last of `nparts`, 0 if
+// not, -1 if the update did not go through (device error word set).  A ticket
+// left by another launch (another epoch) counts as zero arrivals.
+__device__ int sk_ticket(unsigned long long* ctr, uint32_t epoch, uint32_t nparts) {
+  unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(ctr);
+  const unsigned long long base = static_cast<unsigned long long>(epoch) << 32;
+  for (int i = 0; i < (1 << 16); ++i) {
+    const unsigned long long nv = ((cur >> 32) == epoch) ? cur + 1 : base + 1;
+    const unsigned long long prev = atomicCAS(ctr, cur, nv);
+    if (prev == cur) return static_cast<uint32_t>(nv) >= nparts ? 1 : 0;
+    cur = prev;
+  }
+  atomicOr(&g_w4a4_device_error, 4);
+  return -1;
+}
+// A tile cut by the stream-K ranges: each of its worker warps stores its fp32
+// partial accumulators (sk_store, in the worker), then takes a ticket.  The warp
+// that arrives last for its (tile, warp) region sums every contributor's partial
+// in CTA order -- the same order whichever CTA comes last, so the result does not
+// depend on timing -- and writes those outputs.  No CTA waits for another.
+__device__ __forceinline__ float4* sk_slot(const TcArgs& p, int64_t cta, bool first, int w, int lane) {
+  return p.sk_part + ((2 * cta + (first ? 0 : 1)) * 8 + w) * 1024 + lane;
+}
+__device__ __forceinline__ bool sk_arrive(const TcArgs& p, int64_t t, int nst, int w, int lane) {
+  __threadfence();
+  __syncwarp();
+  const int64_t u_lo = t * nst;
+  const int64_t nparts = sk_cta_of_unit(p, u_lo + nst - 1) - sk_cta_of_unit(p, u_lo) + 1;
+  int last = 0;
+  if (lane == 0) last = sk_ticket(p.sk_count + t * 8 + w, p.sk_epoch, static_cast<uint32_t>(nparts));
+  last = __shfl_sync(0xFFFFFFFFu, last, 0);
+  if (last == 1) __threadfence();
+  return last == 1;
+}
+// Sum the partials of this warp's region and write them to Y (row m0 + col,
+// feature n).  Four float4 (16 columns) at a time: each contributor's four
+// loads are issued together, so one L2 round trip is paid per contributor and
+// group, not per value.
+__device__ __forceinline__ void sk_finish(const TcArgs& p, int64_t t, int nst, int w, int lane, int h, int64_t m0,
+                                          int ntok, int64_t n, bool n_ok) {
+  const int64_t u_lo = t * nst;
+  const int64_t c_lo = sk_cta_of_unit(p, u_lo), c_hi = sk_cta_of_unit(p, u_lo + nst - 1);
+#pragma unroll 1
+  for (int g = 0; g < 8; ++g) {
+    float4 a[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) a[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+    for (int64_t c = c_lo; c <= c_hi; ++c) {
+      const float4* src = sk_slot(p, c, sk_begin(p, c) >= u_lo, w, lane) + g * 4 * 32;
+      float4 v[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) v[k] = __ldcg(src + k * 32);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        a[k].x += v[k].x;
+        a[k].y += v[k].y;
+        a[k].z += v[k].z;
+        a[k].w += v[k].w;
+      }
+    }
+    if (n_ok) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int col = (h + 2 * (g >> 1)) * 32 + 16 * (g & 1) + 4 * k;  // float4 q = 4 g + k
+        float* yc = p.y + (m0 + col) * p.ldy + n;
+        if (col + 0 < ntok) yc[0] = a[k].x;
+        if (col + 1 < ntok) yc[p.ldy] = a[k].y;
+        if (col + 2 < ntok) yc[2 * p.ldy] = a[k].z;
+        if (col + 3 < ntok) yc[3 * p.ldy] = a[k].w;
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------------ roles
 __device__ void producer(const TcArgs& p, Smem& S, const CUtensorMap* wmap, const CUtensorMap* amap) {
   const int64_t B = p.K / 32;
-  const int64_t nst = (B + KB - 1) / KB;
-  const int64_t ntiles = num_tiles(p);
+  const int nst = static_cast<int>((B + KB - 1) / KB);
   const uint32_t bytes = static_cast<uint32_t>(KB * 16 * (TW + p.tt));  // full boxes, zero fill included
   uint32_t gstage = 0;
-  for (int64_t t = blockIdx.x; t < ntiles && !S.abort; t += gridDim.x) {
-    const Tile T = decode_tile(p, t);
-    for (int64_t s = 0; s < nst; ++s) {
+  SegIter si = seg_iter(p);
+  Seg sg;
+  while (!S.abort && seg_next(p, nst, si, sg)) {
+    const Tile T = decode_tile(p, sg.t);
+    for (int s = sg.s0; s < sg.s1; ++s) {
       const int slot = gstage % RAW;
       if (!mbar_wait(&S.empty_raw[slot], ((gstage / RAW) & 1) ^ 1, S)) break;
       mbar_expect_tx(&S.full_raw[slot], bytes);
@@ -286,12 +418,15 @@ __device__ void producer(const TcArgs& p, Smem& S, const CUtensorMap* wmap, cons
 
 __device__ void mma_issuer(const TcArgs& p, Smem& S, uint32_t tmem) {
   const int64_t B = p.K / 32;
-  const int64_t ntiles = num_tiles(p);
+  const int nst = static_cast<int>((B + KB - 1) / KB);
   uint32_t gblk = 0;
-  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
-    const Tile T = decode_tile(p, t);
+  SegIter si = seg_iter(p);
+  Seg sg;
+  while (seg_next(p, nst, si, sg)) {
+    const Tile T = decode_tile(p, sg.t);
     const uint32_t idesc = f8_idesc(T.nmma);
-    for (int64_t b = 0; b < B; ++b, ++gblk) {
+    const int64_t b_end = static_cast<int64_t>(sg.s1) * KB < B ? static_cast<int64_t>(sg.s1) * KB : B;
+    for (int64_t b = static_cast<int64_t>(sg.s0) * KB; b < b_end; ++b, ++gblk) {
       const int f = gblk % F8;
       const int tb = gblk & 1;
       if (!mbar_wait(&S.f8_full[f], (gblk / F8) & 1, S)) goto done;
@@ -320,12 +455,13 @@ __device__ void converters(const TcArgs& p, Smem& S) {
   const int ct = threadIdx.x - 64;  // 0..63
   const int lane = threadIdx.x & 31;
   const int64_t B = p.K / 32;
-  const int64_t nst = (B + KB - 1) / KB;
-  const int64_t ntiles = num_tiles(p);
+  const int nst = static_cast<int>((B + KB - 1) / KB);
   uint32_t gstage = 0, gblk = 0;
-  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
-    const Tile T = decode_tile(p, t);
-    for (int64_t s = 0; s < nst; ++s, ++gstage) {
+  SegIter si = seg_iter(p);
+  Seg sg;
+  while (seg_next(p, nst, si, sg)) {
+    const Tile T = decode_tile(p, sg.t);
+    for (int s = sg.s0; s < sg.s1; ++s, ++gstage) {
       const int nbk = static_cast<int>(B - s * KB < KB ? B - s * KB : KB);
       const int slot = gstage % RAW;
       if (!mbar_wait(&S.full_raw[slot], (gstage / RAW) & 1, S)) return;
@@ -387,26 +523,26 @@ __device__ void workers(const TcArgs& p, Smem& S, uint32_t tmem) {
   const int n_in = 32 * q + lane;     // this thread's weight row within the tile
   const int B = static_cast<int>(p.K / 32);
   const int nst = (B + KB - 1) / KB;
-  const int64_t ntiles = num_tiles(p);
   uint32_t gfold = 0, gsc = 0, gtile = 0;
 
-  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++gtile) {
-    // the scale slots are reused across tiles: start only when every warp is done
+  SegIter si = seg_iter(p);
+  Seg sg;
+  for (; seg_next(p, nst, si, sg); ++gtile) {
+    // the scale slots are reused across segments: start only when every warp is done
     if (gtile > 0 && !mbar_wait(&S.tile_done, (gtile - 1) & 1, S)) return;
-    const Tile T = decode_tile(p, t);
+    const Tile T = decode_tile(p, sg.t);
     const int nchunks = T.nmma / 32;
     // scale sources of this thread: activation row wt, weight row wt (wt < 128)
     const bool a_ok = wt < T.ntok;
     const bool w_ok = wt < T.rows_w;
-    const float* as_row = p.a_scales + (T.m0 + (a_ok ? wt : 0)) * B;
-    const uint16_t* ws_row = p.w_scales + (T.wrow0 + (w_ok ? wt : 0)) * B;
-    const int16_t* wsum_row = p.w_sums + (T.wrow0 + (w_ok ? wt : 0)) * B;
+    // element offsets of this thread's scale rows: activation row wt, weight row wt
+    const int64_t a_off = (T.m0 + (a_ok ? wt : 0)) * B;
+    const int64_t w_off = (T.wrow0 + (w_ok ? wt : 0)) * B;
     // Scales of the next stage, prefetched into registers one stage ahead and kept
-    // as loaded (no arithmetic on them until they are published, so the warp does
-    // not wait for the loads).
-    float da_r[KB];
-    unsigned short dw_r[KB];
-    short sw_r[KB];
+    // packed as loaded (no arithmetic on them until they are published, so the
+    // warp does not wait for the loads): 4 fp32 d_a, 4 fp16 d_w, 4 int16 S_w.
+    uint4 da_r;
+    uint2 dw_r, sw_r;
     // Loads are unconditional (clamped to valid addresses); validity is applied
     // when publishing, so nothing consumes a loaded value early.
     // Rows whose KB-block groups are aligned take one vector load per array.
@@ -415,39 +551,38 @@ __device__ void workers(const TcArgs& p, Smem& S, uint32_t tmem) {
                      (reinterpret_cast<uintptr_t>(p.w_sums) & 7) == 0;
     auto load_scales = [&](int s) {
       if (vec) {
-        const float4 a4 = __ldg(reinterpret_cast<const float4*>(as_row + s * KB));
-        const uint2 w2 = __ldg(reinterpret_cast<const uint2*>(ws_row + s * KB));
-        const uint2 s2 = __ldg(reinterpret_cast<const uint2*>(wsum_row + s * KB));
-        da_r[0] = a4.x; da_r[1] = a4.y; da_r[2] = a4.z; da_r[3] = a4.w;
-        dw_r[0] = static_cast<unsigned short>(w2.x & 0xFFFFu);
-        dw_r[1] = static_cast<unsigned short>(w2.x >> 16);
-        dw_r[2] = static_cast<unsigned short>(w2.y & 0xFFFFu);
-        dw_r[3] = static_cast<unsigned short>(w2.y >> 16);
-        sw_r[0] = static_cast<short>(s2.x & 0xFFFFu);
-        sw_r[1] = static_cast<short>(s2.x >> 16);
-        sw_r[2] = static_cast<short>(s2.y & 0xFFFFu);
-        sw_r[3] = static_cast<short>(s2.y >> 16);
+        da_r = __ldg(reinterpret_cast<const uint4*>(p.a_scales + a_off + s * KB));
+        dw_r = __ldg(reinterpret_cast<const uint2*>(p.w_scales + w_off + s * KB));
+        sw_r = __ldg(reinterpret_cast<const uint2*>(p.w_sums + w_off + s * KB));
         return;
       }
+      uint32_t a[KB], w[KB], u[KB];
 #pragma unroll
       for (int k = 0; k < KB; ++k) {
         const int b = min(s * KB + k, B - 1);
-        da_r[k] = __ldg(as_row + b);
-        dw_r[k] = __ldg(ws_row + b);
-        sw_r[k] = __ldg(wsum_row + b);
+        a[k] = __float_as_uint(__ldg(p.a_scales + a_off + b));
+        w[k] = __ldg(p.w_scales + w_off + b);
+        u[k] = static_cast<uint16_t>(__ldg(p.w_sums + w_off + b));
       }
+      da_r = make_uint4(a[0], a[1], a[2], a[3]);
+      dw_r = make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
+      sw_r = make_uint2(u[0] | (u[1] << 16), u[2] | (u[3] << 16));
     };
     // Store the registers' scales into a slot and arrive; waiting is separate.
     auto publish_scales = [&](int slot, int s) {
+      const uint32_t da[KB] = {da_r.x, da_r.y, da_r.z, da_r.w};
+      const uint32_t dwp[2] = {dw_r.x, dw_r.y}, swp[2] = {sw_r.x, sw_r.y};
 #pragma unroll
       for (int k = 0; k < KB; ++k) {
         const bool bok = s * KB + k < B;
-        S.sda[slot][k][wt] = (a_ok && bok) ? da_r[k] : 0.f;
+        S.sda[slot][k][wt] = (a_ok && bok) ? __uint_as_float(da[k]) : 0.f;
         if (wt < TW) {
-          const float dw = (w_ok && bok) ? __half2float(__ushort_as_half(dw_r[k])) * fp8_unscale() : 0.f;
+          const unsigned short dh = static_cast<unsigned short>(dwp[k >> 1] >> (16 * (k & 1)));
+          const short sw = static_cast<short>(swp[k >> 1] >> (16 * (k & 1)));
+          const float dw = (w_ok && bok) ? __half2float(__ushort_as_half(dh)) * fp8_unscale() : 0.f;
           S.sdw[slot][k][wt] = dw;
           // -d_w * 8 S_w, exact: (d_w 2^18) * (S_w 2^-15), at most 20 significant bits
-          S.scorr[slot][k][wt] = (w_ok && bok) ? -dw * (static_cast<float>(sw_r[k]) * 3.0517578125e-05f) : 0.f;
+          S.scorr[slot][k][wt] = (w_ok && bok) ? -dw * (static_cast<float>(sw) * 3.0517578125e-05f) : 0.f;
         }
       }
       __syncwarp();
@@ -465,22 +600,23 @@ __device__ void workers(const TcArgs& p, Smem& S, uint32_t tmem) {
     // block b - 2, so every warp is past stage s - 1, the slot's previous user),
     // then stage s + 2 is prefetched.  A stage's slot is waited for at kb = 0.
     const uint32_t gsc0 = gsc;
-    load_scales(0);
-    publish_scales(gsc0 & 1, 0);
-    if (nst > 1) load_scales(1);
+    load_scales(sg.s0);
+    publish_scales(gsc0 & 1, sg.s0);
+    if (sg.s0 + 1 < sg.s1) load_scales(sg.s0 + 1);
 
-    for (int b = 0; b < B; ++b) {
+    const int b_end = sg.s1 * KB < B ? sg.s1 * KB : B;
+    for (int b = sg.s0 * KB; b < b_end; ++b) {
       const int s = b / KB;
       const int kb = b - s * KB;
-      const uint32_t gs = gsc0 + static_cast<uint32_t>(s);
+      const uint32_t gs = gsc0 + static_cast<uint32_t>(s - sg.s0);
       if (kb == 0 && !mbar_wait(&S.sc_ready[gs & 1], (gs >> 1) & 1, S)) return;
       // ---- fold block b
       const int tb = gfold & 1;
       if (!mbar_wait(&S.tm_full[tb], (gfold >> 1) & 1, S)) return;
       tc_fence_after();
-      if (kb == 2 && s + 1 < nst) {
+      if (kb == 2 && s + 1 < sg.s1) {
         publish_scales((gs + 1) & 1, s + 1);
-        if (s + 2 < nst) load_scales(s + 2);
+        if (s + 2 < sg.s1) load_scales(s + 2);
       }
       const int slot = gs & 1;
       const float dw = S.sdw[slot][kb][n_in];
@@ -569,10 +705,22 @@ __device__ void workers(const TcArgs& p, Smem& S, uint32_t tmem) {
       if (lane == 0) mbar_arrive(&S.tm_empty[tb]);
       ++gfold;
     }
-    gsc = gsc0 + static_cast<uint32_t>(nst);
+    gsc = gsc0 + static_cast<uint32_t>(sg.s1 - sg.s0);
 
     if constexpr (!PARTIALS) {
-      if (n_in < T.rows_w) {
+      // a tile cut by the stream-K ranges is written by its last contributor
+      const bool split = p.sk_units && (sg.s0 > 0 || sg.s1 < nst);
+      if (split) {
+        float4* mine = sk_slot(p, blockIdx.x, sg.first, warp - 4, lane);
+#pragma unroll
+        for (int qq = 0; qq < 32; ++qq) {
+          const int i = qq >> 3, j = 2 * (qq & 7);
+          __stcg(mine + qq * 32, make_float4(acc[i][j].x, acc[i][j].y, acc[i][j + 1].x, acc[i][j + 1].y));
+        }
+        if (sk_arrive(p, sg.t, nst, warp - 4, lane))
+          sk_finish(p, sg.t, nst, warp - 4, lane, h, T.m0, T.ntok, T.n0 + n_in, n_in < T.rows_w);
+      }
+      if (!split && n_in < T.rows_w) {
         const int64_t n = T.n0 + n_in;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -732,11 +880,50 @@ int token_tile(int64_t M) {
   return static_cast<int>(r < TT ? r : TT);
 }
 
+// Stream-K or one tile per CTA pass.  Whole tiles leave SMs idle in the last
+// wave (80 tiles of M512 x N5120 on 152 SMs: one wave at 53%); stream-K gives
+// every CTA the same number of K stages and pays for it with one partial
+// store + reload per cut tile.  It is used where it shortens the longest CTA
+// by more than 10% (fixup counted as two stages).
+struct SkPlan {
+  bool on;
+  int64_t units;
+  int grid;
+  size_t count_bytes;  // tickets, padded to 256 bytes
+  size_t ws_bytes;     // tickets + partials
+};
+constexpr int kSkFixupStages = 2;
+constexpr size_t kSkPartBytes = size_t(8) * 1024 * sizeof(float4);  // one CTA segment: 8 warps x 32 x 32 float4
+
+SkPlan plan_stream_k(int64_t M, int64_t N, int64_t K) {
+  SkPlan pl{};
+  if (M <= 0 || N <= 0 || K <= 0) return pl;
+  const int64_t tt = token_tile(M);
+  const int64_t tiles = ((N + TW - 1) / TW) * ((M + tt - 1) / tt);
+  const int64_t nst = (K / 32 + KB - 1) / KB;
+  const int64_t sms = num_sms();
+  const int64_t dp_span = ((tiles + sms - 1) / sms) * nst;
+  const int64_t U = tiles * nst;
+  const int64_t G = U < sms ? U : sms;
+  const int64_t sk_span = (U + G - 1) / G + kSkFixupStages;
+  if (G < 2 || 10 * sk_span >= 9 * dp_span) return pl;
+  pl.on = true;
+  pl.units = U;
+  pl.grid = static_cast<int>(G);
+  pl.count_bytes = (static_cast<size_t>(tiles) * 8 * sizeof(unsigned long long) + 255) & ~size_t(255);
+  pl.ws_bytes = pl.count_bytes + 2 * static_cast<size_t>(G) * kSkPartBytes;
+  return pl;
+}
+
+std::atomic<uint32_t> g_sk_epoch{0};
+
 }  // namespace
+
+size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) { return plan_stream_k(M, N, K).ws_bytes; }
 
 cudaError_t launch_gemm_tc(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums, int64_t N,
                            const uint8_t* a_codes, const float* a_scales, int64_t M, int64_t K, float* y, int64_t ldy,
-                           int32_t* P, cudaStream_t stream) {
+                           int32_t* P, void* ws, size_t ws_bytes, cudaStream_t stream) {
   TcArgs a{};
   a.w_scales = w_scales; a.w_sums = w_sums; a.a_scales = a_scales;
   a.M = M; a.N = N; a.K = K; a.y = y; a.ldy = ldy; a.P = P;
@@ -745,8 +932,19 @@ cudaError_t launch_gemm_tc(const uint8_t* w_codes, const uint16_t* w_scales, con
   cudaError_t e = codes_map(&wmap, w_codes, N, K, TW);
   if (e == cudaSuccess) e = codes_map(&amap, a_codes, M, K, a.tt);
   if (e != cudaSuccess) return e;
-  const int64_t tiles = ((N + TW - 1) / TW) * ((M + a.tt - 1) / a.tt);
-  return P ? launch_tc<true>(wmap, amap, a, tiles, stream) : launch_tc<false>(wmap, amap, a, tiles, stream);
+  int64_t grid = ((N + TW - 1) / TW) * ((M + a.tt - 1) / a.tt);
+  if (P) return launch_tc<true>(wmap, amap, a, grid, stream);
+  const SkPlan pl = plan_stream_k(M, N, K);
+  if (pl.on && ws && ws_bytes >= pl.ws_bytes) {
+    uint32_t ep = ++g_sk_epoch;
+    if (ep == 0) ep = ++g_sk_epoch;
+    a.sk_units = pl.units;
+    a.sk_count = static_cast<unsigned long long*>(ws);
+    a.sk_part = reinterpret_cast<float4*>(static_cast<uint8_t*>(ws) + pl.count_bytes);
+    a.sk_epoch = ep;
+    grid = pl.grid;
+  }
+  return launch_tc<false>(wmap, amap, a, grid, stream);
 }
 
 cudaError_t launch_gemm_tc_routed(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums, int E,

@@ -39,10 +39,14 @@ cudaError_t launch_pack_q4_0(const void* w, int w_dtype, int64_t N, int64_t K, i
                              uint8_t* codes, uint16_t* scales, int16_t* sums, cudaStream_t stream);
 cudaError_t launch_import_q4_0(const void* blocks, int64_t N, int64_t K, uint8_t* codes, uint16_t* scales,
                                int16_t* sums, cudaStream_t stream);
+// Dense product (P == nullptr) or exact partials (P != nullptr).  With a
+// workspace of at least gemm_workspace_bytes(M, N, K) bytes (16-byte aligned,
+// zero before its first use) the dense product may run a stream-K schedule.
 cudaError_t launch_gemm_tc(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums, int64_t N,
                            const uint8_t* a_codes,
                            const float* a_scales, int64_t M, int64_t K, float* y, int64_t ldy, int32_t* P,
-                           cudaStream_t stream);
+                           void* ws, size_t ws_bytes, cudaStream_t stream);
+size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_gemm_tc_routed(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums, int E,
                                   int64_t N,
                                   const uint8_t* g_codes, const float* g_scales, int64_t K, int64_t npairs,

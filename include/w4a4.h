@@ -171,9 +171,22 @@ w4a4_status w4a4_rotate_quantize_act(const float* x, int64_t M, int64_t K, int64
  * w->K must equal a->K and both tags must agree on rotation, else
  * W4A4_ERR_MISMATCH.  The per-block integer partials are exact on the tensor
  * cores; the scale fold is fp32.
+ *   ws  : optional device workspace (NULL, or w4a4_gemm_workspace_bytes(M, N,
+ *         K) bytes or more, 16-byte aligned, all zero before its first use;
+ *         the library leaves it valid for later calls).  With it, shapes whose
+ *         tiles would leave SMs idle in the last wave run a stream-K schedule:
+ *         the K work of all tiles is split evenly over the SMs and a tile cut
+ *         between CTAs is summed in a fixed order, so the result does not depend
+ *         on timing.  Without it (or when the size query returns 0) each CTA
+ *         takes whole tiles.  A smaller non-NULL ws is W4A4_ERR_WORKSPACE.
+ *         Calls that share a workspace must not overlap on the GPU.
  */
-w4a4_status w4a4_gemm(const w4a4_q4_0* w, const w4a4_act4* a, float* y, int64_t ldy,
-                      w4a4_stream_t stream);
+w4a4_status w4a4_gemm(const w4a4_q4_0* w, const w4a4_act4* a, float* y, int64_t ldy, void* ws,
+                      size_t ws_bytes, w4a4_stream_t stream);
+
+/* Workspace bytes for w4a4_gemm at this shape on the current device; 0 when the
+ * whole-tile schedule is used (no workspace needed). */
+size_t w4a4_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 /*
  * w4a4_gemm_partials -- the exact per-block integer dot products

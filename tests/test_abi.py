@@ -65,42 +65,42 @@ def status(lib, fn, *args):
 
 
 def test_gemm_refuses_rotation_mismatch(lib):
-    s, msg = status(lib, "w4a4_gemm", ctypes.byref(q4(rotated=True)), ctypes.byref(a4(rotated=False)), FAKE, 64, None)
+    s, msg = status(lib, "w4a4_gemm", ctypes.byref(q4(rotated=True)), ctypes.byref(a4(rotated=False)), FAKE, 64, None, 0, None)
     assert s == "W4A4_ERR_MISMATCH" and "silently wrong" in msg
-    s, _ = status(lib, "w4a4_gemm", ctypes.byref(q4(rotated=False)), ctypes.byref(a4(rotated=True)), FAKE, 64, None)
+    s, _ = status(lib, "w4a4_gemm", ctypes.byref(q4(rotated=False)), ctypes.byref(a4(rotated=True)), FAKE, 64, None, 0, None)
     assert s == "W4A4_ERR_MISMATCH"
 
 
 def test_gemm_refuses_k_mismatch_and_bad_tags(lib):
-    s, _ = status(lib, "w4a4_gemm", ctypes.byref(q4(K=256)), ctypes.byref(a4(K=512)), FAKE, 64, None)
+    s, _ = status(lib, "w4a4_gemm", ctypes.byref(q4(K=256)), ctypes.byref(a4(K=512)), FAKE, 64, None, 0, None)
     assert s == "W4A4_ERR_MISMATCH"
-    s, _ = status(lib, "w4a4_gemm", ctypes.byref(q4(tag=w4.TAG_ACT4)), ctypes.byref(a4()), FAKE, 64, None)
+    s, _ = status(lib, "w4a4_gemm", ctypes.byref(q4(tag=w4.TAG_ACT4)), ctypes.byref(a4()), FAKE, 64, None, 0, None)
     assert s == "W4A4_ERR_INVALID_ARG"
-    s, _ = status(lib, "w4a4_gemm", None, ctypes.byref(a4()), FAKE, 64, None)
+    s, _ = status(lib, "w4a4_gemm", None, ctypes.byref(a4()), FAKE, 64, None, 0, None)
     assert s == "W4A4_ERR_INVALID_ARG"
 
 
 def test_gemm_argument_checks(lib):
-    s, _ = status(lib, "w4a4_gemm", ctypes.byref(q4(K=48)), ctypes.byref(a4(K=48)), FAKE, 64, None)
+    s, _ = status(lib, "w4a4_gemm", ctypes.byref(q4(K=48)), ctypes.byref(a4(K=48)), FAKE, 64, None, 0, None)
     assert s == "W4A4_ERR_INVALID_ARG"
-    s, _ = status(lib, "w4a4_gemm", ctypes.byref(q4()), ctypes.byref(a4()), FAKE, 32, None)  # ldy < N
+    s, _ = status(lib, "w4a4_gemm", ctypes.byref(q4()), ctypes.byref(a4()), FAKE, 32, None, 0, None)  # ldy < N
     assert s == "W4A4_ERR_INVALID_ARG"
-    s, _ = status(lib, "w4a4_gemm", ctypes.byref(q4()), ctypes.byref(a4()), FAKE + 2, 64, None)  # y not 4B aligned
+    s, _ = status(lib, "w4a4_gemm", ctypes.byref(q4()), ctypes.byref(a4()), FAKE + 2, 64, None, 0, None)  # y not 4B aligned
     assert s == "W4A4_ERR_ALIGNMENT"
     bad = _Q4_0Desc(FAKE + 8, FAKE, FAKE, 64, 256, w4.TAG_Q4_0 | 1)
-    s, _ = status(lib, "w4a4_gemm", ctypes.byref(bad), ctypes.byref(a4()), FAKE, 64, None)
+    s, _ = status(lib, "w4a4_gemm", ctypes.byref(bad), ctypes.byref(a4()), FAKE, 64, None, 0, None)
     assert s == "W4A4_ERR_ALIGNMENT"
     bad = _Q4_0Desc(FAKE, FAKE, FAKE + 4, 64, 256, w4.TAG_Q4_0 | 1)  # sums not 16-byte aligned
-    s, _ = status(lib, "w4a4_gemm", ctypes.byref(bad), ctypes.byref(a4()), FAKE, 64, None)
+    s, _ = status(lib, "w4a4_gemm", ctypes.byref(bad), ctypes.byref(a4()), FAKE, 64, None, 0, None)
     assert s == "W4A4_ERR_ALIGNMENT"
-    s, _ = status(lib, "w4a4_gemm", ctypes.byref(q4()), ctypes.byref(a4()), None, 64, None)
+    s, _ = status(lib, "w4a4_gemm", ctypes.byref(q4()), ctypes.byref(a4()), None, 64, None, 0, None)
     assert s == "W4A4_ERR_INVALID_ARG"
 
 
 def test_empty_problems_are_no_ops(lib):
-    s, _ = status(lib, "w4a4_gemm", ctypes.byref(q4(rows=0)), ctypes.byref(a4()), None, 0, None)
+    s, _ = status(lib, "w4a4_gemm", ctypes.byref(q4(rows=0)), ctypes.byref(a4()), None, 0, None, 0, None)
     assert s == "W4A4_OK"
-    s, _ = status(lib, "w4a4_gemm", ctypes.byref(q4()), ctypes.byref(a4(rows=0)), None, 64, None)
+    s, _ = status(lib, "w4a4_gemm", ctypes.byref(q4()), ctypes.byref(a4(rows=0)), None, 64, None, 0, None)
     assert s == "W4A4_OK"
     d = _Act4Desc(FAKE, FAKE, 0, 0, 0)
     s, _ = status(lib, "w4a4_rotate_quantize_act", FAKE, 0, 256, 256, 1, ctypes.byref(d), None)
@@ -141,3 +141,17 @@ def test_gemm_id_argument_checks(lib):
     assert call(a=a4(rows=M, rotated=False)) == "W4A4_ERR_MISMATCH"
     assert call(ws=FAKE + 8) == "W4A4_ERR_ALIGNMENT"
     assert status(lib, "w4a4_gemm_id_status", None, None)[0] == "W4A4_ERR_INVALID_ARG"
+
+
+def test_gemm_workspace_query_and_short_workspace(lib):
+    # M300 x N640 x K1024: 10 tiles of 8 stages leave most SMs idle as whole tiles,
+    # so the split schedule applies and wants a workspace
+    need = lib.w4a4_gemm_workspace_bytes(300, 640, 1024)
+    assert need > 0 and need % 16 == 0
+    assert lib.w4a4_gemm_workspace_bytes(300, 640, 1000) == 0  # K not a multiple of 32
+    s, msg = status(lib, "w4a4_gemm", ctypes.byref(q4(rows=640, K=1024)), ctypes.byref(a4(rows=300, K=1024)), FAKE,
+                    640, FAKE, 16, None)
+    assert s == "W4A4_ERR_WORKSPACE", msg
+    s, _ = status(lib, "w4a4_gemm", ctypes.byref(q4(rows=640, K=1024)), ctypes.byref(a4(rows=300, K=1024)), FAKE,
+                  640, FAKE + 8, need, None)
+    assert s == "W4A4_ERR_ALIGNMENT"

@@ -213,6 +213,50 @@ def test_empty_activation_rows(dev):
     assert y.shape == (0, 8)
 
 
+# ------------------------------------------------------------------ stream-K schedule
+# Shapes whose whole tiles would leave SMs idle: the K stages of all tiles are
+# split evenly over the CTAs and cut tiles are summed from a workspace.
+SK_SHAPES = [(300, 1024, 640), (64, 2048, 128), (1024, 17408, 640), (512, 5120, 5120)]
+
+
+@pytest.mark.parametrize("M,K,N", SK_SHAPES)
+def test_stream_k_matches_oracle_and_is_deterministic(dev, M, K, N):
+    need = w4.w4a4_gemm_workspace_bytes(M, N, K)
+    assert need > 0, "the split schedule should apply at this shape"
+    d = si.dense_inputs("c1") if (M, K, N) == (512, 5120, 5120) else si.random_dense(M, K, N, seed=M + 7 * K + N)
+    wq, aq = _gpu_pair(dev, d)
+    ws = torch.zeros(need, dtype=torch.uint8, device=dev)
+    y1 = w4.w4a4_gemm(wq, aq, ws=ws)
+    y2 = w4.w4a4_gemm(wq, aq, ws=ws)  # the tickets of the first launch are stale for the second
+    y_whole = w4.w4a4_gemm(wq, aq, ws=None)
+    w4.w4a4_check()
+    assert torch.equal(y1, y2), "stream-K result changed between identical launches"
+    rng = np.random.default_rng(M)
+    rows = np.arange(M) if M * N <= 300 * 640 else np.sort(rng.choice(M, 24, replace=False))
+    R = oracle.w4a4_matmul(oracle.pack_weights(d["w_bf16"]), oracle.quantize_activations(d["x"][rows]))
+    ridx = torch.from_numpy(rows).to(dev)
+    assert_close(y1[ridx].cpu().numpy(), R)
+    assert_close(y_whole[ridx].cpu().numpy(), R)
+
+
+def test_stream_k_workspace_reused_across_shapes(dev):
+    shapes = [(300, 1024, 640), (64, 2048, 128), (300, 1024, 640)]
+    ws = torch.zeros(max(w4.w4a4_gemm_workspace_bytes(M, N, K) for M, K, N in shapes), dtype=torch.uint8, device=dev)
+    for i, (M, K, N) in enumerate(shapes):
+        d = si.random_dense(M, K, N, seed=40 + i)
+        wq, aq = _gpu_pair(dev, d)
+        Y = w4.w4a4_gemm(wq, aq, ws=ws).cpu().numpy()
+        assert_close(Y, oracle.w4a4_matmul(oracle.pack_weights(d["w_bf16"]), oracle.quantize_activations(d["x"])))
+
+
+def test_stream_k_short_workspace_refused(dev):
+    d = si.random_dense(300, 1024, 640, seed=3)
+    wq, aq = _gpu_pair(dev, d)
+    with pytest.raises(w4.W4A4Error) as e:
+        w4.w4a4_gemm(wq, aq, ws=torch.zeros(64, dtype=torch.uint8, device=dev))
+    assert e.value.status_name == "W4A4_ERR_WORKSPACE"
+
+
 # ------------------------------------------------------------------ full-size workloads
 @pytest.mark.parametrize("cfg", ["c1", "c2", "c3"])
 def test_full_size_dense(dev, cfg):
