@@ -47,6 +47,40 @@ __device__ __forceinline__ uint32_t nib(float y, float inv) {
   return static_cast<uint32_t>(static_cast<int>(r)) & 0xFu;
 }
 
+// One 32-element block held by this lane: rotate (optional), d_a = amax / 7,
+// int4 codes (round half away, clamp -8..7), stored at block index i if ok.
+__device__ __forceinline__ void quantize_block(float (&y)[32], int rotate, bool ok, uint8_t* __restrict__ codes,
+                                               float* __restrict__ scales, int64_t i) {
+  if (rotate) {
+    fwht32(y);
+    const float cst = c_h32();
+#pragma unroll
+    for (int k = 0; k < 32; ++k) y[k] = __fmul_rn(y[k], cst);
+  }
+  float a = 0.f;
+#pragma unroll
+  for (int k = 0; k < 32; ++k) a = fmaxf(a, fabsf(y[k]));
+  const float d = __fdiv_rn(a, 7.0f);
+  const float inv = (d != 0.0f) ? __frcp_rn(d) : 0.0f;
+  // byte t of the 16 = element t (low nibble) | element t + 16 (high nibble)
+  uint32_t w[4];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    uint32_t word = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t lo = nib(y[4 * t + k], inv);
+      const uint32_t hi = nib(y[16 + 4 * t + k], inv);
+      word |= (lo | (hi << 4)) << (8 * k);
+    }
+    w[t] = word;
+  }
+  if (ok) {
+    reinterpret_cast<uint4*>(codes)[i] = make_uint4(w[0], w[1], w[2], w[3]);
+    scales[i] = d;
+  }
+}
+
 __global__ void __launch_bounds__(32 * kWarps) act_rotate_quantize_kernel(const float* __restrict__ x, int64_t M,
                                                                           int64_t K, int64_t ldx, int rotate,
                                                                           uint8_t* __restrict__ codes,
@@ -90,34 +124,131 @@ __global__ void __launch_bounds__(32 * kWarps) act_rotate_quantize_kernel(const 
       y[4 * k + 3] = v.w;
     }
     __syncwarp();
-    if (rotate) {
-      fwht32(y);
-      const float cst = c_h32();
-#pragma unroll
-      for (int k = 0; k < 32; ++k) y[k] = __fmul_rn(y[k], cst);
+    quantize_block(y, rotate, ok, codes, scales, i);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Contiguous rows (ldx == K): the input is one array of M * B blocks of 128
+// bytes.  Each warp streams its chunks of 32 blocks (4 KB) through a 3-deep
+// ring of TMA loads (2D map [M*B][32 floats], 128-byte swizzle), the next
+// chunk's load issued before the current one is computed, so every SM keeps
+// up to 2 x 8 x 3 x 4 KB of reads in flight.  The swizzle puts 16-byte piece j
+// of block row r at piece j ^ (r % 8): lane r reads its own block with eight
+// conflict-free 16-byte loads, no transposition pass.
+constexpr int kTmaWarps = 8;
+#ifndef W4A4_ACT_STAGES
+#define W4A4_ACT_STAGES 3
+#endif
+#ifndef W4A4_ACT_CTAS_PER_SM
+#define W4A4_ACT_CTAS_PER_SM 2
+#endif
+constexpr int kTmaStages = W4A4_ACT_STAGES;
+constexpr uint32_t kChunkBytes = 32 * 32 * sizeof(float);
+constexpr uint64_t kActTimeoutNs = 1000000000ull;  // 1 s
+
+struct __align__(1024) ActSmem {
+  float buf[kTmaWarps][kTmaStages][32 * 32];
+  uint64_t full[kTmaWarps][kTmaStages];
+};
+
+__device__ __forceinline__ uint32_t su32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t gtime() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(su32(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: false after 1 s (the caller records the error and winds down).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* b, uint32_t parity) {
+  if (mbar_try(b, parity)) return true;
+  const uint64_t t0 = gtime();
+  while (!mbar_try(b, parity)) {
+    if (gtime() - t0 > kActTimeoutNs) return false;
+  }
+  return true;
+}
+__device__ __forceinline__ void tma_load_chunk(float* dst, const CUtensorMap* map, int32_t row, uint64_t* bar) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(bar)), "r"(kChunkBytes)
+               : "memory");
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(su32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(row), "r"(su32(bar))
+      : "memory");
+}
+
+__global__ void __launch_bounds__(32 * kTmaWarps) act_rotate_quantize_tma_kernel(
+    const __grid_constant__ CUtensorMap xmap, int64_t nblk, int rotate, uint8_t* __restrict__ codes,
+    float* __restrict__ scales, int* err) {
+  extern __shared__ __align__(1024) uint8_t act_smem[];
+  ActSmem& S = *reinterpret_cast<ActSmem*>(act_smem);
+  const int lane = threadIdx.x & 31;
+  const int wib = threadIdx.x >> 5;
+  if ((su32(act_smem) & 1023u) != 0) {  // the swizzle pattern assumes 1024-byte aligned stages; never expected
+    if (threadIdx.x == 0 && err) atomicOr(err, 16);
+    return;
+  }
+  const int64_t nchunks = (nblk + 31) / 32;
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * kTmaWarps + wib;
+  const int64_t nw = static_cast<int64_t>(gridDim.x) * kTmaWarps;
+  const int64_t n_my = gw < nchunks ? (nchunks - gw + nw - 1) / nw : 0;
+  if (lane == 0) {
+    for (int st = 0; st < kTmaStages; ++st)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&S.full[wib][st])));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&xmap)) : "memory");
+  }
+  __syncwarp();
+  int64_t issued = 0;  // meaningful in lane 0
+  if (lane == 0) {
+    for (; issued < n_my && issued < kTmaStages; ++issued)
+      tma_load_chunk(S.buf[wib][issued], &xmap, static_cast<int32_t>((gw + issued * nw) * 32),
+                     &S.full[wib][issued]);
+  }
+  bool failed = false;
+  for (int64_t it = 0; it < n_my; ++it) {
+    const int st = static_cast<int>(it % kTmaStages);
+    if (!mbar_wait_bounded(&S.full[wib][st], static_cast<uint32_t>((it / kTmaStages) & 1))) {
+      failed = true;
+      break;
     }
-    float a = 0.f;
+    const float* row = S.buf[wib][st] + lane * 32;
+    float y[32];
 #pragma unroll
-    for (int k = 0; k < 32; ++k) a = fmaxf(a, fabsf(y[k]));
-    const float d = __fdiv_rn(a, 7.0f);
-    const float inv = (d != 0.0f) ? __frcp_rn(d) : 0.0f;
-    // byte t of the 16 = element t (low nibble) | element t + 16 (high nibble)
-    uint32_t w[4];
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      uint32_t word = 0;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint32_t lo = nib(y[4 * t + k], inv);
-        const uint32_t hi = nib(y[16 + 4 * t + k], inv);
-        word |= (lo | (hi << 4)) << (8 * k);
-      }
-      w[t] = word;
+    for (int j = 0; j < 8; ++j) {
+      const float4 v = *reinterpret_cast<const float4*>(row + 4 * (j ^ (lane & 7)));
+      y[4 * j + 0] = v.x;
+      y[4 * j + 1] = v.y;
+      y[4 * j + 2] = v.z;
+      y[4 * j + 3] = v.w;
     }
-    if (ok) {
-      reinterpret_cast<uint4*>(codes)[i] = make_uint4(w[0], w[1], w[2], w[3]);
-      scales[i] = d;
+    __syncwarp();  // every lane has its block in registers: the stage may be refilled
+    if (lane == 0 && issued < n_my) {
+      tma_load_chunk(S.buf[wib][st], &xmap, static_cast<int32_t>((gw + issued * nw) * 32), &S.full[wib][st]);
+      ++issued;
     }
+    const int64_t i = (gw + it * nw) * 32 + lane;
+    quantize_block(y, rotate, i < nblk, codes, scales, i);
+  }
+  if (__any_sync(0xFFFFFFFFu, failed)) {
+    // a load never completed: record it and wait (bounded) for the copies still
+    // in flight, so that none lands after the block has exited
+    if (lane == 0) {
+      if (err) atomicOr(err, 8);
+      for (int64_t it = issued > kTmaStages ? issued - kTmaStages : 0; it < issued; ++it)
+        mbar_wait_bounded(&S.full[wib][it % kTmaStages], static_cast<uint32_t>((it / kTmaStages) & 1));
+    }
+    __syncwarp();
   }
 }
 
@@ -125,7 +256,31 @@ __global__ void __launch_bounds__(32 * kWarps) act_rotate_quantize_kernel(const 
 
 cudaError_t launch_act_rotate_quantize(const float* x, int64_t M, int64_t K, int64_t ldx, int rotate,
                                        uint8_t* codes, float* scales, cudaStream_t stream) {
-  const int64_t nchunks = (M * (K / 32) + 31) / 32;
+  const int64_t nblk = M * (K / 32);
+  const int64_t nchunks = (nblk + 31) / 32;
+  if (ldx == K && nblk < (int64_t(1) << 31) - 64) {
+    CUtensorMap xmap;
+    cudaError_t e = encode_2d_map(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, x, 32, static_cast<uint64_t>(nblk),
+                                  32 * sizeof(float), 32, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (e == cudaSuccess) {
+      static bool configured[64] = {};
+      int dev = 0;
+      cudaGetDevice(&dev);
+      if (dev >= 0 && dev < 64 && !configured[dev]) {
+        e = cudaFuncSetAttribute(act_rotate_quantize_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(sizeof(ActSmem)));
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+      }
+      int64_t ctas = (nchunks + kTmaWarps - 1) / kTmaWarps;
+      const int64_t cap = static_cast<int64_t>(num_sms()) * W4A4_ACT_CTAS_PER_SM;
+      if (ctas > cap) ctas = cap;
+      if (ctas < 1) ctas = 1;
+      act_rotate_quantize_tma_kernel<<<static_cast<unsigned>(ctas), 32 * kTmaWarps, sizeof(ActSmem), stream>>>(
+          xmap, nblk, rotate, codes, scales, device_error_word());
+      return cudaGetLastError();
+    }
+  }
   int64_t ctas = (nchunks + kWarps - 1) / kWarps;
   const int64_t cap = static_cast<int64_t>(num_sms()) * 4;  // 4 x 256 threads per SM
   if (ctas > cap) ctas = cap;

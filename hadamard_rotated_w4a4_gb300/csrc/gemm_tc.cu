@@ -38,7 +38,6 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
-#include <atomic>
 
 #include "w4a4_kernels.cuh"
 
@@ -59,12 +58,24 @@ constexpr int TW = 128;         // weight rows per tile
 constexpr int TT = 256;         // token columns per tile (max)
 constexpr int KB = 4;           // 32-blocks per stage (64 code bytes per row)
 static_assert(KB == 4, "the vector scale loads take 4 blocks per stage");
-constexpr int RAW = 3;          // stages of raw codes in flight
-constexpr int F8 = 8;           // fp8 operand buffers (two stages)
+#ifndef W4A4_RAW_STAGES
+#define W4A4_RAW_STAGES 3
+#endif
+#ifndef W4A4_F8_BUFFERS
+#define W4A4_F8_BUFFERS 8
+#endif
+constexpr int RAW = W4A4_RAW_STAGES;  // stages of raw codes in flight
+constexpr int F8 = W4A4_F8_BUFFERS;   // fp8 operand buffers (two stages)
 constexpr int WF8 = TW * 32 + 32;  // buffer strides padded by 32 bytes: the converters'
 constexpr int AF8 = TT * 32 + 32;  // 16-byte stores to 4 buffers hit distinct banks
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kTimeoutNs = 1000000000ull;  // 1 s
+#ifndef W4A4_WAIT_HINT_NS
+#define W4A4_WAIT_HINT_NS 0
+#endif
+// Suspend-time hint of the mbarrier waits; 0 = poll without suspending, which
+// measured about 2% faster than a 20 us hint on the dense workloads.
+constexpr uint32_t kWaitHintNs = W4A4_WAIT_HINT_NS;
 
 
 struct __align__(128) Smem {
@@ -88,6 +99,7 @@ struct __align__(128) Smem {
   volatile int abort;
 };
 constexpr size_t kSmemBytes = sizeof(Smem);
+static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA is at most 227 KB");
 
 struct TcArgs {
   const uint16_t* w_scales;
@@ -108,9 +120,8 @@ struct TcArgs {
   // sk_units units, cut into gridDim.x equal contiguous ranges.  0 = each CTA
   // takes whole tiles blockIdx.x, blockIdx.x + gridDim.x, ...
   int64_t sk_units;
-  unsigned long long* sk_count;  // [tiles][8 worker warps]: (epoch << 32) | arrivals
+  uint32_t* sk_count;            // [tiles][8 worker warps] arrivals; zero between launches
   float4* sk_part;               // [2 * gridDim.x][8 warps][32][32 lanes] fp32 partials
-  uint32_t sk_epoch;             // distinct per launch
 };
 
 // ------------------------------------------------------------------ PTX helpers
@@ -156,7 +167,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, Smem& S)
   if (mbar_try(b, parity)) return true;
   const uint64_t t0 = gtime();
   for (;;) {
-    if (mbar_try_sleep(b, parity, 20000u)) return true;
+    if (kWaitHintNs ? mbar_try_sleep(b, parity, kWaitHintNs) : mbar_try(b, parity)) return true;
     if (S.abort) return false;
     if (gtime() - t0 > kTimeoutNs) {
       S.abort = 1;
@@ -311,20 +322,15 @@ __device__ __forceinline__ int64_t sk_cta_of_unit(const TcArgs& p, int64_t u) {
   for (int i = 0; i < 4 && c + 1 < G && sk_begin(p, c + 1) <= u; ++i) ++c;
   return c;
 }
-// One arrival on a (tile, warp) ticket; 1 if it was the last of `nparts`, 0 if
-// not, -1 if the update did not go through (device error word set).  A ticket
-// left by another launch (another epoch) counts as zero arrivals.
-__device__ int sk_ticket(unsigned long long* ctr, uint32_t epoch, uint32_t nparts) {
-  unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(ctr);
-  const unsigned long long base = static_cast<unsigned long long>(epoch) << 32;
-  for (int i = 0; i < (1 << 16); ++i) {
-    const unsigned long long nv = ((cur >> 32) == epoch) ? cur + 1 : base + 1;
-    const unsigned long long prev = atomicCAS(ctr, cur, nv);
-    if (prev == cur) return static_cast<uint32_t>(nv) >= nparts ? 1 : 0;
-    cur = prev;
-  }
-  atomicOr(&g_w4a4_device_error, 4);
-  return -1;
+// One arrival on a (tile, warp) ticket: true for the last of `nparts`, which
+// also puts the ticket back to zero (no other arrival for it follows in this
+// launch), so the workspace needs no clearing between launches, graph replays
+// included.
+__device__ __forceinline__ bool sk_ticket(uint32_t* ctr, uint32_t nparts) {
+  const uint32_t before = atomicAdd(ctr, 1u);
+  if (before + 1 != nparts) return false;
+  atomicExch(ctr, 0u);
+  return true;
 }
 // A tile cut by the stream-K ranges: each of its worker warps stores its fp32
 // partial accumulators (sk_store, in the worker), then takes a ticket.  The warp
@@ -340,10 +346,10 @@ __device__ __forceinline__ bool sk_arrive(const TcArgs& p, int64_t t, int nst, i
   const int64_t u_lo = t * nst;
   const int64_t nparts = sk_cta_of_unit(p, u_lo + nst - 1) - sk_cta_of_unit(p, u_lo) + 1;
   int last = 0;
-  if (lane == 0) last = sk_ticket(p.sk_count + t * 8 + w, p.sk_epoch, static_cast<uint32_t>(nparts));
+  if (lane == 0) last = sk_ticket(p.sk_count + t * 8 + w, static_cast<uint32_t>(nparts)) ? 1 : 0;
   last = __shfl_sync(0xFFFFFFFFu, last, 0);
-  if (last == 1) __threadfence();
-  return last == 1;
+  if (last) __threadfence();
+  return last != 0;
 }
 // Sum the partials of this warp's region and write them to Y (row m0 + col,
 // feature n).  Four float4 (16 columns) at a time: each contributor's four
@@ -447,13 +453,19 @@ done:
   }
 }
 
-// Two warps convert one stage (4 blocks) at a time.  Lane l of a pass takes row
-// (pass base + l / 4) and block l % 4, so 8 lanes read 128 contiguous raw bytes;
-// the destination buffers are padded so that the four blocks' stores of the
-// same 8 lanes land in distinct banks too.
+// Two warps convert one stage (4 blocks) at a time.  Thread ct always takes
+// block k = ct % 4 of rows r0 + 16 i (r0 = ct / 4): 8 lanes read one row's 64
+// contiguous raw bytes, and the lanes of one block write 8 consecutive 16-byte
+// core-matrix rows of its fp8 buffer (the buffers are padded so that the four
+// blocks' stores land in distinct banks).  Source and destination advance by
+// constant strides (16 rows = 1024 raw bytes = 512 fp8 bytes per half).
 __device__ void converters(const TcArgs& p, Smem& S) {
   const int ct = threadIdx.x - 64;  // 0..63
   const int lane = threadIdx.x & 31;
+  const int k = ct & 3;
+  const int r0 = ct >> 2;
+  const uint32_t src_off = static_cast<uint32_t>(r0 * (KB * 16) + k * 16);
+  const uint32_t dst_off = static_cast<uint32_t>((r0 >> 3) * 256 + (r0 & 7) * 16);
   const int64_t B = p.K / 32;
   const int nst = static_cast<int>((B + KB - 1) / KB);
   uint32_t gstage = 0, gblk = 0;
@@ -461,51 +473,49 @@ __device__ void converters(const TcArgs& p, Smem& S) {
   Seg sg;
   while (seg_next(p, nst, si, sg)) {
     const Tile T = decode_tile(p, sg.t);
+    const int a_iters = T.nmma / 16;
     for (int s = sg.s0; s < sg.s1; ++s, ++gstage) {
       const int nbk = static_cast<int>(B - s * KB < KB ? B - s * KB : KB);
       const int slot = gstage % RAW;
       if (!mbar_wait(&S.full_raw[slot], (gstage / RAW) & 1, S)) return;
-      for (int k = 0; k < nbk; ++k) {
-        const uint32_t g = gblk + k;
+      for (int kk = 0; kk < nbk; ++kk) {
+        const uint32_t g = gblk + kk;
         if (!mbar_wait(&S.f8_empty[g % F8], ((g / F8) & 1) ^ 1, S)) return;
       }
-      // weights: 128 rows x 4 blocks, signed q - 8
-#pragma unroll 2
-      for (int it = 0; it < TW * KB / 64; ++it) {
-        const int rb = it * 64 + ct;
-        const int r = rb >> 2, k = rb & 3;
-        if (k < nbk) {
-          const uint4 raw = *reinterpret_cast<const uint4*>(S.wraw[slot] + r * (KB * 16) + k * 16);
+      if (k < nbk) {
+        const int f = (gblk + k) % F8;
+        // weights: 128 rows, signed q - 8
+        const uint8_t* ws = S.wraw[slot] + src_off;
+        uint8_t* wd = S.wf8[f] + dst_off;
+#pragma unroll 4
+        for (int i = 0; i < TW / 16; ++i) {
+          const uint4 raw = *reinterpret_cast<const uint4*>(ws + i * 1024);
           uint32_t l0, h0, l1, h1, l2, h2, l3, h3;
           q4_0_word_to_e4m3(raw.x, l0, h0);
           q4_0_word_to_e4m3(raw.y, l1, h1);
           q4_0_word_to_e4m3(raw.z, l2, h2);
           q4_0_word_to_e4m3(raw.w, l3, h3);
-          const int f = (gblk + k) % F8;
-          uint8_t* dst = S.wf8[f] + (r >> 3) * 256 + (r & 7) * 16;
-          *reinterpret_cast<uint4*>(dst) = make_uint4(l0, l1, l2, l3);
-          *reinterpret_cast<uint4*>(dst + 128) = make_uint4(h0, h1, h2, h3);
+          *reinterpret_cast<uint4*>(wd + i * 512) = make_uint4(l0, l1, l2, l3);
+          *reinterpret_cast<uint4*>(wd + i * 512 + 128) = make_uint4(h0, h1, h2, h3);
         }
-      }
-      // activations: nmma rows x 4 blocks; the offset codes u = a + 8 are the e4m3 bytes
-      for (int it = 0; it < T.nmma * KB / 64; ++it) {
-        const int rb = it * 64 + ct;
-        const int r = rb >> 2, k = rb & 3;
-        if (k < nbk) {
-          const uint4 raw = *reinterpret_cast<const uint4*>(S.araw[slot] + r * (KB * 16) + k * 16);
+        // activations: nmma rows; the offset codes u = a + 8 are the e4m3 bytes
+        const uint8_t* as = S.araw[slot] + src_off;
+        uint8_t* ad = S.af8[f] + dst_off;
+#pragma unroll 4
+        for (int i = 0; i < a_iters; ++i) {
+          const uint4 raw = *reinterpret_cast<const uint4*>(as + i * 1024);
           const uint32_t x0 = raw.x ^ 0x88888888u, x1 = raw.y ^ 0x88888888u;
           const uint32_t x2 = raw.z ^ 0x88888888u, x3 = raw.w ^ 0x88888888u;
-          uint8_t* dst = S.af8[(gblk + k) % F8] + (r >> 3) * 256 + (r & 7) * 16;
-          *reinterpret_cast<uint4*>(dst) =
+          *reinterpret_cast<uint4*>(ad + i * 512) =
               make_uint4(x0 & 0x0F0F0F0Fu, x1 & 0x0F0F0F0Fu, x2 & 0x0F0F0F0Fu, x3 & 0x0F0F0F0Fu);
-          *reinterpret_cast<uint4*>(dst + 128) = make_uint4((x0 >> 4) & 0x0F0F0F0Fu, (x1 >> 4) & 0x0F0F0F0Fu,
-                                                            (x2 >> 4) & 0x0F0F0F0Fu, (x3 >> 4) & 0x0F0F0F0Fu);
+          *reinterpret_cast<uint4*>(ad + i * 512 + 128) = make_uint4(
+              (x0 >> 4) & 0x0F0F0F0Fu, (x1 >> 4) & 0x0F0F0F0Fu, (x2 >> 4) & 0x0F0F0F0Fu, (x3 >> 4) & 0x0F0F0F0Fu);
         }
       }
       fence_async_smem();
       __syncwarp();
       if (lane == 0) {
-        for (int k = 0; k < nbk; ++k) mbar_arrive(&S.f8_full[(gblk + k) % F8]);
+        for (int kk = 0; kk < nbk; ++kk) mbar_arrive(&S.f8_full[(gblk + kk) % F8]);
         mbar_arrive(&S.empty_raw[slot]);
       }
       gblk += nbk;
@@ -889,10 +899,15 @@ struct SkPlan {
   bool on;
   int64_t units;
   int grid;
-  size_t count_bytes;  // tickets, padded to 256 bytes
+  size_t count_bytes;  // the ticket region
   size_t ws_bytes;     // tickets + partials
 };
 constexpr int kSkFixupStages = 2;
+// The tickets sit in a fixed region at the start of the workspace, the same for
+// every shape, so that partials written for one shape never land on the tickets
+// of another when callers reuse one workspace across shapes.
+constexpr int64_t kSkMaxTiles = 32768;
+constexpr size_t kSkTicketBytes = static_cast<size_t>(kSkMaxTiles) * 8 * sizeof(uint32_t);  // 1 MiB
 constexpr size_t kSkPartBytes = size_t(8) * 1024 * sizeof(float4);  // one CTA segment: 8 warps x 32 x 32 float4
 
 SkPlan plan_stream_k(int64_t M, int64_t N, int64_t K) {
@@ -906,20 +921,43 @@ SkPlan plan_stream_k(int64_t M, int64_t N, int64_t K) {
   const int64_t U = tiles * nst;
   const int64_t G = U < sms ? U : sms;
   const int64_t sk_span = (U + G - 1) / G + kSkFixupStages;
-  if (G < 2 || 10 * sk_span >= 9 * dp_span) return pl;
+  if (G < 2 || tiles > kSkMaxTiles || 10 * sk_span >= 9 * dp_span) return pl;
   pl.on = true;
   pl.units = U;
   pl.grid = static_cast<int>(G);
-  pl.count_bytes = (static_cast<size_t>(tiles) * 8 * sizeof(unsigned long long) + 255) & ~size_t(255);
+  pl.count_bytes = kSkTicketBytes;
   pl.ws_bytes = pl.count_bytes + 2 * static_cast<size_t>(G) * kSkPartBytes;
   return pl;
 }
 
-std::atomic<uint32_t> g_sk_epoch{0};
-
 }  // namespace
 
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) { return plan_stream_k(M, N, K).ws_bytes; }
+
+cudaError_t encode_2d_map(CUtensorMap* m, CUtensorMapDataType dtype, const void* base, uint64_t inner, uint64_t rows,
+                          uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swizzle) {
+  auto fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {row_stride_bytes};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(m, dtype, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+int* device_error_word() {
+  static int* cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!cached[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_w4a4_device_error) != cudaSuccess) return nullptr;
+    cached[dev] = static_cast<int*>(p);
+  }
+  return cached[dev];
+}
 
 cudaError_t launch_gemm_tc(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums, int64_t N,
                            const uint8_t* a_codes, const float* a_scales, int64_t M, int64_t K, float* y, int64_t ldy,
@@ -936,12 +974,9 @@ cudaError_t launch_gemm_tc(const uint8_t* w_codes, const uint16_t* w_scales, con
   if (P) return launch_tc<true>(wmap, amap, a, grid, stream);
   const SkPlan pl = plan_stream_k(M, N, K);
   if (pl.on && ws && ws_bytes >= pl.ws_bytes) {
-    uint32_t ep = ++g_sk_epoch;
-    if (ep == 0) ep = ++g_sk_epoch;
     a.sk_units = pl.units;
-    a.sk_count = static_cast<unsigned long long*>(ws);
+    a.sk_count = static_cast<uint32_t*>(ws);
     a.sk_part = reinterpret_cast<float4*>(static_cast<uint8_t*>(ws) + pl.count_bytes);
-    a.sk_epoch = ep;
     grid = pl.grid;
   }
   return launch_tc<false>(wmap, amap, a, grid, stream);

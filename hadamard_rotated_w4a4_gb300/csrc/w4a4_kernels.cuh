@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "w4a4_device.cuh"
@@ -55,6 +56,12 @@ cudaError_t launch_gemm_tc_routed(const uint8_t* w_codes, const uint16_t* w_scal
 int routed_tile_tokens(int64_t npairs, int E);
 // Reads the GEMM kernels' device error word (bounded waits that gave up) and clears it.
 cudaError_t read_and_clear_device_error(int* value);
+// Device address of the error word the GEMM and activation kernels set when a
+// bounded wait gives up (nullptr on failure).
+int* device_error_word();
+// 2D tiled TMA descriptor over `rows` rows of `inner` elements.
+cudaError_t encode_2d_map(CUtensorMap* m, CUtensorMapDataType dtype, const void* base, uint64_t inner, uint64_t rows,
+                          uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swizzle);
 cudaError_t launch_gemm_id(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums, int E, int64_t N,
                            const uint8_t* a_codes, const float* a_scales, int64_t K, const int32_t* ids, int64_t M,
                            int top_k, int act_per_slot, float* y, const Routing& r, cudaStream_t stream);

@@ -172,8 +172,10 @@ w4a4_status w4a4_rotate_quantize_act(const float* x, int64_t M, int64_t K, int64
  * W4A4_ERR_MISMATCH.  The per-block integer partials are exact on the tensor
  * cores; the scale fold is fp32.
  *   ws  : optional device workspace (NULL, or w4a4_gemm_workspace_bytes(M, N,
- *         K) bytes or more, 16-byte aligned, all zero before its first use;
- *         the library leaves it valid for later calls).  With it, shapes whose
+ *         K) bytes or more, 16-byte aligned, all zero before its first use).
+ *         Its first MiB holds arrival counters that every call leaves at zero
+ *         again (CUDA-graph replays included), so one workspace serves any
+ *         sequence of shapes; after W4A4_ERR_TIMEOUT, zero it before reuse.  With it, shapes whose
  *         tiles would leave SMs idle in the last wave run a stream-K schedule:
  *         the K work of all tiles is split evenly over the SMs and a tile cut
  *         between CTAs is summed in a fixed order, so the result does not depend

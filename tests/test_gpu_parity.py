@@ -239,6 +239,36 @@ def test_stream_k_matches_oracle_and_is_deterministic(dev, M, K, N):
     assert_close(y_whole[ridx].cpu().numpy(), R)
 
 
+def test_stream_k_under_cuda_graph_replay(dev):
+    """A captured split-schedule GEMM replays correctly: the tickets return to zero after every launch."""
+    M, K, N = 300, 1024, 640
+    d = si.random_dense(M, K, N, seed=77)
+    wq, aq = _gpu_pair(dev, d)
+    ws = torch.zeros(w4.w4a4_gemm_workspace_bytes(M, N, K), dtype=torch.uint8, device=dev)
+    y = torch.empty(M, N, dtype=torch.float32, device=dev)
+    w4.w4a4_gemm(wq, aq, y=y, ws=ws)  # set-up outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            w4.w4a4_gemm(wq, aq, y=y, ws=ws, stream=s)
+    first = None
+    for _ in range(3):
+        y.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        cur = y.clone()
+        if first is None:
+            first = cur
+        assert torch.equal(cur, first)
+    w4.w4a4_check()
+    R = oracle.w4a4_matmul(oracle.pack_weights(d["w_bf16"]), oracle.quantize_activations(d["x"]))
+    assert_close(first.cpu().numpy(), R)
+    # the tickets (10 tiles x 8 warps x 4 bytes at the start of the workspace) are back at zero
+    assert torch.count_nonzero(ws[:1 << 20]).item() == 0
+
+
 def test_stream_k_workspace_reused_across_shapes(dev):
     shapes = [(300, 1024, 640), (64, 2048, 128), (300, 1024, 640)]
     ws = torch.zeros(max(w4.w4a4_gemm_workspace_bytes(M, N, K) for M, K, N in shapes), dtype=torch.uint8, device=dev)
