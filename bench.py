@@ -200,6 +200,70 @@ GEMM_SOURCES = ("gemm_tc.cu", "w4a4_device.cuh", "w4a4_kernels.cuh")
 ACT_SOURCES = ("act_quant.cu", "w4a4_device.cuh", "w4a4_kernels.cuh")
 
 
+def graph_time(fn, n: int = 20, reps: int = 5) -> float:
+    """Device milliseconds per call of fn(i, stream): n calls captured in one CUDA graph,
+    the graph replayed `reps` times between CUDA events on the capturing stream (best kept).
+
+    Timing a replayed graph measures the kernels themselves: a Python loop of short
+    launches would time the host's launch rate instead.
+    """
+    import torch
+    fn(0, torch.cuda.current_stream())  # any one-time set-up happens outside the capture
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for i in range(n):
+                fn(i, s)
+    with torch.cuda.stream(s):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    best = float("inf")
+    for _ in range(reps):
+        with torch.cuda.stream(s):
+            e0.record(s)
+            g.replay()
+            e1.record(s)
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1) / n)
+    return best
+
+
+def moe_extra(dev) -> dict:
+    """The expert-routed workload (1024 tokens, 128 experts, top-8): activation
+    quantisation and w4a4_gemm_id for gate/up (K2048 -> N768, activations per
+    token) and down (K768 -> N2048, activations per token-slot), device time."""
+    import torch
+    import hadamard_rotated_w4a4_gb300 as w4
+    mi = si.moe_inputs("c4")
+    s = mi["shape"]
+    ids = torch.from_numpy(np.ascontiguousarray(mi["ids"], dtype=np.int32)).to(dev)
+    out = {"workload": s.what}
+    for name, wkey, xkey, N, per_slot in (("gate", "wg_bf16", "x_gate", s.N_gate, False),
+                                          ("down", "wd_bf16", "x_down", s.N_down, True)):
+        w = torch.from_numpy(mi[wkey].reshape(s.E * N, -1).view(np.int16)).to(dev).view(torch.bfloat16)
+        wq = w4.h32_q4_0_pack_weights(w)
+        del w
+        x = torch.from_numpy(mi[xkey]).to(dev)
+        K = x.shape[1]
+        aq = w4.alloc_act4(x.shape[0], K, dev)
+        ws = torch.zeros(w4.w4a4_gemm_id_workspace_bytes(s.M, s.top_k, s.E, K), dtype=torch.uint8, device=dev)
+        y = torch.empty(s.M, s.top_k, N, dtype=torch.float32, device=dev)
+        act_ms = graph_time(lambda i, st: w4.w4a4_rotate_quantize_act(x, out=aq, stream=st))
+        gid_ms = graph_time(lambda i, st: w4.w4a4_gemm_id(wq, s.E, aq, ids, s.top_k, per_slot, y=y, ws=ws, stream=st))
+        ops = 2.0 * s.M * s.top_k * N * K
+        out[name] = {"K": K, "N": N, "act_ms": act_ms, "gemm_id_ms": gid_ms,
+                     "gemm_id_effective_tops": ops / (gid_ms * 1e-3) / 1e12,
+                     "weight_mb": s.E * N * K * 0.5625 / 1e6}
+        w4.w4a4_gemm_id_status(ws)
+        del wq, x, aq, ws, y
+    del mi
+    torch.cuda.empty_cache()
+    return out
+
+
 def prefill_proxy(dev, stream, nrep: int) -> dict:
     """GEMM-only prefill proxy for one dense layer at 512 tokens.
 
@@ -213,18 +277,6 @@ def prefill_proxy(dev, stream, nrep: int) -> dict:
     """
     import torch
     import hadamard_rotated_w4a4_gb300 as w4
-
-    def timed(fn, n):
-        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        for i in range(3):
-            fn(i)
-        torch.cuda.synchronize()
-        a0.record(stream)
-        for i in range(n):
-            fn(i)
-        a1.record(stream)
-        torch.cuda.synchronize()
-        return a0.elapsed_time(a1) / n
 
     out = {}
     for name, rows in (("c1", 512), ("c2", 512), ("c3", 512)):
@@ -247,11 +299,14 @@ def prefill_proxy(dev, stream, nrep: int) -> dict:
         del wq0
         for s_ in sets:
             w4.w4a4_rotate_quantize_act(s_[1], out=s_[2])
+        gws = torch.zeros(max(16, w4.w4a4_gemm_workspace_bytes(rows, N, K)), dtype=torch.uint8, device=dev)
         out[name] = {
-            "act_ms": timed(lambda i: w4.w4a4_rotate_quantize_act(sets[i % nsets][1], out=sets[i % nsets][2]), nrep),
-            "gemm_ms": timed(lambda i: w4.w4a4_gemm(sets[i % nsets][0], sets[i % nsets][2], y=sets[i % nsets][3]),
-                             nrep),
+            "act_ms": graph_time(lambda i, st: w4.w4a4_rotate_quantize_act(sets[i % nsets][1], out=sets[i % nsets][2],
+                                                                            stream=st), nrep),
+            "gemm_ms": graph_time(lambda i, st: w4.w4a4_gemm(sets[i % nsets][0], sets[i % nsets][2],
+                                                             y=sets[i % nsets][3], ws=gws, stream=st), nrep),
         }
+        del gws
         del sets
         torch.cuda.empty_cache()
     layer_ms = (4 * out["c1"]["gemm_ms"] + 2 * out["c2"]["gemm_ms"] + out["c3"]["gemm_ms"]
@@ -324,10 +379,12 @@ def run_ours(args, shape) -> dict | None:
     del w_dev
     torch.cuda.synchronize()
 
+    gws = torch.zeros(max(16, w4.w4a4_gemm_workspace_bytes(M, N, K)), dtype=torch.uint8, device=dev)
+
     def step(i):
         wq, xs, aq, y = sets[i % nsets]
         w4.w4a4_rotate_quantize_act(xs, out=aq)
-        w4.w4a4_gemm(wq, aq, y=y)
+        w4.w4a4_gemm(wq, aq, y=y, ws=gws)
 
     for i in range(args.warmup):
         step(i)
@@ -349,22 +406,13 @@ def run_ours(args, shape) -> dict | None:
 
     # per-kernel device time: each kernel back to back over the same rotating input sets,
     # events only around the loops (on the launching stream)
-    def time_loop(fn, n):
-        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        for i in range(3):
-            fn(i)
-        torch.cuda.synchronize()
-        a0.record(stream)
-        for i in range(n):
-            fn(i)
-        a1.record(stream)
-        torch.cuda.synchronize()
-        return a0.elapsed_time(a1) / n
-
-    act_avg = time_loop(lambda i: w4.w4a4_rotate_quantize_act(sets[i % nsets][1], out=sets[i % nsets][2]),
-                        args.steps)
-    gemm_avg = time_loop(lambda i: w4.w4a4_gemm(sets[i % nsets][0], sets[i % nsets][2], y=sets[i % nsets][3]),
-                         args.steps)
+    # per-kernel device time: each kernel alone, replayed from a CUDA graph over the
+    # same rotating input sets (events on the replaying stream)
+    nk = max(nsets, 16)
+    act_avg = graph_time(lambda i, st: w4.w4a4_rotate_quantize_act(sets[i % nsets][1], out=sets[i % nsets][2],
+                                                                    stream=st), nk)
+    gemm_avg = graph_time(lambda i, st: w4.w4a4_gemm(sets[i % nsets][0], sets[i % nsets][2], y=sets[i % nsets][3],
+                                                     ws=gws, stream=st), nk)
     w4.w4a4_check()
     if world > 1:
         tt = torch.tensor([total_ms], device=dev)
@@ -382,7 +430,7 @@ def run_ours(args, shape) -> dict | None:
     def e2e_step():
         xs_e.copy_(x_host, non_blocking=True)
         w4.w4a4_rotate_quantize_act(xs_e, out=aq_e)
-        w4.w4a4_gemm(wq_e, aq_e, y=y_e)
+        w4.w4a4_gemm(wq_e, aq_e, y=y_e, ws=gws)
         y_host.copy_(y_e, non_blocking=True)
 
     for _ in range(args.warmup):
@@ -405,8 +453,10 @@ def run_ours(args, shape) -> dict | None:
     peaks = read_peaks()
     probes = run_probes() if not args.no_probes else {}
     B = K // 32
-    # GEMM roofline: the per-block scale fold on the fp32 pipe (2 flops per (m, n, block))
-    fold_flops = 2.0 * M * N * B
+    # GEMM roofline: the per-block scale fold on the fp32 pipe.  Per (m, n, block) it
+    # takes two fp32-pipe operations (the product by d_w, with the offset correction
+    # folded in, and the fused multiply-add with d_a): 4 flops in the FMA convention.
+    fold_flops = 4.0 * M * N * B
     sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
     fp32_peak = sm_count * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
     gemm_traffic, gemm_traffic_src = profiled_traffic(f"gemm_tc_{shape.name}.md", GEMM_SOURCES)
@@ -427,7 +477,10 @@ def run_ours(args, shape) -> dict | None:
     int8_peak = probes.get("int8_mma_sync_tops") if probes else None
     proxy = None
     if not args.no_proxy and world == 1:
-        proxy = prefill_proxy(dev, stream, max(10, args.steps // 2))
+        proxy = prefill_proxy(dev, stream, 16)
+    moe = None
+    if not args.no_moe and world == 1:
+        moe = moe_extra(dev)
 
     cpu = None
     if not args.no_cpu_baseline:
@@ -452,6 +505,7 @@ def run_ours(args, shape) -> dict | None:
         "gemm_effective_tops": eff_tops_gemm,
         "pct_int8_peak": (eff_tops_gemm / int8_peak) if int8_peak else None,
         "prefill_tok_s_proxy": proxy,
+        "moe": moe,
         "kernel_ms": {"act_rotate_quantize": act_avg, "gemm": gemm_avg},
         "pack_weights_ms": pack_ms,
         "probes": probes,
@@ -477,6 +531,7 @@ def main():
     ap.add_argument("--no-probes", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-proxy", action="store_true", help="skip the per-layer prefill proxy")
+    ap.add_argument("--no-moe", action="store_true", help="skip the expert-routed workload timing")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
