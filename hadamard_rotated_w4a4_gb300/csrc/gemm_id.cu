@@ -93,12 +93,17 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint8_t* __restr
 
 }  // namespace
 
+#ifndef W4A4_ROUTED_TILE_MULT
+#define W4A4_ROUTED_TILE_MULT 2
+#endif
 int routed_tile_tokens(int64_t npairs, int E) {
-  // about one tile per expert: the mean number of rows an expert receives, in 32s
-  const int64_t mean = (npairs + E - 1) / E;
+  // about one tile per expert: twice the mean number of rows an expert receives,
+  // in 32s, so that an expert a little above the mean still takes one tile (its
+  // weights are converted once per weight tile, not twice)
+  const int64_t mean = W4A4_ROUTED_TILE_MULT * ((npairs + E - 1) / E);
   int64_t t = (mean + 31) & ~int64_t(31);
   if (t < 32) t = 32;
-  if (t > 256) t = 256;
+  if (t > kRoutedTileMax) t = kRoutedTileMax;
   return static_cast<int>(t);
 }
 

@@ -55,7 +55,9 @@ constexpr int kThreads = 128 + 32 * kWorkerWarps;
 constexpr int kRegsLow = 64;    // warpgroup 0 after setmaxnreg.dec
 constexpr int kRegsHigh = 216;  // warpgroups 1-2 after setmaxnreg.inc
 constexpr int TW = 128;         // weight rows per tile
-constexpr int TT = 256;         // token columns per tile (max)
+// The token tile is a template parameter TTM (256 or 128 token columns).  A
+// tile of TTM columns has 512 / TTM accumulator buffers in TMEM, and each worker
+// thread holds TTM / 2 accumulators (chunks h + 2i of 32 columns, i < TTM / 64).
 constexpr int KB = 4;           // 32-blocks per stage (64 code bytes per row)
 static_assert(KB == 4, "the vector scale loads take 4 blocks per stage");
 #ifndef W4A4_RAW_STAGES
@@ -67,7 +69,8 @@ static_assert(KB == 4, "the vector scale loads take 4 blocks per stage");
 constexpr int RAW = W4A4_RAW_STAGES;  // stages of raw codes in flight
 constexpr int F8 = W4A4_F8_BUFFERS;   // fp8 operand buffers (two stages)
 constexpr int WF8 = TW * 32 + 32;  // buffer strides padded by 32 bytes: the converters'
-constexpr int AF8 = TT * 32 + 32;  // 16-byte stores to 4 buffers hit distinct banks
+template <int TTM>
+constexpr int af8_stride() { return TTM * 32 + 32; }  // 16-byte stores to 4 buffers hit distinct banks
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kTimeoutNs = 1000000000ull;  // 1 s
 #ifndef W4A4_WAIT_HINT_NS
@@ -78,28 +81,35 @@ constexpr uint64_t kTimeoutNs = 1000000000ull;  // 1 s
 constexpr uint32_t kWaitHintNs = W4A4_WAIT_HINT_NS;
 
 
+template <int TTM>
 struct __align__(128) Smem {
+  static constexpr int TT = TTM;
+  static constexpr int NBUF = 512 / TTM;  // TMEM accumulator buffers
+  // Stage-scale slots.  Stage s + 1's scales are published during block kb = 2
+  // of stage s into slot (s + 1) % 3, last read by stage s - 2; that block's MMA
+  // needed every warp to release block 4s + 2 - NBUF >= 4s - 2, past stage s - 2.
+  static constexpr int NSC = 3;
   uint8_t wraw[RAW][TW * KB * 16];  // TMA box: 128 rows x 64 bytes
-  uint8_t araw[RAW][TT * KB * 16];  // TMA box: tt rows x 64 bytes
+  uint8_t araw[RAW][TTM * KB * 16];  // TMA box: tt rows x 64 bytes
   uint8_t wf8[F8][WF8];
-  uint8_t af8[F8][AF8];
-  float sda[2][KB][TT];              // d_a per stage, block-major
-  float sdw[2][KB][TW];              // d_w * 2^18
-  float scorr[2][KB][TW];            // -d_w * 8 S_w (exact)
+  uint8_t af8[F8][af8_stride<TTM>()];
+  float sda[NSC][KB][TTM];              // d_a per stage, block-major
+  float sdw[NSC][KB][TW];              // d_w * 2^18
+  float scorr[NSC][KB][TW];            // -d_w * 8 S_w (exact)
   uint64_t full_raw[RAW];
   uint64_t empty_raw[RAW];
   uint64_t f8_full[F8];
   uint64_t f8_empty[F8];   // the MMA has read the operand buffer
-  uint64_t tm_full[2];
-  uint64_t tm_empty[2];
-  uint64_t sc_ready[2];
+  uint64_t tm_full[NBUF];
+  uint64_t tm_empty[NBUF];
+  uint64_t sc_ready[NSC];
   uint64_t tile_done;      // every worker warp has finished its previous tile
   uint64_t mma_done;
   uint32_t tmem_base;
   volatile int abort;
 };
-constexpr size_t kSmemBytes = sizeof(Smem);
-static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA is at most 227 KB");
+static_assert(sizeof(Smem<256>) <= 227 * 1024, "shared memory per CTA is at most 227 KB");
+static_assert(sizeof(Smem<128>) <= 227 * 1024, "shared memory per CTA is at most 227 KB");
 
 struct TcArgs {
   const uint16_t* w_scales;
@@ -111,7 +121,7 @@ struct TcArgs {
   float* y;
   int64_t ldy;
   int32_t* P;
-  int tt;                 // token tile (multiple of 32, <= TT): the A box height
+  int tt;                 // token tile (multiple of 32, <= the kernel's TTM): the A box height
   const int32_t* perm;    // routed: gathered row -> pair index (the Y row)
   const int32_t* offsets;
   const int32_t* tile_off;
@@ -163,7 +173,8 @@ __device__ __forceinline__ bool mbar_try_sleep(uint64_t* b, uint32_t parity, uin
   return ok != 0;
 }
 // Bounded wait on phase `parity`; false if it (or another role) gave up.
-__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, Smem& S) {
+template <class SM>
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, SM& S) {
   if (mbar_try(b, parity)) return true;
   const uint64_t t0 = gtime();
   for (;;) {
@@ -225,6 +236,35 @@ __device__ __forceinline__ void tmem_wait(uint32_t (&r)[16]) {
                  "+r"(r[15])
                :
                : "memory");
+}
+// 32 consecutive TMEM columns of this thread's lane; asynchronous until a wait.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+// Ties 16 registers to a preceding wait (an empty volatile statement: volatile
+// statements keep their order, so no use of them moves above the wait).
+__device__ __forceinline__ void tie16(uint32_t* r) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15])
+               :
+               : "memory");
+}
+// Wait for this thread's TMEM loads into two 32-register buffers.
+__device__ __forceinline__ void tmem_wait32x2(uint32_t (&a)[32], uint32_t (&b)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+  tie16(a);
+  tie16(a + 16);
+  tie16(b);
+  tie16(b + 16);
 }
 // ------------------------------------------------------------------ tiles
 struct Tile {
@@ -355,12 +395,13 @@ __device__ __forceinline__ bool sk_arrive(const TcArgs& p, int64_t t, int nst, i
 // feature n).  Four float4 (16 columns) at a time: each contributor's four
 // loads are issued together, so one L2 round trip is paid per contributor and
 // group, not per value.
+template <int CPW>
 __device__ __forceinline__ void sk_finish(const TcArgs& p, int64_t t, int nst, int w, int lane, int h, int64_t m0,
                                           int ntok, int64_t n, bool n_ok) {
   const int64_t u_lo = t * nst;
   const int64_t c_lo = sk_cta_of_unit(p, u_lo), c_hi = sk_cta_of_unit(p, u_lo + nst - 1);
 #pragma unroll 1
-  for (int g = 0; g < 8; ++g) {
+  for (int g = 0; g < 2 * CPW; ++g) {
     float4 a[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) a[k] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -393,7 +434,8 @@ __device__ __forceinline__ void sk_finish(const TcArgs& p, int64_t t, int nst, i
 }
 
 // ------------------------------------------------------------------ roles
-__device__ void producer(const TcArgs& p, Smem& S, const CUtensorMap* wmap, const CUtensorMap* amap) {
+template <class SM>
+__device__ void producer(const TcArgs& p, SM& S, const CUtensorMap* wmap, const CUtensorMap* amap) {
   const int64_t B = p.K / 32;
   const int nst = static_cast<int>((B + KB - 1) / KB);
   const uint32_t bytes = static_cast<uint32_t>(KB * 16 * (TW + p.tt));  // full boxes, zero fill included
@@ -422,7 +464,8 @@ __device__ void producer(const TcArgs& p, Smem& S, const CUtensorMap* wmap, cons
   }
 }
 
-__device__ void mma_issuer(const TcArgs& p, Smem& S, uint32_t tmem) {
+template <class SM>
+__device__ void mma_issuer(const TcArgs& p, SM& S, uint32_t tmem) {
   const int64_t B = p.K / 32;
   const int nst = static_cast<int>((B + KB - 1) / KB);
   uint32_t gblk = 0;
@@ -434,11 +477,11 @@ __device__ void mma_issuer(const TcArgs& p, Smem& S, uint32_t tmem) {
     const int64_t b_end = static_cast<int64_t>(sg.s1) * KB < B ? static_cast<int64_t>(sg.s1) * KB : B;
     for (int64_t b = static_cast<int64_t>(sg.s0) * KB; b < b_end; ++b, ++gblk) {
       const int f = gblk % F8;
-      const int tb = gblk & 1;
+      const int tb = static_cast<int>(gblk % SM::NBUF);
       if (!mbar_wait(&S.f8_full[f], (gblk / F8) & 1, S)) goto done;
-      if (!mbar_wait(&S.tm_empty[tb], ((gblk >> 1) & 1) ^ 1, S)) goto done;
+      if (!mbar_wait(&S.tm_empty[tb], ((gblk / SM::NBUF) & 1) ^ 1, S)) goto done;
       tc_fence_after();
-      mma_f8(tmem + static_cast<uint32_t>(tb * TT), kmajor_desc(S.wf8[f]), kmajor_desc(S.af8[f]), idesc);
+      mma_f8(tmem + static_cast<uint32_t>(tb * SM::TT), kmajor_desc(S.wf8[f]), kmajor_desc(S.af8[f]), idesc);
       mma_commit(&S.tm_full[tb]);
       mma_commit(&S.f8_empty[f]);
     }
@@ -459,7 +502,8 @@ done:
 // core-matrix rows of its fp8 buffer (the buffers are padded so that the four
 // blocks' stores land in distinct banks).  Source and destination advance by
 // constant strides (16 rows = 1024 raw bytes = 512 fp8 bytes per half).
-__device__ void converters(const TcArgs& p, Smem& S) {
+template <class SM>
+__device__ void converters(const TcArgs& p, SM& S) {
   const int ct = threadIdx.x - 64;  // 0..63
   const int lane = threadIdx.x & 31;
   const int k = ct & 3;
@@ -523,8 +567,10 @@ __device__ void converters(const TcArgs& p, Smem& S) {
   }
 }
 
-template <bool PARTIALS>
-__device__ void workers(const TcArgs& p, Smem& S, uint32_t tmem) {
+template <bool PARTIALS, class SM>
+__device__ void workers(const TcArgs& p, SM& S, uint32_t tmem) {
+  constexpr int TT = SM::TT;
+  constexpr int CPW = TT / 64;  // 32-column chunks per worker warp: h + 2i, i < CPW
   const int wt = threadIdx.x - 128;  // 0..255
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;  // 4..11
@@ -585,7 +631,7 @@ __device__ void workers(const TcArgs& p, Smem& S, uint32_t tmem) {
 #pragma unroll
       for (int k = 0; k < KB; ++k) {
         const bool bok = s * KB + k < B;
-        S.sda[slot][k][wt] = (a_ok && bok) ? __uint_as_float(da[k]) : 0.f;
+        if (wt < TT) S.sda[slot][k][wt] = (a_ok && bok) ? __uint_as_float(da[k]) : 0.f;
         if (wt < TW) {
           const unsigned short dh = static_cast<unsigned short>(dwp[k >> 1] >> (16 * (k & 1)));
           const short sw = static_cast<short>(swp[k >> 1] >> (16 * (k & 1)));
@@ -598,20 +644,19 @@ __device__ void workers(const TcArgs& p, Smem& S, uint32_t tmem) {
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.sc_ready[slot]);
     };
-    float2 acc[4][16];  // column pairs (2j, 2j + 1) of chunk h + 2i
+    float2 acc[CPW][16];  // column pairs (2j, 2j + 1) of chunk h + 2i
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < CPW; ++i)
 #pragma unroll
       for (int j = 0; j < 16; ++j) acc[i][j] = make_float2(0.f, 0.f);
 
-    // Stage s's scales live in slot (gsc0 + s) & 1.  During stage s the registers
-    // hold stage s + 1's scales; they are published once block kb = 2 of stage s
-    // has its accumulator (the MMA of block b needs every warp to have released
-    // block b - 2, so every warp is past stage s - 1, the slot's previous user),
+    // Stage s's scales live in slot (gsc0 + s - s0) % NSC.  During stage s the
+    // registers hold stage s + 1's scales; they are published once block kb = 2
+    // of stage s has its accumulator (see Smem::NSC for why the slot is free),
     // then stage s + 2 is prefetched.  A stage's slot is waited for at kb = 0.
     const uint32_t gsc0 = gsc;
     load_scales(sg.s0);
-    publish_scales(gsc0 & 1, sg.s0);
+    publish_scales(static_cast<int>(gsc0 % SM::NSC), sg.s0);
     if (sg.s0 + 1 < sg.s1) load_scales(sg.s0 + 1);
 
     const int b_end = sg.s1 * KB < B ? sg.s1 * KB : B;
@@ -619,34 +664,58 @@ __device__ void workers(const TcArgs& p, Smem& S, uint32_t tmem) {
       const int s = b / KB;
       const int kb = b - s * KB;
       const uint32_t gs = gsc0 + static_cast<uint32_t>(s - sg.s0);
-      if (kb == 0 && !mbar_wait(&S.sc_ready[gs & 1], (gs >> 1) & 1, S)) return;
+      if (kb == 0 && !mbar_wait(&S.sc_ready[gs % SM::NSC], (gs / SM::NSC) & 1, S)) return;
       // ---- fold block b
-      const int tb = gfold & 1;
-      if (!mbar_wait(&S.tm_full[tb], (gfold >> 1) & 1, S)) return;
+      const int tb = static_cast<int>(gfold % SM::NBUF);
+      if (!mbar_wait(&S.tm_full[tb], (gfold / SM::NBUF) & 1, S)) return;
       tc_fence_after();
       if (kb == 2 && s + 1 < sg.s1) {
-        publish_scales((gs + 1) & 1, s + 1);
+        publish_scales(static_cast<int>((gs + 1) % SM::NSC), s + 1);
         if (s + 2 < sg.s1) load_scales(s + 2);
       }
-      const int slot = gs & 1;
+      const int slot = static_cast<int>(gs % SM::NSC);
       const float dw = S.sdw[slot][kb][n_in];
       const float corr = S.scorr[slot][kb][n_in];
       const float2 dw2 = make_float2(dw, dw);
       const float2 corr2 = make_float2(corr, corr);
       const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(tb * TT);
-      if (!PARTIALS && nchunks == TT / 32) {
-        // Full-width tile: straight-line fold, TMEM columns and d_a addresses at
-        // fixed offsets from this warp's base (chunk h + 2i, piece half).
+      if (!PARTIALS && TT == 128 && nchunks == TT / 32) {
+        // Full 128-column tile: this warp's two 32-column chunks h and h + 2 are
+        // loaded together (one TMEM round trip per block), then folded.
+        const uint32_t tw = tbase + static_cast<uint32_t>(h * 32);
+        const float* dab = &S.sda[slot][kb][h * 32];
+        uint32_t ra[32], rb[32];
+        tmem_ld32(tw, ra);
+        tmem_ld32(tw + 64u, rb);
+        tmem_wait32x2(ra, rb);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const uint32_t(&cur)[32] = i ? rb : ra;
+          const float4* da4 = reinterpret_cast<const float4*>(dab + 64 * i);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float4 d = da4[j];
+            const float2 t0 = __ffma2_rn(
+                make_float2(__uint_as_float(cur[4 * j + 0]), __uint_as_float(cur[4 * j + 1])), dw2, corr2);
+            const float2 t1 = __ffma2_rn(
+                make_float2(__uint_as_float(cur[4 * j + 2]), __uint_as_float(cur[4 * j + 3])), dw2, corr2);
+            acc[i][2 * j + 0] = __ffma2_rn(t0, make_float2(d.x, d.y), acc[i][2 * j + 0]);
+            acc[i][2 * j + 1] = __ffma2_rn(t1, make_float2(d.z, d.w), acc[i][2 * j + 1]);
+          }
+        }
+      } else if (!PARTIALS && TT == 256 && nchunks == TT / 32) {
+        // Full 256-column tile: straight-line fold, TMEM columns and d_a addresses
+        // at fixed offsets from this warp's base (chunk h + 2i, piece half).
         const uint32_t tw = tbase + static_cast<uint32_t>(h * 32);
         const float* dab = &S.sda[slot][kb][h * 32];
         uint32_t ra[16], rb[16];
         tmem_ld16(tw, ra);
         tmem_wait(ra);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < 2 * CPW; ++k) {
           uint32_t(&cur)[16] = (k & 1) ? rb : ra;
           uint32_t(&nxt)[16] = (k & 1) ? ra : rb;
-          if (k < 7) tmem_ld16(tw + static_cast<uint32_t>(64 * ((k + 1) >> 1) + 16 * ((k + 1) & 1)), nxt);
+          if (k < 2 * CPW - 1) tmem_ld16(tw + static_cast<uint32_t>(64 * ((k + 1) >> 1) + 16 * ((k + 1) & 1)), nxt);
           const int i = k >> 1, half = k & 1;
           const float4* da4 = reinterpret_cast<const float4*>(dab + 64 * i + 16 * half);
 #pragma unroll
@@ -660,17 +729,17 @@ __device__ void workers(const TcArgs& p, Smem& S, uint32_t tmem) {
             acc[i][o + 0] = __ffma2_rn(t0, make_float2(d.x, d.y), acc[i][o + 0]);
             acc[i][o + 1] = __ffma2_rn(t1, make_float2(d.z, d.w), acc[i][o + 1]);
           }
-          if (k < 7) tmem_wait(nxt);
+          if (k < 2 * CPW - 1) tmem_wait(nxt);
         }
       } else {
-        // This warp's 16-column pieces: k = 0..7 -> chunk h + 2 (k / 2), half k % 2.
+        // This warp's 16-column pieces: k -> chunk h + 2 (k / 2), half k % 2.
         // The load of piece k + 1 is in flight while piece k is folded.
         const int npieces = 2 * ((nchunks - h + 1) / 2);
         uint32_t ra[16], rb[16];
         tmem_ld16(tbase + static_cast<uint32_t>(h * 32), ra);
         tmem_wait(ra);
   #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < 2 * CPW; ++k) {
           if (k < npieces) {
             uint32_t(&cur)[16] = (k & 1) ? rb : ra;
             uint32_t(&nxt)[16] = (k & 1) ? ra : rb;
@@ -723,17 +792,17 @@ __device__ void workers(const TcArgs& p, Smem& S, uint32_t tmem) {
       if (split) {
         float4* mine = sk_slot(p, blockIdx.x, sg.first, warp - 4, lane);
 #pragma unroll
-        for (int qq = 0; qq < 32; ++qq) {
+        for (int qq = 0; qq < 8 * CPW; ++qq) {
           const int i = qq >> 3, j = 2 * (qq & 7);
           __stcg(mine + qq * 32, make_float4(acc[i][j].x, acc[i][j].y, acc[i][j + 1].x, acc[i][j + 1].y));
         }
         if (sk_arrive(p, sg.t, nst, warp - 4, lane))
-          sk_finish(p, sg.t, nst, warp - 4, lane, h, T.m0, T.ntok, T.n0 + n_in, n_in < T.rows_w);
+          sk_finish<CPW>(p, sg.t, nst, warp - 4, lane, h, T.m0, T.ntok, T.n0 + n_in, n_in < T.rows_w);
       }
       if (!split && n_in < T.rows_w) {
         const int64_t n = T.n0 + n_in;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < CPW; ++i) {
           const int c = h + 2 * i;
           if (c < nchunks) {
 #pragma unroll
@@ -758,15 +827,16 @@ __device__ void workers(const TcArgs& p, Smem& S, uint32_t tmem) {
   }
 }
 
-template <bool PARTIALS>
+template <bool PARTIALS, int TTM>
 __global__ void __launch_bounds__(kThreads, 1)
     w4a4_gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap amap,
                         const TcArgs p) {
+  using SmemT = Smem<TTM>;
   // Smem is taken straight from the __shared__ array (no integer round trip), so
   // the compiler keeps every access in the shared address space (LDS/STS).  The
   // operands need 16-byte alignment (no swizzle), the TMA boxes 128 bytes.
   extern __shared__ __align__(1024) uint8_t smem_dyn[];
-  Smem& S = *reinterpret_cast<Smem*>(smem_dyn);
+  SmemT& S = *reinterpret_cast<SmemT*>(smem_dyn);
   const int warp = threadIdx.x >> 5;
   if ((static_cast<uint32_t>(__cvta_generic_to_shared(smem_dyn)) & 127u) != 0) {  // never expected
     if (threadIdx.x == 0) atomicOr(&g_w4a4_device_error, 2);
@@ -782,11 +852,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&S.f8_full[i], kConvWarps);
       mbar_init(&S.f8_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < SmemT::NBUF; ++i) {
       mbar_init(&S.tm_full[i], 1);
       mbar_init(&S.tm_empty[i], kWorkerWarps);
-      mbar_init(&S.sc_ready[i], kWorkerWarps);
     }
+    for (int i = 0; i < SmemT::NSC; ++i) mbar_init(&S.sc_ready[i], kWorkerWarps);
     mbar_init(&S.tile_done, kWorkerWarps);
     mbar_init(&S.mma_done, 1);
     S.abort = 0;
@@ -857,10 +927,11 @@ cudaError_t codes_map(CUtensorMap* m, const uint8_t* codes, int64_t rows, int64_
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <bool PARTIALS>
+template <bool PARTIALS, int TTM>
 cudaError_t launch_tc(const CUtensorMap& wmap, const CUtensorMap& amap, const TcArgs& a, int64_t max_tiles,
                       cudaStream_t stream) {
-  auto kern = w4a4_gemm_tc_kernel<PARTIALS>;
+  auto kern = w4a4_gemm_tc_kernel<PARTIALS, TTM>;
+  constexpr size_t kSmemBytes = sizeof(Smem<TTM>);
   static bool configured[64] = {};
   static int regs_ok[64] = {};
   int dev = 0;
@@ -885,9 +956,15 @@ cudaError_t launch_tc(const CUtensorMap& wmap, const CUtensorMap& amap, const Tc
   return cudaGetLastError();
 }
 
-int token_tile(int64_t M) {
+// Token tile of the dense product (the kernel instance's TTM).
+#ifndef W4A4_DENSE_TT
+#define W4A4_DENSE_TT 256
+#endif
+constexpr int kDenseTT = W4A4_DENSE_TT;
+
+int token_tile(int64_t M, int ttm) {
   const int64_t r = (M + 31) & ~int64_t(31);
-  return static_cast<int>(r < TT ? r : TT);
+  return static_cast<int>(r < ttm ? r : ttm);
 }
 
 // Stream-K or one tile per CTA pass.  Whole tiles leave SMs idle in the last
@@ -913,7 +990,7 @@ constexpr size_t kSkPartBytes = size_t(8) * 1024 * sizeof(float4);  // one CTA s
 SkPlan plan_stream_k(int64_t M, int64_t N, int64_t K) {
   SkPlan pl{};
   if (M <= 0 || N <= 0 || K <= 0) return pl;
-  const int64_t tt = token_tile(M);
+  const int64_t tt = token_tile(M, kDenseTT);
   const int64_t tiles = ((N + TW - 1) / TW) * ((M + tt - 1) / tt);
   const int64_t nst = (K / 32 + KB - 1) / KB;
   const int64_t sms = num_sms();
@@ -965,13 +1042,13 @@ cudaError_t launch_gemm_tc(const uint8_t* w_codes, const uint16_t* w_scales, con
   TcArgs a{};
   a.w_scales = w_scales; a.w_sums = w_sums; a.a_scales = a_scales;
   a.M = M; a.N = N; a.K = K; a.y = y; a.ldy = ldy; a.P = P;
-  a.tt = token_tile(M);
+  a.tt = token_tile(M, P ? 256 : kDenseTT);
   CUtensorMap wmap, amap;
   cudaError_t e = codes_map(&wmap, w_codes, N, K, TW);
   if (e == cudaSuccess) e = codes_map(&amap, a_codes, M, K, a.tt);
   if (e != cudaSuccess) return e;
   int64_t grid = ((N + TW - 1) / TW) * ((M + a.tt - 1) / a.tt);
-  if (P) return launch_tc<true>(wmap, amap, a, grid, stream);
+  if (P) return launch_tc<true, 256>(wmap, amap, a, grid, stream);
   const SkPlan pl = plan_stream_k(M, N, K);
   if (pl.on && ws && ws_bytes >= pl.ws_bytes) {
     a.sk_units = pl.units;
@@ -979,7 +1056,7 @@ cudaError_t launch_gemm_tc(const uint8_t* w_codes, const uint16_t* w_scales, con
     a.sk_part = reinterpret_cast<float4*>(static_cast<uint8_t*>(ws) + pl.count_bytes);
     grid = pl.grid;
   }
-  return launch_tc<false>(wmap, amap, a, grid, stream);
+  return launch_tc<false, kDenseTT>(wmap, amap, a, grid, stream);
 }
 
 cudaError_t launch_gemm_tc_routed(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums, int E,
@@ -995,7 +1072,7 @@ cudaError_t launch_gemm_tc_routed(const uint8_t* w_codes, const uint16_t* w_scal
   if (e == cudaSuccess) e = codes_map(&amap, g_codes, npairs, K, a.tt);
   if (e != cudaSuccess) return e;
   const int64_t max_tiles = (npairs / tile_tokens + E) * ((N + TW - 1) / TW);
-  return launch_tc<false>(wmap, amap, a, max_tiles, stream);
+  return launch_tc<false, kRoutedTileMax>(wmap, amap, a, max_tiles, stream);
 }
 
 cudaError_t read_and_clear_device_error(int* value) {

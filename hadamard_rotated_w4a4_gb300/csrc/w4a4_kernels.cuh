@@ -53,6 +53,8 @@ cudaError_t launch_gemm_tc_routed(const uint8_t* w_codes, const uint16_t* w_scal
                                   const uint8_t* g_codes, const float* g_scales, int64_t K, int64_t npairs,
                                   int tile_tokens, float* y, const Routing& r, cudaStream_t stream);
 // Token rows per routed tile for a MUL_MAT_ID problem (multiple of 32, <= 256).
+// Largest token tile of the routed product (the GEMM instance it launches).
+constexpr int kRoutedTileMax = 128;
 int routed_tile_tokens(int64_t npairs, int E);
 // Reads the GEMM kernels' device error word (bounded waits that gave up) and clears it.
 cudaError_t read_and_clear_device_error(int* value);
