@@ -49,11 +49,7 @@ __device__ int g_w4a4_device_error;
 
 namespace {
 
-constexpr int kWorkerWarps = 8;
-constexpr int kConvWarps = 2;
-constexpr int kThreads = 128 + 32 * kWorkerWarps;
-constexpr int kRegsLow = 64;    // warpgroup 0 after setmaxnreg.dec
-constexpr int kRegsHigh = 216;  // warpgroups 1-2 after setmaxnreg.inc
+constexpr int kWorkerWarps = 8;  // warps 4-11, warpgroups 1-2
 constexpr int TW = 128;         // weight rows per tile
 // The token tile is a template parameter TTM (256 or 128 token columns).  A
 // tile of TTM columns has 512 / TTM accumulator buffers in TMEM, and each worker
@@ -67,7 +63,6 @@ static_assert(KB == 4, "the vector scale loads take 4 blocks per stage");
 #define W4A4_F8_BUFFERS 8
 #endif
 constexpr int RAW = W4A4_RAW_STAGES;  // stages of raw codes in flight
-constexpr int F8 = W4A4_F8_BUFFERS;   // fp8 operand buffers (two stages)
 constexpr int WF8 = TW * 32 + 32;  // buffer strides padded by 32 bytes: the converters'
 template <int TTM>
 constexpr int af8_stride() { return TTM * 32 + 32; }  // 16-byte stores to 4 buffers hit distinct banks
@@ -81,10 +76,21 @@ constexpr uint64_t kTimeoutNs = 1000000000ull;  // 1 s
 constexpr uint32_t kWaitHintNs = W4A4_WAIT_HINT_NS;
 
 
+// Warp roles by token tile.  Warp 0 produces (TMA), warp 1 issues the MMAs,
+// warps 4-11 fold.  The 256-column instance has two converter warps (2-3) and
+// 384 threads; the 128-column instance, whose workers need fewer registers,
+// adds warpgroup 3 as four more converter warps (512 threads) and a third fp8
+// stage.  Registers after setmaxnreg: 128 x 64 + 256 x 216 <= 168 x 384, and
+// 256 x 56 + 256 x 200 = 128 x 512.
 template <int TTM>
 struct __align__(128) Smem {
   static constexpr int TT = TTM;
   static constexpr int NBUF = 512 / TTM;  // TMEM accumulator buffers
+  static constexpr int CONV = TTM == 256 ? 2 : 6;                   // converter warps
+  static constexpr int THREADS = TTM == 256 ? 384 : 512;
+  static constexpr int REGS_LOW = TTM == 256 ? 64 : 56;             // warpgroups 0 and 3
+  static constexpr int REGS_HIGH = TTM == 256 ? 216 : 200;          // warpgroups 1-2
+  static constexpr int F8 = TTM == 256 ? W4A4_F8_BUFFERS : 12;      // fp8 operand buffers
   // Stage-scale slots.  Stage s + 1's scales are published during block kb = 2
   // of stage s into slot (s + 1) % 3, last read by stage s - 2; that block's MMA
   // needed every warp to release block 4s + 2 - NBUF >= 4s - 2, past stage s - 2.
@@ -476,9 +482,9 @@ __device__ void mma_issuer(const TcArgs& p, SM& S, uint32_t tmem) {
     const uint32_t idesc = f8_idesc(T.nmma);
     const int64_t b_end = static_cast<int64_t>(sg.s1) * KB < B ? static_cast<int64_t>(sg.s1) * KB : B;
     for (int64_t b = static_cast<int64_t>(sg.s0) * KB; b < b_end; ++b, ++gblk) {
-      const int f = gblk % F8;
+      const int f = gblk % SM::F8;
       const int tb = static_cast<int>(gblk % SM::NBUF);
-      if (!mbar_wait(&S.f8_full[f], (gblk / F8) & 1, S)) goto done;
+      if (!mbar_wait(&S.f8_full[f], (gblk / SM::F8) & 1, S)) goto done;
       if (!mbar_wait(&S.tm_empty[tb], ((gblk / SM::NBUF) & 1) ^ 1, S)) goto done;
       tc_fence_after();
       mma_f8(tmem + static_cast<uint32_t>(tb * SM::TT), kmajor_desc(S.wf8[f]), kmajor_desc(S.af8[f]), idesc);
@@ -504,7 +510,10 @@ done:
 // constant strides (16 rows = 1024 raw bytes = 512 fp8 bytes per half).
 template <class SM>
 __device__ void converters(const TcArgs& p, SM& S) {
-  const int ct = threadIdx.x - 64;  // 0..63
+  constexpr int F8 = SM::F8;
+  constexpr int RS = 8 * SM::CONV;  // rows per pass (a multiple of 8)
+  // converter threads: warps 2-3, then warps 12-15 where present
+  const int ct = threadIdx.x < 128 ? threadIdx.x - 64 : 64 + threadIdx.x - 384;
   const int lane = threadIdx.x & 31;
   const int k = ct & 3;
   const int r0 = ct >> 2;
@@ -517,7 +526,7 @@ __device__ void converters(const TcArgs& p, SM& S) {
   Seg sg;
   while (seg_next(p, nst, si, sg)) {
     const Tile T = decode_tile(p, sg.t);
-    const int a_iters = T.nmma / 16;
+    const int a_iters = (T.nmma - r0 + RS - 1) / RS;
     for (int s = sg.s0; s < sg.s1; ++s, ++gstage) {
       const int nbk = static_cast<int>(B - s * KB < KB ? B - s * KB : KB);
       const int slot = gstage % RAW;
@@ -532,27 +541,27 @@ __device__ void converters(const TcArgs& p, SM& S) {
         const uint8_t* ws = S.wraw[slot] + src_off;
         uint8_t* wd = S.wf8[f] + dst_off;
 #pragma unroll 4
-        for (int i = 0; i < TW / 16; ++i) {
-          const uint4 raw = *reinterpret_cast<const uint4*>(ws + i * 1024);
+        for (int i = 0; i < (TW - r0 + RS - 1) / RS; ++i) {
+          const uint4 raw = *reinterpret_cast<const uint4*>(ws + i * RS * 64);
           uint32_t l0, h0, l1, h1, l2, h2, l3, h3;
           q4_0_word_to_e4m3(raw.x, l0, h0);
           q4_0_word_to_e4m3(raw.y, l1, h1);
           q4_0_word_to_e4m3(raw.z, l2, h2);
           q4_0_word_to_e4m3(raw.w, l3, h3);
-          *reinterpret_cast<uint4*>(wd + i * 512) = make_uint4(l0, l1, l2, l3);
-          *reinterpret_cast<uint4*>(wd + i * 512 + 128) = make_uint4(h0, h1, h2, h3);
+          *reinterpret_cast<uint4*>(wd + i * RS * 32) = make_uint4(l0, l1, l2, l3);
+          *reinterpret_cast<uint4*>(wd + i * RS * 32 + 128) = make_uint4(h0, h1, h2, h3);
         }
         // activations: nmma rows; the offset codes u = a + 8 are the e4m3 bytes
         const uint8_t* as = S.araw[slot] + src_off;
         uint8_t* ad = S.af8[f] + dst_off;
 #pragma unroll 4
         for (int i = 0; i < a_iters; ++i) {
-          const uint4 raw = *reinterpret_cast<const uint4*>(as + i * 1024);
+          const uint4 raw = *reinterpret_cast<const uint4*>(as + i * RS * 64);
           const uint32_t x0 = raw.x ^ 0x88888888u, x1 = raw.y ^ 0x88888888u;
           const uint32_t x2 = raw.z ^ 0x88888888u, x3 = raw.w ^ 0x88888888u;
-          *reinterpret_cast<uint4*>(ad + i * 512) =
+          *reinterpret_cast<uint4*>(ad + i * RS * 32) =
               make_uint4(x0 & 0x0F0F0F0Fu, x1 & 0x0F0F0F0Fu, x2 & 0x0F0F0F0Fu, x3 & 0x0F0F0F0Fu);
-          *reinterpret_cast<uint4*>(ad + i * 512 + 128) = make_uint4(
+          *reinterpret_cast<uint4*>(ad + i * RS * 32 + 128) = make_uint4(
               (x0 >> 4) & 0x0F0F0F0Fu, (x1 >> 4) & 0x0F0F0F0Fu, (x2 >> 4) & 0x0F0F0F0Fu, (x3 >> 4) & 0x0F0F0F0Fu);
         }
       }
@@ -679,17 +688,21 @@ __device__ void workers(const TcArgs& p, SM& S, uint32_t tmem) {
       const float2 dw2 = make_float2(dw, dw);
       const float2 corr2 = make_float2(corr, corr);
       const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(tb * TT);
-      if (!PARTIALS && TT == 128 && nchunks == TT / 32) {
-        // Full 128-column tile: this warp's two 32-column chunks h and h + 2 are
-        // loaded together (one TMEM round trip per block), then folded.
+      if (!PARTIALS && TT == 128) {
+        // 128-column instance, any tile width: this warp's chunks h and h + 2
+        // (those below nchunks) are loaded together, one TMEM round trip per
+        // block, then folded.  Columns past ntok inside a chunk are computed and
+        // never stored.
         const uint32_t tw = tbase + static_cast<uint32_t>(h * 32);
         const float* dab = &S.sda[slot][kb][h * 32];
+        const bool c0 = h < nchunks, c1 = h + 2 < nchunks;
         uint32_t ra[32], rb[32];
-        tmem_ld32(tw, ra);
-        tmem_ld32(tw + 64u, rb);
+        if (c0) tmem_ld32(tw, ra);
+        if (c1) tmem_ld32(tw + 64u, rb);
         tmem_wait32x2(ra, rb);
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
+          if (i == 0 ? !c0 : !c1) continue;
           const uint32_t(&cur)[32] = i ? rb : ra;
           const float4* da4 = reinterpret_cast<const float4*>(dab + 64 * i);
 #pragma unroll
@@ -828,7 +841,7 @@ __device__ void workers(const TcArgs& p, SM& S, uint32_t tmem) {
 }
 
 template <bool PARTIALS, int TTM>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Smem<TTM>::THREADS, 1)
     w4a4_gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap amap,
                         const TcArgs p) {
   using SmemT = Smem<TTM>;
@@ -846,10 +859,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < RAW; ++i) {
       mbar_init(&S.full_raw[i], 1);
-      mbar_init(&S.empty_raw[i], kConvWarps);
+      mbar_init(&S.empty_raw[i], SmemT::CONV);
     }
-    for (int i = 0; i < F8; ++i) {
-      mbar_init(&S.f8_full[i], kConvWarps);
+    for (int i = 0; i < SmemT::F8; ++i) {
+      mbar_init(&S.f8_full[i], SmemT::CONV);
       mbar_init(&S.f8_empty[i], 1);
     }
     for (int i = 0; i < SmemT::NBUF; ++i) {
@@ -874,8 +887,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = S.tmem_base;
 
-  if (warp < 4) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
+  if (warp < 4 || warp >= 12) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(SmemT::REGS_LOW));
     if (warp == 0) {
       if ((threadIdx.x & 31) == 0) producer(p, S, &wmap, &amap);
       __syncwarp();
@@ -886,7 +899,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       converters(p, S);
     }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(SmemT::REGS_HIGH));
     workers<PARTIALS>(p, S, tmem);
   }
 
@@ -946,13 +959,15 @@ cudaError_t launch_tc(const CUtensorMap& wmap, const CUtensorMap& amap, const Tc
     cudaFuncAttributes fa{};
     e = cudaFuncGetAttributes(&fa, kern);
     if (e != cudaSuccess) return e;
-    regs_ok[dev] = (fa.numRegs * kThreads >= 128 * kRegsLow + 256 * kRegsHigh) ? 1 : -1;
+    using SM = Smem<TTM>;
+    const int low_threads = SM::THREADS - 256;  // warpgroup 0 (and 3)
+    regs_ok[dev] = (fa.numRegs * SM::THREADS >= low_threads * SM::REGS_LOW + 256 * SM::REGS_HIGH) ? 1 : -1;
     configured[dev] = true;
   }
   if (regs_ok[dev] < 0) return cudaErrorInvalidConfiguration;
   int64_t grid = max_tiles < num_sms() ? max_tiles : num_sms();
   if (grid < 1) grid = 1;
-  kern<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(wmap, amap, a);
+  kern<<<static_cast<unsigned>(grid), Smem<TTM>::THREADS, kSmemBytes, stream>>>(wmap, amap, a);
   return cudaGetLastError();
 }
 
