@@ -81,20 +81,27 @@ constexpr uint32_t kWaitHintNs = W4A4_WAIT_HINT_NS;
 // 384 threads; the 128-column instance, whose workers need fewer registers,
 // adds warpgroup 3 as four more converter warps (512 threads) and a third fp8
 // stage.  Registers after setmaxnreg: 128 x 64 + 256 x 216 <= 168 x 384, and
-// 256 x 56 + 256 x 200 = 128 x 512.
+// 256 x 72 + 256 x 184 = 128 x 512.
 template <int TTM>
 struct __align__(128) Smem {
   static constexpr int TT = TTM;
   static constexpr int NBUF = 512 / TTM;  // TMEM accumulator buffers
   static constexpr int CONV = TTM == 256 ? 2 : 6;                   // converter warps
   static constexpr int THREADS = TTM == 256 ? 384 : 512;
-  static constexpr int REGS_LOW = TTM == 256 ? 64 : 56;             // warpgroups 0 and 3
-  static constexpr int REGS_HIGH = TTM == 256 ? 216 : 200;          // warpgroups 1-2
+  static constexpr int REGS_LOW = TTM == 256 ? 64 : 72;             // warpgroups 0 and 3
+  static constexpr int REGS_HIGH = TTM == 256 ? 216 : 184;          // warpgroups 1-2
   static constexpr int F8 = TTM == 256 ? W4A4_F8_BUFFERS : 12;      // fp8 operand buffers
-  // Stage-scale slots.  Stage s + 1's scales are published during block kb = 2
-  // of stage s into slot (s + 1) % 3, last read by stage s - 2; that block's MMA
-  // needed every warp to release block 4s + 2 - NBUF >= 4s - 2, past stage s - 2.
-  static constexpr int NSC = 3;
+  // Who writes the per-stage scale slots.  The 128-column instance has converter
+  // warps to spare and lets them do it: stage s's scales go to slot s % 4 while
+  // stage s is converted, after the converters waited for the MMA to release
+  // stage s - F8/4 >= s - 3's operand buffers; those MMAs needed the workers to
+  // release every block before them by NBUF = 4 blocks, so the workers are done
+  // with stage s - 4, the slot's previous user.  In the 256-column instance the
+  // workers publish stage s + 1's scales during block kb = 2 of stage s into slot
+  // (s + 1) % 3, last read by stage s - 2; that block's MMA needed every warp to
+  // release block 4s + 2 - NBUF = 4s, past stage s - 2.
+  static constexpr bool CONV_SCALES = TTM == 128;
+  static constexpr int NSC = CONV_SCALES ? 4 : 3;
   uint8_t wraw[RAW][TW * KB * 16];  // TMA box: 128 rows x 64 bytes
   uint8_t araw[RAW][TTM * KB * 16];  // TMA box: tt rows x 64 bytes
   uint8_t wf8[F8][WF8];
@@ -502,6 +509,23 @@ done:
   }
 }
 
+// Stage s's four scales of one row: a vector load when the row's groups are
+// aligned, else four clamped scalar loads (validity is applied when stored).
+__device__ __forceinline__ uint4 load_scales4(const float* row, int s, int B, bool vec) {
+  if (vec) return __ldg(reinterpret_cast<const uint4*>(row + s * KB));
+  uint32_t v[KB];
+#pragma unroll
+  for (int k = 0; k < KB; ++k) v[k] = __float_as_uint(__ldg(row + min(s * KB + k, B - 1)));
+  return make_uint4(v[0], v[1], v[2], v[3]);
+}
+__device__ __forceinline__ uint2 load_halves4(const uint16_t* row, int s, int B, bool vec) {
+  if (vec) return __ldg(reinterpret_cast<const uint2*>(row + s * KB));
+  uint32_t v[KB];
+#pragma unroll
+  for (int k = 0; k < KB; ++k) v[k] = __ldg(row + min(s * KB + k, B - 1));
+  return make_uint2(v[0] | (v[1] << 16), v[2] | (v[3] << 16));
+}
+
 // Two warps convert one stage (4 blocks) at a time.  Thread ct always takes
 // block k = ct % 4 of rows r0 + 16 i (r0 = ct / 4): 8 lanes read one row's 64
 // contiguous raw bytes, and the lanes of one block write 8 consecutive 16-byte
@@ -521,6 +545,13 @@ __device__ void converters(const TcArgs& p, SM& S) {
   const uint32_t dst_off = static_cast<uint32_t>((r0 >> 3) * 256 + (r0 & 7) * 16);
   const int64_t B = p.K / 32;
   const int nst = static_cast<int>((B + KB - 1) / KB);
+  constexpr int CT = 32 * SM::CONV;             // converter threads
+  constexpr int AR = (SM::TT + CT - 1) / CT;    // activation scale rows per thread
+  constexpr int WR = (TW + CT - 1) / CT;        // weight scale rows per thread
+  // rows whose 4-block groups are aligned take one vector load per array
+  const bool vec = (B % KB) == 0 && (reinterpret_cast<uintptr_t>(p.a_scales) & 15) == 0 &&
+                   (reinterpret_cast<uintptr_t>(p.w_scales) & 7) == 0 &&
+                   (reinterpret_cast<uintptr_t>(p.w_sums) & 7) == 0;
   uint32_t gstage = 0, gblk = 0;
   SegIter si = seg_iter(p);
   Seg sg;
@@ -530,6 +561,25 @@ __device__ void converters(const TcArgs& p, SM& S) {
     for (int s = sg.s0; s < sg.s1; ++s, ++gstage) {
       const int nbk = static_cast<int>(B - s * KB < KB ? B - s * KB : KB);
       const int slot = gstage % RAW;
+      // this stage's scales: loaded now, stored into slot gstage % NSC once the
+      // stage's codes are converted (the loads' latency hides behind that)
+      uint4 sa[AR];
+      uint2 swd[WR], sws[WR];
+      if constexpr (SM::CONV_SCALES) {
+#pragma unroll
+      for (int i = 0; i < AR; ++i) {
+        const int m = ct + CT * i;
+        const int64_t row = T.m0 + (m < T.ntok ? m : 0);
+        sa[i] = load_scales4(p.a_scales + row * B, s, static_cast<int>(B), vec);
+      }
+#pragma unroll
+      for (int i = 0; i < WR; ++i) {
+        const int n = ct + CT * i;
+        const int64_t row = T.wrow0 + (n < T.rows_w ? n : 0);
+        swd[i] = load_halves4(p.w_scales + row * B, s, static_cast<int>(B), vec);
+        sws[i] = load_halves4(reinterpret_cast<const uint16_t*>(p.w_sums) + row * B, s, static_cast<int>(B), vec);
+      }
+      }
       if (!mbar_wait(&S.full_raw[slot], (gstage / RAW) & 1, S)) return;
       for (int kk = 0; kk < nbk; ++kk) {
         const uint32_t g = gblk + kk;
@@ -565,11 +615,43 @@ __device__ void converters(const TcArgs& p, SM& S) {
               (x0 >> 4) & 0x0F0F0F0Fu, (x1 >> 4) & 0x0F0F0F0Fu, (x2 >> 4) & 0x0F0F0F0Fu, (x3 >> 4) & 0x0F0F0F0Fu);
         }
       }
+      if constexpr (SM::CONV_SCALES) {
+        const int sc = static_cast<int>(gstage % SM::NSC);
+#pragma unroll
+        for (int i = 0; i < AR; ++i) {
+          const int m = ct + CT * i;
+          if (m < SM::TT) {
+            const bool ok = m < T.ntok;
+            const uint32_t v[KB] = {sa[i].x, sa[i].y, sa[i].z, sa[i].w};
+#pragma unroll
+            for (int kk = 0; kk < KB; ++kk) S.sda[sc][kk][m] = (ok && kk < nbk) ? __uint_as_float(v[kk]) : 0.f;
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < WR; ++i) {
+          const int n = ct + CT * i;
+          if (n < TW) {
+            const bool ok = n < T.rows_w;
+#pragma unroll
+            for (int kk = 0; kk < KB; ++kk) {
+              const uint32_t wd2 = kk < 2 ? swd[i].x : swd[i].y, ws2 = kk < 2 ? sws[i].x : sws[i].y;
+              const unsigned short dh = static_cast<unsigned short>(wd2 >> (16 * (kk & 1)));
+              const short sw = static_cast<short>(ws2 >> (16 * (kk & 1)));
+              const bool v = ok && kk < nbk;
+              const float dw = v ? __half2float(__ushort_as_half(dh)) * fp8_unscale() : 0.f;
+              S.sdw[sc][kk][n] = dw;
+              // -d_w * 8 S_w, exact: (d_w 2^18) * (S_w 2^-15), at most 20 significant bits
+              S.scorr[sc][kk][n] = v ? -dw * (static_cast<float>(sw) * 3.0517578125e-05f) : 0.f;
+            }
+          }
+        }
+      }
       fence_async_smem();
       __syncwarp();
       if (lane == 0) {
         for (int kk = 0; kk < nbk; ++kk) mbar_arrive(&S.f8_full[(gblk + kk) % F8]);
         mbar_arrive(&S.empty_raw[slot]);
+        if constexpr (SM::CONV_SCALES) mbar_arrive(&S.sc_ready[gstage % SM::NSC]);
       }
       gblk += nbk;
     }
@@ -615,6 +697,7 @@ __device__ void workers(const TcArgs& p, SM& S, uint32_t tmem) {
                      (reinterpret_cast<uintptr_t>(p.w_scales) & 7) == 0 &&
                      (reinterpret_cast<uintptr_t>(p.w_sums) & 7) == 0;
     auto load_scales = [&](int s) {
+      if constexpr (SM::CONV_SCALES) return;
       if (vec) {
         da_r = __ldg(reinterpret_cast<const uint4*>(p.a_scales + a_off + s * KB));
         dw_r = __ldg(reinterpret_cast<const uint2*>(p.w_scales + w_off + s * KB));
@@ -635,6 +718,7 @@ __device__ void workers(const TcArgs& p, SM& S, uint32_t tmem) {
     };
     // Store the registers' scales into a slot and arrive; waiting is separate.
     auto publish_scales = [&](int slot, int s) {
+      if constexpr (SM::CONV_SCALES) return;
       const uint32_t da[KB] = {da_r.x, da_r.y, da_r.z, da_r.w};
       const uint32_t dwp[2] = {dw_r.x, dw_r.y}, swp[2] = {sw_r.x, sw_r.y};
 #pragma unroll
@@ -659,14 +743,15 @@ __device__ void workers(const TcArgs& p, SM& S, uint32_t tmem) {
 #pragma unroll
       for (int j = 0; j < 16; ++j) acc[i][j] = make_float2(0.f, 0.f);
 
-    // Stage s's scales live in slot (gsc0 + s - s0) % NSC.  During stage s the
-    // registers hold stage s + 1's scales; they are published once block kb = 2
-    // of stage s has its accumulator (see Smem::NSC for why the slot is free),
-    // then stage s + 2 is prefetched.  A stage's slot is waited for at kb = 0.
+    // Stage s's scales live in slot (gsc0 + s - s0) % NSC (see Smem::NSC for
+    // who writes them); a stage's slot is waited for at its first block.  When
+    // the workers publish, the registers hold stage s + 1's scales during stage s.
     const uint32_t gsc0 = gsc;
-    load_scales(sg.s0);
-    publish_scales(static_cast<int>(gsc0 % SM::NSC), sg.s0);
-    if (sg.s0 + 1 < sg.s1) load_scales(sg.s0 + 1);
+    if constexpr (!SM::CONV_SCALES) {
+      load_scales(sg.s0);
+      publish_scales(static_cast<int>(gsc0 % SM::NSC), sg.s0);
+      if (sg.s0 + 1 < sg.s1) load_scales(sg.s0 + 1);
+    }
 
     const int b_end = sg.s1 * KB < B ? sg.s1 * KB : B;
     for (int b = sg.s0 * KB; b < b_end; ++b) {
@@ -678,7 +763,7 @@ __device__ void workers(const TcArgs& p, SM& S, uint32_t tmem) {
       const int tb = static_cast<int>(gfold % SM::NBUF);
       if (!mbar_wait(&S.tm_full[tb], (gfold / SM::NBUF) & 1, S)) return;
       tc_fence_after();
-      if (kb == 2 && s + 1 < sg.s1) {
+      if (!SM::CONV_SCALES && kb == 2 && s + 1 < sg.s1) {
         publish_scales(static_cast<int>((gs + 1) % SM::NSC), s + 1);
         if (s + 2 < sg.s1) load_scales(s + 2);
       }
@@ -869,7 +954,7 @@ __global__ void __launch_bounds__(Smem<TTM>::THREADS, 1)
       mbar_init(&S.tm_full[i], 1);
       mbar_init(&S.tm_empty[i], kWorkerWarps);
     }
-    for (int i = 0; i < SmemT::NSC; ++i) mbar_init(&S.sc_ready[i], kWorkerWarps);
+    for (int i = 0; i < SmemT::NSC; ++i) mbar_init(&S.sc_ready[i], SmemT::CONV_SCALES ? SmemT::CONV : kWorkerWarps);
     mbar_init(&S.tile_done, kWorkerWarps);
     mbar_init(&S.mma_done, 1);
     S.abort = 0;
