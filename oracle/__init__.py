@@ -31,6 +31,10 @@ function                       pinned by
 ``w4a4_matmul``                brute-force fp64 loops; constant-block closed
                                form d_w d_a P = 32 alpha beta
 ``w4a4_matmul_id``             reduces to dense per (token, slot); brute force
+``quantize_act_int8``          round-trip bound; amax -> +-127; 2^k scale
+                               invariance; hand-derived blocks
+``w4a8_matmul``                brute-force fp64 loops; constant-block closed
+                               form d_w d_a P = 32 alpha beta
 ``exact_matmul``               brute-force fp64 loops
 =============================  ==============================================
 
@@ -51,13 +55,16 @@ from .quant import (
     q4_0_from_aos,
     pack_weights,
     quantize_activations,
+    quantize_act_int8,
+    quantize_activations_int8,
 )
-from .matmul import block_partials, w4a4_matmul, w4a4_matmul_id, exact_matmul
+from .matmul import block_partials, w4a4_matmul, w4a4_matmul_id, w4a8_matmul, exact_matmul
 
 __all__ = [
     "C_H32", "sylvester_h32", "fwht32", "rotate_h32",
     "round_half_away", "quantize_weights_q4_0", "quantize_act_int4",
     "pack_nibbles", "unpack_nibbles", "act_codes_from_nibbles", "weight_codes_from_nibbles",
     "q4_0_to_aos", "q4_0_from_aos", "pack_weights", "quantize_activations",
-    "block_partials", "w4a4_matmul", "w4a4_matmul_id", "exact_matmul",
+    "quantize_act_int8", "quantize_activations_int8",
+    "block_partials", "w4a4_matmul", "w4a4_matmul_id", "w4a8_matmul", "exact_matmul",
 ]

@@ -37,7 +37,11 @@ def _avals(ap: dict) -> np.ndarray:
 
 
 def block_partials(wp: dict, ap: dict, m_idx=None, n_idx=None) -> np.ndarray:
-    """Integer per-block dot products P [M][N][K/32] (int64)."""
+    """Integer per-block dot products P [M][N][K/32] (int64).
+
+    With int4 activations |P| <= 2048; with the int8 activations of the exact
+    path (``quantize_activations_int8``) |P| <= 32 * 8 * 127 = 32512.
+    """
     wv = _wvals(wp)
     av = _avals(ap)
     if m_idx is not None:
@@ -48,7 +52,7 @@ def block_partials(wp: dict, ap: dict, m_idx=None, n_idx=None) -> np.ndarray:
     N = wv.shape[0]
     B = K // 32
     P = np.einsum("mbj,nbj->mnb", av.reshape(M, B, 32), wv.reshape(N, B, 32))
-    assert np.abs(P).max(initial=0) <= 2048
+    assert np.abs(P).max(initial=0) <= (2048 if np.abs(av).max(initial=0) <= 8 else 32512)
     return P
 
 
@@ -80,6 +84,13 @@ def w4a4_matmul(wp: dict, ap: dict, m_idx=None, n_idx=None) -> np.ndarray:
         n_idx = np.asarray(n_idx)
         wv, dw = wv[n_idx], dw[n_idx]
     return _matmul_vals(av, da, wv, dw)
+
+
+def w4a8_matmul(wp: dict, ap8: dict, m_idx=None, n_idx=None) -> np.ndarray:
+    """The exact path's product, rotated Q4_0 weights times int8 activations:
+    Y = sum_b d_w d_a P with P = sum_j (q_w - 8) q_a, q_a in -127..127 (fp64).
+    The same block-scaled sum as ``w4a4_matmul``; only the activation codes differ."""
+    return w4a4_matmul(wp, ap8, m_idx, n_idx)
 
 
 def w4a4_matmul_id(wp_experts: dict, E: int, ap: dict, ids: np.ndarray,

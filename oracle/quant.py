@@ -82,6 +82,26 @@ def quantize_act_int4(y: np.ndarray) -> dict:
     return {"q": q.reshape(y.shape), "d_a": d_a}
 
 
+def quantize_act_int8(y: np.ndarray) -> dict:
+    """int8-quantise fp32 values y [..., K] per 32-block (the exact path's
+    8-bit activations, engine docs page above, section "Hadamard-rotated Q4_0:
+    W4A4 prompt processing": with W4A4 switched off the rotated file runs on
+    the exact int8 path).
+
+    Reading: a = max |y|; d_a = a / 127 in fp32; id = 1/d_a (0 when d_a == 0);
+    q = clamp(round_half_away(fl(y * id)), -127, 127).  Returns q (int8,
+    [..., K]) and d_a (fp32, [..., K/32]).
+    """
+    y = np.asarray(y, dtype=np.float32)
+    blk = _blocks(y)
+    a = np.max(np.abs(blk), axis=-1)
+    d_a = (a / np.float32(127.0)).astype(np.float32)
+    inv = _safe_recip(d_a)
+    v = (blk * inv[..., None]).astype(np.float32)
+    q = np.clip(round_half_away(v), -127.0, 127.0).astype(np.int8)
+    return {"q": q.reshape(y.shape), "d_a": d_a}
+
+
 def pack_nibbles(nib: np.ndarray) -> np.ndarray:
     """Pack 4-bit values (uint8 0..15, [..., K]) into [..., K/2] bytes, Q4_0 order."""
     blk = _blocks(np.asarray(nib, dtype=np.uint8))
@@ -166,3 +186,11 @@ def quantize_activations(x: np.ndarray, rotate: bool = True) -> dict:
     qa = quantize_act_int4(y)
     nib = (qa["q"].astype(np.int16) & 0x0F).astype(np.uint8)
     return {"codes": pack_nibbles(nib), "d_a": qa["d_a"], "q": qa["q"], "rotated": bool(rotate)}
+
+
+def quantize_activations_int8(x: np.ndarray, rotate: bool = True) -> dict:
+    """Activations [M][K] fp32 -> rotated int8 codes [M][K] + fp32 per-block scales."""
+    xf = np.asarray(x, dtype=np.float32)
+    y = rotate_h32(xf) if rotate else xf
+    qa = quantize_act_int8(y)
+    return {"codes8": qa["q"].copy(), "d_a": qa["d_a"], "q": qa["q"], "rotated": bool(rotate)}

@@ -342,3 +342,95 @@ def test_rotation_reduces_w4a4_error_on_outlier_activations():
     err_r = np.linalg.norm(Yr - R) / np.linalg.norm(R)
     err_u = np.linalg.norm(Yu - R) / np.linalg.norm(R)
     assert err_r < err_u
+
+
+# ---------------------------------------------------------------- the exact int8 path
+def test_int8_hand_worked_blocks(golden_dir):
+    for name, d, vals, codes in read_golden(os.path.join(golden_dir, "int8_act_hand_blocks.txt")):
+        out = oracle.quantize_act_int8(vals[None, :])
+        assert float(out["d_a"][0, 0]) == d, name
+        assert np.array_equal(out["q"][0].astype(np.int64), codes), name
+
+
+def test_int8_round_trip_bounds_and_amax():
+    rng = np.random.default_rng(21)
+    y = (rng.standard_normal((64, 256)) * rng.uniform(0.01, 50, (64, 1))).astype(np.float32)
+    out = oracle.quantize_act_int8(y)
+    q = out["q"].astype(np.float64).reshape(64, 8, 32)
+    d = out["d_a"].astype(np.float64)[..., None]
+    yb = y.astype(np.float64).reshape(64, 8, 32)
+    # |y - d q| <= d / 2 (plus the fp32 rounding of y * (1/d))
+    assert np.all(np.abs(yb - d * q) <= d * (0.5 + 1e-5))
+    # the element of largest magnitude maps to +-127
+    idx = np.argmax(np.abs(yb), axis=-1)
+    top = np.take_along_axis(q, idx[..., None], axis=-1)[..., 0]
+    assert np.all(np.abs(top) == 127)
+    assert np.abs(q).max() <= 127
+
+
+def test_int8_scale_invariance_powers_of_two():
+    rng = np.random.default_rng(22)
+    x = rng.standard_normal((8, 128)).astype(np.float32)
+    a = oracle.quantize_activations_int8(x)
+    for k in (-3, 5):
+        b = oracle.quantize_activations_int8((x * np.float32(2.0 ** k)).astype(np.float32))
+        assert np.array_equal(a["q"], b["q"])
+        assert np.array_equal(b["d_a"], (a["d_a"] * np.float32(2.0 ** k)).astype(np.float32))
+
+
+def test_w4a8_matmul_brute_force():
+    rng = np.random.default_rng(23)
+    w = rng.standard_normal((4, 64)).astype(np.float32)
+    x = rng.standard_normal((3, 64)).astype(np.float32)
+    wp = oracle.pack_weights(w)
+    ap = oracle.quantize_activations_int8(x)
+    Y = oracle.w4a8_matmul(wp, ap)
+    wq, aq = wp["q"], ap["q"]
+    for m in range(3):
+        for n in range(4):
+            acc = Fraction(0)
+            for b in range(2):
+                s = sum((int(wq[n, 32 * b + j]) - 8) * int(aq[m, 32 * b + j]) for j in range(32))
+                acc += Fraction(float(wp["d16"][n, b])) * Fraction(float(ap["d_a"][m, b])) * s
+            assert abs(Y[m, n] - float(acc)) <= 1e-15 * max(1.0, abs(float(acc)))
+    P = oracle.block_partials(wp, ap)
+    for m in range(3):
+        for n in range(4):
+            for b in range(2):
+                s = sum((int(wq[n, 32 * b + j]) - 8) * int(aq[m, 32 * b + j]) for j in range(32))
+                assert P[m, n, b] == s
+
+
+def test_w4a8_constant_blocks_closed_form():
+    """Weight block constant alpha, activation block constant beta: rotated, the
+    activation block is (32 beta c, 0, ...), int8 codes (+-127, 0, ...), and
+    P = -8 * (+-127) = -1016 sign(beta); d_w d_a P = 32 alpha beta up to the fp16 scale."""
+    rng = np.random.default_rng(24)
+    B = 6
+    alpha = rng.uniform(0.1, 2.0, B) * rng.choice([-1, 1], B)
+    beta = rng.uniform(0.1, 2.0, B) * rng.choice([-1, 1], B)
+    w = np.repeat(alpha, 32).astype(np.float32)[None, :]
+    x = np.repeat(beta, 32).astype(np.float32)[None, :]
+    wp = oracle.pack_weights(w)
+    ap = oracle.quantize_activations_int8(x)
+    for b in range(B):
+        qa = ap["q"][0, 32 * b:32 * b + 32].astype(np.int64)
+        assert qa[0] == 127 * np.sign(beta[b]) and np.all(qa[1:] == 0)
+    P = oracle.block_partials(wp, ap)[0, 0]
+    assert np.array_equal(P, -1016 * np.sign(beta).astype(np.int64))
+    Y = oracle.w4a8_matmul(wp, ap)[0, 0]
+    exact = float(np.sum(32 * np.float32(alpha).astype(np.float64) * np.float32(beta).astype(np.float64)))
+    assert abs(Y - exact) <= 2.0 ** -10 * float(np.sum(np.abs(32 * alpha * beta)))
+
+
+def test_int8_path_is_closer_than_int4_to_the_exact_product():
+    """Against the product of the (exact) Q4_0 weights with the unrounded rotated
+    activations, eight-bit activations lose far less than four-bit ones."""
+    d = si.random_dense(16, 512, 24, seed=25)
+    wp = oracle.pack_weights(d["w_bf16"])
+    w_deq = ((wp["q"].astype(np.float64) - 8).reshape(24, 16, 32)
+             * wp["d16"].astype(np.float64)[..., None]).reshape(24, 512)
+    ref = oracle.exact_matmul(oracle.rotate_h32(d["x"]), w_deq)
+    e4 = np.abs(oracle.w4a4_matmul(wp, oracle.quantize_activations(d["x"])) - ref).mean()
+    e8 = np.abs(oracle.w4a8_matmul(wp, oracle.quantize_activations_int8(d["x"])) - ref).mean()
+    assert e8 < 0.1 * e4
