@@ -33,6 +33,7 @@ __all__ = [
     "h32_q4_0_pack_weights", "q4_0_import", "w4a4_rotate_quantize_act",
     "w4a4_gemm", "w4a4_gemm_workspace_bytes", "w4a4_gemm_partials", "w4a4_gemm_id", "w4a4_gemm_id_status",
     "w4a4_gemm_id_workspace_bytes", "w4a4_gemm_id_static", "w4a4_check", "STATUS",
+    "Act8", "w4a8_rotate_quantize_act", "w4a8_gemm", "w4a8_gemm_partials", "w4a8_gemm_workspace_bytes",
 ]
 
 STATUS = {
@@ -42,6 +43,7 @@ STATUS = {
 }
 TAG_Q4_0 = 0x51340000
 TAG_ACT4 = 0x41340000
+TAG_ACT8 = 0x41380000
 TAG_ROTATED = 0x1
 
 #: every symbol include/w4a4.h declares
@@ -49,7 +51,8 @@ EXPORTS = [
     "w4a4_q4_0_codes_bytes", "w4a4_q4_0_scales_bytes", "w4a4_q4_0_sums_bytes", "w4a4_act4_codes_bytes",
     "w4a4_act4_scales_bytes", "h32_q4_0_pack_weights", "q4_0_import", "w4a4_rotate_quantize_act", "w4a4_gemm", "w4a4_gemm_workspace_bytes",
     "w4a4_gemm_partials", "w4a4_gemm_id", "w4a4_gemm_id_workspace_bytes", "w4a4_gemm_id_status", "w4a4_gemm_id_static", "w4a4_check", "w4a4_last_error",
-    "w4a4_status_name", "w4a4_abi_version",
+    "w4a4_status_name", "w4a4_abi_version", "w4a4_act8_codes_bytes", "w4a4_act8_scales_bytes",
+    "w4a8_rotate_quantize_act", "w4a8_gemm", "w4a8_gemm_partials", "w4a8_gemm_workspace_bytes",
 ]
 
 
@@ -90,7 +93,7 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
     lib = ctypes.CDLL(path)
     i64, vp, i32, u = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
     for name in ("w4a4_q4_0_codes_bytes", "w4a4_q4_0_scales_bytes", "w4a4_q4_0_sums_bytes", "w4a4_act4_codes_bytes",
-                 "w4a4_act4_scales_bytes"):
+                 "w4a4_act4_scales_bytes", "w4a4_act8_codes_bytes", "w4a4_act8_scales_bytes"):
         f = getattr(lib, name)
         f.argtypes, f.restype = [i64, i64], u
     lib.h32_q4_0_pack_weights.argtypes = [vp, i32, i64, i64, i64, i32, ctypes.POINTER(_Q4_0Desc), vp]
@@ -98,6 +101,10 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.w4a4_rotate_quantize_act.argtypes = [vp, i64, i64, i64, i32, ctypes.POINTER(_Act4Desc), vp]
     lib.w4a4_gemm.argtypes = [ctypes.POINTER(_Q4_0Desc), ctypes.POINTER(_Act4Desc), vp, i64, vp, u, vp]
     lib.w4a4_gemm_workspace_bytes.argtypes, lib.w4a4_gemm_workspace_bytes.restype = [i64, i64, i64], u
+    lib.w4a8_rotate_quantize_act.argtypes = [vp, i64, i64, i64, i32, ctypes.POINTER(_Act4Desc), vp]
+    lib.w4a8_gemm.argtypes = [ctypes.POINTER(_Q4_0Desc), ctypes.POINTER(_Act4Desc), vp, i64, vp, u, vp]
+    lib.w4a8_gemm_partials.argtypes = [ctypes.POINTER(_Q4_0Desc), ctypes.POINTER(_Act4Desc), vp, vp]
+    lib.w4a8_gemm_workspace_bytes.argtypes, lib.w4a8_gemm_workspace_bytes.restype = [i64, i64, i64], u
     lib.w4a4_gemm_partials.argtypes = [ctypes.POINTER(_Q4_0Desc), ctypes.POINTER(_Act4Desc), vp, vp]
     lib.w4a4_gemm_id.argtypes = [ctypes.POINTER(_Q4_0Desc), i32, i64, ctypes.POINTER(_Act4Desc), vp, i64, i32, i32,
                                  vp, vp, u, vp]
@@ -107,7 +114,8 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
                                          i32, vp, vp]
     lib.w4a4_check.argtypes = [vp]
     for name in ("h32_q4_0_pack_weights", "q4_0_import", "w4a4_rotate_quantize_act", "w4a4_gemm",
-                 "w4a4_gemm_partials", "w4a4_gemm_id", "w4a4_gemm_id_status", "w4a4_check"):
+                 "w4a4_gemm_partials", "w4a4_gemm_id", "w4a4_gemm_id_status", "w4a4_check",
+                 "w4a8_rotate_quantize_act", "w4a8_gemm", "w4a8_gemm_partials"):
         getattr(lib, name).restype = ctypes.c_int
     lib.w4a4_last_error.argtypes, lib.w4a4_last_error.restype = [], ctypes.c_char_p
     lib.w4a4_status_name.argtypes, lib.w4a4_status_name.restype = [ctypes.c_int], ctypes.c_char_p
@@ -272,12 +280,14 @@ def w4a4_gemm_workspace_bytes(M: int, N: int, K: int) -> int:
 _GEMM_WS: dict = {}
 
 
-def gemm_workspace(M: int, N: int, K: int, device, stream=None) -> torch.Tensor | None:
+def gemm_workspace(M: int, N: int, K: int, device, stream=None, need: int | None = None) -> torch.Tensor | None:
     """A zero-initialised GEMM workspace kept per (device, stream), grown on demand.
 
     One per stream, because calls sharing a workspace must not overlap on the GPU.
+    ``need`` overrides the size query (the exact path has its own).
     """
-    need = w4a4_gemm_workspace_bytes(M, N, K)
+    if need is None:
+        need = w4a4_gemm_workspace_bytes(M, N, K)
     if need == 0:
         return None
     key = (torch.device(device).index, _stream(stream))
@@ -375,3 +385,84 @@ def w4a4_check(stream=None) -> None:
 def w4a4_gemm_id_status(ws: torch.Tensor, stream=None) -> None:
     """Synchronise and raise W4A4Error(W4A4_ERR_DEVICE_FLAG) if the last gemm_id on ws saw a bad id."""
     _check(load_library().w4a4_gemm_id_status(ws.data_ptr(), _stream(stream)))
+
+
+# ---------------------------------------------------------------- the exact path (int8 activations)
+@dataclass
+class Act8:
+    """int8 activations of the exact path: codes int8 [rows][K] (element order), scales fp32 [rows][K/32]."""
+    codes: torch.Tensor
+    scales_buf: torch.Tensor
+    rows: int
+    K: int
+    rotated: bool
+
+    @property
+    def scales(self) -> torch.Tensor:
+        n = self.rows * (self.K // 32)
+        return self.scales_buf[: 4 * n].view(torch.float32).view(self.rows, self.K // 32)
+
+    @property
+    def tag(self) -> int:
+        return TAG_ACT8 | (TAG_ROTATED if self.rotated else 0)
+
+    def desc(self) -> _Act4Desc:
+        return _Act4Desc(self.codes.data_ptr(), self.scales_buf.data_ptr(), self.rows, self.K, self.tag)
+
+
+def alloc_act8(rows: int, K: int, device, rotated: bool = True) -> Act8:
+    lib = load_library()
+    if K <= 0 or K % 32:
+        raise W4A4Error(1, f"K={K} must be a positive multiple of 32")
+    nc, ns = lib.w4a4_act8_codes_bytes(rows, K), lib.w4a4_act8_scales_bytes(rows, K)
+    codes = torch.empty(max(nc, 16), dtype=torch.int8, device=device)[:nc].view(rows, K)
+    sbuf = torch.empty(max(ns, 16), dtype=torch.uint8, device=device)
+    return Act8(codes, sbuf, rows, K, rotated)
+
+
+def w4a8_rotate_quantize_act(x: torch.Tensor, rotate: bool = True, out: Act8 | None = None, stream=None) -> Act8:
+    """Rotate (H32) and int8-quantise fp32 activations x [M][K] (CUDA) per 32-block (d_a = amax / 127)."""
+    _cuda(x, "x")
+    if x.dtype != torch.float32 or x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be a 2-D fp32 tensor with unit stride along K")
+    M, K = x.shape
+    out = out or alloc_act8(M, K, x.device, rotate)
+    d = out.desc()
+    ldx = x.stride(0) if M > 1 else K
+    _check(load_library().w4a8_rotate_quantize_act(x.data_ptr(), M, K, ldx, int(rotate), ctypes.byref(d),
+                                                    _stream(stream)))
+    out.rotated = bool(rotate)
+    return out
+
+
+def w4a8_gemm_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(load_library().w4a8_gemm_workspace_bytes(M, N, K))
+
+
+def w4a8_gemm(w: Q4_0Weights, a: Act8, y: torch.Tensor | None = None, ws: torch.Tensor | None | bool = True,
+              stream=None) -> torch.Tensor:
+    """The exact path: Y[m][n] = sum_b d_w d_a P with int8 activations (fp32 [M][N]); ws as for w4a4_gemm."""
+    if y is None:
+        y = torch.empty(a.rows, w.rows, dtype=torch.float32, device=w.codes.device)
+    _cuda(y, "y")
+    if y.dtype != torch.float32 or y.dim() != 2 or y.stride(1) != 1:
+        raise ValueError("y must be a 2-D fp32 tensor with unit stride along N")
+    ldy = y.stride(0) if y.shape[0] > 1 else max(w.rows, 1)
+    if ws is True:
+        ws = gemm_workspace(a.rows, w.rows, w.K, y.device, stream, need=w4a8_gemm_workspace_bytes(a.rows, w.rows, w.K))
+    elif ws is False:
+        ws = None
+    ws_ptr, ws_bytes = (ws.data_ptr(), ws.numel() * ws.element_size()) if ws is not None else (None, 0)
+    _check(load_library().w4a8_gemm(ctypes.byref(w.desc()), ctypes.byref(a.desc()), y.data_ptr(), ldy, ws_ptr,
+                                    ws_bytes, _stream(stream)))
+    return y
+
+
+def w4a8_gemm_partials(w: Q4_0Weights, a: Act8, P: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Exact per-block integer partials of the exact path, P[m][n][b] (int32)."""
+    if P is None:
+        P = torch.empty(a.rows, w.rows, w.K // 32, dtype=torch.int32, device=w.codes.device)
+    _cuda(P, "P")
+    _check(load_library().w4a8_gemm_partials(ctypes.byref(w.desc()), ctypes.byref(a.desc()), P.data_ptr(),
+                                             _stream(stream)))
+    return P

@@ -47,8 +47,13 @@ __device__ __forceinline__ uint32_t nib(float y, float inv) {
   return static_cast<uint32_t>(static_cast<int>(r)) & 0xFu;
 }
 
-// One 32-element block held by this lane: rotate (optional), d_a = amax / 7,
-// int4 codes (round half away, clamp -8..7), stored at block index i if ok.
+// One 32-element block held by this lane: rotate (optional), then
+//   BITS = 4: d_a = amax / 7, int4 codes (round half away, clamp -8..7), 16
+//             bytes in the Q4_0 nibble order;
+//   BITS = 8: d_a = amax / 127, int8 codes (round half away, clamp -127..127),
+//             32 bytes in element order (the exact path's activations);
+// stored at block index i if ok.
+template <int BITS>
 __device__ __forceinline__ void quantize_block(float (&y)[32], int rotate, bool ok, uint8_t* __restrict__ codes,
                                                float* __restrict__ scales, int64_t i) {
   if (rotate) {
@@ -60,6 +65,29 @@ __device__ __forceinline__ void quantize_block(float (&y)[32], int rotate, bool 
   float a = 0.f;
 #pragma unroll
   for (int k = 0; k < 32; ++k) a = fmaxf(a, fabsf(y[k]));
+  if constexpr (BITS == 8) {
+    const float d = __fdiv_rn(a, 127.0f);
+    const float inv = (d != 0.0f) ? __frcp_rn(d) : 0.0f;
+    uint32_t w[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      uint32_t word = 0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        float r = round_half_away(__fmul_rn(y[4 * t + k], inv));
+        r = fminf(fmaxf(r, -127.0f), 127.0f);
+        word |= (static_cast<uint32_t>(static_cast<int>(r)) & 0xFFu) << (8 * k);
+      }
+      w[t] = word;
+    }
+    if (ok) {
+      uint4* dst = reinterpret_cast<uint4*>(codes) + 2 * i;
+      dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      scales[i] = d;
+    }
+    return;
+  }
   const float d = __fdiv_rn(a, 7.0f);
   const float inv = (d != 0.0f) ? __frcp_rn(d) : 0.0f;
   // byte t of the 16 = element t (low nibble) | element t + 16 (high nibble)
@@ -81,6 +109,7 @@ __device__ __forceinline__ void quantize_block(float (&y)[32], int rotate, bool 
   }
 }
 
+template <int BITS>
 __global__ void __launch_bounds__(32 * kWarps) act_rotate_quantize_kernel(const float* __restrict__ x, int64_t M,
                                                                           int64_t K, int64_t ldx, int rotate,
                                                                           uint8_t* __restrict__ codes,
@@ -124,7 +153,7 @@ __global__ void __launch_bounds__(32 * kWarps) act_rotate_quantize_kernel(const 
       y[4 * k + 3] = v.w;
     }
     __syncwarp();
-    quantize_block(y, rotate, ok, codes, scales, i);
+    quantize_block<BITS>(y, rotate, ok, codes, scales, i);
   }
 }
 
@@ -187,6 +216,7 @@ __device__ __forceinline__ void tma_load_chunk(float* dst, const CUtensorMap* ma
       : "memory");
 }
 
+template <int BITS>
 __global__ void __launch_bounds__(32 * kTmaWarps) act_rotate_quantize_tma_kernel(
     const __grid_constant__ CUtensorMap xmap, int64_t nblk, int rotate, uint8_t* __restrict__ codes,
     float* __restrict__ scales, int* err) {
@@ -238,7 +268,7 @@ __global__ void __launch_bounds__(32 * kTmaWarps) act_rotate_quantize_tma_kernel
       ++issued;
     }
     const int64_t i = (gw + it * nw) * 32 + lane;
-    quantize_block(y, rotate, i < nblk, codes, scales, i);
+    quantize_block<BITS>(y, rotate, i < nblk, codes, scales, i);
   }
   if (__any_sync(0xFFFFFFFFu, failed)) {
     // a load never completed: record it and wait (bounded) for the copies still
@@ -254,8 +284,10 @@ __global__ void __launch_bounds__(32 * kTmaWarps) act_rotate_quantize_tma_kernel
 
 }  // namespace
 
-cudaError_t launch_act_rotate_quantize(const float* x, int64_t M, int64_t K, int64_t ldx, int rotate,
-                                       uint8_t* codes, float* scales, cudaStream_t stream) {
+namespace {
+template <int BITS>
+cudaError_t launch_act(const float* x, int64_t M, int64_t K, int64_t ldx, int rotate, uint8_t* codes, float* scales,
+                       cudaStream_t stream) {
   const int64_t nblk = M * (K / 32);
   const int64_t nchunks = (nblk + 31) / 32;
   if (ldx == K && nblk < (int64_t(1) << 31) - 64) {
@@ -267,7 +299,7 @@ cudaError_t launch_act_rotate_quantize(const float* x, int64_t M, int64_t K, int
       int dev = 0;
       cudaGetDevice(&dev);
       if (dev >= 0 && dev < 64 && !configured[dev]) {
-        e = cudaFuncSetAttribute(act_rotate_quantize_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(act_rotate_quantize_tma_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(sizeof(ActSmem)));
         if (e != cudaSuccess) return e;
         configured[dev] = true;
@@ -276,7 +308,7 @@ cudaError_t launch_act_rotate_quantize(const float* x, int64_t M, int64_t K, int
       const int64_t cap = static_cast<int64_t>(num_sms()) * W4A4_ACT_CTAS_PER_SM;
       if (ctas > cap) ctas = cap;
       if (ctas < 1) ctas = 1;
-      act_rotate_quantize_tma_kernel<<<static_cast<unsigned>(ctas), 32 * kTmaWarps, sizeof(ActSmem), stream>>>(
+      act_rotate_quantize_tma_kernel<BITS><<<static_cast<unsigned>(ctas), 32 * kTmaWarps, sizeof(ActSmem), stream>>>(
           xmap, nblk, rotate, codes, scales, device_error_word());
       return cudaGetLastError();
     }
@@ -285,9 +317,20 @@ cudaError_t launch_act_rotate_quantize(const float* x, int64_t M, int64_t K, int
   const int64_t cap = static_cast<int64_t>(num_sms()) * 4;  // 4 x 256 threads per SM
   if (ctas > cap) ctas = cap;
   if (ctas < 1) ctas = 1;
-  act_rotate_quantize_kernel<<<static_cast<unsigned>(ctas), 32 * kWarps, 0, stream>>>(x, M, K, ldx, rotate, codes,
+  act_rotate_quantize_kernel<BITS><<<static_cast<unsigned>(ctas), 32 * kWarps, 0, stream>>>(x, M, K, ldx, rotate, codes,
                                                                                        scales);
   return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_act_rotate_quantize(const float* x, int64_t M, int64_t K, int64_t ldx, int rotate,
+                                       uint8_t* codes, float* scales, cudaStream_t stream) {
+  return launch_act<4>(x, M, K, ldx, rotate, codes, scales, stream);
+}
+
+cudaError_t launch_act_rotate_quantize8(const float* x, int64_t M, int64_t K, int64_t ldx, int rotate,
+                                        int8_t* codes, float* scales, cudaStream_t stream) {
+  return launch_act<8>(x, M, K, ldx, rotate, reinterpret_cast<uint8_t*>(codes), scales, stream);
 }
 
 }  // namespace w4a4

@@ -63,9 +63,6 @@ static_assert(KB == 4, "the vector scale loads take 4 blocks per stage");
 #define W4A4_F8_BUFFERS 8
 #endif
 constexpr int RAW = W4A4_RAW_STAGES;  // stages of raw codes in flight
-constexpr int WF8 = TW * 32 + 32;  // buffer strides padded by 32 bytes: the converters'
-template <int TTM>
-constexpr int af8_stride() { return TTM * 32 + 32; }  // 16-byte stores to 4 buffers hit distinct banks
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kTimeoutNs = 1000000000ull;  // 1 s
 #ifndef W4A4_WAIT_HINT_NS
@@ -82,15 +79,24 @@ constexpr uint32_t kWaitHintNs = W4A4_WAIT_HINT_NS;
 // adds warpgroup 3 as four more converter warps (512 threads) and a third fp8
 // stage.  Registers after setmaxnreg: 128 x 64 + 256 x 216 <= 168 x 384, and
 // 256 x 72 + 256 x 184 = 128 x 512.
-template <int TTM>
+// AB: activation code width.  4 = the W4A4 product (int4 activations, e4m3
+// operands, one kind::f8f6f4 MMA per block); 8 = the exact path (int8
+// activations, f16 operands, two kind::f16 MMAs of K = 16 per block; int8 and
+// int4 values are exact in f16 and so are the 32-term block sums in fp32).
+template <int TTM, int AB = 4>
 struct __align__(128) Smem {
   static constexpr int TT = TTM;
+  static constexpr int ABITS = AB;
+  static constexpr int ARAW_ROW = KB * 4 * AB;  // raw activation bytes per row and stage: 64 or 128
+  static constexpr int OPB = AB == 4 ? 1 : 2;   // operand bytes per element: e4m3 or f16
+  static constexpr int WOP = TW * 32 * OPB + 32;   // operand buffer strides, padded by 32 bytes so that the
+  static constexpr int AOP = TTM * 32 * OPB + 32;  // converters' stores to 4 buffers hit distinct banks
   static constexpr int NBUF = 512 / TTM;  // TMEM accumulator buffers
   static constexpr int CONV = TTM == 256 ? 2 : 6;                   // converter warps
   static constexpr int THREADS = TTM == 256 ? 384 : 512;
   static constexpr int REGS_LOW = TTM == 256 ? 64 : 72;             // warpgroups 0 and 3
   static constexpr int REGS_HIGH = TTM == 256 ? 216 : 184;          // warpgroups 1-2
-  static constexpr int F8 = TTM == 256 ? W4A4_F8_BUFFERS : 12;      // fp8 operand buffers
+  static constexpr int F8 = AB == 8 ? 6 : (TTM == 256 ? W4A4_F8_BUFFERS : 12);  // operand buffers
   // Who writes the per-stage scale slots.  The 128-column instance has converter
   // warps to spare and lets them do it: stage s's scales go to slot s % 4 while
   // stage s is converted, after the converters waited for the MMA to release
@@ -103,9 +109,9 @@ struct __align__(128) Smem {
   static constexpr bool CONV_SCALES = TTM == 128;
   static constexpr int NSC = CONV_SCALES ? 4 : 3;
   uint8_t wraw[RAW][TW * KB * 16];  // TMA box: 128 rows x 64 bytes
-  uint8_t araw[RAW][TTM * KB * 16];  // TMA box: tt rows x 64 bytes
-  uint8_t wf8[F8][WF8];
-  uint8_t af8[F8][af8_stride<TTM>()];
+  uint8_t araw[RAW][TTM * ARAW_ROW];  // TMA box: tt rows x 64 (int4) or 128 (int8) bytes
+  uint8_t wf8[F8][WOP];
+  uint8_t af8[F8][AOP];
   float sda[NSC][KB][TTM];              // d_a per stage, block-major
   float sdw[NSC][KB][TW];              // d_w * 2^18
   float scorr[NSC][KB][TW];            // -d_w * 8 S_w (exact)
@@ -123,6 +129,7 @@ struct __align__(128) Smem {
 };
 static_assert(sizeof(Smem<256>) <= 227 * 1024, "shared memory per CTA is at most 227 KB");
 static_assert(sizeof(Smem<128>) <= 227 * 1024, "shared memory per CTA is at most 227 KB");
+static_assert(sizeof(Smem<128, 8>) <= 227 * 1024, "shared memory per CTA is at most 227 KB");
 
 struct TcArgs {
   const uint16_t* w_scales;
@@ -227,6 +234,21 @@ __device__ __forceinline__ void mma_f8(uint32_t d, uint64_t a, uint64_t b, uint3
       "{\n.reg .pred p;\nsetp.ne.b32 p, 0, 0;\n"
       "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
       "l"(a), "l"(b), "r"(idesc));
+}
+// K-major operand of 16-bit elements: 8-row x 16-byte core matrices, K-adjacent
+// core matrices 128 bytes apart, 8-row groups `sbo` bytes apart.
+__device__ __forceinline__ uint64_t kmajor_desc_sbo(const void* smem, uint32_t sbo) {
+  const uint32_t a = su32(smem);
+  return static_cast<uint64_t>((a >> 4) & 0x3FFFu) | (static_cast<uint64_t>(128 >> 4) << 16) |
+         (static_cast<uint64_t>(sbo >> 4) << 32) | (static_cast<uint64_t>(1) << 46);
+}
+// kind::f16 MMA, f16 x f16 -> f32 (same instruction-descriptor layout as above:
+// format code 0 is f16 for this kind); accumulate into D when acc != 0.
+__device__ __forceinline__ void mma_f16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc));
 }
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(bar))
@@ -451,7 +473,7 @@ template <class SM>
 __device__ void producer(const TcArgs& p, SM& S, const CUtensorMap* wmap, const CUtensorMap* amap) {
   const int64_t B = p.K / 32;
   const int nst = static_cast<int>((B + KB - 1) / KB);
-  const uint32_t bytes = static_cast<uint32_t>(KB * 16 * (TW + p.tt));  // full boxes, zero fill included
+  const uint32_t bytes = static_cast<uint32_t>(KB * 16 * TW + SM::ARAW_ROW * p.tt);  // full boxes, zero fill included
   uint32_t gstage = 0;
   SegIter si = seg_iter(p);
   Seg sg;
@@ -463,7 +485,7 @@ __device__ void producer(const TcArgs& p, SM& S, const CUtensorMap* wmap, const 
       mbar_expect_tx(&S.full_raw[slot], bytes);
       const int32_t x = static_cast<int32_t>(s * KB * 16);
       tma_2d(S.wraw[slot], wmap, x, static_cast<int32_t>(T.wrow0), &S.full_raw[slot]);
-      tma_2d(S.araw[slot], amap, x, static_cast<int32_t>(T.m0), &S.full_raw[slot]);
+      tma_2d(S.araw[slot], amap, static_cast<int32_t>(s * SM::ARAW_ROW), static_cast<int32_t>(T.m0), &S.full_raw[slot]);
       ++gstage;
     }
   }
@@ -494,7 +516,14 @@ __device__ void mma_issuer(const TcArgs& p, SM& S, uint32_t tmem) {
       if (!mbar_wait(&S.f8_full[f], (gblk / SM::F8) & 1, S)) goto done;
       if (!mbar_wait(&S.tm_empty[tb], ((gblk / SM::NBUF) & 1) ^ 1, S)) goto done;
       tc_fence_after();
-      mma_f8(tmem + static_cast<uint32_t>(tb * SM::TT), kmajor_desc(S.wf8[f]), kmajor_desc(S.af8[f]), idesc);
+      const uint32_t dt = tmem + static_cast<uint32_t>(tb * SM::TT);
+      if constexpr (SM::ABITS == 4) {
+        mma_f8(dt, kmajor_desc(S.wf8[f]), kmajor_desc(S.af8[f]), idesc);
+      } else {  // two K = 16 halves of the block (core-matrix pairs 256 bytes apart)
+        const uint64_t ad = kmajor_desc_sbo(S.wf8[f], 512), bd = kmajor_desc_sbo(S.af8[f], 512);
+        mma_f16(dt, ad, bd, idesc, 0u);
+        mma_f16(dt, ad + (256 >> 4), bd + (256 >> 4), idesc, 1u);
+      }
       mma_commit(&S.tm_full[tb]);
       mma_commit(&S.f8_empty[f]);
     }
@@ -507,6 +536,26 @@ done:
     while (!mbar_try(&S.mma_done, 0) && gtime() - t0 < kTimeoutNs) {
     }
   }
+}
+
+// f16x2 of two int4 codes (the low nibbles of the bytes `sel` picks from w, as
+// q - 8) and of two int8 codes (bytes of x = codes ^ 0x80, as the signed value):
+// prmt places each byte under the f16 exponent byte 0x64 (the value 1024 + byte),
+// then one exact f16x2 subtraction removes the offset.
+__device__ __forceinline__ uint32_t f16x2_sub(uint32_t h, uint32_t c) {
+  __half2 a, b;
+  memcpy(&a, &h, 4);
+  memcpy(&b, &c, 4);
+  const __half2 r = __hsub2(a, b);
+  uint32_t out;
+  memcpy(&out, &r, 4);
+  return out;
+}
+__device__ __forceinline__ uint32_t q4_pair_f16(uint32_t w, uint32_t sel) {
+  return f16x2_sub(prmt(w, 0x64646464u, sel) & 0xFF0FFF0Fu, 0x64086408u);  // - 1032
+}
+__device__ __forceinline__ uint32_t s8_pair_f16(uint32_t x, uint32_t sel) {
+  return f16x2_sub(prmt(x, 0x64646464u, sel), 0x64806480u);  // - 1152
 }
 
 // Stage s's four scales of one row: a vector load when the row's groups are
@@ -541,8 +590,11 @@ __device__ void converters(const TcArgs& p, SM& S) {
   const int lane = threadIdx.x & 31;
   const int k = ct & 3;
   const int r0 = ct >> 2;
+  constexpr int AROW = SM::ARAW_ROW;        // raw activation bytes per row and stage
+  constexpr int SBO = 256 * SM::OPB;        // operand bytes per 8-row group of a block
   const uint32_t src_off = static_cast<uint32_t>(r0 * (KB * 16) + k * 16);
-  const uint32_t dst_off = static_cast<uint32_t>((r0 >> 3) * 256 + (r0 & 7) * 16);
+  const uint32_t asrc_off = static_cast<uint32_t>(r0 * AROW + k * (AROW / KB));
+  const uint32_t dst_off = static_cast<uint32_t>((r0 >> 3) * SBO + (r0 & 7) * 16);
   const int64_t B = p.K / 32;
   const int nst = static_cast<int>((B + KB - 1) / KB);
   constexpr int CT = 32 * SM::CONV;             // converter threads
@@ -590,6 +642,40 @@ __device__ void converters(const TcArgs& p, SM& S) {
         // weights: 128 rows, signed q - 8
         const uint8_t* ws = S.wraw[slot] + src_off;
         uint8_t* wd = S.wf8[f] + dst_off;
+        if constexpr (SM::ABITS == 8) {
+          // f16 operands: chunk c (elements 8c..8c+7) at c * 128; a code q becomes
+          // the f16 1024 + q (exponent byte 0x64 above the nibble), minus 1032
+#pragma unroll 4
+          for (int i = 0; i < (TW - r0 + RS - 1) / RS; ++i) {
+            const uint4 raw = *reinterpret_cast<const uint4*>(ws + i * RS * 64);
+            const uint32_t hx = raw.x >> 4, hy = raw.y >> 4, hz = raw.z >> 4, hw = raw.w >> 4;
+            uint8_t* d = wd + i * RS * 64;
+            *reinterpret_cast<uint4*>(d) = make_uint4(q4_pair_f16(raw.x, 0x4140u), q4_pair_f16(raw.x, 0x4342u),
+                                                      q4_pair_f16(raw.y, 0x4140u), q4_pair_f16(raw.y, 0x4342u));
+            *reinterpret_cast<uint4*>(d + 128) = make_uint4(q4_pair_f16(raw.z, 0x4140u), q4_pair_f16(raw.z, 0x4342u),
+                                                            q4_pair_f16(raw.w, 0x4140u), q4_pair_f16(raw.w, 0x4342u));
+            *reinterpret_cast<uint4*>(d + 256) = make_uint4(q4_pair_f16(hx, 0x4140u), q4_pair_f16(hx, 0x4342u),
+                                                            q4_pair_f16(hy, 0x4140u), q4_pair_f16(hy, 0x4342u));
+            *reinterpret_cast<uint4*>(d + 384) = make_uint4(q4_pair_f16(hz, 0x4140u), q4_pair_f16(hz, 0x4342u),
+                                                            q4_pair_f16(hw, 0x4140u), q4_pair_f16(hw, 0x4342u));
+          }
+          // activations: int8 codes s become 1024 + (s + 128), minus 1152
+          const uint8_t* as = S.araw[slot] + asrc_off;
+          uint8_t* ad = S.af8[f] + dst_off;
+#pragma unroll 2
+          for (int i = 0; i < a_iters; ++i) {
+            const uint4 r0v = *reinterpret_cast<const uint4*>(as + i * RS * AROW);
+            const uint4 r1v = *reinterpret_cast<const uint4*>(as + i * RS * AROW + 16);
+            const uint32_t v[8] = {r0v.x, r0v.y, r0v.z, r0v.w, r1v.x, r1v.y, r1v.z, r1v.w};
+            uint8_t* d = ad + i * RS * 64;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const uint32_t xa = v[2 * c] ^ 0x80808080u, xb = v[2 * c + 1] ^ 0x80808080u;
+              *reinterpret_cast<uint4*>(d + 128 * c) = make_uint4(s8_pair_f16(xa, 0x4140u), s8_pair_f16(xa, 0x4342u),
+                                                                  s8_pair_f16(xb, 0x4140u), s8_pair_f16(xb, 0x4342u));
+            }
+          }
+        } else {
 #pragma unroll 4
         for (int i = 0; i < (TW - r0 + RS - 1) / RS; ++i) {
           const uint4 raw = *reinterpret_cast<const uint4*>(ws + i * RS * 64);
@@ -602,7 +688,7 @@ __device__ void converters(const TcArgs& p, SM& S) {
           *reinterpret_cast<uint4*>(wd + i * RS * 32 + 128) = make_uint4(h0, h1, h2, h3);
         }
         // activations: nmma rows; the offset codes u = a + 8 are the e4m3 bytes
-        const uint8_t* as = S.araw[slot] + src_off;
+        const uint8_t* as = S.araw[slot] + asrc_off;
         uint8_t* ad = S.af8[f] + dst_off;
 #pragma unroll 4
         for (int i = 0; i < a_iters; ++i) {
@@ -613,6 +699,7 @@ __device__ void converters(const TcArgs& p, SM& S) {
               make_uint4(x0 & 0x0F0F0F0Fu, x1 & 0x0F0F0F0Fu, x2 & 0x0F0F0F0Fu, x3 & 0x0F0F0F0Fu);
           *reinterpret_cast<uint4*>(ad + i * RS * 32 + 128) = make_uint4(
               (x0 >> 4) & 0x0F0F0F0Fu, (x1 >> 4) & 0x0F0F0F0Fu, (x2 >> 4) & 0x0F0F0F0Fu, (x3 >> 4) & 0x0F0F0F0Fu);
+        }
         }
       }
       if constexpr (SM::CONV_SCALES) {
@@ -638,10 +725,15 @@ __device__ void converters(const TcArgs& p, SM& S) {
               const unsigned short dh = static_cast<unsigned short>(wd2 >> (16 * (kk & 1)));
               const short sw = static_cast<short>(ws2 >> (16 * (kk & 1)));
               const bool v = ok && kk < nbk;
-              const float dw = v ? __half2float(__ushort_as_half(dh)) * fp8_unscale() : 0.f;
-              S.sdw[sc][kk][n] = dw;
-              // -d_w * 8 S_w, exact: (d_w 2^18) * (S_w 2^-15), at most 20 significant bits
-              S.scorr[sc][kk][n] = v ? -dw * (static_cast<float>(sw) * 3.0517578125e-05f) : 0.f;
+              if constexpr (SM::ABITS == 4) {
+                const float dw = v ? __half2float(__ushort_as_half(dh)) * fp8_unscale() : 0.f;
+                S.sdw[sc][kk][n] = dw;
+                // -d_w * 8 S_w, exact: (d_w 2^18) * (S_w 2^-15), at most 20 significant bits
+                S.scorr[sc][kk][n] = v ? -dw * (static_cast<float>(sw) * 3.0517578125e-05f) : 0.f;
+              } else {  // f16 operands: D is P itself, no offset to remove
+                S.sdw[sc][kk][n] = v ? __half2float(__ushort_as_half(dh)) : 0.f;
+                S.scorr[sc][kk][n] = 0.f;
+              }
             }
           }
         }
@@ -852,10 +944,14 @@ __device__ void workers(const TcArgs& p, SM& S, uint32_t tmem) {
                 const int col = c0 + j;
                 if (col < T.ntok && n_in < T.rows_w) {
                   const int64_t m = T.m0 + col;
-                  // D = P + 8 S_w, an exact integer times 2^-18
-                  const int sw = p.w_sums[(T.wrow0 + n_in) * B + b];
-                  p.P[(m * p.N + n) * B + b] =
-                      static_cast<int32_t>(__uint_as_float(cur[j]) * fp8_unscale()) - 8 * sw;
+                  if constexpr (SM::ABITS == 4) {
+                    // D = P + 8 S_w, an exact integer times 2^-18
+                    const int sw = p.w_sums[(T.wrow0 + n_in) * B + b];
+                    p.P[(m * p.N + n) * B + b] =
+                        static_cast<int32_t>(__uint_as_float(cur[j]) * fp8_unscale()) - 8 * sw;
+                  } else {  // D = P, an exact integer
+                    p.P[(m * p.N + n) * B + b] = static_cast<int32_t>(__uint_as_float(cur[j]));
+                  }
                 }
               }
             } else {
@@ -925,11 +1021,11 @@ __device__ void workers(const TcArgs& p, SM& S, uint32_t tmem) {
   }
 }
 
-template <bool PARTIALS, int TTM>
-__global__ void __launch_bounds__(Smem<TTM>::THREADS, 1)
+template <bool PARTIALS, int TTM, int AB>
+__global__ void __launch_bounds__(Smem<TTM, AB>::THREADS, 1)
     w4a4_gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap amap,
                         const TcArgs p) {
-  using SmemT = Smem<TTM>;
+  using SmemT = Smem<TTM, AB>;
   // Smem is taken straight from the __shared__ array (no integer round trip), so
   // the compiler keeps every access in the shared address space (LDS/STS).  The
   // operands need 16-byte alignment (no swizzle), the TMA boxes 128 bytes.
@@ -1025,11 +1121,12 @@ cudaError_t codes_map(CUtensorMap* m, const uint8_t* codes, int64_t rows, int64_
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <bool PARTIALS, int TTM>
+template <bool PARTIALS, int TTM, int AB = 4>
 cudaError_t launch_tc(const CUtensorMap& wmap, const CUtensorMap& amap, const TcArgs& a, int64_t max_tiles,
                       cudaStream_t stream) {
-  auto kern = w4a4_gemm_tc_kernel<PARTIALS, TTM>;
-  constexpr size_t kSmemBytes = sizeof(Smem<TTM>);
+  auto kern = w4a4_gemm_tc_kernel<PARTIALS, TTM, AB>;
+  using SM = Smem<TTM, AB>;
+  constexpr size_t kSmemBytes = sizeof(SM);
   static bool configured[64] = {};
   static int regs_ok[64] = {};
   int dev = 0;
@@ -1044,7 +1141,6 @@ cudaError_t launch_tc(const CUtensorMap& wmap, const CUtensorMap& amap, const Tc
     cudaFuncAttributes fa{};
     e = cudaFuncGetAttributes(&fa, kern);
     if (e != cudaSuccess) return e;
-    using SM = Smem<TTM>;
     const int low_threads = SM::THREADS - 256;  // warpgroup 0 (and 3)
     regs_ok[dev] = (fa.numRegs * SM::THREADS >= low_threads * SM::REGS_LOW + 256 * SM::REGS_HIGH) ? 1 : -1;
     configured[dev] = true;
@@ -1052,7 +1148,7 @@ cudaError_t launch_tc(const CUtensorMap& wmap, const CUtensorMap& amap, const Tc
   if (regs_ok[dev] < 0) return cudaErrorInvalidConfiguration;
   int64_t grid = max_tiles < num_sms() ? max_tiles : num_sms();
   if (grid < 1) grid = 1;
-  kern<<<static_cast<unsigned>(grid), Smem<TTM>::THREADS, kSmemBytes, stream>>>(wmap, amap, a);
+  kern<<<static_cast<unsigned>(grid), SM::THREADS, kSmemBytes, stream>>>(wmap, amap, a);
   return cudaGetLastError();
 }
 
@@ -1087,10 +1183,10 @@ constexpr int64_t kSkMaxTiles = 32768;
 constexpr size_t kSkTicketBytes = static_cast<size_t>(kSkMaxTiles) * 8 * sizeof(uint32_t);  // 1 MiB
 constexpr size_t kSkPartBytes = size_t(8) * 1024 * sizeof(float4);  // one CTA segment: 8 warps x 32 x 32 float4
 
-SkPlan plan_stream_k(int64_t M, int64_t N, int64_t K) {
+SkPlan plan_stream_k(int64_t M, int64_t N, int64_t K, int ttm = kDenseTT) {
   SkPlan pl{};
   if (M <= 0 || N <= 0 || K <= 0) return pl;
-  const int64_t tt = token_tile(M, kDenseTT);
+  const int64_t tt = token_tile(M, ttm);
   const int64_t tiles = ((N + TW - 1) / TW) * ((M + tt - 1) / tt);
   const int64_t nst = (K / 32 + KB - 1) / KB;
   const int64_t sms = num_sms();
@@ -1109,7 +1205,13 @@ SkPlan plan_stream_k(int64_t M, int64_t N, int64_t K) {
 
 }  // namespace
 
+// The exact path's product runs the 128-column instance with int8 activations.
+constexpr int kW4A8TT = 128;
+
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) { return plan_stream_k(M, N, K).ws_bytes; }
+size_t gemm_w4a8_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  return plan_stream_k(M, N, K, kW4A8TT).ws_bytes;
+}
 
 cudaError_t encode_2d_map(CUtensorMap* m, CUtensorMapDataType dtype, const void* base, uint64_t inner, uint64_t rows,
                           uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swizzle) {
@@ -1157,6 +1259,32 @@ cudaError_t launch_gemm_tc(const uint8_t* w_codes, const uint16_t* w_scales, con
     grid = pl.grid;
   }
   return launch_tc<false, kDenseTT>(wmap, amap, a, grid, stream);
+}
+
+cudaError_t launch_gemm_w4a8(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums, int64_t N,
+                             const int8_t* a_codes, const float* a_scales, int64_t M, int64_t K, float* y, int64_t ldy,
+                             int32_t* P, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  TcArgs a{};
+  a.w_scales = w_scales; a.w_sums = w_sums; a.a_scales = a_scales;
+  a.M = M; a.N = N; a.K = K; a.y = y; a.ldy = ldy; a.P = P;
+  a.tt = token_tile(M, kW4A8TT);
+  CUtensorMap wmap, amap;
+  cudaError_t e = codes_map(&wmap, w_codes, N, K, TW);
+  // int8 codes [M][K]: box of 4 blocks (128 bytes) x tt rows
+  if (e == cudaSuccess)
+    e = encode_2d_map(&amap, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_codes, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
+                      static_cast<uint64_t>(K), KB * 32, static_cast<uint32_t>(a.tt), CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (e != cudaSuccess) return e;
+  int64_t grid = ((N + TW - 1) / TW) * ((M + a.tt - 1) / a.tt);
+  if (P) return launch_tc<true, kW4A8TT, 8>(wmap, amap, a, grid, stream);
+  const SkPlan pl = plan_stream_k(M, N, K, kW4A8TT);
+  if (pl.on && ws && ws_bytes >= pl.ws_bytes) {
+    a.sk_units = pl.units;
+    a.sk_count = static_cast<uint32_t*>(ws);
+    a.sk_part = reinterpret_cast<float4*>(static_cast<uint8_t*>(ws) + pl.count_bytes);
+    grid = pl.grid;
+  }
+  return launch_tc<false, kW4A8TT, 8>(wmap, amap, a, grid, stream);
 }
 
 cudaError_t launch_gemm_tc_routed(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums, int E,

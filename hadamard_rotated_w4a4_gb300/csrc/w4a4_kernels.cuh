@@ -36,6 +36,9 @@ cudaError_t id_static_scratch(void** addr);
 
 cudaError_t launch_act_rotate_quantize(const float* x, int64_t M, int64_t K, int64_t ldx, int rotate,
                                        uint8_t* codes, float* scales, cudaStream_t stream);
+// The exact path's 8-bit activations: int8 codes [M][K] (element order), fp32 scales.
+cudaError_t launch_act_rotate_quantize8(const float* x, int64_t M, int64_t K, int64_t ldx, int rotate,
+                                        int8_t* codes, float* scales, cudaStream_t stream);
 cudaError_t launch_pack_q4_0(const void* w, int w_dtype, int64_t N, int64_t K, int64_t ldw, int rotate,
                              uint8_t* codes, uint16_t* scales, int16_t* sums, cudaStream_t stream);
 cudaError_t launch_import_q4_0(const void* blocks, int64_t N, int64_t K, uint8_t* codes, uint16_t* scales,
@@ -48,6 +51,12 @@ cudaError_t launch_gemm_tc(const uint8_t* w_codes, const uint16_t* w_scales, con
                            const float* a_scales, int64_t M, int64_t K, float* y, int64_t ldy, int32_t* P,
                            void* ws, size_t ws_bytes, cudaStream_t stream);
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
+// The exact path (rotated Q4_0 weights x int8 activations, f16 tensor-core
+// MMAs): dense product (P == nullptr) or exact partials; workspace as above.
+cudaError_t launch_gemm_w4a8(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums, int64_t N,
+                             const int8_t* a_codes, const float* a_scales, int64_t M, int64_t K, float* y, int64_t ldy,
+                             int32_t* P, void* ws, size_t ws_bytes, cudaStream_t stream);
+size_t gemm_w4a8_workspace_bytes(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_gemm_tc_routed(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums, int E,
                                   int64_t N,
                                   const uint8_t* g_codes, const float* g_scales, int64_t K, int64_t npairs,

@@ -67,6 +67,7 @@ typedef enum {
 /* Operand tags: a magic in the high half, flags in the low half. */
 #define W4A4_TAG_Q4_0 0x51340000u    /* Q4_0 weights                          */
 #define W4A4_TAG_ACT4 0x41340000u    /* int4 activations                      */
+#define W4A4_TAG_ACT8 0x41380000u    /* int8 activations (the exact path)     */
 #define W4A4_TAG_MAGIC_MASK 0xFFFF0000u
 #define W4A4_TAG_ROTATED 0x00000001u /* values were rotated by H32 per block  */
 
@@ -109,12 +110,29 @@ typedef struct {
   uint32_t tag; /* W4A4_TAG_ACT4 | (W4A4_TAG_ROTATED if rotated) */
 } w4a4_act4;
 
+/*
+ * int8 activations of the exact path, per 32-element block along K (section
+ * "Hadamard-rotated Q4_0: W4A4 prompt processing": with W4A4 off, a rotated
+ * file runs on the exact int8 path):
+ *   codes : device, [rows][K] int8 in element order, each in -127..127.
+ *   scales: device, [rows][K/32] fp32, the block scale d_a = amax / 127.
+ */
+typedef struct {
+  int8_t* codes;
+  float* scales;
+  int64_t rows;
+  int64_t K;
+  uint32_t tag; /* W4A4_TAG_ACT8 | (W4A4_TAG_ROTATED if rotated) */
+} w4a4_act8;
+
 /* Bytes needed for the two arrays of a Q4_0 / int4 operand (0 if K is invalid). */
 size_t w4a4_q4_0_codes_bytes(int64_t rows, int64_t K);
 size_t w4a4_q4_0_scales_bytes(int64_t rows, int64_t K);
 size_t w4a4_q4_0_sums_bytes(int64_t rows, int64_t K);
 size_t w4a4_act4_codes_bytes(int64_t rows, int64_t K);
 size_t w4a4_act4_scales_bytes(int64_t rows, int64_t K);
+size_t w4a4_act8_codes_bytes(int64_t rows, int64_t K);
+size_t w4a4_act8_scales_bytes(int64_t rows, int64_t K);
 
 /*
  * h32_q4_0_pack_weights -- rotate weights per 32-block along K and quantise to
@@ -189,6 +207,32 @@ w4a4_status w4a4_gemm(const w4a4_q4_0* w, const w4a4_act4* a, float* y, int64_t 
 /* Workspace bytes for w4a4_gemm at this shape on the current device; 0 when the
  * whole-tile schedule is used (no workspace needed). */
 size_t w4a4_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/*
+ * The exact path: rotated Q4_0 weights times int8 activations (section
+ * "Hadamard-rotated Q4_0: W4A4 prompt processing" compares W4A4 with it, about
+ * 400 against 509 tok/s on the pages' hardware).
+ *
+ * w4a8_rotate_quantize_act -- as w4a4_rotate_quantize_act, with 8-bit codes:
+ *   per block, y as there; a = max |y|; d_a = a / 127 (fp32, stored);
+ *   q = clamp(round_half_away(y * (1/d_a)), -127, 127) (q = 0 when d_a = 0).
+ *   out->codes / out->scales are caller buffers of w4a4_act8_codes_bytes /
+ *   _scales_bytes; rows, K and tag are written.
+ *
+ * w4a8_gemm -- Y[m][n] = sum_b d_w d_a P with P = sum_j (q_w - 8) q_a exact;
+ *   arguments, layout, workspace and errors as w4a4_gemm (its workspace size
+ *   from w4a8_gemm_workspace_bytes).  The integer products run as f16
+ *   tensor-core MMAs, in which every int4 and int8 value and every 32-term
+ *   block sum is exact.
+ *
+ * w4a8_gemm_partials -- the exact P[m][n][b] (int32 [M][N][K/32]), |P| <= 32512.
+ */
+w4a4_status w4a8_rotate_quantize_act(const float* x, int64_t M, int64_t K, int64_t ldx, int rotate,
+                                     w4a4_act8* out, w4a4_stream_t stream);
+w4a4_status w4a8_gemm(const w4a4_q4_0* w, const w4a4_act8* a, float* y, int64_t ldy, void* ws,
+                      size_t ws_bytes, w4a4_stream_t stream);
+w4a4_status w4a8_gemm_partials(const w4a4_q4_0* w, const w4a4_act8* a, int32_t* P, w4a4_stream_t stream);
+size_t w4a8_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 /*
  * w4a4_gemm_partials -- the exact per-block integer dot products

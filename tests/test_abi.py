@@ -155,3 +155,18 @@ def test_gemm_workspace_query_and_short_workspace(lib):
     s, _ = status(lib, "w4a4_gemm", ctypes.byref(q4(rows=640, K=1024)), ctypes.byref(a4(rows=300, K=1024)), FAKE,
                   640, FAKE + 8, need, None)
     assert s == "W4A4_ERR_ALIGNMENT"
+
+
+def test_exact_path_validation(lib):
+    assert lib.w4a4_act8_codes_bytes(3, 64) == 192
+    assert lib.w4a4_act8_scales_bytes(3, 64) == 32  # 3 x 2 fp32, padded to 16 bytes
+    a8 = _Act4Desc(FAKE, FAKE, 64, 256, w4.TAG_ACT8 | 1)
+    # an int4 descriptor is not an int8 one
+    s, _ = status(lib, "w4a8_gemm", ctypes.byref(q4()), ctypes.byref(a4()), FAKE, 64, None, 0, None)
+    assert s == "W4A4_ERR_INVALID_ARG"
+    s, _ = status(lib, "w4a8_gemm", ctypes.byref(q4(rotated=False)), ctypes.byref(a8), FAKE, 64, None, 0, None)
+    assert s == "W4A4_ERR_MISMATCH"
+    s, _ = status(lib, "w4a8_gemm_partials", ctypes.byref(q4(K=512)), ctypes.byref(a8), FAKE, None)
+    assert s == "W4A4_ERR_MISMATCH"
+    d = _Act4Desc(FAKE, FAKE, 0, 0, 0)
+    assert status(lib, "w4a8_rotate_quantize_act", FAKE, 4, 100, 100, 1, ctypes.byref(d), None)[0] == "W4A4_ERR_INVALID_ARG"
