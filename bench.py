@@ -413,6 +413,20 @@ def run_ours(args, shape) -> dict | None:
                                                                     stream=st), nk)
     gemm_avg = graph_time(lambda i, st: w4.w4a4_gemm(sets[i % nsets][0], sets[i % nsets][2], y=sets[i % nsets][3],
                                                      ws=gws, stream=st), nk)
+    # the exact path (int8 activations) on the same sets: the pages' comparison
+    exact = None
+    if not args.no_exact and world == 1:
+        a8s = [w4.alloc_act8(M, K, dev) for _ in range(nsets)]
+        ws8 = torch.zeros(max(16, w4.w4a8_gemm_workspace_bytes(M, N, K)), dtype=torch.uint8, device=dev)
+        act8_avg = graph_time(lambda i, st: w4.w4a8_rotate_quantize_act(sets[i % nsets][1], out=a8s[i % nsets],
+                                                                         stream=st), nk)
+        gemm8_avg = graph_time(lambda i, st: w4.w4a8_gemm(sets[i % nsets][0], a8s[i % nsets], y=sets[i % nsets][3],
+                                                          ws=ws8, stream=st), nk)
+        exact = {"what": "rotated Q4_0 x int8 activations (the pages' exact path), same workload",
+                 "act_ms": act8_avg, "gemm_ms": gemm8_avg,
+                 "gemm_effective_tops": 2.0 * M * N * K / (gemm8_avg * 1e-3) / 1e12,
+                 "w4a4_speedup": (act8_avg + gemm8_avg) / (act_avg + gemm_avg)}
+        del a8s, ws8
     w4.w4a4_check()
     if world > 1:
         tt = torch.tensor([total_ms], device=dev)
@@ -506,6 +520,7 @@ def run_ours(args, shape) -> dict | None:
         "pct_int8_peak": (eff_tops_gemm / int8_peak) if int8_peak else None,
         "prefill_tok_s_proxy": proxy,
         "moe": moe,
+        "exact_path": exact,
         "kernel_ms": {"act_rotate_quantize": act_avg, "gemm": gemm_avg},
         "pack_weights_ms": pack_ms,
         "probes": probes,
@@ -532,6 +547,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-proxy", action="store_true", help="skip the per-layer prefill proxy")
     ap.add_argument("--no-moe", action="store_true", help="skip the expert-routed workload timing")
+    ap.add_argument("--no-exact", action="store_true", help="skip the exact-path (int8 activations) timing")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
