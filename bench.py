@@ -427,6 +427,19 @@ def run_ours(args, shape) -> dict | None:
                  "gemm_effective_tops": 2.0 * M * N * K / (gemm8_avg * 1e-3) / 1e12,
                  "w4a4_speedup": (act8_avg + gemm8_avg) / (act_avg + gemm_avg)}
         del a8s, ws8
+    # a drafter's verification batch: the first 8 tokens of the workload
+    verify = None
+    if not args.no_verify and world == 1:
+        x8 = sets[0][1][:8].contiguous()
+        a4v = w4.w4a4_rotate_quantize_act(x8)
+        y8 = torch.empty(8, N, dtype=torch.float32, device=dev)
+        wsv = torch.zeros(max(16, w4.w4a4_gemm_workspace_bytes(8, N, K)), dtype=torch.uint8, device=dev)
+        tc_ms = graph_time(lambda i, st: w4.w4a4_gemm(sets[i % nsets][0], a4v, y=y8, ws=wsv, stream=st), nk)
+        sm_ms = graph_time(lambda i, st: w4.w4a4_gemm_small_m(sets[i % nsets][0], a4v, y=y8, stream=st), nk)
+        wbytes = N * K // 2 + N * (K // 32) * 2
+        verify = {"what": "8-token verification batch, same weights", "tensor_core_ms": tc_ms, "small_m_ms": sm_ms,
+                  "small_m_weight_gbs": wbytes / (sm_ms * 1e-3) / 1e9}
+        del x8, a4v, y8, wsv
     w4.w4a4_check()
     if world > 1:
         tt = torch.tensor([total_ms], device=dev)
@@ -521,6 +534,7 @@ def run_ours(args, shape) -> dict | None:
         "prefill_tok_s_proxy": proxy,
         "moe": moe,
         "exact_path": exact,
+        "verification_batch": verify,
         "kernel_ms": {"act_rotate_quantize": act_avg, "gemm": gemm_avg},
         "pack_weights_ms": pack_ms,
         "probes": probes,
@@ -548,6 +562,7 @@ def main():
     ap.add_argument("--no-proxy", action="store_true", help="skip the per-layer prefill proxy")
     ap.add_argument("--no-moe", action="store_true", help="skip the expert-routed workload timing")
     ap.add_argument("--no-exact", action="store_true", help="skip the exact-path (int8 activations) timing")
+    ap.add_argument("--no-verify", action="store_true", help="skip the 8-token verification-batch timing")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -34,6 +34,7 @@ __all__ = [
     "w4a4_gemm", "w4a4_gemm_workspace_bytes", "w4a4_gemm_partials", "w4a4_gemm_id", "w4a4_gemm_id_status",
     "w4a4_gemm_id_workspace_bytes", "w4a4_gemm_id_static", "w4a4_check", "STATUS",
     "Act8", "w4a8_rotate_quantize_act", "w4a8_gemm", "w4a8_gemm_partials", "w4a8_gemm_workspace_bytes",
+    "w4a4_gemm_small_m",
 ]
 
 STATUS = {
@@ -51,7 +52,7 @@ EXPORTS = [
     "w4a4_q4_0_codes_bytes", "w4a4_q4_0_scales_bytes", "w4a4_q4_0_sums_bytes", "w4a4_act4_codes_bytes",
     "w4a4_act4_scales_bytes", "h32_q4_0_pack_weights", "q4_0_import", "w4a4_rotate_quantize_act", "w4a4_gemm", "w4a4_gemm_workspace_bytes",
     "w4a4_gemm_partials", "w4a4_gemm_id", "w4a4_gemm_id_workspace_bytes", "w4a4_gemm_id_status", "w4a4_gemm_id_static", "w4a4_check", "w4a4_last_error",
-    "w4a4_status_name", "w4a4_abi_version", "w4a4_act8_codes_bytes", "w4a4_act8_scales_bytes",
+    "w4a4_status_name", "w4a4_abi_version", "w4a4_act8_codes_bytes", "w4a4_act8_scales_bytes", "w4a4_gemm_small_m",
     "w4a8_rotate_quantize_act", "w4a8_gemm", "w4a8_gemm_partials", "w4a8_gemm_workspace_bytes",
 ]
 
@@ -105,6 +106,7 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.w4a8_gemm.argtypes = [ctypes.POINTER(_Q4_0Desc), ctypes.POINTER(_Act4Desc), vp, i64, vp, u, vp]
     lib.w4a8_gemm_partials.argtypes = [ctypes.POINTER(_Q4_0Desc), ctypes.POINTER(_Act4Desc), vp, vp]
     lib.w4a8_gemm_workspace_bytes.argtypes, lib.w4a8_gemm_workspace_bytes.restype = [i64, i64, i64], u
+    lib.w4a4_gemm_small_m.argtypes = [ctypes.POINTER(_Q4_0Desc), ctypes.POINTER(_Act4Desc), vp, i64, vp]
     lib.w4a4_gemm_partials.argtypes = [ctypes.POINTER(_Q4_0Desc), ctypes.POINTER(_Act4Desc), vp, vp]
     lib.w4a4_gemm_id.argtypes = [ctypes.POINTER(_Q4_0Desc), i32, i64, ctypes.POINTER(_Act4Desc), vp, i64, i32, i32,
                                  vp, vp, u, vp]
@@ -115,7 +117,7 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.w4a4_check.argtypes = [vp]
     for name in ("h32_q4_0_pack_weights", "q4_0_import", "w4a4_rotate_quantize_act", "w4a4_gemm",
                  "w4a4_gemm_partials", "w4a4_gemm_id", "w4a4_gemm_id_status", "w4a4_check",
-                 "w4a8_rotate_quantize_act", "w4a8_gemm", "w4a8_gemm_partials"):
+                 "w4a8_rotate_quantize_act", "w4a8_gemm", "w4a8_gemm_partials", "w4a4_gemm_small_m"):
         getattr(lib, name).restype = ctypes.c_int
     lib.w4a4_last_error.argtypes, lib.w4a4_last_error.restype = [], ctypes.c_char_p
     lib.w4a4_status_name.argtypes, lib.w4a4_status_name.restype = [ctypes.c_int], ctypes.c_char_p
@@ -318,6 +320,20 @@ def w4a4_gemm(w: Q4_0Weights, a: Act4, y: torch.Tensor | None = None, ws: torch.
     ws_ptr, ws_bytes = (ws.data_ptr(), ws.numel() * ws.element_size()) if ws is not None else (None, 0)
     _check(load_library().w4a4_gemm(ctypes.byref(w.desc()), ctypes.byref(a.desc()), y.data_ptr(), ldy, ws_ptr,
                                     ws_bytes, _stream(stream)))
+    return y
+
+
+def w4a4_gemm_small_m(w: Q4_0Weights, a: Act4, y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """w4a4_gemm for 1 to 8 activation rows (a verification batch): the weight-streaming kernel,
+    bit for bit the tensor-core kernel's whole-tile result."""
+    if y is None:
+        y = torch.empty(a.rows, w.rows, dtype=torch.float32, device=w.codes.device)
+    _cuda(y, "y")
+    if y.dtype != torch.float32 or y.dim() != 2 or y.stride(1) != 1:
+        raise ValueError("y must be a 2-D fp32 tensor with unit stride along N")
+    ldy = y.stride(0) if y.shape[0] > 1 else max(w.rows, 1)
+    _check(load_library().w4a4_gemm_small_m(ctypes.byref(w.desc()), ctypes.byref(a.desc()), y.data_ptr(), ldy,
+                                            _stream(stream)))
     return y
 
 

@@ -222,6 +222,22 @@ w4a4_status w4a4_gemm(const w4a4_q4_0* w, const w4a4_act4* a, float* y, int64_t 
                                           ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream)), fn);
 }
 
+w4a4_status w4a4_gemm_small_m(const w4a4_q4_0* w, const w4a4_act4* a, float* y, int64_t ldy, w4a4_stream_t stream) {
+  const char* fn = "w4a4_gemm_small_m";
+  w4a4_status s = check_q4_0(w, fn);
+  if (s != W4A4_OK) return s;
+  if ((s = check_act4(a, fn)) != W4A4_OK) return s;
+  if ((s = check_pair(w, a, fn)) != W4A4_OK) return s;
+  const int64_t M = a->rows, N = w->rows;
+  if (M > 8) return fail(W4A4_ERR_UNSUPPORTED, "%s: %lld activation rows; this kernel takes 1 to 8", fn, (long long)M);
+  if (ldy < N) return fail(W4A4_ERR_INVALID_ARG, "%s: ldy=%lld < N=%lld", fn, (long long)ldy, (long long)N);
+  if (M == 0 || N == 0) return ok();
+  if (!y) return fail(W4A4_ERR_INVALID_ARG, "%s: y is NULL", fn);
+  if ((reinterpret_cast<uintptr_t>(y) & 3u) != 0) return fail(W4A4_ERR_ALIGNMENT, "%s: y must be 4-byte aligned", fn);
+  return cuda_status(w4a4::launch_gemm_small_m(w->codes, w->scales, N, a->codes, a->scales, static_cast<int>(M), a->K,
+                                               y, ldy, reinterpret_cast<cudaStream_t>(stream)), fn);
+}
+
 w4a4_status w4a4_gemm_partials(const w4a4_q4_0* w, const w4a4_act4* a, int32_t* P, w4a4_stream_t stream) {
   const char* fn = "w4a4_gemm_partials";
   w4a4_status s = check_q4_0(w, fn);

@@ -57,6 +57,10 @@ cudaError_t launch_gemm_w4a8(const uint8_t* w_codes, const uint16_t* w_scales, c
                              const int8_t* a_codes, const float* a_scales, int64_t M, int64_t K, float* y, int64_t ldy,
                              int32_t* P, void* ws, size_t ws_bytes, cudaStream_t stream);
 size_t gemm_w4a8_workspace_bytes(int64_t M, int64_t N, int64_t K);
+// Small token batches (1 <= M <= 8): CUDA-core kernel, bit-identical to the
+// tensor-core kernel's whole-tile schedule.
+cudaError_t launch_gemm_small_m(const uint8_t* w_codes, const uint16_t* w_scales, int64_t N, const uint8_t* a_codes,
+                                const float* a_scales, int M, int64_t K, float* y, int64_t ldy, cudaStream_t stream);
 cudaError_t launch_gemm_tc_routed(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums, int E,
                                   int64_t N,
                                   const uint8_t* g_codes, const float* g_scales, int64_t K, int64_t npairs,

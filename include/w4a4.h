@@ -209,6 +209,17 @@ w4a4_status w4a4_gemm(const w4a4_q4_0* w, const w4a4_act4* a, float* y, int64_t 
 size_t w4a4_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 /*
+ * w4a4_gemm_small_m -- w4a4_gemm for batches of 1 to 8 tokens (a drafter's
+ * verification batch; the engine docs page above keeps a row-tiled Q4_0 kernel
+ * for 8-column verification batches, each weight unpacked once for all columns).
+ * A weight-streaming CUDA-core kernel; its output is bit for bit that of
+ * w4a4_gemm without a workspace (the whole-tile schedule).  Arguments, layouts
+ * and errors as w4a4_gemm; a->rows > 8 is W4A4_ERR_UNSUPPORTED.
+ */
+w4a4_status w4a4_gemm_small_m(const w4a4_q4_0* w, const w4a4_act4* a, float* y, int64_t ldy,
+                              w4a4_stream_t stream);
+
+/*
  * The exact path: rotated Q4_0 weights times int8 activations (section
  * "Hadamard-rotated Q4_0: W4A4 prompt processing" compares W4A4 with it, about
  * 400 against 509 tok/s on the pages' hardware).
