@@ -36,6 +36,13 @@ function                       pinned by
 ``w4a8_matmul``                brute-force fp64 loops; constant-block closed
                                form d_w d_a P = 32 alpha beta
 ``exact_matmul``               brute-force fp64 loops
+``round_bf16`` / bf16_to_f32   hand-worked ties and overflow; torch's own
+                               fp32->bf16 conversion on random and edge values
+``rotate_activations_bf16``    unit vectors -> bf16(+-c) (hand-derived);
+                               rotate=False is bf16(x)
+``w4a16_matmul``               brute-force fp64 loops; Q4_0-exact weights and
+                               bf16 activations reduce it to x @ w^T; constant
+                               blocks: 32 d_w alpha (q - 8)
 =============================  ==============================================
 
 Every function above is pinned; none is "parity unpinned".  The informative
@@ -57,8 +64,11 @@ from .quant import (
     quantize_activations,
     quantize_act_int8,
     quantize_activations_int8,
+    round_bf16,
+    bf16_to_f32,
+    rotate_activations_bf16,
 )
-from .matmul import block_partials, w4a4_matmul, w4a4_matmul_id, w4a8_matmul, exact_matmul
+from .matmul import block_partials, w4a4_matmul, w4a4_matmul_id, w4a8_matmul, w4a16_matmul, exact_matmul
 
 __all__ = [
     "C_H32", "sylvester_h32", "fwht32", "rotate_h32",
@@ -66,5 +76,6 @@ __all__ = [
     "pack_nibbles", "unpack_nibbles", "act_codes_from_nibbles", "weight_codes_from_nibbles",
     "q4_0_to_aos", "q4_0_from_aos", "pack_weights", "quantize_activations",
     "quantize_act_int8", "quantize_activations_int8",
-    "block_partials", "w4a4_matmul", "w4a4_matmul_id", "w4a8_matmul", "exact_matmul",
+    "round_bf16", "bf16_to_f32", "rotate_activations_bf16",
+    "block_partials", "w4a4_matmul", "w4a4_matmul_id", "w4a8_matmul", "w4a16_matmul", "exact_matmul",
 ]

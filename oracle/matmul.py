@@ -93,6 +93,34 @@ def w4a8_matmul(wp: dict, ap8: dict, m_idx=None, n_idx=None) -> np.ndarray:
     return w4a4_matmul(wp, ap8, m_idx, n_idx)
 
 
+def w4a16_matmul(wp: dict, ap16: dict, m_idx=None, n_idx=None) -> np.ndarray:
+    """The rotate-only route: rotated Q4_0 weights times rotated activations that
+    were not quantised (bf16 values xr from ``rotate_activations_bf16``):
+
+        Y[m][n] = sum_b d_w[n][b] * sum_{j<32} xr[m][32b+j] * (q_w[n][32b+j] - 8)
+
+    in fp64.  Each product xr * (q - 8) has at most 8 + 4 significant bits and
+    each d_w * (block sum) is exact in fp64 for the value ranges here; the sums
+    over j and b round only in fp64.
+    """
+    wv, dw = _wvals(wp), np.asarray(wp["d16"], dtype=np.float64)
+    xr = np.asarray(ap16["xr"], dtype=np.float64)
+    if m_idx is not None:
+        xr = xr[np.asarray(m_idx)]
+    if n_idx is not None:
+        n_idx = np.asarray(n_idx)
+        wv, dw = wv[n_idx], dw[n_idx]
+    M, K = xr.shape
+    N = wv.shape[0]
+    B = K // 32
+    xb = xr.reshape(M, B, 32)
+    wb = wv.astype(np.float64).reshape(N, B, 32)
+    Y = np.zeros((M, N), dtype=np.float64)
+    for b in range(B):
+        Y += (xb[:, b, :] @ wb[:, b, :].T) * dw[:, b][None, :]
+    return Y
+
+
 def w4a4_matmul_id(wp_experts: dict, E: int, ap: dict, ids: np.ndarray,
                    act_per_slot: bool, n_idx=None) -> np.ndarray:
     """Expert-routed product: Y [M][top_k][N] in fp64.

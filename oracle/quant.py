@@ -194,3 +194,33 @@ def quantize_activations_int8(x: np.ndarray, rotate: bool = True) -> dict:
     y = rotate_h32(xf) if rotate else xf
     qa = quantize_act_int8(y)
     return {"codes8": qa["q"].copy(), "d_a": qa["d_a"], "q": qa["q"], "rotated": bool(rotate)}
+
+
+def round_bf16(v: np.ndarray) -> np.ndarray:
+    """fp32 values -> bf16 bit patterns (uint16), round to nearest, ties to even.
+
+    Integer arithmetic on the fp32 bits: add 0x7FFF plus the lowest kept bit,
+    keep the top 16 bits.  A finite value that rounds past the largest bf16
+    becomes infinity, as IEEE rounding does.
+    """
+    bits = np.asarray(v, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    keep_lsb = (bits >> 16) & 1
+    return ((bits + 0x7FFF + keep_lsb) >> 16).astype(np.uint16)
+
+
+def bf16_to_f32(h: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> fp32 values (exact widening)."""
+    return (np.asarray(h, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def rotate_activations_bf16(x: np.ndarray, rotate: bool = True) -> dict:
+    """The rotate-only route: activations [M][K] fp32 rotated per 32-block (the
+    same fp32 rotation the quantisers see) and not rounded to 4 bits; they are
+    carried as bf16 (round to nearest even), the tensor-core operand type.
+
+    Returns x16 (bf16 bits [M][K]) and xr (their fp32 values).
+    """
+    xf = np.asarray(x, dtype=np.float32)
+    y = rotate_h32(xf) if rotate else xf
+    h = round_bf16(y)
+    return {"x16": h, "xr": bf16_to_f32(h), "rotated": bool(rotate)}

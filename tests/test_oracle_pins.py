@@ -434,3 +434,126 @@ def test_int8_path_is_closer_than_int4_to_the_exact_product():
     e4 = np.abs(oracle.w4a4_matmul(wp, oracle.quantize_activations(d["x"])) - ref).mean()
     e8 = np.abs(oracle.w4a8_matmul(wp, oracle.quantize_activations_int8(d["x"])) - ref).mean()
     assert e8 < 0.1 * e4
+
+
+# ---------------------------------------------------------------- rotate-only route (bf16 activations)
+def test_bf16_rounding_hand_worked():
+    """Round to nearest even at the bf16 boundary (7 stored mantissa bits): the
+    fp32 values halfway between two bf16 neighbours go to the even one."""
+    cases = [
+        (1.0, 0x3F80),
+        (1.0 + 2.0 ** -8, 0x3F80),            # halfway 1 .. 1 + 2^-7, mantissa 0 is even
+        (1.0 + 3 * 2.0 ** -8, 0x3F82),        # halfway 1 + 2^-7 .. 1 + 2^-6, mantissa 2 is even
+        (1.0 + 2.0 ** -8 + 2.0 ** -20, 0x3F81),  # just past halfway rounds up
+        (-2.5, 0xC020),
+        (0.0, 0x0000),
+        (-0.0, 0x8000),
+        (2.0 ** -133, 0x0001),                # smallest bf16 subnormal, exact
+        (float(np.float32(3.3895314e38)), 0x7F7F),  # largest finite bf16, exact
+        (float(np.finfo(np.float32).max), 0x7F80),  # rounds past it: infinity
+    ]
+    v = np.array([c[0] for c in cases], dtype=np.float32)
+    got = oracle.round_bf16(v)
+    assert [int(g) for g in got] == [c[1] for c in cases]
+    # widening is exact: bf16 bits -> fp32 value with the low half zero
+    assert np.array_equal(oracle.bf16_to_f32(got[:8]).view(np.uint32), got[:8].astype(np.uint32) << 16)
+
+
+def test_bf16_rounding_matches_torch_conversion():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(31)
+    v = np.concatenate([
+        rng.standard_normal(20000).astype(np.float32) * np.float32(10.0) ** rng.integers(-30, 30, 20000),
+        # every fp32 whose low 16 bits are exactly 0x8000 (ties) or next to it
+        (rng.integers(0, 0x7F7F, 4000).astype(np.uint32) << 16 | np.uint32(0x8000)).view(np.float32),
+        (rng.integers(0, 0x7F7F, 4000).astype(np.uint32) << 16 | np.uint32(0x7FFF)).view(np.float32),
+        (rng.integers(0, 0x7F7F, 4000).astype(np.uint32) << 16 | np.uint32(0x8001)).view(np.float32),
+    ]).astype(np.float32)
+    v = np.concatenate([v, -v])
+    ref = torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(oracle.round_bf16(v), ref)
+
+
+def test_rotate_only_unit_vectors_hand_derived():
+    """e_i in a block rotates to c * (column i of H32): every entry +-c, and
+    c = 0x3E3504F3 rounds to the bf16 0x3E35 (low half 0x04F3 < 0x8000)."""
+    x = np.zeros((32, 64), dtype=np.float32)
+    for i in range(32):
+        x[i, 32 + i] = 1.0
+    r = oracle.rotate_activations_bf16(x)
+    assert np.all(r["x16"][:, :32] == 0)
+    want = np.where(H32.T > 0, 0x3E35, 0xBE35).astype(np.uint16)
+    assert np.array_equal(r["x16"][:, 32:], want)
+    # without the rotation the route is the plain bf16 rounding of x
+    y = np.random.default_rng(32).standard_normal((3, 96)).astype(np.float32)
+    assert np.array_equal(oracle.rotate_activations_bf16(y, rotate=False)["x16"], oracle.round_bf16(y))
+
+
+def test_w4a16_matmul_brute_force():
+    rng = np.random.default_rng(33)
+    w = rng.standard_normal((4, 64)).astype(np.float32)
+    x = rng.standard_normal((3, 64)).astype(np.float32) * 3
+    wp = oracle.pack_weights(w)
+    ap = oracle.rotate_activations_bf16(x)
+    Y = oracle.w4a16_matmul(wp, ap)
+    wq = wp["q"]
+    xr = [[struct.unpack("<f", struct.pack("<I", int(h) << 16))[0] for h in row] for row in ap["x16"]]
+    for m in range(3):
+        for n in range(4):
+            acc = Fraction(0)
+            for b in range(2):
+                s = sum(Fraction(xr[m][32 * b + j]) * (int(wq[n, 32 * b + j]) - 8) for j in range(32))
+                acc += Fraction(float(wp["d16"][n, b])) * s
+            assert abs(Y[m, n] - float(acc)) <= 1e-14 * max(1.0, abs(float(acc)))
+    Ys = oracle.w4a16_matmul(wp, ap, m_idx=[1], n_idx=[3, 0])
+    assert np.array_equal(Ys, Y[np.ix_([1], [3, 0])])
+
+
+def test_w4a16_reduces_to_plain_matmul_on_exact_inputs():
+    """Weights that Q4_0 stores exactly (each block d (q - 8) with a code 0 at
+    the signed max, fp16 d) and bf16 activations, no rotation: the route's
+    product is the ordinary matmul x @ w^T."""
+    rng = np.random.default_rng(34)
+    N, M, K = 5, 4, 128
+    B = K // 32
+    q = rng.integers(0, 16, (N, B, 32))
+    q[:, :, 0] = 0                                   # value -8 d: the signed max
+    q[:, :, 1:] = np.clip(q[:, :, 1:], 1, 15)        # |q - 8| <= 7 elsewhere
+    d = np.float16(rng.uniform(0.01, 0.2, (N, B)) * rng.choice([-1, 1], (N, B))).astype(np.float32)
+    w = (d[..., None] * (q - 8)).astype(np.float32).reshape(N, K)
+    x = oracle.bf16_to_f32(oracle.round_bf16(rng.standard_normal((M, K)).astype(np.float32)))
+    wp = oracle.pack_weights(w, rotate=False)
+    assert np.array_equal(wp["q"].reshape(N, B, 32), q) and np.array_equal(wp["d16"].astype(np.float32), d)
+    Y = oracle.w4a16_matmul(wp, oracle.rotate_activations_bf16(x, rotate=False))
+    ref = x.astype(np.float64) @ w.astype(np.float64).T
+    assert np.allclose(Y, ref, rtol=1e-13, atol=1e-13)
+
+
+def test_w4a16_constant_blocks_closed_form():
+    """Unrotated: weight block constant alpha (codes 0 everywhere, d = -alpha/8)
+    and activation block constant beta (bf16-exact): Y = sum_b 32 d (-8) beta."""
+    rng = np.random.default_rng(35)
+    B = 5
+    alpha = np.float32(rng.uniform(0.1, 2.0, B) * rng.choice([-1, 1], B))
+    beta = oracle.bf16_to_f32(oracle.round_bf16(np.float32(rng.uniform(0.1, 2.0, B) * rng.choice([-1, 1], B))))
+    w = np.repeat(alpha, 32).astype(np.float32)[None, :]
+    x = np.repeat(beta, 32).astype(np.float32)[None, :]
+    wp = oracle.pack_weights(w, rotate=False)
+    assert np.all(wp["q"] == 0)
+    Y = oracle.w4a16_matmul(wp, oracle.rotate_activations_bf16(x, rotate=False))[0, 0]
+    d = wp["d16"][0].astype(np.float64)
+    assert Y == pytest.approx(float(np.sum(32 * d * -8 * beta.astype(np.float64))), rel=1e-15)
+    assert abs(Y - float(np.sum(32 * alpha.astype(np.float64) * beta))) <= 2.0 ** -10 * float(np.sum(np.abs(32 * alpha * beta)))
+
+
+def test_rotate_only_is_closer_than_int8_to_the_exact_product():
+    """Against the exact Q4_0 weights times the unrounded rotated activations,
+    bf16 activations lose less than the int8 codes of the exact path."""
+    d = si.random_dense(16, 512, 24, seed=36)
+    wp = oracle.pack_weights(d["w_bf16"])
+    w_deq = ((wp["q"].astype(np.float64) - 8).reshape(24, 16, 32)
+             * wp["d16"].astype(np.float64)[..., None]).reshape(24, 512)
+    ref = oracle.exact_matmul(oracle.rotate_h32(d["x"]), w_deq)
+    e8 = np.abs(oracle.w4a8_matmul(wp, oracle.quantize_activations_int8(d["x"])) - ref).mean()
+    e16 = np.abs(oracle.w4a16_matmul(wp, oracle.rotate_activations_bf16(d["x"])) - ref).mean()
+    assert e16 < 0.5 * e8
