@@ -45,6 +45,7 @@ STATUS = {
 TAG_Q4_0 = 0x51340000
 TAG_ACT4 = 0x41340000
 TAG_ACT8 = 0x41380000
+TAG_ACT16 = 0x41420000
 TAG_ROTATED = 0x1
 
 #: every symbol include/w4a4.h declares
@@ -54,6 +55,7 @@ EXPORTS = [
     "w4a4_gemm_partials", "w4a4_gemm_id", "w4a4_gemm_id_workspace_bytes", "w4a4_gemm_id_status", "w4a4_gemm_id_static", "w4a4_check", "w4a4_last_error",
     "w4a4_status_name", "w4a4_abi_version", "w4a4_act8_codes_bytes", "w4a4_act8_scales_bytes", "w4a4_gemm_small_m",
     "w4a8_rotate_quantize_act", "w4a8_gemm", "w4a8_gemm_partials", "w4a8_gemm_workspace_bytes",
+    "w4a4_act16_values_bytes", "w4a16_rotate_act", "w4a16_gemm", "w4a16_gemm_workspace_bytes",
 ]
 
 
@@ -72,6 +74,11 @@ class _Q4_0Desc(ctypes.Structure):
 class _Act4Desc(ctypes.Structure):
     _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("rows", ctypes.c_int64),
                 ("K", ctypes.c_int64), ("tag", ctypes.c_uint32)]
+
+
+class _Act16Desc(ctypes.Structure):
+    _fields_ = [("values", ctypes.c_void_p), ("rows", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("tag", ctypes.c_uint32)]
 
 
 _LIB = None
@@ -106,6 +113,9 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.w4a8_gemm.argtypes = [ctypes.POINTER(_Q4_0Desc), ctypes.POINTER(_Act4Desc), vp, i64, vp, u, vp]
     lib.w4a8_gemm_partials.argtypes = [ctypes.POINTER(_Q4_0Desc), ctypes.POINTER(_Act4Desc), vp, vp]
     lib.w4a8_gemm_workspace_bytes.argtypes, lib.w4a8_gemm_workspace_bytes.restype = [i64, i64, i64], u
+    lib.w4a16_rotate_act.argtypes = [vp, i64, i64, i64, i32, ctypes.POINTER(_Act16Desc), vp]
+    lib.w4a16_gemm.argtypes = [ctypes.POINTER(_Q4_0Desc), ctypes.POINTER(_Act16Desc), vp, i64, vp, u, vp]
+    lib.w4a16_gemm_workspace_bytes.argtypes, lib.w4a16_gemm_workspace_bytes.restype = [i64, i64, i64], u
     lib.w4a4_gemm_small_m.argtypes = [ctypes.POINTER(_Q4_0Desc), ctypes.POINTER(_Act4Desc), vp, i64, vp]
     lib.w4a4_gemm_partials.argtypes = [ctypes.POINTER(_Q4_0Desc), ctypes.POINTER(_Act4Desc), vp, vp]
     lib.w4a4_gemm_id.argtypes = [ctypes.POINTER(_Q4_0Desc), i32, i64, ctypes.POINTER(_Act4Desc), vp, i64, i32, i32,
@@ -482,3 +492,66 @@ def w4a8_gemm_partials(w: Q4_0Weights, a: Act8, P: torch.Tensor | None = None, s
     _check(load_library().w4a8_gemm_partials(ctypes.byref(w.desc()), ctypes.byref(a.desc()), P.data_ptr(),
                                              _stream(stream)))
     return P
+
+
+# ---------------------------------------------------------------- the rotate-only route (bf16 activations)
+@dataclass
+class Act16:
+    """Rotated activations that were not quantised: bf16 values [rows][K] (element order)."""
+    values: torch.Tensor
+    rows: int
+    K: int
+    rotated: bool
+
+    @property
+    def tag(self) -> int:
+        return TAG_ACT16 | (TAG_ROTATED if self.rotated else 0)
+
+    def desc(self) -> _Act16Desc:
+        return _Act16Desc(self.values.data_ptr(), self.rows, self.K, self.tag)
+
+
+def alloc_act16(rows: int, K: int, device, rotated: bool = True) -> Act16:
+    lib = load_library()
+    if K <= 0 or K % 32:
+        raise W4A4Error(1, f"K={K} must be a positive multiple of 32")
+    nv = lib.w4a4_act16_values_bytes(rows, K)
+    buf = torch.empty(max(nv, 16), dtype=torch.uint8, device=device)
+    return Act16(buf[: 2 * rows * K].view(torch.bfloat16).view(rows, K), rows, K, rotated)
+
+
+def w4a16_rotate_act(x: torch.Tensor, rotate: bool = True, out: Act16 | None = None, stream=None) -> Act16:
+    """Rotate (H32) fp32 activations x [M][K] (CUDA) per 32-block and store them as bf16, not quantised."""
+    _cuda(x, "x")
+    if x.dtype != torch.float32 or x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be a 2-D fp32 tensor with unit stride along K")
+    M, K = x.shape
+    out = out or alloc_act16(M, K, x.device, rotate)
+    d = out.desc()
+    ldx = x.stride(0) if M > 1 else K
+    _check(load_library().w4a16_rotate_act(x.data_ptr(), M, K, ldx, int(rotate), ctypes.byref(d), _stream(stream)))
+    out.rotated = bool(rotate)
+    return out
+
+
+def w4a16_gemm_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(load_library().w4a16_gemm_workspace_bytes(M, N, K))
+
+
+def w4a16_gemm(w: Q4_0Weights, a: Act16, y: torch.Tensor | None = None, ws: torch.Tensor | None | bool = True,
+               stream=None) -> torch.Tensor:
+    """The rotate-only route: Y[m][n] = sum_b d_w sum_j y (q_w - 8) with bf16 activations (fp32 [M][N])."""
+    if y is None:
+        y = torch.empty(a.rows, w.rows, dtype=torch.float32, device=w.codes.device)
+    _cuda(y, "y")
+    if y.dtype != torch.float32 or y.dim() != 2 or y.stride(1) != 1:
+        raise ValueError("y must be a 2-D fp32 tensor with unit stride along N")
+    ldy = y.stride(0) if y.shape[0] > 1 else max(w.rows, 1)
+    if ws is True:
+        ws = gemm_workspace(a.rows, w.rows, w.K, y.device, stream, need=w4a16_gemm_workspace_bytes(a.rows, w.rows, w.K))
+    elif ws is False:
+        ws = None
+    ws_ptr, ws_bytes = (ws.data_ptr(), ws.numel() * ws.element_size()) if ws is not None else (None, 0)
+    _check(load_library().w4a16_gemm(ctypes.byref(w.desc()), ctypes.byref(a.desc()), y.data_ptr(), ldy, ws_ptr,
+                                     ws_bytes, _stream(stream)))
+    return y

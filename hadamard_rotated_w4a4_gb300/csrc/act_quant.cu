@@ -17,6 +17,8 @@
 // Butterfly order: stages h = 1, 2, 4, 8, 16, pairs (i, i + h) -> (a + b, a - b),
 // then one multiply by fl32(1/sqrt 32) -- the fp32 evaluation order the
 // quantiser's decisions are defined on.
+#include <cuda_bf16.h>
+
 #include "w4a4_kernels.cuh"
 
 namespace w4a4 {
@@ -52,15 +54,34 @@ __device__ __forceinline__ uint32_t nib(float y, float inv) {
 //             bytes in the Q4_0 nibble order;
 //   BITS = 8: d_a = amax / 127, int8 codes (round half away, clamp -127..127),
 //             32 bytes in element order (the exact path's activations);
+//   BITS = 16: no quantisation (the rotate-only route): the 32 rotated values
+//             as bf16, round to nearest even, 64 bytes in element order, no
+//             scale;
 // stored at block index i if ok.
+__device__ __forceinline__ void rotate_block(float (&y)[32]) {
+  fwht32(y);
+  const float cst = c_h32();
+#pragma unroll
+  for (int k = 0; k < 32; ++k) y[k] = __fmul_rn(y[k], cst);
+}
+
 template <int BITS>
 __device__ __forceinline__ void quantize_block(float (&y)[32], int rotate, bool ok, uint8_t* __restrict__ codes,
                                                float* __restrict__ scales, int64_t i) {
-  if (rotate) {
-    fwht32(y);
-    const float cst = c_h32();
+  if (rotate) rotate_block(y);
+  if constexpr (BITS == 16) {
+    uint32_t w[16];
 #pragma unroll
-    for (int k = 0; k < 32; ++k) y[k] = __fmul_rn(y[k], cst);
+    for (int t = 0; t < 16; ++t) {
+      const __nv_bfloat162 h = __floats2bfloat162_rn(y[2 * t], y[2 * t + 1]);  // .x = element 2t
+      memcpy(&w[t], &h, 4);
+    }
+    if (ok) {
+      uint4* dst = reinterpret_cast<uint4*>(codes) + 4 * i;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+    }
+    return;
   }
   float a = 0.f;
 #pragma unroll
@@ -262,13 +283,19 @@ __global__ void __launch_bounds__(32 * kTmaWarps) act_rotate_quantize_tma_kernel
       y[4 * j + 2] = v.z;
       y[4 * j + 3] = v.w;
     }
-    __syncwarp();  // every lane has its block in registers: the stage may be refilled
+    // Before the stage is refilled by the TMA (the async proxy), every lane's
+    // reads of it (the generic proxy) must have completed: the rotation consumes
+    // all 32 values first, and the proxy fence orders the reads before the copy
+    // lane 0 issues after the warp barrier.
+    if (rotate) rotate_block(y);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
     if (lane == 0 && issued < n_my) {
       tma_load_chunk(S.buf[wib][st], &xmap, static_cast<int32_t>((gw + issued * nw) * 32), &S.full[wib][st]);
       ++issued;
     }
     const int64_t i = (gw + it * nw) * 32 + lane;
-    quantize_block<BITS>(y, rotate, i < nblk, codes, scales, i);
+    quantize_block<BITS>(y, 0, i < nblk, codes, scales, i);
   }
   if (__any_sync(0xFFFFFFFFu, failed)) {
     // a load never completed: record it and wait (bounded) for the copies still
@@ -331,6 +358,11 @@ cudaError_t launch_act_rotate_quantize(const float* x, int64_t M, int64_t K, int
 cudaError_t launch_act_rotate_quantize8(const float* x, int64_t M, int64_t K, int64_t ldx, int rotate,
                                         int8_t* codes, float* scales, cudaStream_t stream) {
   return launch_act<8>(x, M, K, ldx, rotate, reinterpret_cast<uint8_t*>(codes), scales, stream);
+}
+
+cudaError_t launch_act_rotate_bf16(const float* x, int64_t M, int64_t K, int64_t ldx, int rotate, uint16_t* out,
+                                   cudaStream_t stream) {
+  return launch_act<16>(x, M, K, ldx, rotate, reinterpret_cast<uint8_t*>(out), nullptr, stream);
 }
 
 }  // namespace w4a4

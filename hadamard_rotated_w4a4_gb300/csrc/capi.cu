@@ -96,6 +96,17 @@ w4a4_status check_act8(const w4a4_act8* a, const char* fn) {
   return W4A4_OK;
 }
 
+w4a4_status check_act16(const w4a4_act16* a, const char* fn) {
+  if (!a) return fail(W4A4_ERR_INVALID_ARG, "%s: activation descriptor is NULL", fn);
+  if ((a->tag & W4A4_TAG_MAGIC_MASK) != W4A4_TAG_ACT16)
+    return fail(W4A4_ERR_INVALID_ARG, "%s: activation descriptor tag 0x%08x is not a bf16 tag", fn, a->tag);
+  w4a4_status s = check_k_rows(a->rows, a->K, fn);
+  if (s != W4A4_OK) return s;
+  if (a->rows > 0 && !a->values) return fail(W4A4_ERR_INVALID_ARG, "%s: activation values are NULL", fn);
+  if (!aligned16(a->values)) return fail(W4A4_ERR_ALIGNMENT, "%s: activation values must be 16-byte aligned", fn);
+  return W4A4_OK;
+}
+
 template <class A>
 w4a4_status check_pair(const w4a4_q4_0* w, const A* a, const char* fn) {
   if (w->K != a->K)
@@ -127,6 +138,10 @@ size_t w4a4_act8_codes_bytes(int64_t rows, int64_t K) {
   return round16(static_cast<size_t>(rows) * static_cast<size_t>(K));
 }
 size_t w4a4_act8_scales_bytes(int64_t rows, int64_t K) { return w4a4_act4_scales_bytes(rows, K); }
+size_t w4a4_act16_values_bytes(int64_t rows, int64_t K) {
+  if (!valid_k(K) || rows < 0) return 0;
+  return round16(static_cast<size_t>(rows) * static_cast<size_t>(K) * 2);
+}
 size_t w4a4_act4_scales_bytes(int64_t rows, int64_t K) {
   if (!valid_k(K) || rows < 0) return 0;
   return round16(static_cast<size_t>(rows) * static_cast<size_t>(K / 32) * 4);
@@ -295,6 +310,52 @@ w4a4_status w4a8_gemm(const w4a4_q4_0* w, const w4a4_act8* a, float* y, int64_t 
   }
   return cuda_status(w4a4::launch_gemm_w4a8(w->codes, w->scales, w->sums, N, a->codes, a->scales, M, a->K, y, ldy,
                                             nullptr, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream)), fn);
+}
+
+w4a4_status w4a16_rotate_act(const float* x, int64_t M, int64_t K, int64_t ldx, int rotate, w4a4_act16* out,
+                             w4a4_stream_t stream) {
+  const char* fn = "w4a16_rotate_act";
+  if (!out) return fail(W4A4_ERR_INVALID_ARG, "%s: out is NULL", fn);
+  w4a4_status s = check_k_rows(M, K, fn);
+  if (s != W4A4_OK) return s;
+  if (rotate != 0 && rotate != 1) return fail(W4A4_ERR_INVALID_ARG, "%s: rotate must be 0 or 1", fn);
+  if (ldx < K) return fail(W4A4_ERR_INVALID_ARG, "%s: ldx=%lld < K=%lld", fn, (long long)ldx, (long long)K);
+  if (M > 0 && (!x || !out->values)) return fail(W4A4_ERR_INVALID_ARG, "%s: NULL pointer", fn);
+  if (!aligned16(x) || !aligned16(out->values) || (ldx % 4) != 0)
+    return fail(W4A4_ERR_ALIGNMENT, "%s: pointers and rows (ldx * 4 bytes) must be 16-byte aligned", fn);
+  out->rows = M;
+  out->K = K;
+  out->tag = W4A4_TAG_ACT16 | (rotate ? W4A4_TAG_ROTATED : 0u);
+  if (M == 0) return ok();
+  return cuda_status(w4a4::launch_act_rotate_bf16(x, M, K, ldx, rotate, out->values,
+                                                  reinterpret_cast<cudaStream_t>(stream)), fn);
+}
+
+size_t w4a16_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  if (M < 0 || N < 0 || !valid_k(K)) return 0;
+  return w4a4::gemm_w4a8_workspace_bytes(M, N, K);
+}
+
+w4a4_status w4a16_gemm(const w4a4_q4_0* w, const w4a4_act16* a, float* y, int64_t ldy, void* ws, size_t ws_bytes,
+                       w4a4_stream_t stream) {
+  const char* fn = "w4a16_gemm";
+  w4a4_status s = check_q4_0(w, fn);
+  if (s != W4A4_OK) return s;
+  if ((s = check_act16(a, fn)) != W4A4_OK) return s;
+  if ((s = check_pair(w, a, fn)) != W4A4_OK) return s;
+  const int64_t M = a->rows, N = w->rows;
+  if (ldy < N) return fail(W4A4_ERR_INVALID_ARG, "%s: ldy=%lld < N=%lld", fn, (long long)ldy, (long long)N);
+  if (M == 0 || N == 0) return ok();
+  if (!y) return fail(W4A4_ERR_INVALID_ARG, "%s: y is NULL", fn);
+  if ((reinterpret_cast<uintptr_t>(y) & 3u) != 0) return fail(W4A4_ERR_ALIGNMENT, "%s: y must be 4-byte aligned", fn);
+  if (ws) {
+    const size_t need = w4a4::gemm_w4a8_workspace_bytes(M, N, a->K);
+    if (ws_bytes < need)
+      return fail(W4A4_ERR_WORKSPACE, "%s: workspace %zu bytes < %zu needed", fn, ws_bytes, need);
+    if (!aligned16(ws)) return fail(W4A4_ERR_ALIGNMENT, "%s: ws must be 16-byte aligned", fn);
+  }
+  return cuda_status(w4a4::launch_gemm_w4a16(w->codes, w->scales, w->sums, N, a->values, M, a->K, y, ldy, ws,
+                                             ws_bytes, reinterpret_cast<cudaStream_t>(stream)), fn);
 }
 
 w4a4_status w4a8_gemm_partials(const w4a4_q4_0* w, const w4a4_act8* a, int32_t* P, w4a4_stream_t stream) {

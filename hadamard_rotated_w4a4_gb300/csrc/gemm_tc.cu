@@ -39,6 +39,8 @@
 #include <cudaTypedefs.h>
 
 
+#include <cuda_bf16.h>
+
 #include "w4a4_kernels.cuh"
 
 namespace w4a4 {
@@ -82,7 +84,10 @@ constexpr uint32_t kWaitHintNs = W4A4_WAIT_HINT_NS;
 // AB: activation code width.  4 = the W4A4 product (int4 activations, e4m3
 // operands, one kind::f8f6f4 MMA per block); 8 = the exact path (int8
 // activations, f16 operands, two kind::f16 MMAs of K = 16 per block; int8 and
-// int4 values are exact in f16 and so are the 32-term block sums in fp32).
+// int4 values are exact in f16 and so are the 32-term block sums in fp32);
+// 16 = the rotate-only route (bf16 activations that were not quantised, bf16
+// weight operands q - 8, two kind::f16 MMAs per block with the bf16 format;
+// the block sums round in the tensor core's fp32 accumulation, d_a = 1).
 template <int TTM, int AB = 4>
 struct __align__(128) Smem {
   static constexpr int TT = TTM;
@@ -96,7 +101,7 @@ struct __align__(128) Smem {
   static constexpr int THREADS = TTM == 256 ? 384 : 512;
   static constexpr int REGS_LOW = TTM == 256 ? 64 : 72;             // warpgroups 0 and 3
   static constexpr int REGS_HIGH = TTM == 256 ? 216 : 184;          // warpgroups 1-2
-  static constexpr int F8 = AB == 8 ? 6 : (TTM == 256 ? W4A4_F8_BUFFERS : 12);  // operand buffers
+  static constexpr int F8 = AB == 16 ? 4 : AB == 8 ? 6 : (TTM == 256 ? W4A4_F8_BUFFERS : 12);  // operand buffers
   // Who writes the per-stage scale slots.  The 128-column instance has converter
   // warps to spare and lets them do it: stage s's scales go to slot s % 4 while
   // stage s is converted, after the converters waited for the MMA to release
@@ -130,6 +135,7 @@ struct __align__(128) Smem {
 static_assert(sizeof(Smem<256>) <= 227 * 1024, "shared memory per CTA is at most 227 KB");
 static_assert(sizeof(Smem<128>) <= 227 * 1024, "shared memory per CTA is at most 227 KB");
 static_assert(sizeof(Smem<128, 8>) <= 227 * 1024, "shared memory per CTA is at most 227 KB");
+static_assert(sizeof(Smem<128, 16>) <= 227 * 1024, "shared memory per CTA is at most 227 KB");
 
 struct TcArgs {
   const uint16_t* w_scales;
@@ -229,6 +235,8 @@ __device__ __forceinline__ uint64_t kmajor_desc(const void* smem) {
 __device__ __forceinline__ uint32_t f8_idesc(int n) {
   return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(128 >> 4) << 24);
 }
+// kind::f16 with bf16 A and B (format code 1 in the A and B type fields).
+__device__ __forceinline__ uint32_t bf16_idesc(int n) { return f8_idesc(n) | (1u << 7) | (1u << 10); }
 __device__ __forceinline__ void mma_f8(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc) {
   asm volatile(
       "{\n.reg .pred p;\nsetp.ne.b32 p, 0, 0;\n"
@@ -508,7 +516,7 @@ __device__ void mma_issuer(const TcArgs& p, SM& S, uint32_t tmem) {
   Seg sg;
   while (seg_next(p, nst, si, sg)) {
     const Tile T = decode_tile(p, sg.t);
-    const uint32_t idesc = f8_idesc(T.nmma);
+    const uint32_t idesc = SM::ABITS == 16 ? bf16_idesc(T.nmma) : f8_idesc(T.nmma);
     const int64_t b_end = static_cast<int64_t>(sg.s1) * KB < B ? static_cast<int64_t>(sg.s1) * KB : B;
     for (int64_t b = static_cast<int64_t>(sg.s0) * KB; b < b_end; ++b, ++gblk) {
       const int f = gblk % SM::F8;
@@ -556,6 +564,19 @@ __device__ __forceinline__ uint32_t q4_pair_f16(uint32_t w, uint32_t sel) {
 }
 __device__ __forceinline__ uint32_t s8_pair_f16(uint32_t x, uint32_t sel) {
   return f16x2_sub(prmt(x, 0x64646464u, sel), 0x64806480u);  // - 1152
+}
+// bf16x2 of two int4 codes as q - 8: the nibble under the bf16 exponent byte
+// 0x43 is 128 + q (7 stored mantissa bits hold 0..15), minus 136 (0x4308),
+// exactly.
+__device__ __forceinline__ uint32_t q4_pair_bf16(uint32_t w, uint32_t sel) {
+  __nv_bfloat162 a, b;
+  const uint32_t h = prmt(w, 0x43434343u, sel) & 0xFF0FFF0Fu, c = 0x43084308u;
+  memcpy(&a, &h, 4);
+  memcpy(&b, &c, 4);
+  const __nv_bfloat162 r = __hsub2(a, b);
+  uint32_t out;
+  memcpy(&out, &r, 4);
+  return out;
 }
 
 // Stage s's four scales of one row: a vector load when the row's groups are
@@ -618,11 +639,13 @@ __device__ void converters(const TcArgs& p, SM& S) {
       uint4 sa[AR];
       uint2 swd[WR], sws[WR];
       if constexpr (SM::CONV_SCALES) {
+      if constexpr (SM::ABITS != 16) {  // the rotate-only route has no activation scales
 #pragma unroll
       for (int i = 0; i < AR; ++i) {
         const int m = ct + CT * i;
         const int64_t row = T.m0 + (m < T.ntok ? m : 0);
         sa[i] = load_scales4(p.a_scales + row * B, s, static_cast<int>(B), vec);
+      }
       }
 #pragma unroll
       for (int i = 0; i < WR; ++i) {
@@ -642,7 +665,34 @@ __device__ void converters(const TcArgs& p, SM& S) {
         // weights: 128 rows, signed q - 8
         const uint8_t* ws = S.wraw[slot] + src_off;
         uint8_t* wd = S.wf8[f] + dst_off;
-        if constexpr (SM::ABITS == 8) {
+        if constexpr (SM::ABITS == 16) {
+          // bf16 operands, same layout as the f16 ones: weights q - 8 ...
+#pragma unroll 4
+          for (int i = 0; i < (TW - r0 + RS - 1) / RS; ++i) {
+            const uint4 raw = *reinterpret_cast<const uint4*>(ws + i * RS * 64);
+            const uint32_t hx = raw.x >> 4, hy = raw.y >> 4, hz = raw.z >> 4, hw = raw.w >> 4;
+            uint8_t* d = wd + i * RS * 64;
+            *reinterpret_cast<uint4*>(d) = make_uint4(q4_pair_bf16(raw.x, 0x4140u), q4_pair_bf16(raw.x, 0x4342u),
+                                                      q4_pair_bf16(raw.y, 0x4140u), q4_pair_bf16(raw.y, 0x4342u));
+            *reinterpret_cast<uint4*>(d + 128) = make_uint4(q4_pair_bf16(raw.z, 0x4140u), q4_pair_bf16(raw.z, 0x4342u),
+                                                            q4_pair_bf16(raw.w, 0x4140u), q4_pair_bf16(raw.w, 0x4342u));
+            *reinterpret_cast<uint4*>(d + 256) = make_uint4(q4_pair_bf16(hx, 0x4140u), q4_pair_bf16(hx, 0x4342u),
+                                                            q4_pair_bf16(hy, 0x4140u), q4_pair_bf16(hy, 0x4342u));
+            *reinterpret_cast<uint4*>(d + 384) = make_uint4(q4_pair_bf16(hz, 0x4140u), q4_pair_bf16(hz, 0x4342u),
+                                                            q4_pair_bf16(hw, 0x4140u), q4_pair_bf16(hw, 0x4342u));
+          }
+          // ... and the activations' bf16 values as they are: the block's 64 raw
+          // bytes of a row are its four 8-element chunks
+          const uint8_t* as = S.araw[slot] + asrc_off;
+          uint8_t* ad = S.af8[f] + dst_off;
+#pragma unroll 2
+          for (int i = 0; i < a_iters; ++i) {
+            const uint4* src = reinterpret_cast<const uint4*>(as + i * RS * AROW);
+            uint8_t* d = ad + i * RS * 64;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(d + 128 * c) = src[c];
+          }
+        } else if constexpr (SM::ABITS == 8) {
           // f16 operands: chunk c (elements 8c..8c+7) at c * 128; a code q becomes
           // the f16 1024 + q (exponent byte 0x64 above the nibble), minus 1032
 #pragma unroll 4
@@ -709,9 +759,13 @@ __device__ void converters(const TcArgs& p, SM& S) {
           const int m = ct + CT * i;
           if (m < SM::TT) {
             const bool ok = m < T.ntok;
-            const uint32_t v[KB] = {sa[i].x, sa[i].y, sa[i].z, sa[i].w};
+            uint32_t v[KB] = {0u, 0u, 0u, 0u};
+            if constexpr (SM::ABITS != 16) {
+              v[0] = sa[i].x; v[1] = sa[i].y; v[2] = sa[i].z; v[3] = sa[i].w;
+            }
 #pragma unroll
-            for (int kk = 0; kk < KB; ++kk) S.sda[sc][kk][m] = (ok && kk < nbk) ? __uint_as_float(v[kk]) : 0.f;
+            for (int kk = 0; kk < KB; ++kk)
+              S.sda[sc][kk][m] = (ok && kk < nbk) ? (SM::ABITS == 16 ? 1.0f : __uint_as_float(v[kk])) : 0.f;
           }
         }
 #pragma unroll
@@ -1285,6 +1339,32 @@ cudaError_t launch_gemm_w4a8(const uint8_t* w_codes, const uint16_t* w_scales, c
     grid = pl.grid;
   }
   return launch_tc<false, kW4A8TT, 8>(wmap, amap, a, grid, stream);
+}
+
+cudaError_t launch_gemm_w4a16(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums, int64_t N,
+                              const uint16_t* a_bf16, int64_t M, int64_t K, float* y, int64_t ldy, void* ws,
+                              size_t ws_bytes, cudaStream_t stream) {
+  TcArgs a{};
+  a.w_scales = w_scales; a.w_sums = w_sums; a.a_scales = nullptr;
+  a.M = M; a.N = N; a.K = K; a.y = y; a.ldy = ldy; a.P = nullptr;
+  a.tt = token_tile(M, kW4A8TT);
+  CUtensorMap wmap, amap;
+  cudaError_t e = codes_map(&wmap, w_codes, N, K, TW);
+  // bf16 values [M][K] as bytes: box of 4 blocks (256 bytes) x tt rows
+  if (e == cudaSuccess)
+    e = encode_2d_map(&amap, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_bf16, static_cast<uint64_t>(2 * K),
+                      static_cast<uint64_t>(M), static_cast<uint64_t>(2 * K), KB * 64, static_cast<uint32_t>(a.tt),
+                      CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (e != cudaSuccess) return e;
+  int64_t grid = ((N + TW - 1) / TW) * ((M + a.tt - 1) / a.tt);
+  const SkPlan pl = plan_stream_k(M, N, K, kW4A8TT);
+  if (pl.on && ws && ws_bytes >= pl.ws_bytes) {
+    a.sk_units = pl.units;
+    a.sk_count = static_cast<uint32_t*>(ws);
+    a.sk_part = reinterpret_cast<float4*>(static_cast<uint8_t*>(ws) + pl.count_bytes);
+    grid = pl.grid;
+  }
+  return launch_tc<false, kW4A8TT, 16>(wmap, amap, a, grid, stream);
 }
 
 cudaError_t launch_gemm_tc_routed(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums, int E,

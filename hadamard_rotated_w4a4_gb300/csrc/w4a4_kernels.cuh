@@ -57,6 +57,14 @@ cudaError_t launch_gemm_w4a8(const uint8_t* w_codes, const uint16_t* w_scales, c
                              const int8_t* a_codes, const float* a_scales, int64_t M, int64_t K, float* y, int64_t ldy,
                              int32_t* P, void* ws, size_t ws_bytes, cudaStream_t stream);
 size_t gemm_w4a8_workspace_bytes(int64_t M, int64_t N, int64_t K);
+// The rotate-only route: activations rotated and carried as bf16 [M][K] (not
+// quantised), bf16 tensor-core MMAs against the Q4_0 weights; its workspace
+// plan is the exact path's (gemm_w4a8_workspace_bytes).
+cudaError_t launch_act_rotate_bf16(const float* x, int64_t M, int64_t K, int64_t ldx, int rotate, uint16_t* out,
+                                   cudaStream_t stream);
+cudaError_t launch_gemm_w4a16(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums, int64_t N,
+                              const uint16_t* a_bf16, int64_t M, int64_t K, float* y, int64_t ldy, void* ws,
+                              size_t ws_bytes, cudaStream_t stream);
 // Small token batches (1 <= M <= 8): CUDA-core kernel, bit-identical to the
 // tensor-core kernel's whole-tile schedule.
 cudaError_t launch_gemm_small_m(const uint8_t* w_codes, const uint16_t* w_scales, int64_t N, const uint8_t* a_codes,

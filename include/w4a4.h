@@ -68,6 +68,7 @@ typedef enum {
 #define W4A4_TAG_Q4_0 0x51340000u    /* Q4_0 weights                          */
 #define W4A4_TAG_ACT4 0x41340000u    /* int4 activations                      */
 #define W4A4_TAG_ACT8 0x41380000u    /* int8 activations (the exact path)     */
+#define W4A4_TAG_ACT16 0x41420000u   /* bf16 activations (rotate-only route)  */
 #define W4A4_TAG_MAGIC_MASK 0xFFFF0000u
 #define W4A4_TAG_ROTATED 0x00000001u /* values were rotated by H32 per block  */
 
@@ -125,6 +126,20 @@ typedef struct {
   uint32_t tag; /* W4A4_TAG_ACT8 | (W4A4_TAG_ROTATED if rotated) */
 } w4a4_act8;
 
+/*
+ * Activations of the rotate-only route (section "Hadamard-rotated Q4_0: W4A4
+ * prompt processing": the same rotated files also run with the activations
+ * rotated and not rounded to 4 bits):
+ *   values: device, [rows][K] bf16 (bit patterns) in element order: the rotated
+ *           fp32 values rounded to nearest even.  No scales.
+ */
+typedef struct {
+  uint16_t* values;
+  int64_t rows;
+  int64_t K;
+  uint32_t tag; /* W4A4_TAG_ACT16 | (W4A4_TAG_ROTATED if rotated) */
+} w4a4_act16;
+
 /* Bytes needed for the two arrays of a Q4_0 / int4 operand (0 if K is invalid). */
 size_t w4a4_q4_0_codes_bytes(int64_t rows, int64_t K);
 size_t w4a4_q4_0_scales_bytes(int64_t rows, int64_t K);
@@ -133,6 +148,7 @@ size_t w4a4_act4_codes_bytes(int64_t rows, int64_t K);
 size_t w4a4_act4_scales_bytes(int64_t rows, int64_t K);
 size_t w4a4_act8_codes_bytes(int64_t rows, int64_t K);
 size_t w4a4_act8_scales_bytes(int64_t rows, int64_t K);
+size_t w4a4_act16_values_bytes(int64_t rows, int64_t K);
 
 /*
  * h32_q4_0_pack_weights -- rotate weights per 32-block along K and quantise to
@@ -244,6 +260,30 @@ w4a4_status w4a8_gemm(const w4a4_q4_0* w, const w4a4_act8* a, float* y, int64_t 
                       size_t ws_bytes, w4a4_stream_t stream);
 w4a4_status w4a8_gemm_partials(const w4a4_q4_0* w, const w4a4_act8* a, int32_t* P, w4a4_stream_t stream);
 size_t w4a8_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/*
+ * The rotate-only route (section "Hadamard-rotated Q4_0: W4A4 prompt
+ * processing": on the backend without W4A4, the rotated files run with the
+ * activations rotated as a matmul and not rounded to 4 bits).  This build
+ * carries the rotated activations as bf16, the tensor cores' 16-bit type.
+ *
+ * w4a16_rotate_act -- per 32-element block of each row of x (fp32, device,
+ *   [M][ldx]): y = fl32(FWHT32(x_blk) * c) as in w4a4_rotate_quantize_act
+ *   (rotate = 1) or y = x_blk (rotate = 0), stored as bf16 (round to nearest
+ *   even) in out->values, a caller buffer of w4a4_act16_values_bytes(M, K)
+ *   bytes; rows, K and tag are written.  Errors as w4a4_rotate_quantize_act.
+ *
+ * w4a16_gemm -- Y[m][n] = sum_b d_w[n][b] * sum_j y[m][32b+j] * (q_w - 8):
+ *   bf16 tensor-core MMAs (every q - 8 is exact in bf16) with fp32 block sums,
+ *   folded by the fp16 weight scale in fp32.  Arguments, layout, workspace
+ *   (size from w4a16_gemm_workspace_bytes) and errors as w4a4_gemm; the
+ *   rotation tags of w and a must agree (W4A4_ERR_MISMATCH otherwise).
+ */
+w4a4_status w4a16_rotate_act(const float* x, int64_t M, int64_t K, int64_t ldx, int rotate, w4a4_act16* out,
+                             w4a4_stream_t stream);
+w4a4_status w4a16_gemm(const w4a4_q4_0* w, const w4a4_act16* a, float* y, int64_t ldy, void* ws, size_t ws_bytes,
+                       w4a4_stream_t stream);
+size_t w4a16_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 /*
  * w4a4_gemm_partials -- the exact per-block integer dot products
