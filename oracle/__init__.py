@@ -40,6 +40,13 @@ function                       pinned by
                                fp32->bf16 conversion on random and edge values
 ``rotate_activations_bf16``    unit vectors -> bf16(+-c) (hand-derived);
                                rotate=False is bf16(x)
+``rotate_importance``          closed form: the block mean (H32 entries are
+                               +-1); one-hot blocks; trace preserved
+``weighted_block_scale`` /     dense scans over d find nothing better;
+``quantize_weights_q4_0_       Q4_0-exact blocks give error 0; never worse
+weighted``                     than the plain scale; 2^k weight invariance
+``pack_weights_imatrix``       rotated: equal to uniform weights (the pages:
+                               on the rotated file an imatrix does nothing)
 ``w4a16_matmul``               brute-force fp64 loops; Q4_0-exact weights and
                                bf16 activations reduce it to x @ w^T; constant
                                blocks: 32 d_w alpha (q - 8)
@@ -67,6 +74,10 @@ from .quant import (
     round_bf16,
     bf16_to_f32,
     rotate_activations_bf16,
+    rotate_importance,
+    weighted_block_scale,
+    quantize_weights_q4_0_weighted,
+    pack_weights_imatrix,
 )
 from .matmul import block_partials, w4a4_matmul, w4a4_matmul_id, w4a8_matmul, w4a16_matmul, exact_matmul
 
@@ -77,5 +88,6 @@ __all__ = [
     "q4_0_to_aos", "q4_0_from_aos", "pack_weights", "quantize_activations",
     "quantize_act_int8", "quantize_activations_int8",
     "round_bf16", "bf16_to_f32", "rotate_activations_bf16",
+    "rotate_importance", "weighted_block_scale", "quantize_weights_q4_0_weighted", "pack_weights_imatrix",
     "block_partials", "w4a4_matmul", "w4a4_matmul_id", "w4a8_matmul", "w4a16_matmul", "exact_matmul",
 ]

@@ -224,3 +224,121 @@ def rotate_activations_bf16(x: np.ndarray, rotate: bool = True) -> dict:
     y = rotate_h32(xf) if rotate else xf
     h = round_bf16(y)
     return {"x16": h, "xr": bf16_to_f32(h), "rotated": bool(rotate)}
+
+
+# ---------------------------------------------------------------- importance-weighted Q4_0 (converter)
+def rotate_importance(imp: np.ndarray) -> np.ndarray:
+    """The importance the rotated input channels inherit (section "Hadamard-
+    rotated Q4_0: W4A4 prompt processing": the converter gives the imatrix the
+    matching change).  An imatrix keeps one value per input channel, the
+    diagonal of E[x x^T]; with rotated inputs Hn x (Hn = H32 / sqrt 32, per
+    block) that diagonal becomes diag(Hn diag(imp) Hn^T), evaluated here with
+    the explicit matrices in fp64.
+    """
+    from .hadamard import sylvester_h32
+
+    imp = np.asarray(imp, dtype=np.float64)
+    K = imp.shape[-1]
+    assert K % 32 == 0, "K must be a multiple of 32"
+    Hn = sylvester_h32().astype(np.float64) / np.sqrt(32.0)
+    out = np.empty_like(imp)
+    for b in range(K // 32):
+        A = Hn @ np.diag(imp[..., 32 * b:32 * b + 32]) @ Hn.T
+        out[..., 32 * b:32 * b + 32] = np.diag(A)
+    return out
+
+
+def _clean_weights(w: np.ndarray) -> np.ndarray:
+    w = np.asarray(w, dtype=np.float64)
+    w = np.where(np.isfinite(w) & (w > 0), w, 0.0)
+    return w if w.sum() > 0 else np.ones_like(w)
+
+
+def _codes_for(y32: np.ndarray, d16: np.float16) -> np.ndarray:
+    """The Q4_0 code rule for a stored scale: id = fl32(1/d) (0 if d == 0),
+    q = clamp(round_half_away(fl32(y * id)) + 8, 0, 15)."""
+    d = np.float32(d16)
+    inv = np.float32(1.0) / d if d != 0 else np.float32(0.0)
+    v = (y32 * inv).astype(np.float32)
+    return np.clip(round_half_away(v) + 8.0, 0.0, 15.0).astype(np.int64)
+
+
+def _weighted_error(y32: np.ndarray, w: np.ndarray, d16: np.float16) -> float:
+    q = _codes_for(y32, d16)
+    return float(np.sum(w * (y32.astype(np.float64) - float(d16) * (q - 8)) ** 2))
+
+
+def weighted_block_scale(y32: np.ndarray, w: np.ndarray) -> float:
+    """The real scale d minimising sum_j w_j (y_j - d c_j)^2 with every c_j the
+    nearest integer to y_j / d in -8..7 (fp64; 0 for an all-zero block).
+
+    With s = 1/d the nearest codes change only where some y_j s crosses a
+    half-integer k + 1/2 (k = -8..6); between consecutive crossings the codes c
+    are fixed and the best d is the weighted least-squares d = sum w y c /
+    sum w c^2, with error sum w y^2 - (sum w y c)^2 / sum w c^2.  Every interval
+    (each evaluated at its midpoint, plus one point beyond each end) is tried;
+    the first largest (sum w y c)^2 / sum w c^2 wins.
+    """
+    y = np.asarray(y32, dtype=np.float64)
+    nz = y != 0
+    if not nz.any():
+        return 0.0
+    ks = np.arange(-8, 7, dtype=np.float64) + 0.5
+    bps = np.unique((ks[None, :] / y[nz][:, None]).ravel())
+    pts = np.concatenate([[bps[0] - abs(bps[0]) - 1.0], (bps[:-1] + bps[1:]) / 2, [bps[-1] + abs(bps[-1]) + 1.0]])
+    c = np.clip(np.rint(y[None, :] * pts[:, None]), -8, 7)
+    num = (c * (w * y)[None, :]).sum(axis=1)
+    den = (c * c * w[None, :]).sum(axis=1)
+    ok = den > 0
+    score = np.full(len(pts), -1.0)
+    score[ok] = num[ok] ** 2 / den[ok]
+    i = int(np.argmax(score))
+    return float(num[i] / den[i]) if ok[i] else 0.0
+
+
+def quantize_weights_q4_0_weighted(y: np.ndarray, omega: np.ndarray) -> dict:
+    """Importance-weighted Q4_0 of fp32 values y [..., K] with per-element
+    weights omega (broadcast against y; negative or non-finite weights count
+    as 0, an all-zero block of weights as uniform).
+
+    Per block: d* = weighted_block_scale; the stored fp16 scale is the best, by
+    the weighted error under the code rule of ``_codes_for``, of (in order) the
+    plain Q4_0 scale fp16(m / -8), fp16(d*) and the two fp16 neighbours of
+    fp16(d*); the first smallest error wins.  Returns codes, d16.
+    """
+    y = np.asarray(y, dtype=np.float32)
+    blk = _blocks(y)
+    om = np.broadcast_to(np.asarray(omega, dtype=np.float64), y.shape)
+    wblk = _blocks(om)
+    plain = quantize_weights_q4_0(y)["d16"]
+    flat_y = blk.reshape(-1, 32)
+    flat_w = wblk.reshape(-1, 32)
+    flat_p = np.asarray(plain).reshape(-1)
+    d16 = np.empty(flat_y.shape[0], dtype=np.float16)
+    codes = np.empty(flat_y.shape, dtype=np.uint8)
+    for i in range(flat_y.shape[0]):
+        yb, wb = flat_y[i], _clean_weights(flat_w[i])
+        ds = np.float16(weighted_block_scale(yb, wb))
+        cands = [flat_p[i], ds, np.nextafter(ds, np.float16(-np.inf)), np.nextafter(ds, np.float16(np.inf))]
+        best, best_e = None, None
+        for cd in cands:
+            if not np.isfinite(cd):
+                continue
+            e = _weighted_error(yb, wb, cd)
+            if best_e is None or e < best_e:
+                best, best_e = cd, e
+        d16[i] = best
+        codes[i] = _codes_for(yb, best)
+    return {"codes": codes.reshape(y.shape), "d16": d16.reshape(blk.shape[:-1])}
+
+
+def pack_weights_imatrix(w: np.ndarray, imp: np.ndarray, rotate: bool = True) -> dict:
+    """Weights [N][K] (fp32 or bf16 bits) and an importance vector imp [K] ->
+    importance-weighted Q4_0: the weights rotated as in ``pack_weights`` and the
+    importance given the matching change (``rotate_importance``), or both as
+    they are when rotate is False.  Returns codes (packed), d16, q."""
+    wf = _weights_fp32(w)
+    y = rotate_h32(wf) if rotate else wf
+    om = rotate_importance(imp) if rotate else np.asarray(imp, dtype=np.float64)
+    qz = quantize_weights_q4_0_weighted(y, om[None, :] if om.ndim == 1 else om)
+    return {"codes": pack_nibbles(qz["codes"]), "d16": qz["d16"], "q": qz["codes"], "rotated": bool(rotate)}

@@ -557,3 +557,94 @@ def test_rotate_only_is_closer_than_int8_to_the_exact_product():
     e8 = np.abs(oracle.w4a8_matmul(wp, oracle.quantize_activations_int8(d["x"])) - ref).mean()
     e16 = np.abs(oracle.w4a16_matmul(wp, oracle.rotate_activations_bf16(d["x"])) - ref).mean()
     assert e16 < 0.5 * e8
+
+
+# ---------------------------------------------------------------- importance-weighted Q4_0 (converter)
+def _nearest_error(y, w, d):
+    """Independent restatement: error of scale d with each code the nearest integer in -8..7 (fp64)."""
+    y = np.asarray(y, np.float64)
+    c = np.clip(np.floor(y / d + 0.5), -8, 7)
+    return float(np.sum(w * (y - d * c) ** 2))
+
+
+def test_rotate_importance_is_the_block_mean():
+    """Every entry of H32 is +-1, so diag(Hn D Hn^T)_i = sum_j imp_j / 32."""
+    rng = np.random.default_rng(50)
+    imp = rng.uniform(0, 5, 256)
+    r = oracle.rotate_importance(imp)
+    want = np.repeat(imp.reshape(8, 32).mean(axis=1), 32)
+    assert np.allclose(r, want, rtol=1e-14, atol=0)
+    # a one-hot block spreads evenly; the trace (total importance) is kept
+    one = np.zeros(64)
+    one[37] = 3.0
+    assert np.allclose(oracle.rotate_importance(one), np.r_[np.zeros(32), np.full(32, 3.0 / 32)], rtol=1e-14, atol=1e-17)
+    assert oracle.rotate_importance(imp).sum() == pytest.approx(imp.sum(), rel=1e-14)
+
+
+def test_weighted_scale_beats_a_dense_scan():
+    """No scale on a fine grid (nor next to d*) has a smaller weighted error."""
+    rng = np.random.default_rng(51)
+    for trial in range(12):
+        y = (rng.standard_normal(32) * (1 + 5 * (trial % 3 == 0) * (np.arange(32) == trial))).astype(np.float32)
+        w = rng.uniform(0, 3, 32) if trial % 2 else np.ones(32)
+        d = oracle.weighted_block_scale(y, w)
+        e = _nearest_error(y, w, d)
+        a = float(np.max(np.abs(y)))
+        grid = np.concatenate([np.linspace(-a / 4, -a / 20, 20000), np.linspace(a / 20, a / 4, 20000)])
+        scan = min(_nearest_error(y, w, g) for g in grid)
+        assert e <= scan * (1 + 1e-12), (trial, e, scan)
+        for f in (1 - 1e-7, 1 + 1e-7):
+            assert e <= _nearest_error(y, w, d * f) * (1 + 1e-12)
+
+
+def test_weighted_q4_0_exact_blocks_and_plain_scale():
+    """A block Q4_0 holds exactly keeps error 0 (its plain scale); elsewhere the
+    weighted choice is never worse than the plain scale under the same code
+    rule, and clearly better on average for Gaussian blocks."""
+    rng = np.random.default_rng(52)
+    q = rng.integers(1, 16, (6, 32))
+    q[:, 0] = 0
+    d0 = np.float16(rng.uniform(0.02, 0.5, 6) * rng.choice([-1, 1], 6)).astype(np.float32)
+    y = (d0[:, None] * (q - 8)).astype(np.float32)
+    r = oracle.quantize_weights_q4_0_weighted(y, np.ones(32))
+    assert np.array_equal(r["d16"][:, 0].astype(np.float32), d0) and np.array_equal(r["codes"], q)
+    y = rng.standard_normal((400, 32)).astype(np.float32)
+    w = rng.uniform(0.1, 2.0, (400, 32))
+    r = oracle.quantize_weights_q4_0_weighted(y, w)
+    plain = oracle.quantize_weights_q4_0(y)
+    ew, ep = [], []
+    for i in range(400):
+        cw = r["codes"][i].astype(np.float64) - 8
+        ew.append(np.sum(w[i] * (y[i] - np.float64(r["d16"][i, 0]) * cw) ** 2))
+        dp = np.float32(plain["d16"][i, 0])
+        cp = np.clip(np.copysign(np.floor(np.abs(y[i] * (np.float32(1) / dp)) + 0.5), y[i] * (np.float32(1) / dp)), -8, 7)
+        ep.append(np.sum(w[i] * (y[i] - np.float64(dp) * cp) ** 2))
+    ew, ep = np.array(ew), np.array(ep)
+    assert np.all(ew <= ep * (1 + 1e-12))
+    assert ew.mean() < 0.9 * ep.mean()
+
+
+def test_weighted_q4_0_power_of_two_weight_invariance():
+    rng = np.random.default_rng(53)
+    y = rng.standard_normal((50, 64)).astype(np.float32)
+    w = rng.uniform(0, 2, (50, 64))
+    a = oracle.quantize_weights_q4_0_weighted(y, w)
+    b = oracle.quantize_weights_q4_0_weighted(y, w * 8.0)
+    assert np.array_equal(a["codes"], b["codes"]) and np.array_equal(a["d16"], b["d16"])
+
+
+def test_rotated_imatrix_does_nothing():
+    """The pages: on the rotated file an imatrix does nothing, Q4_0 having one
+    scale per 32 values.  With the matching change the rotated importance is
+    flat inside every block, so the weighted choice is the unweighted one."""
+    rng = np.random.default_rng(54)
+    w = rng.standard_normal((20, 256)).astype(np.float32)
+    imp = rng.uniform(0, 10, 256) ** 3
+    a = oracle.pack_weights_imatrix(w, imp, rotate=True)
+    b = oracle.pack_weights_imatrix(w, np.ones(256), rotate=True)
+    same = np.all(a["q"].reshape(20, 8, 32) == b["q"].reshape(20, 8, 32), axis=-1) & (a["d16"] == b["d16"])
+    assert same.mean() >= 0.99
+    # unrotated, the same importance does move the scales
+    c = oracle.pack_weights_imatrix(w, imp, rotate=False)
+    d = oracle.pack_weights_imatrix(w, np.ones(256), rotate=False)
+    assert np.mean(c["d16"] != d["d16"]) > 0.3
