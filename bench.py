@@ -366,6 +366,18 @@ def run_ours(args, shape) -> dict | None:
     e_pack1.record(stream)
     torch.cuda.synchronize()
     pack_ms = e_pack0.elapsed_time(e_pack1)
+    # the converter's importance-weighted packing of the same weights (a synthetic
+    # importance vector; once per model, like the plain packing)
+    imx_ms = None
+    if not args.no_exact and world == 1:
+        imp = torch.from_numpy(np.random.default_rng(7).uniform(0, 3, K).astype(np.float32) ** 4).to(dev)
+        wq_imx = w4.h32_q4_0_pack_weights_imatrix(w_dev, imp)  # warm-up
+        e_pack0.record(stream)
+        w4.h32_q4_0_pack_weights_imatrix(w_dev, imp, out=wq_imx)
+        e_pack1.record(stream)
+        torch.cuda.synchronize()
+        imx_ms = e_pack0.elapsed_time(e_pack1)
+        del wq_imx, imp
     sets = []
     for i in range(nsets):
         wq = w4.alloc_q4_0(N, K, dev)
@@ -427,6 +439,21 @@ def run_ours(args, shape) -> dict | None:
                  "gemm_effective_tops": 2.0 * M * N * K / (gemm8_avg * 1e-3) / 1e12,
                  "w4a4_speedup": (act8_avg + gemm8_avg) / (act_avg + gemm_avg)}
         del a8s, ws8
+    # the rotate-only route (bf16 activations, not quantised) on the same sets
+    rotate_only = None
+    if not args.no_exact and world == 1:
+        a16s = [w4.alloc_act16(M, K, dev) for _ in range(nsets)]
+        ws16 = torch.zeros(max(16, w4.w4a16_gemm_workspace_bytes(M, N, K)), dtype=torch.uint8, device=dev)
+        act16_avg = graph_time(lambda i, st: w4.w4a16_rotate_act(sets[i % nsets][1], out=a16s[i % nsets], stream=st),
+                               nk)
+        gemm16_avg = graph_time(lambda i, st: w4.w4a16_gemm(sets[i % nsets][0], a16s[i % nsets],
+                                                            y=sets[i % nsets][3], ws=ws16, stream=st), nk)
+        rotate_only = {"what": "rotated Q4_0 x rotated bf16 activations, not quantised (the pages' rotate-only "
+                               "route), same workload",
+                       "act_ms": act16_avg, "gemm_ms": gemm16_avg,
+                       "gemm_effective_tops": 2.0 * M * N * K / (gemm16_avg * 1e-3) / 1e12,
+                       "w4a4_speedup": (act16_avg + gemm16_avg) / (act_avg + gemm_avg)}
+        del a16s, ws16
     # a drafter's verification batch: the first 8 tokens of the workload
     verify = None
     if not args.no_verify and world == 1:
@@ -534,9 +561,11 @@ def run_ours(args, shape) -> dict | None:
         "prefill_tok_s_proxy": proxy,
         "moe": moe,
         "exact_path": exact,
+        "rotate_only": rotate_only,
         "verification_batch": verify,
         "kernel_ms": {"act_rotate_quantize": act_avg, "gemm": gemm_avg},
         "pack_weights_ms": pack_ms,
+        "pack_weights_imatrix_ms": imx_ms,
         "probes": probes,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(M * K * 4),

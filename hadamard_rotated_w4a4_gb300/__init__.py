@@ -56,6 +56,7 @@ EXPORTS = [
     "w4a4_status_name", "w4a4_abi_version", "w4a4_act8_codes_bytes", "w4a4_act8_scales_bytes", "w4a4_gemm_small_m",
     "w4a8_rotate_quantize_act", "w4a8_gemm", "w4a8_gemm_partials", "w4a8_gemm_workspace_bytes",
     "w4a4_act16_values_bytes", "w4a16_rotate_act", "w4a16_gemm", "w4a16_gemm_workspace_bytes",
+    "h32_q4_0_pack_weights_imatrix",
 ]
 
 
@@ -105,6 +106,7 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         f = getattr(lib, name)
         f.argtypes, f.restype = [i64, i64], u
     lib.h32_q4_0_pack_weights.argtypes = [vp, i32, i64, i64, i64, i32, ctypes.POINTER(_Q4_0Desc), vp]
+    lib.h32_q4_0_pack_weights_imatrix.argtypes = [vp, i32, i64, i64, i64, i32, vp, ctypes.POINTER(_Q4_0Desc), vp]
     lib.q4_0_import.argtypes = [vp, i64, i64, i32, ctypes.POINTER(_Q4_0Desc), vp]
     lib.w4a4_rotate_quantize_act.argtypes = [vp, i64, i64, i64, i32, ctypes.POINTER(_Act4Desc), vp]
     lib.w4a4_gemm.argtypes = [ctypes.POINTER(_Q4_0Desc), ctypes.POINTER(_Act4Desc), vp, i64, vp, u, vp]
@@ -249,6 +251,31 @@ def h32_q4_0_pack_weights(w: torch.Tensor, rotate: bool = True, out: Q4_0Weights
     ldw = w.stride(0) if N > 1 else K  # a single row's stride is meaningless (may be 0)
     _check(load_library().h32_q4_0_pack_weights(w.data_ptr(), dtype, N, K, ldw, int(rotate),
                                                  ctypes.byref(d), _stream(stream)))
+    out.rotated = bool(d.tag & TAG_ROTATED)
+    return out
+
+
+def h32_q4_0_pack_weights_imatrix(w: torch.Tensor, imatrix: torch.Tensor | None, rotate: bool = True,
+                                  out: Q4_0Weights | None = None, stream=None) -> Q4_0Weights:
+    """As h32_q4_0_pack_weights, with each block's scale chosen against the importance vector
+    imatrix (fp32 [K], CUDA, the unrotated input channels' importance; None = uniform)."""
+    _cuda(w, "w")
+    if w.dim() != 2 or w.stride(1) != 1:
+        raise ValueError("w must be a 2-D tensor with unit stride along K")
+    dtype = {torch.bfloat16: 0, torch.float32: 1}.get(w.dtype)
+    if dtype is None:
+        raise ValueError("w must be bf16 or fp32")
+    N, K = w.shape
+    if imatrix is not None:
+        _cuda(imatrix, "imatrix")
+        if imatrix.dtype != torch.float32 or imatrix.numel() != K or not imatrix.is_contiguous():
+            raise ValueError("imatrix must be a contiguous fp32 tensor of K values")
+    out = out or alloc_q4_0(N, K, w.device, rotate)
+    d = out.desc()
+    ldw = w.stride(0) if N > 1 else K
+    _check(load_library().h32_q4_0_pack_weights_imatrix(
+        w.data_ptr(), dtype, N, K, ldw, int(rotate), imatrix.data_ptr() if imatrix is not None else None,
+        ctypes.byref(d), _stream(stream)))
     out.rotated = bool(d.tag & TAG_ROTATED)
     return out
 

@@ -171,6 +171,30 @@ w4a4_status h32_q4_0_pack_weights(const void* w, int w_dtype, int64_t N, int64_t
                                             reinterpret_cast<cudaStream_t>(stream)), fn);
 }
 
+w4a4_status h32_q4_0_pack_weights_imatrix(const void* w, int w_dtype, int64_t N, int64_t K, int64_t ldw, int rotate,
+                                          const float* imatrix, w4a4_q4_0* out, w4a4_stream_t stream) {
+  const char* fn = "h32_q4_0_pack_weights_imatrix";
+  if (!out) return fail(W4A4_ERR_INVALID_ARG, "%s: out is NULL", fn);
+  w4a4_status s = check_k_rows(N, K, fn);
+  if (s != W4A4_OK) return s;
+  if (w_dtype != W4A4_DTYPE_BF16 && w_dtype != W4A4_DTYPE_F32)
+    return fail(W4A4_ERR_INVALID_ARG, "%s: w_dtype %d is neither bf16 (0) nor f32 (1)", fn, w_dtype);
+  if (rotate != 0 && rotate != 1) return fail(W4A4_ERR_INVALID_ARG, "%s: rotate must be 0 or 1", fn);
+  if (ldw < K) return fail(W4A4_ERR_INVALID_ARG, "%s: ldw=%lld < K=%lld", fn, (long long)ldw, (long long)K);
+  const int64_t esz = (w_dtype == W4A4_DTYPE_BF16) ? 2 : 4;
+  if (N > 0 && (!w || !out->codes || !out->scales || !out->sums))
+    return fail(W4A4_ERR_INVALID_ARG, "%s: NULL pointer", fn);
+  if (!aligned16(w) || !aligned16(out->codes) || !aligned16(out->scales) || !aligned16(out->sums) ||
+      !aligned16(imatrix) || (ldw * esz) % 16 != 0)
+    return fail(W4A4_ERR_ALIGNMENT, "%s: pointers and rows (ldw * element size) must be 16-byte aligned", fn);
+  out->rows = N;
+  out->K = K;
+  out->tag = W4A4_TAG_Q4_0 | (rotate ? W4A4_TAG_ROTATED : 0u);
+  if (N == 0) return ok();
+  return cuda_status(w4a4::launch_pack_q4_0_weighted(w, w_dtype, N, K, ldw, rotate, imatrix, out->codes, out->scales,
+                                                     out->sums, reinterpret_cast<cudaStream_t>(stream)), fn);
+}
+
 w4a4_status q4_0_import(const void* blocks, int64_t N, int64_t K, int rotated, w4a4_q4_0* out,
                         w4a4_stream_t stream) {
   const char* fn = "q4_0_import";

@@ -41,6 +41,11 @@ cudaError_t launch_act_rotate_quantize8(const float* x, int64_t M, int64_t K, in
                                         int8_t* codes, float* scales, cudaStream_t stream);
 cudaError_t launch_pack_q4_0(const void* w, int w_dtype, int64_t N, int64_t K, int64_t ldw, int rotate,
                              uint8_t* codes, uint16_t* scales, int16_t* sums, cudaStream_t stream);
+// Importance-weighted Q4_0 (the converter's imatrix quantisation): imp is a
+// device fp32 vector of K per-input-channel importances (unrotated), or null.
+cudaError_t launch_pack_q4_0_weighted(const void* w, int w_dtype, int64_t N, int64_t K, int64_t ldw, int rotate,
+                                      const float* imp, uint8_t* codes, uint16_t* scales, int16_t* sums,
+                                      cudaStream_t stream);
 cudaError_t launch_import_q4_0(const void* blocks, int64_t N, int64_t K, uint8_t* codes, uint16_t* scales,
                                int16_t* sums, cudaStream_t stream);
 // Dense product (P == nullptr) or exact partials (P != nullptr).  With a

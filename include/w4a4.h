@@ -169,6 +169,29 @@ w4a4_status h32_q4_0_pack_weights(const void* w, int w_dtype, int64_t N, int64_t
                                   int rotate, w4a4_q4_0* out, w4a4_stream_t stream);
 
 /*
+ * h32_q4_0_pack_weights_imatrix -- as h32_q4_0_pack_weights, with the block
+ * scales chosen against an importance vector (the converter's imatrix
+ * quantisation, section "Hadamard-rotated Q4_0: W4A4 prompt processing": the
+ * tensors are quantised with the imatrix given the change matching the
+ * rotation).
+ *   imatrix : device, K fp32 importances of the (unrotated) input channels, or
+ *             NULL for uniform importance; 16-byte aligned.  Negative or
+ *             non-finite entries count as 0, a block of zeros as uniform.
+ *             With rotate = 1 the importance of the rotated channels is
+ *             diag(Hn diag(imp) Hn^T) (Hn = H32/sqrt 32 per block): the block
+ *             mean, flat across the block.
+ *   Per block (values y, weights om): d minimises sum om (y - d c)^2 with each
+ *   c the nearest integer to y/d in -8..7 (every interval where the nearest
+ *   codes are fixed is tried); the stored fp16 scale is the best of fp16(m/-8),
+ *   fp16(d) and its two fp16 neighbours by that weighted error, with the codes
+ *   q = clamp(round_half_away(y * fl32(1/d16)) + 8, 0, 15).  Layout, tags and
+ *   errors as h32_q4_0_pack_weights.  Runs once per model: about 10^5 fp32
+ *   operations per block.
+ */
+w4a4_status h32_q4_0_pack_weights_imatrix(const void* w, int w_dtype, int64_t N, int64_t K, int64_t ldw, int rotate,
+                                          const float* imatrix, w4a4_q4_0* out, w4a4_stream_t stream);
+
+/*
  * q4_0_import -- take existing Q4_0 weights bit for bit (section "Hadamard-
  * rotated Q4_0: W4A4 prompt processing": the kernel reads plain Q4_0 weights
  * bit for bit).

@@ -45,8 +45,9 @@ function                       pinned by
 ``weighted_block_scale`` /     dense scans over d find nothing better;
 ``quantize_weights_q4_0_       Q4_0-exact blocks give error 0; never worse
 weighted``                     than the plain scale; 2^k weight invariance
-``pack_weights_imatrix``       rotated: equal to uniform weights (the pages:
-                               on the rotated file an imatrix does nothing)
+``pack_weights_imatrix`` /     rotated: equal to uniform weights (the pages:
+``effective_importance``       on the rotated file an imatrix does nothing);
+                               bad entries count as 0 before the rotation
 ``w4a16_matmul``               brute-force fp64 loops; Q4_0-exact weights and
                                bf16 activations reduce it to x @ w^T; constant
                                blocks: 32 d_w alpha (q - 8)
@@ -78,6 +79,7 @@ from .quant import (
     weighted_block_scale,
     quantize_weights_q4_0_weighted,
     pack_weights_imatrix,
+    effective_importance,
 )
 from .matmul import block_partials, w4a4_matmul, w4a4_matmul_id, w4a8_matmul, w4a16_matmul, exact_matmul
 
@@ -89,5 +91,6 @@ __all__ = [
     "quantize_act_int8", "quantize_activations_int8",
     "round_bf16", "bf16_to_f32", "rotate_activations_bf16",
     "rotate_importance", "weighted_block_scale", "quantize_weights_q4_0_weighted", "pack_weights_imatrix",
+    "effective_importance",
     "block_partials", "w4a4_matmul", "w4a4_matmul_id", "w4a8_matmul", "w4a16_matmul", "exact_matmul",
 ]

@@ -277,7 +277,9 @@ def weighted_block_scale(y32: np.ndarray, w: np.ndarray) -> float:
     are fixed and the best d is the weighted least-squares d = sum w y c /
     sum w c^2, with error sum w y^2 - (sum w y c)^2 / sum w c^2.  Every interval
     (each evaluated at its midpoint, plus one point beyond each end) is tried;
-    the first largest (sum w y c)^2 / sum w c^2 wins.
+    the first largest (sum w y c)^2 / sum w c^2 wins.  When the winning codes
+    avoid -8, (-d, -c) is an equally good twin: the sign of the plain Q4_0
+    scale m / -8 is kept.
     """
     y = np.asarray(y32, dtype=np.float64)
     nz = y != 0
@@ -293,7 +295,13 @@ def weighted_block_scale(y32: np.ndarray, w: np.ndarray) -> float:
     score = np.full(len(pts), -1.0)
     score[ok] = num[ok] ** 2 / den[ok]
     i = int(np.argmax(score))
-    return float(num[i] / den[i]) if ok[i] else 0.0
+    if not ok[i]:
+        return 0.0
+    d = float(num[i] / den[i])
+    m = y[int(np.argmax(np.abs(y)))]
+    if not np.any(c[i] == -8) and d * -m < 0:
+        d = -d
+    return d
 
 
 def quantize_weights_q4_0_weighted(y: np.ndarray, omega: np.ndarray) -> dict:
@@ -332,13 +340,22 @@ def quantize_weights_q4_0_weighted(y: np.ndarray, omega: np.ndarray) -> dict:
     return {"codes": codes.reshape(y.shape), "d16": d16.reshape(blk.shape[:-1])}
 
 
-def pack_weights_imatrix(w: np.ndarray, imp: np.ndarray, rotate: bool = True) -> dict:
-    """Weights [N][K] (fp32 or bf16 bits) and an importance vector imp [K] ->
-    importance-weighted Q4_0: the weights rotated as in ``pack_weights`` and the
-    importance given the matching change (``rotate_importance``), or both as
+def effective_importance(imp, K: int, rotate: bool) -> np.ndarray:
+    """The per-element weights of the weighted packer: imp [K] (None: ones) with
+    negative or non-finite entries set to 0, then, when rotating, given the
+    matching change (``rotate_importance``)."""
+    imp = np.ones(K) if imp is None else np.asarray(imp, dtype=np.float64)
+    imp = np.where(np.isfinite(imp) & (imp > 0), imp, 0.0)
+    return rotate_importance(imp) if rotate else imp
+
+
+def pack_weights_imatrix(w: np.ndarray, imp, rotate: bool = True) -> dict:
+    """Weights [N][K] (fp32 or bf16 bits) and an importance vector imp [K] (or
+    None) -> importance-weighted Q4_0: the weights rotated as in
+    ``pack_weights`` and the importance given the matching change, or both as
     they are when rotate is False.  Returns codes (packed), d16, q."""
     wf = _weights_fp32(w)
     y = rotate_h32(wf) if rotate else wf
-    om = rotate_importance(imp) if rotate else np.asarray(imp, dtype=np.float64)
-    qz = quantize_weights_q4_0_weighted(y, om[None, :] if om.ndim == 1 else om)
+    om = effective_importance(imp, wf.shape[-1], rotate)
+    qz = quantize_weights_q4_0_weighted(y, om[None, :])
     return {"codes": pack_nibbles(qz["codes"]), "d16": qz["d16"], "q": qz["codes"], "rotated": bool(rotate)}

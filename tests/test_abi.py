@@ -118,6 +118,12 @@ def test_act_and_pack_argument_checks(lib):
     assert status(lib, "h32_q4_0_pack_weights", FAKE, 2, 4, 64, 64, 1, ctypes.byref(w), None)[0] == "W4A4_ERR_INVALID_ARG"
     assert status(lib, "h32_q4_0_pack_weights", FAKE, 0, 4, 64, 68, 1, ctypes.byref(w), None)[0] == "W4A4_ERR_ALIGNMENT"
     assert status(lib, "h32_q4_0_pack_weights", FAKE + 2, 0, 4, 64, 64, 1, ctypes.byref(w), None)[0] == "W4A4_ERR_ALIGNMENT"
+    pw = "h32_q4_0_pack_weights_imatrix"
+    assert status(lib, pw, FAKE, 0, 4, 64, 64, 1, FAKE + 4, ctypes.byref(w), None)[0] == "W4A4_ERR_ALIGNMENT"
+    assert status(lib, pw, FAKE, 0, 4, 64, 64, 3, FAKE, ctypes.byref(w), None)[0] == "W4A4_ERR_INVALID_ARG"
+    assert status(lib, pw, FAKE, 5, 4, 64, 64, 1, None, ctypes.byref(w), None)[0] == "W4A4_ERR_INVALID_ARG"
+    s, _ = status(lib, pw, FAKE, 0, 0, 64, 64, 1, None, ctypes.byref(w), None)  # no rows: nothing to do
+    assert s == "W4A4_OK" and w.tag == w4.TAG_Q4_0 | 1 and w.K == 64
     assert status(lib, "q4_0_import", FAKE + 1, 4, 64, 1, ctypes.byref(w), None)[0] == "W4A4_ERR_ALIGNMENT"
     assert status(lib, "q4_0_import", FAKE, 4, 64, 3, ctypes.byref(w), None)[0] == "W4A4_ERR_INVALID_ARG"
 

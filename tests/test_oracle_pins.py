@@ -648,3 +648,10 @@ def test_rotated_imatrix_does_nothing():
     c = oracle.pack_weights_imatrix(w, imp, rotate=False)
     d = oracle.pack_weights_imatrix(w, np.ones(256), rotate=False)
     assert np.mean(c["d16"] != d["d16"]) > 0.3
+
+
+def test_effective_importance_cleans_before_rotating():
+    imp = np.r_[np.full(32, 2.0), [-1.0, np.nan, np.inf] + [4.0] * 29]
+    e = oracle.effective_importance(imp, 64, rotate=True)
+    assert np.allclose(e[:32], 2.0, rtol=1e-14) and np.allclose(e[32:], 4.0 * 29 / 32, rtol=1e-14)
+    assert np.array_equal(oracle.effective_importance(None, 64, rotate=False), np.ones(64))
