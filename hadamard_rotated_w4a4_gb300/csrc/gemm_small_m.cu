@@ -8,12 +8,10 @@
 // core tile.  Here each block's integer dot products run on the warp-level f16
 // tensor core: mma.sync m16n8k16, A = 16 weight rows, B = the 8 token columns.
 // A code nibble n placed under the f16 exponent byte 0x64 (prmt) is the f16
-// 1024 + n.  The activations take one f16x2 subtraction of 1032 (nibbles
-// flipped by ^ 8 give a + 8, so the result is the signed a); the weights enter
-// as 1024 + q, and two more MMAs with the constant A = -1032 add -1032 S_a, so
-//   D = sum (1024 + q) a - 1032 sum a = sum (q - 8) a = P.
-// Every product and partial sum is an integer below 2^19: D = P exactly in
-// fp32.  Four MMAs per 32-element block (two K halves of each pair).
+// 1024 + n, and one exact f16x2 subtraction of 1032 leaves n - 8: q - 8 for a
+// weight code q, and the signed a for an activation nibble flipped by ^ 8.
+// Every product and partial sum is an integer below 2^12, so the two MMAs of a
+// block (its two K halves) give D = P exactly in fp32.
 //
 // A CTA owns 16 weight rows; its 4 warps split K round robin in chunks of 8
 // blocks (warp w takes chunks w, w + 4, ...).  Each warp streams its chunks'
@@ -75,12 +73,11 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
   return r;
 }
-// f16x2 (1024 + n0, 1024 + n1) of the nibbles in the two bytes `sel` picks
-// from x (bytes holding one nibble each): the byte under the exponent byte 0x64.
-__device__ __forceinline__ uint32_t nib_pair_f16(uint32_t x, uint32_t sel) { return prmt(x, 0x64646464u, sel); }
-// ... minus 1032 (exact): the signed activation a from its nibble a + 8.
-__device__ __forceinline__ uint32_t act_pair_f16(uint32_t x, uint32_t sel) {
-  const uint32_t h = nib_pair_f16(x, sel);
+// f16x2 (n0 - 8, n1 - 8) of the nibbles in the two bytes `sel` picks from x
+// (bytes holding one nibble each): the byte under the exponent byte 0x64 is
+// 1024 + n, minus 1032 exactly.
+__device__ __forceinline__ uint32_t nib_pair_f16(uint32_t x, uint32_t sel) {
+  const uint32_t h = prmt(x, 0x64646464u, sel);
   __half2 a, b;
   const uint32_t c = 0x64086408u;
   memcpy(&a, &h, 4);
@@ -90,8 +87,6 @@ __device__ __forceinline__ uint32_t act_pair_f16(uint32_t x, uint32_t sel) {
   memcpy(&out, &r, 4);
   return out;
 }
-constexpr uint32_t kNeg1032x2 = 0xE408E408u;  // f16x2 (-1032, -1032)
-
 // D += A B, m16n8k16, f16 operands, fp32 accumulators.
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                         uint32_t b0, uint32_t b1) {
@@ -199,29 +194,33 @@ __global__ void __launch_bounds__(32 * kSmWarps, kSmCtasPerSm) w4a4_small_m_kern
     const uint4 dwv1 = *reinterpret_cast<const uint4*>(&s.ws[g + 8][0]);  // and of row g + 8
     const uint32_t dw0w[4] = {dwv0.x, dwv0.y, dwv0.z, dwv0.w}, dw1w[4] = {dwv1.x, dwv1.y, dwv1.z, dwv1.w};
     constexpr uint32_t kLow = 0x0F0F0F0Fu;
+    auto block_t = [&](int bb) {
+      const uint32_t x0 = w_lo[bb * 4], x1 = w_hi[bb * 4];
+      const uint32_t xa = a_r[bb * 4] ^ 0x88888888u;  // a + 8 in every nibble
+      const uint32_t l0 = x0 & kLow, h0 = (x0 >> 4) & kLow, l1 = x1 & kLow, h1 = (x1 >> 4) & kLow;
+      const uint32_t la = xa & kLow, ha = (xa >> 4) & kLow;
+      // k 4tq..4tq+3 (low nibbles) in the first K half, k 16+4tq.. (high) in the
+      // second; in each, byte pair (0, 1) -> k slots 2tq, 2tq+1, (2, 3) -> 2tq+8, 2tq+9
+      const uint32_t b1a = nib_pair_f16(la, 0x4140u), b1b = nib_pair_f16(la, 0x4342u);
+      const uint32_t b2a = nib_pair_f16(ha, 0x4140u), b2b = nib_pair_f16(ha, 0x4342u);
+      float d[4];
+      mma_f16_first(d, nib_pair_f16(l0, 0x4140u), nib_pair_f16(l1, 0x4140u), nib_pair_f16(l0, 0x4342u),
+                    nib_pair_f16(l1, 0x4342u), b1a, b1b);
+      mma_f16(d, nib_pair_f16(h0, 0x4140u), nib_pair_f16(h1, 0x4140u), nib_pair_f16(h0, 0x4342u),
+              nib_pair_f16(h1, 0x4342u), b2a, b2b);
+      const float dw0 = __half2float(__ushort_as_half(static_cast<unsigned short>(dw0w[bb >> 1] >> (16 * (bb & 1)))));
+      const float dw1 = __half2float(__ushort_as_half(static_cast<unsigned short>(dw1w[bb >> 1] >> (16 * (bb & 1)))));
+      t01[bb] = __fmul2_rn(make_float2(d[0], d[1]), make_float2(dw0, dw0));
+      t23[bb] = __fmul2_rn(make_float2(d[2], d[3]), make_float2(dw1, dw1));
+    };
+    const bool full = nb == kSmChunk;  // every chunk but a ragged last one: no per-block tests
+    if (full) {
 #pragma unroll
-    for (int bb = 0; bb < kSmChunk; ++bb) {
-      if (bb < nb) {
-        const uint32_t x0 = w_lo[bb * 4], x1 = w_hi[bb * 4];
-        const uint32_t xa = a_r[bb * 4] ^ 0x88888888u;  // a + 8 in every nibble
-        const uint32_t l0 = x0 & kLow, h0 = (x0 >> 4) & kLow, l1 = x1 & kLow, h1 = (x1 >> 4) & kLow;
-        const uint32_t la = xa & kLow, ha = (xa >> 4) & kLow;
-        // k 4tq..4tq+3 (low nibbles) in the first K half, k 16+4tq.. (high) in the
-        // second; in each, byte pair (0, 1) -> k slots 2tq, 2tq+1, (2, 3) -> 2tq+8, 2tq+9
-        const uint32_t b1a = act_pair_f16(la, 0x4140u), b1b = act_pair_f16(la, 0x4342u);
-        const uint32_t b2a = act_pair_f16(ha, 0x4140u), b2b = act_pair_f16(ha, 0x4342u);
-        float d[4];
-        mma_f16_first(d, nib_pair_f16(l0, 0x4140u), nib_pair_f16(l1, 0x4140u), nib_pair_f16(l0, 0x4342u),
-                      nib_pair_f16(l1, 0x4342u), b1a, b1b);
-        mma_f16(d, nib_pair_f16(h0, 0x4140u), nib_pair_f16(h1, 0x4140u), nib_pair_f16(h0, 0x4342u),
-                nib_pair_f16(h1, 0x4342u), b2a, b2b);
-        mma_f16(d, kNeg1032x2, kNeg1032x2, kNeg1032x2, kNeg1032x2, b1a, b1b);
-        mma_f16(d, kNeg1032x2, kNeg1032x2, kNeg1032x2, kNeg1032x2, b2a, b2b);
-        const float dw0 = __half2float(__ushort_as_half(static_cast<unsigned short>(dw0w[bb >> 1] >> (16 * (bb & 1)))));
-        const float dw1 = __half2float(__ushort_as_half(static_cast<unsigned short>(dw1w[bb >> 1] >> (16 * (bb & 1)))));
-        t01[bb] = __fmul2_rn(make_float2(d[0], d[1]), make_float2(dw0, dw0));
-        t23[bb] = __fmul2_rn(make_float2(d[2], d[3]), make_float2(dw1, dw1));
-      }
+      for (int bb = 0; bb < kSmChunk; ++bb) block_t(bb);
+    } else {
+#pragma unroll
+      for (int bb = 0; bb < kSmChunk; ++bb)
+        if (bb < nb) block_t(bb);
     }
     float2 da[kSmChunk];  // d_a of tokens (2tq, 2tq + 1)
     {
@@ -242,11 +241,20 @@ __global__ void __launch_bounds__(32 * kSmWarps, kSmCtasPerSm) w4a4_small_m_kern
       acc01 = make_float2(h.x, h.y);
       acc23 = make_float2(h.z, h.w);
     }
+    // each lane of the f32x2 FMA rounds as fmaf
+    if (full) {
 #pragma unroll
-    for (int bb = 0; bb < kSmChunk; ++bb) {
-      if (bb < nb) {  // each lane of the f32x2 FMA rounds as fmaf
+      for (int bb = 0; bb < kSmChunk; ++bb) {
         acc01 = __ffma2_rn(t01[bb], da[bb], acc01);
         acc23 = __ffma2_rn(t23[bb], da[bb], acc23);
+      }
+    } else {
+#pragma unroll
+      for (int bb = 0; bb < kSmChunk; ++bb) {
+        if (bb < nb) {
+          acc01 = __ffma2_rn(t01[bb], da[bb], acc01);
+          acc23 = __ffma2_rn(t23[bb], da[bb], acc23);
+        }
       }
     }
     if (c + 1 < nchunks) {
