@@ -42,6 +42,32 @@ def env_rank():
     return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("LOCAL_RANK", "0"))
 
 
+# ----------------------------------------------------------------------------- replicas (N > 1)
+def max_over_ranks(ms: float, world: int, device=None) -> float:
+    """The slowest replica's time, returned on every rank (all_reduce MAX; the
+    process group must be up when world > 1)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(world: int, ops_per_replica: float, ms_per_step: float) -> float:
+    """Throughput of the whole job: the work of all replicas over the slowest one's step time."""
+    return world * ops_per_replica / (ms_per_step * 1e-3) / 1e12
+
+
+def emit(line: dict | None, rank: int) -> bool:
+    """Rank 0 alone prints the JSON line."""
+    if line is None or rank != 0:
+        return False
+    print(json.dumps(line), flush=True)
+    return True
+
+
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
     """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
@@ -468,13 +494,10 @@ def run_ours(args, shape) -> dict | None:
                   "small_m_weight_gbs": wbytes / (sm_ms * 1e-3) / 1e9}
         del x8, a4v, y8, wsv
     w4.w4a4_check()
-    if world > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
     ms_per_step = total_ms / args.steps
     ops = 2.0 * M * N * K
-    value = world * ops / (ms_per_step * 1e-3) / 1e12
+    value = whole_job_value(world, ops, ms_per_step)
 
     # ---- end to end through the public API: host activations in, host output back, every step.
     # Each step copies its own fp32 activations in from pinned host memory and reads its
@@ -510,6 +533,8 @@ def run_ours(args, shape) -> dict | None:
     for i in range(args.warmup):
         e2e_step(i)
     torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
     a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a0.record(s_in)
     for i in range(args.steps):
@@ -520,8 +545,10 @@ def run_ours(args, shape) -> dict | None:
         s_out.wait_event(a1_wait)
     a1.record(s_out)
     torch.cuda.synchronize()
-    e2e_ms = a0.elapsed_time(a1) / args.steps
-    e2e_value = world * ops / (e2e_ms * 1e-3) / 1e12
+    if world > 1:
+        torch.distributed.barrier()
+    e2e_ms = max_over_ranks(a0.elapsed_time(a1), world, dev) / args.steps
+    e2e_value = whole_job_value(world, ops, e2e_ms)
     # the results read back are the device results of the last two steps
     assert torch.equal(y_hosts[(args.steps - 1) % 2], ybufs[(args.steps - 1) % 2].cpu())
 
@@ -625,8 +652,7 @@ def main():
         ap.error("--warmup must be at least 3")
     shape = si.DENSE[args.config]
     line = run_reference(args, shape) if args.impl == "reference" else run_ours(args, shape)
-    if line is not None:
-        print(json.dumps(line), flush=True)
+    emit(line, env_rank()[0])
 
 
 if __name__ == "__main__":
