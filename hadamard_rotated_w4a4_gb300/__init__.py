@@ -50,7 +50,8 @@ TAG_ROTATED = 0x1
 
 #: every symbol include/w4a4.h declares
 EXPORTS = [
-    "w4a4_q4_0_codes_bytes", "w4a4_q4_0_scales_bytes", "w4a4_q4_0_sums_bytes", "w4a4_act4_codes_bytes",
+    "w4a4_q4_0_codes_bytes", "w4a4_q4_0_scales_bytes", "w4a4_q4_0_sums_bytes", "w4a4_q4_0_expanded_bytes",
+    "w4a4_act4_codes_bytes",
     "w4a4_act4_scales_bytes", "h32_q4_0_pack_weights", "q4_0_import", "w4a4_rotate_quantize_act", "w4a4_gemm", "w4a4_gemm_workspace_bytes",
     "w4a4_gemm_partials", "w4a4_gemm_id", "w4a4_gemm_id_workspace_bytes", "w4a4_gemm_id_status", "w4a4_gemm_id_static", "w4a4_check", "w4a4_last_error",
     "w4a4_status_name", "w4a4_abi_version", "w4a4_act8_codes_bytes", "w4a4_act8_scales_bytes", "w4a4_gemm_small_m",
@@ -69,7 +70,8 @@ class W4A4Error(RuntimeError):
 
 class _Q4_0Desc(ctypes.Structure):
     _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("sums", ctypes.c_void_p),
-                ("rows", ctypes.c_int64), ("K", ctypes.c_int64), ("tag", ctypes.c_uint32)]
+                ("rows", ctypes.c_int64), ("K", ctypes.c_int64), ("tag", ctypes.c_uint32),
+                ("expanded", ctypes.c_void_p)]
 
 
 class _Act4Desc(ctypes.Structure):
@@ -101,7 +103,8 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         _build.build()
     lib = ctypes.CDLL(path)
     i64, vp, i32, u = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
-    for name in ("w4a4_q4_0_codes_bytes", "w4a4_q4_0_scales_bytes", "w4a4_q4_0_sums_bytes", "w4a4_act4_codes_bytes",
+    for name in ("w4a4_q4_0_codes_bytes", "w4a4_q4_0_scales_bytes", "w4a4_q4_0_sums_bytes", "w4a4_q4_0_expanded_bytes",
+                 "w4a4_act4_codes_bytes",
                  "w4a4_act4_scales_bytes", "w4a4_act8_codes_bytes", "w4a4_act8_scales_bytes"):
         f = getattr(lib, name)
         f.argtypes, f.restype = [i64, i64], u
@@ -158,13 +161,16 @@ def _cuda(t: torch.Tensor, name: str) -> None:
 @dataclass
 class Q4_0Weights:
     """Q4_0 weights in the library's layout: codes uint8 [rows][K/2], scales fp16 [rows][K/32],
-    and the derived per-block code sums int16 [rows][K/32]."""
+    the derived per-block code sums int16 [rows][K/32] and, optionally, the expanded operand
+    (e4m3 bytes of q - 8, [round_up(rows, 8)][K]) that lets the dense GEMM skip converting
+    the weights."""
     codes: torch.Tensor
     scales_buf: torch.Tensor  # uint8 buffer (padded to 16 bytes) holding the fp16 scales
     sums_buf: torch.Tensor    # uint8 buffer (padded to 16 bytes) holding the int16 block sums
     rows: int
     K: int
     rotated: bool
+    expanded: torch.Tensor | None = None  # uint8 buffer of w4a4_q4_0_expanded_bytes, or None
 
     @property
     def sums(self) -> torch.Tensor:
@@ -182,11 +188,16 @@ class Q4_0Weights:
 
     def desc(self) -> _Q4_0Desc:
         return _Q4_0Desc(self.codes.data_ptr(), self.scales_buf.data_ptr(), self.sums_buf.data_ptr(), self.rows,
-                         self.K, self.tag)
+                         self.K, self.tag, self.expanded.data_ptr() if self.expanded is not None else None)
 
     def head(self, rows: int) -> "Q4_0Weights":
         """The first `rows` rows (views of the same buffers)."""
-        return Q4_0Weights(self.codes[:rows], self.scales_buf, self.sums_buf, rows, self.K, self.rotated)
+        return Q4_0Weights(self.codes[:rows], self.scales_buf, self.sums_buf, rows, self.K, self.rotated,
+                           self.expanded)
+
+    def without_expanded(self) -> "Q4_0Weights":
+        """The same weights without the expanded operand (the GEMM then converts the codes)."""
+        return Q4_0Weights(self.codes, self.scales_buf, self.sums_buf, self.rows, self.K, self.rotated)
 
 
 @dataclass
@@ -215,7 +226,7 @@ class Act4:
         return _Act4Desc(self.codes.data_ptr(), self.scales_buf.data_ptr(), self.rows, self.K, self.tag)
 
 
-def alloc_q4_0(rows: int, K: int, device, rotated: bool = True) -> Q4_0Weights:
+def alloc_q4_0(rows: int, K: int, device, rotated: bool = True, expanded: bool = True) -> Q4_0Weights:
     lib = load_library()
     nc, ns = lib.w4a4_q4_0_codes_bytes(rows, K), lib.w4a4_q4_0_scales_bytes(rows, K)
     if K <= 0 or K % 32:
@@ -223,7 +234,9 @@ def alloc_q4_0(rows: int, K: int, device, rotated: bool = True) -> Q4_0Weights:
     codes = torch.empty(max(nc, 16), dtype=torch.uint8, device=device)[:nc].view(rows, K // 2)
     sbuf = torch.empty(max(ns, 16), dtype=torch.uint8, device=device)
     ubuf = torch.empty(max(lib.w4a4_q4_0_sums_bytes(rows, K), 16), dtype=torch.uint8, device=device)
-    return Q4_0Weights(codes, sbuf, ubuf, rows, K, rotated)
+    ebuf = (torch.empty(max(lib.w4a4_q4_0_expanded_bytes(rows, K), 16), dtype=torch.uint8, device=device)
+            if expanded else None)
+    return Q4_0Weights(codes, sbuf, ubuf, rows, K, rotated, ebuf)
 
 
 def alloc_act4(rows: int, K: int, device, rotated: bool = True) -> Act4:

@@ -65,8 +65,8 @@ w4a4_status check_q4_0(const w4a4_q4_0* w, const char* fn) {
   if (s != W4A4_OK) return s;
   if (w->rows > 0 && (!w->codes || !w->scales || !w->sums))
     return fail(W4A4_ERR_INVALID_ARG, "%s: weight pointers are NULL", fn);
-  if (!aligned16(w->codes) || !aligned16(w->scales) || !aligned16(w->sums))
-    return fail(W4A4_ERR_ALIGNMENT, "%s: weight codes/scales/sums must be 16-byte aligned", fn);
+  if (!aligned16(w->codes) || !aligned16(w->scales) || !aligned16(w->sums) || !aligned16(w->expanded))
+    return fail(W4A4_ERR_ALIGNMENT, "%s: weight codes/scales/sums/expanded must be 16-byte aligned", fn);
   return W4A4_OK;
 }
 
@@ -132,6 +132,10 @@ size_t w4a4_q4_0_scales_bytes(int64_t rows, int64_t K) {
   return round16(static_cast<size_t>(rows) * static_cast<size_t>(K / 32) * 2);
 }
 size_t w4a4_q4_0_sums_bytes(int64_t rows, int64_t K) { return w4a4_q4_0_scales_bytes(rows, K); }
+size_t w4a4_q4_0_expanded_bytes(int64_t rows, int64_t K) {
+  if (!valid_k(K) || rows < 0) return 0;
+  return round16(static_cast<size_t>((rows + 7) / 8 * 8) * static_cast<size_t>(K));
+}
 size_t w4a4_act4_codes_bytes(int64_t rows, int64_t K) { return w4a4_q4_0_codes_bytes(rows, K); }
 size_t w4a4_act8_codes_bytes(int64_t rows, int64_t K) {
   if (!valid_k(K) || rows < 0) return 0;
@@ -167,7 +171,9 @@ w4a4_status h32_q4_0_pack_weights(const void* w, int w_dtype, int64_t N, int64_t
   out->K = K;
   out->tag = W4A4_TAG_Q4_0 | (rotate ? W4A4_TAG_ROTATED : 0u);
   if (N == 0) return ok();
+  if (!aligned16(out->expanded)) return fail(W4A4_ERR_ALIGNMENT, "%s: expanded must be 16-byte aligned", fn);
   return cuda_status(w4a4::launch_pack_q4_0(w, w_dtype, N, K, ldw, rotate, out->codes, out->scales, out->sums,
+                                            out->expanded,
                                             reinterpret_cast<cudaStream_t>(stream)), fn);
 }
 
@@ -191,8 +197,10 @@ w4a4_status h32_q4_0_pack_weights_imatrix(const void* w, int w_dtype, int64_t N,
   out->K = K;
   out->tag = W4A4_TAG_Q4_0 | (rotate ? W4A4_TAG_ROTATED : 0u);
   if (N == 0) return ok();
+  if (!aligned16(out->expanded)) return fail(W4A4_ERR_ALIGNMENT, "%s: expanded must be 16-byte aligned", fn);
   return cuda_status(w4a4::launch_pack_q4_0_weighted(w, w_dtype, N, K, ldw, rotate, imatrix, out->codes, out->scales,
-                                                     out->sums, reinterpret_cast<cudaStream_t>(stream)), fn);
+                                                     out->sums, out->expanded, reinterpret_cast<cudaStream_t>(stream)),
+                     fn);
 }
 
 w4a4_status q4_0_import(const void* blocks, int64_t N, int64_t K, int rotated, w4a4_q4_0* out,
@@ -211,7 +219,8 @@ w4a4_status q4_0_import(const void* blocks, int64_t N, int64_t K, int rotated, w
   out->K = K;
   out->tag = W4A4_TAG_Q4_0 | (rotated ? W4A4_TAG_ROTATED : 0u);
   if (N == 0) return ok();
-  return cuda_status(w4a4::launch_import_q4_0(blocks, N, K, out->codes, out->scales, out->sums,
+  if (!aligned16(out->expanded)) return fail(W4A4_ERR_ALIGNMENT, "%s: expanded must be 16-byte aligned", fn);
+  return cuda_status(w4a4::launch_import_q4_0(blocks, N, K, out->codes, out->scales, out->sums, out->expanded,
                                               reinterpret_cast<cudaStream_t>(stream)), fn);
 }
 
@@ -257,7 +266,7 @@ w4a4_status w4a4_gemm(const w4a4_q4_0* w, const w4a4_act4* a, float* y, int64_t 
       return fail(W4A4_ERR_WORKSPACE, "%s: workspace %zu bytes < %zu needed", fn, ws_bytes, need);
     if (!aligned16(ws)) return fail(W4A4_ERR_ALIGNMENT, "%s: ws must be 16-byte aligned", fn);
   }
-  return cuda_status(w4a4::launch_gemm_tc(w->codes, w->scales, w->sums, N, a->codes, a->scales, M, a->K, y, ldy, nullptr,
+  return cuda_status(w4a4::launch_gemm_tc(w->codes, w->scales, w->sums, w->expanded, N, a->codes, a->scales, M, a->K, y, ldy, nullptr,
                                           ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream)), fn);
 }
 
@@ -286,7 +295,7 @@ w4a4_status w4a4_gemm_partials(const w4a4_q4_0* w, const w4a4_act4* a, int32_t* 
   if (a->rows == 0 || w->rows == 0) return ok();
   if (!P) return fail(W4A4_ERR_INVALID_ARG, "%s: P is NULL", fn);
   if (!aligned16(P)) return fail(W4A4_ERR_ALIGNMENT, "%s: P must be 16-byte aligned", fn);
-  return cuda_status(w4a4::launch_gemm_tc(w->codes, w->scales, w->sums, w->rows, a->codes, a->scales, a->rows, a->K, nullptr,
+  return cuda_status(w4a4::launch_gemm_tc(w->codes, w->scales, w->sums, nullptr, w->rows, a->codes, a->scales, a->rows, a->K, nullptr,
                                           0, P, nullptr, 0, reinterpret_cast<cudaStream_t>(stream)), fn);
 }
 
@@ -427,7 +436,7 @@ w4a4_status w4a4_gemm_id(const w4a4_q4_0* experts, int E, int64_t N, const w4a4_
   if (!aligned16(ws) || (reinterpret_cast<uintptr_t>(y) & 3u) != 0)
     return fail(W4A4_ERR_ALIGNMENT, "%s: ws must be 16-byte aligned and y 4-byte aligned", fn);
   const w4a4::Routing r = w4a4::routing_in(ws, M * top_k, E, a->K);
-  return cuda_status(w4a4::launch_gemm_id(experts->codes, experts->scales, experts->sums, E, N, a->codes, a->scales, a->K, ids, M,
+  return cuda_status(w4a4::launch_gemm_id(experts->codes, experts->scales, experts->sums, experts->expanded, E, N, a->codes, a->scales, a->K, ids, M,
                                           top_k, act_per_slot, y, r, reinterpret_cast<cudaStream_t>(stream)), fn);
 }
 
@@ -477,7 +486,7 @@ w4a4_status w4a4_gemm_id_static(const w4a4_q4_0* experts, int E, int64_t N, cons
   cudaError_t e = w4a4::id_static_scratch(&ws);
   if (e != cudaSuccess) return cuda_status(e, fn);
   const w4a4::Routing r = w4a4::routing_in(ws, M * top_k, E, a->K);
-  return cuda_status(w4a4::launch_gemm_id(experts->codes, experts->scales, experts->sums, E, N, a->codes, a->scales,
+  return cuda_status(w4a4::launch_gemm_id(experts->codes, experts->scales, experts->sums, experts->expanded, E, N, a->codes, a->scales,
                                           a->K, ids, M, top_k, act_per_slot, y, r,
                                           reinterpret_cast<cudaStream_t>(stream)),
                      fn);

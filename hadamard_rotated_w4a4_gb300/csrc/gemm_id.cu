@@ -158,9 +158,10 @@ cudaError_t id_static_scratch(void** addr) {
   return cudaSuccess;
 }
 
-cudaError_t launch_gemm_id(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums, int E, int64_t N,
-                           const uint8_t* a_codes, const float* a_scales, int64_t K, const int32_t* ids, int64_t M,
-                           int top_k, int act_per_slot, float* y, const Routing& r, cudaStream_t stream) {
+cudaError_t launch_gemm_id(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums,
+                           const uint8_t* w_expanded, int E, int64_t N, const uint8_t* a_codes, const float* a_scales,
+                           int64_t K, const int32_t* ids, int64_t M, int top_k, int act_per_slot, float* y,
+                           const Routing& r, cudaStream_t stream) {
   const int64_t npairs = M * top_k;
   const size_t sh = sizeof(int32_t) * 2 * static_cast<size_t>(E);
   const int tile = routed_tile_tokens(npairs, E);
@@ -173,7 +174,8 @@ cudaError_t launch_gemm_id(const uint8_t* w_codes, const uint16_t* w_scales, con
                                                                                  r.gscales);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return launch_gemm_tc_routed(w_codes, w_scales, w_sums, E, N, r.gcodes, r.gscales, K, npairs, tile, y, r, stream);
+  return launch_gemm_tc_routed(w_codes, w_scales, w_sums, w_expanded, E, N, r.gcodes, r.gscales, K, npairs, tile, y, r,
+                               stream);
 }
 
 }  // namespace w4a4

@@ -88,10 +88,15 @@ constexpr uint32_t kWaitHintNs = W4A4_WAIT_HINT_NS;
 // 16 = the rotate-only route (bf16 activations that were not quantised, bf16
 // weight operands q - 8, two kind::f16 MMAs per block with the bf16 format;
 // the block sums round in the tensor core's fp32 accumulation, d_a = 1).
-template <int TTM, int AB = 4>
+// WEXP: the weights come pre-expanded (the e4m3 bytes of q - 8, loaded by a 4D
+// TMA straight into the K-major operand layout) and the MMA reads them from the
+// raw stage; the converters then handle only the activations.
+template <int TTM, int AB = 4, bool WEXP = false>
 struct __align__(128) Smem {
   static constexpr int TT = TTM;
   static constexpr int ABITS = AB;
+  static constexpr bool WX = WEXP;
+  static constexpr int WROW = KB * (WEXP ? 32 : 16);  // raw weight bytes per row and stage
   static constexpr int ARAW_ROW = KB * 4 * AB;  // raw activation bytes per row and stage: 64 or 128
   static constexpr int OPB = AB == 4 ? 1 : 2;   // operand bytes per element: e4m3 or f16
   static constexpr int WOP = TW * 32 * OPB + 32;   // operand buffer strides, padded by 32 bytes so that the
@@ -113,9 +118,9 @@ struct __align__(128) Smem {
   // release block 4s + 2 - NBUF = 4s, past stage s - 2.
   static constexpr bool CONV_SCALES = TTM == 128;
   static constexpr int NSC = CONV_SCALES ? 4 : 3;
-  uint8_t wraw[RAW][TW * KB * 16];  // TMA box: 128 rows x 64 bytes
+  uint8_t wraw[RAW][TW * WROW];  // TMA box: 128 rows x 64 code bytes, or (WEXP) the operand layout of 4 blocks
   uint8_t araw[RAW][TTM * ARAW_ROW];  // TMA box: tt rows x 64 (int4) or 128 (int8) bytes
-  uint8_t wf8[F8][WOP];
+  uint8_t wf8[WEXP ? 1 : F8][WOP];
   uint8_t af8[F8][AOP];
   float sda[NSC][KB][TTM];              // d_a per stage, block-major
   float sdw[NSC][KB][TW];              // d_w * 2^18
@@ -136,6 +141,8 @@ static_assert(sizeof(Smem<256>) <= 227 * 1024, "shared memory per CTA is at most
 static_assert(sizeof(Smem<128>) <= 227 * 1024, "shared memory per CTA is at most 227 KB");
 static_assert(sizeof(Smem<128, 8>) <= 227 * 1024, "shared memory per CTA is at most 227 KB");
 static_assert(sizeof(Smem<128, 16>) <= 227 * 1024, "shared memory per CTA is at most 227 KB");
+static_assert(sizeof(Smem<256, 4, true>) <= 227 * 1024, "shared memory per CTA is at most 227 KB");
+static_assert(sizeof(Smem<128, 4, true>) <= 227 * 1024, "shared memory per CTA is at most 227 KB");
 
 struct TcArgs {
   const uint16_t* w_scales;
@@ -217,6 +224,15 @@ __device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* map, int32_
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
       ::"r"(su32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(su32(bar))
+      : "memory");
+}
+// 4D box (the expanded weights' map): coordinates {byte in chunk, row in group, chunk, group}.
+__device__ __forceinline__ void tma_4d(void* dst, const CUtensorMap* map, int32_t c0, int32_t c1, int32_t c2,
+                                       int32_t c3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+      "[%6];" ::"r"(su32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(su32(bar))
       : "memory");
 }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
@@ -481,7 +497,7 @@ template <class SM>
 __device__ void producer(const TcArgs& p, SM& S, const CUtensorMap* wmap, const CUtensorMap* amap) {
   const int64_t B = p.K / 32;
   const int nst = static_cast<int>((B + KB - 1) / KB);
-  const uint32_t bytes = static_cast<uint32_t>(KB * 16 * TW + SM::ARAW_ROW * p.tt);  // full boxes, zero fill included
+  const uint32_t bytes = static_cast<uint32_t>(SM::WROW * TW + SM::ARAW_ROW * p.tt);  // full boxes, zero fill included
   uint32_t gstage = 0;
   SegIter si = seg_iter(p);
   Seg sg;
@@ -491,8 +507,12 @@ __device__ void producer(const TcArgs& p, SM& S, const CUtensorMap* wmap, const 
       const int slot = gstage % RAW;
       if (!mbar_wait(&S.empty_raw[slot], ((gstage / RAW) & 1) ^ 1, S)) break;
       mbar_expect_tx(&S.full_raw[slot], bytes);
-      const int32_t x = static_cast<int32_t>(s * KB * 16);
-      tma_2d(S.wraw[slot], wmap, x, static_cast<int32_t>(T.wrow0), &S.full_raw[slot]);
+      if constexpr (SM::WX) {  // 4 blocks = 8 chunks of 16 bytes x 16 groups of 8 rows
+        tma_4d(S.wraw[slot], wmap, 0, 0, static_cast<int32_t>(s * KB * 2), static_cast<int32_t>(T.wrow0 / 8),
+               &S.full_raw[slot]);
+      } else {
+        tma_2d(S.wraw[slot], wmap, static_cast<int32_t>(s * KB * 16), static_cast<int32_t>(T.wrow0), &S.full_raw[slot]);
+      }
       tma_2d(S.araw[slot], amap, static_cast<int32_t>(s * SM::ARAW_ROW), static_cast<int32_t>(T.m0), &S.full_raw[slot]);
       ++gstage;
     }
@@ -512,6 +532,7 @@ __device__ void mma_issuer(const TcArgs& p, SM& S, uint32_t tmem) {
   const int64_t B = p.K / 32;
   const int nst = static_cast<int>((B + KB - 1) / KB);
   uint32_t gblk = 0;
+  uint32_t gst = 0;  // raw stages of the finished segments (the producer's stage order)
   SegIter si = seg_iter(p);
   Seg sg;
   while (seg_next(p, nst, si, sg)) {
@@ -525,7 +546,13 @@ __device__ void mma_issuer(const TcArgs& p, SM& S, uint32_t tmem) {
       if (!mbar_wait(&S.tm_empty[tb], ((gblk / SM::NBUF) & 1) ^ 1, S)) goto done;
       tc_fence_after();
       const uint32_t dt = tmem + static_cast<uint32_t>(tb * SM::TT);
-      if constexpr (SM::ABITS == 4) {
+      if constexpr (SM::ABITS == 4 && SM::WX) {
+        // A straight from the raw stage: block kb's two 16-byte chunks of every
+        // row are core matrices 128 bytes apart, 8-row groups 8 chunks apart
+        const int s = static_cast<int>(b / KB), kb = static_cast<int>(b - static_cast<int64_t>(s) * KB);
+        const uint32_t slot = (gst + static_cast<uint32_t>(s - sg.s0)) % RAW;
+        mma_f8(dt, kmajor_desc_sbo(S.wraw[slot] + kb * 256, KB * 2 * 128), kmajor_desc(S.af8[f]), idesc);
+      } else if constexpr (SM::ABITS == 4) {
         mma_f8(dt, kmajor_desc(S.wf8[f]), kmajor_desc(S.af8[f]), idesc);
       } else {  // two K = 16 halves of the block (core-matrix pairs 256 bytes apart)
         const uint64_t ad = kmajor_desc_sbo(S.wf8[f], 512), bd = kmajor_desc_sbo(S.af8[f], 512);
@@ -534,7 +561,13 @@ __device__ void mma_issuer(const TcArgs& p, SM& S, uint32_t tmem) {
       }
       mma_commit(&S.tm_full[tb]);
       mma_commit(&S.f8_empty[f]);
+      if constexpr (SM::WX) {  // the stage's weights are read once its last block's MMA completes
+        const int64_t s = b / KB;
+        const int64_t last = ((s + 1) * KB < B ? (s + 1) * KB : B) - 1;
+        if (b == last) mma_commit(&S.empty_raw[(gst + static_cast<uint32_t>(s - sg.s0)) % RAW]);
+      }
     }
+    gst += static_cast<uint32_t>(sg.s1 - sg.s0);
   }
 done:
   // wait (bounded) until every issued MMA has finished before TMEM is released
@@ -726,6 +759,7 @@ __device__ void converters(const TcArgs& p, SM& S) {
             }
           }
         } else {
+        if constexpr (!SM::WX)  // (pre-expanded weights need no conversion)
 #pragma unroll 4
         for (int i = 0; i < (TW - r0 + RS - 1) / RS; ++i) {
           const uint4 raw = *reinterpret_cast<const uint4*>(ws + i * RS * 64);
@@ -1075,11 +1109,11 @@ __device__ void workers(const TcArgs& p, SM& S, uint32_t tmem) {
   }
 }
 
-template <bool PARTIALS, int TTM, int AB>
-__global__ void __launch_bounds__(Smem<TTM, AB>::THREADS, 1)
+template <bool PARTIALS, int TTM, int AB, bool WEXP>
+__global__ void __launch_bounds__(Smem<TTM, AB, WEXP>::THREADS, 1)
     w4a4_gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap amap,
                         const TcArgs p) {
-  using SmemT = Smem<TTM, AB>;
+  using SmemT = Smem<TTM, AB, WEXP>;
   // Smem is taken straight from the __shared__ array (no integer round trip), so
   // the compiler keeps every access in the shared address space (LDS/STS).  The
   // operands need 16-byte alignment (no swizzle), the TMA boxes 128 bytes.
@@ -1094,7 +1128,7 @@ __global__ void __launch_bounds__(Smem<TTM, AB>::THREADS, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < RAW; ++i) {
       mbar_init(&S.full_raw[i], 1);
-      mbar_init(&S.empty_raw[i], SmemT::CONV);
+      mbar_init(&S.empty_raw[i], SmemT::CONV + (SmemT::WX ? 1 : 0));  // (WEXP: plus the MMA's commit)
     }
     for (int i = 0; i < SmemT::F8; ++i) {
       mbar_init(&S.f8_full[i], SmemT::CONV);
@@ -1175,11 +1209,29 @@ cudaError_t codes_map(CUtensorMap* m, const uint8_t* codes, int64_t rows, int64_
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <bool PARTIALS, int TTM, int AB = 4>
+// 4D map over the expanded weights [rows8][K] bytes that writes a box straight in
+// the K-major operand layout: dims {16 bytes, 8 rows of a group, K/16 chunks,
+// rows8/8 groups}, strides {K, 16, 8K} bytes; a box of 4 blocks (8 chunks) x
+// box_rows rows lands as [group][chunk][row][16 bytes].
+cudaError_t expanded_map(CUtensorMap* m, const uint8_t* wexp, int64_t rows, int64_t K, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  const int64_t groups = (rows + 7) / 8;
+  const cuuint64_t dims[4] = {16, 8, static_cast<cuuint64_t>(K / 16), static_cast<cuuint64_t>(groups)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(K), 16, static_cast<cuuint64_t>(8 * K)};
+  const cuuint32_t box[4] = {16, 8, static_cast<cuuint32_t>(KB * 2), static_cast<cuuint32_t>(box_rows / 8)};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<uint8_t*>(wexp), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <bool PARTIALS, int TTM, int AB = 4, bool WEXP = false>
 cudaError_t launch_tc(const CUtensorMap& wmap, const CUtensorMap& amap, const TcArgs& a, int64_t max_tiles,
                       cudaStream_t stream) {
-  auto kern = w4a4_gemm_tc_kernel<PARTIALS, TTM, AB>;
-  using SM = Smem<TTM, AB>;
+  auto kern = w4a4_gemm_tc_kernel<PARTIALS, TTM, AB, WEXP>;
+  using SM = Smem<TTM, AB, WEXP>;
   constexpr size_t kSmemBytes = sizeof(SM);
   static bool configured[64] = {};
   static int regs_ok[64] = {};
@@ -1292,15 +1344,17 @@ int* device_error_word() {
   return cached[dev];
 }
 
-cudaError_t launch_gemm_tc(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums, int64_t N,
-                           const uint8_t* a_codes, const float* a_scales, int64_t M, int64_t K, float* y, int64_t ldy,
-                           int32_t* P, void* ws, size_t ws_bytes, cudaStream_t stream) {
+cudaError_t launch_gemm_tc(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums,
+                           const uint8_t* w_expanded, int64_t N, const uint8_t* a_codes, const float* a_scales,
+                           int64_t M, int64_t K, float* y, int64_t ldy, int32_t* P, void* ws, size_t ws_bytes,
+                           cudaStream_t stream) {
   TcArgs a{};
   a.w_scales = w_scales; a.w_sums = w_sums; a.a_scales = a_scales;
   a.M = M; a.N = N; a.K = K; a.y = y; a.ldy = ldy; a.P = P;
   a.tt = token_tile(M, P ? 256 : kDenseTT);
+  const bool wexp = w_expanded != nullptr && !P;
   CUtensorMap wmap, amap;
-  cudaError_t e = codes_map(&wmap, w_codes, N, K, TW);
+  cudaError_t e = wexp ? expanded_map(&wmap, w_expanded, N, K, TW) : codes_map(&wmap, w_codes, N, K, TW);
   if (e == cudaSuccess) e = codes_map(&amap, a_codes, M, K, a.tt);
   if (e != cudaSuccess) return e;
   int64_t grid = ((N + TW - 1) / TW) * ((M + a.tt - 1) / a.tt);
@@ -1312,6 +1366,7 @@ cudaError_t launch_gemm_tc(const uint8_t* w_codes, const uint16_t* w_scales, con
     a.sk_part = reinterpret_cast<float4*>(static_cast<uint8_t*>(ws) + pl.count_bytes);
     grid = pl.grid;
   }
+  if (wexp) return launch_tc<false, kDenseTT, 4, true>(wmap, amap, a, grid, stream);
   return launch_tc<false, kDenseTT>(wmap, amap, a, grid, stream);
 }
 
@@ -1367,19 +1422,24 @@ cudaError_t launch_gemm_w4a16(const uint8_t* w_codes, const uint16_t* w_scales, 
   return launch_tc<false, kW4A8TT, 16>(wmap, amap, a, grid, stream);
 }
 
-cudaError_t launch_gemm_tc_routed(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums, int E,
-                                  int64_t N, const uint8_t* g_codes, const float* g_scales, int64_t K, int64_t npairs,
-                                  int tile_tokens, float* y, const Routing& r, cudaStream_t stream) {
+cudaError_t launch_gemm_tc_routed(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums,
+                                  const uint8_t* w_expanded, int E, int64_t N, const uint8_t* g_codes,
+                                  const float* g_scales, int64_t K, int64_t npairs, int tile_tokens, float* y,
+                                  const Routing& r, cudaStream_t stream) {
   TcArgs a{};
   a.w_scales = w_scales; a.w_sums = w_sums; a.a_scales = g_scales;
   a.M = npairs; a.N = N; a.K = K; a.y = y; a.ldy = N;
   a.tt = tile_tokens;
   a.perm = r.perm; a.offsets = r.offsets; a.tile_off = r.tile_off; a.E = E;
+  // the expanded weights' 8-row groups must not straddle experts
+  const bool wexp = w_expanded != nullptr && N % 8 == 0;
   CUtensorMap wmap, amap;
-  cudaError_t e = codes_map(&wmap, w_codes, static_cast<int64_t>(E) * N, K, TW);
+  cudaError_t e = wexp ? expanded_map(&wmap, w_expanded, static_cast<int64_t>(E) * N, K, TW)
+                       : codes_map(&wmap, w_codes, static_cast<int64_t>(E) * N, K, TW);
   if (e == cudaSuccess) e = codes_map(&amap, g_codes, npairs, K, a.tt);
   if (e != cudaSuccess) return e;
   const int64_t max_tiles = (npairs / tile_tokens + E) * ((N + TW - 1) / TW);
+  if (wexp) return launch_tc<false, kRoutedTileMax, 4, true>(wmap, amap, a, max_tiles, stream);
   return launch_tc<false, kRoutedTileMax>(wmap, amap, a, max_tiles, stream);
 }
 

@@ -98,18 +98,27 @@ __device__ __forceinline__ int q4_code(float x, float inv) {
   return static_cast<int>(fminf(fmaxf(__fadd_rn(r, 8.0f), 0.0f), 15.0f));
 }
 
+// The expanded operand byte of a code: q - 8 as an fp8 e4m3 subnormal
+// ((q - 8) * 2^-9), sign and magnitude: q - 8 >= 0 -> q - 8, else 0x80 | (8 - q).
+__device__ __forceinline__ uint32_t e4m3_of_code(int q) {
+  return static_cast<uint32_t>(q >= 8 ? q - 8 : 0x80 | (8 - q));
+}
+
 // Codes of the block for the reciprocal scale inv; stores the 16 code bytes, the
-// fp16 scale bits and the code sum sum_j (q_j - 8).
+// fp16 scale bits, the code sum sum_j (q_j - 8) and, when `expanded` is given,
+// the 32 operand bytes of the block in element order.
 __device__ __forceinline__ void store_block(const float (&v)[4], float inv, uint16_t dbits, int t, bool ok, int64_t n,
                                             int64_t b, int64_t K, uint8_t* __restrict__ codes,
-                                            uint16_t* __restrict__ scales, int16_t* __restrict__ sums) {
+                                            uint16_t* __restrict__ scales, int16_t* __restrict__ sums,
+                                            uint8_t* __restrict__ expanded) {
   const int64_t B = K / 32;
-  uint32_t lo = 0;
+  uint32_t lo = 0, ex = 0;
   int qsum = 0;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int q = q4_code(v[j], inv);
     lo |= static_cast<uint32_t>(q) << (8 * j);
+    ex |= e4m3_of_code(q) << (8 * j);
     qsum += q - 8;
   }
   qsum += __shfl_xor_sync(0xFFFFFFFFu, qsum, 1);
@@ -117,6 +126,7 @@ __device__ __forceinline__ void store_block(const float (&v)[4], float inv, uint
   qsum += __shfl_xor_sync(0xFFFFFFFFu, qsum, 4);
   const uint32_t hi = __shfl_down_sync(0xFFFFFFFFu, lo << 4, 4);
   if (ok) {
+    if (expanded) reinterpret_cast<uint32_t*>(expanded + n * K + b * 32)[t] = ex;  // elements 4t..4t+3
     if (t < 4) reinterpret_cast<uint32_t*>(codes + n * (K / 2) + b * 16)[t] = lo | hi;
     if (t == 0) {
       scales[n * B + b] = dbits;
@@ -129,7 +139,8 @@ __global__ void __launch_bounds__(256) pack_q4_0_kernel(const void* __restrict__
                                                          int64_t K, int64_t ldw, int rotate,
                                                          uint8_t* __restrict__ codes,
                                                          uint16_t* __restrict__ scales,
-                                                         int16_t* __restrict__ sums) {
+                                                         int16_t* __restrict__ sums,
+                                                         uint8_t* __restrict__ expanded) {
   const int lane = threadIdx.x & 31;
   const int sub = lane >> 3;
   const int t = lane & 7;
@@ -148,7 +159,7 @@ __global__ void __launch_bounds__(256) pack_q4_0_kernel(const void* __restrict__
     // d = m / -8 with m the signed max; the codes use the fp32 d, the stored scale is fp16(d)
     const float d = __fdiv_rn(block_signed_max(v, t), -8.0f);
     const float inv = (d != 0.0f) ? __frcp_rn(d) : 0.0f;
-    store_block(v, inv, __half_as_ushort(__float2half_rn(d)), t, ok, n, b, K, codes, scales, sums);
+    store_block(v, inv, __half_as_ushort(__float2half_rn(d)), t, ok, n, b, K, codes, scales, sums, expanded);
   }
 }
 
@@ -210,7 +221,8 @@ __global__ void __launch_bounds__(256) pack_q4_0_weighted_kernel(const void* __r
                                                                   const float* __restrict__ imp,
                                                                   uint8_t* __restrict__ codes,
                                                                   uint16_t* __restrict__ scales,
-                                                                  int16_t* __restrict__ sums) {
+                                                                  int16_t* __restrict__ sums,
+                                                                  uint8_t* __restrict__ expanded) {
   __shared__ __align__(16) float s_y[8][4][32];
   __shared__ __align__(16) float s_w[8][4][32];
   const int lane = threadIdx.x & 31;
@@ -333,7 +345,7 @@ __global__ void __launch_bounds__(256) pack_q4_0_weighted_kernel(const void* __r
       }
     }
     const float dsel = __half2float(__ushort_as_half(best));
-    store_block(v, dsel != 0.0f ? __frcp_rn(dsel) : 0.0f, best, t, ok, n, b, K, codes, scales, sums);
+    store_block(v, dsel != 0.0f ? __frcp_rn(dsel) : 0.0f, best, t, ok, n, b, K, codes, scales, sums, expanded);
   }
 }
 
@@ -342,7 +354,8 @@ __global__ void __launch_bounds__(256) pack_q4_0_weighted_kernel(const void* __r
 __global__ void __launch_bounds__(256) import_q4_0_kernel(const uint8_t* __restrict__ blocks, int64_t nblk,
                                                            uint8_t* __restrict__ codes,
                                                            uint16_t* __restrict__ scales,
-                                                           int16_t* __restrict__ sums) {
+                                                           int16_t* __restrict__ sums,
+                                                           uint8_t* __restrict__ expanded) {
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= nblk) return;
   const uint16_t* src = reinterpret_cast<const uint16_t*>(blocks + i * 18);  // 2-byte aligned
@@ -358,41 +371,75 @@ __global__ void __launch_bounds__(256) import_q4_0_kernel(const uint8_t* __restr
     total += static_cast<int>((nib & 0xFF) + ((nib >> 8) & 0xFF) + ((nib >> 16) & 0xFF) + (nib >> 24));
   }
   sums[i] = static_cast<int16_t>(total - 256);
+  if (expanded) {  // blocks are row-major, so block i's 32 operand bytes sit at 32 i
+    uint32_t e[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {  // word j: elements 4j..4j+3 (low nibbles), 16+4j.. (high)
+      uint32_t lo = 0, hi = 0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int byte = static_cast<int>((q[j] >> (8 * k)) & 0xFFu);
+        lo |= e4m3_of_code(byte & 15) << (8 * k);
+        hi |= e4m3_of_code(byte >> 4) << (8 * k);
+      }
+      e[j] = lo;
+      e[4 + j] = hi;
+    }
+    uint4* dst = reinterpret_cast<uint4*>(expanded + i * 32);
+    dst[0] = make_uint4(e[0], e[1], e[2], e[3]);
+    dst[1] = make_uint4(e[4], e[5], e[6], e[7]);
+  }
 }
 
 }  // namespace
 
+// Rows rows .. round_up(rows, 8) - 1 of the expanded operand are zero (the GEMM
+// loads 8-row groups).
+cudaError_t zero_expanded_pad(uint8_t* expanded, int64_t rows, int64_t K, cudaStream_t stream) {
+  if (!expanded) return cudaSuccess;
+  const int64_t pad = ((rows + 7) / 8) * 8 - rows;
+  if (pad == 0) return cudaSuccess;
+  return cudaMemsetAsync(expanded + rows * K, 0, static_cast<size_t>(pad * K), stream);
+}
+
 cudaError_t launch_pack_q4_0(const void* w, int w_dtype, int64_t N, int64_t K, int64_t ldw, int rotate,
-                             uint8_t* codes, uint16_t* scales, int16_t* sums, cudaStream_t stream) {
+                             uint8_t* codes, uint16_t* scales, int16_t* sums, uint8_t* expanded,
+                             cudaStream_t stream) {
   const int64_t ngroups = (N * (K / 32) + 3) / 4;
   int64_t ctas = (ngroups + 7) / 8;
   const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
   if (ctas > cap) ctas = cap;
   if (ctas < 1) ctas = 1;
+  cudaError_t e = zero_expanded_pad(expanded, N, K, stream);
+  if (e != cudaSuccess) return e;
   pack_q4_0_kernel<<<static_cast<unsigned>(ctas), 256, 0, stream>>>(w, w_dtype, N, K, ldw, rotate, codes, scales,
-                                                                     sums);
+                                                                     sums, expanded);
   return cudaGetLastError();
 }
 
 cudaError_t launch_pack_q4_0_weighted(const void* w, int w_dtype, int64_t N, int64_t K, int64_t ldw, int rotate,
                                       const float* imp, uint8_t* codes, uint16_t* scales, int16_t* sums,
-                                      cudaStream_t stream) {
+                                      uint8_t* expanded, cudaStream_t stream) {
   const int64_t ngroups = (N * (K / 32) + 3) / 4;
   int64_t ctas = (ngroups + 7) / 8;
   const int64_t cap = static_cast<int64_t>(num_sms()) * 16;
   if (ctas > cap) ctas = cap;
   if (ctas < 1) ctas = 1;
+  cudaError_t e = zero_expanded_pad(expanded, N, K, stream);
+  if (e != cudaSuccess) return e;
   pack_q4_0_weighted_kernel<<<static_cast<unsigned>(ctas), 256, 0, stream>>>(w, w_dtype, N, K, ldw, rotate, imp, codes,
-                                                                              scales, sums);
+                                                                              scales, sums, expanded);
   return cudaGetLastError();
 }
 
 cudaError_t launch_import_q4_0(const void* blocks, int64_t N, int64_t K, uint8_t* codes, uint16_t* scales,
-                               int16_t* sums, cudaStream_t stream) {
+                               int16_t* sums, uint8_t* expanded, cudaStream_t stream) {
   const int64_t nblk = N * (K / 32);
   const int64_t ctas = (nblk + 255) / 256;
+  cudaError_t e = zero_expanded_pad(expanded, N, K, stream);
+  if (e != cudaSuccess) return e;
   import_q4_0_kernel<<<static_cast<unsigned>(ctas), 256, 0, stream>>>(static_cast<const uint8_t*>(blocks), nblk,
-                                                                       codes, scales, sums);
+                                                                       codes, scales, sums, expanded);
   return cudaGetLastError();
 }
 

@@ -39,22 +39,27 @@ cudaError_t launch_act_rotate_quantize(const float* x, int64_t M, int64_t K, int
 // The exact path's 8-bit activations: int8 codes [M][K] (element order), fp32 scales.
 cudaError_t launch_act_rotate_quantize8(const float* x, int64_t M, int64_t K, int64_t ldx, int rotate,
                                         int8_t* codes, float* scales, cudaStream_t stream);
+// The packers and the import also write the expanded weight operand (the e4m3
+// bytes of q - 8 in element order, [round_up(N, 8)][K], pad rows zero) when
+// `expanded` is not null.
 cudaError_t launch_pack_q4_0(const void* w, int w_dtype, int64_t N, int64_t K, int64_t ldw, int rotate,
-                             uint8_t* codes, uint16_t* scales, int16_t* sums, cudaStream_t stream);
+                             uint8_t* codes, uint16_t* scales, int16_t* sums, uint8_t* expanded,
+                             cudaStream_t stream);
 // Importance-weighted Q4_0 (the converter's imatrix quantisation): imp is a
 // device fp32 vector of K per-input-channel importances (unrotated), or null.
 cudaError_t launch_pack_q4_0_weighted(const void* w, int w_dtype, int64_t N, int64_t K, int64_t ldw, int rotate,
                                       const float* imp, uint8_t* codes, uint16_t* scales, int16_t* sums,
-                                      cudaStream_t stream);
+                                      uint8_t* expanded, cudaStream_t stream);
 cudaError_t launch_import_q4_0(const void* blocks, int64_t N, int64_t K, uint8_t* codes, uint16_t* scales,
-                               int16_t* sums, cudaStream_t stream);
+                               int16_t* sums, uint8_t* expanded, cudaStream_t stream);
 // Dense product (P == nullptr) or exact partials (P != nullptr).  With a
 // workspace of at least gemm_workspace_bytes(M, N, K) bytes (16-byte aligned,
 // zero before its first use) the dense product may run a stream-K schedule.
-cudaError_t launch_gemm_tc(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums, int64_t N,
-                           const uint8_t* a_codes,
-                           const float* a_scales, int64_t M, int64_t K, float* y, int64_t ldy, int32_t* P,
-                           void* ws, size_t ws_bytes, cudaStream_t stream);
+// w_expanded (optional, the dense product only): the pre-expanded weight operand.
+cudaError_t launch_gemm_tc(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums,
+                           const uint8_t* w_expanded, int64_t N, const uint8_t* a_codes, const float* a_scales,
+                           int64_t M, int64_t K, float* y, int64_t ldy, int32_t* P, void* ws, size_t ws_bytes,
+                           cudaStream_t stream);
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
 // The exact path (rotated Q4_0 weights x int8 activations, f16 tensor-core
 // MMAs): dense product (P == nullptr) or exact partials; workspace as above.
@@ -74,10 +79,10 @@ cudaError_t launch_gemm_w4a16(const uint8_t* w_codes, const uint16_t* w_scales, 
 // tensor-core kernel's whole-tile schedule.
 cudaError_t launch_gemm_small_m(const uint8_t* w_codes, const uint16_t* w_scales, int64_t N, const uint8_t* a_codes,
                                 const float* a_scales, int M, int64_t K, float* y, int64_t ldy, cudaStream_t stream);
-cudaError_t launch_gemm_tc_routed(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums, int E,
-                                  int64_t N,
-                                  const uint8_t* g_codes, const float* g_scales, int64_t K, int64_t npairs,
-                                  int tile_tokens, float* y, const Routing& r, cudaStream_t stream);
+cudaError_t launch_gemm_tc_routed(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums,
+                                  const uint8_t* w_expanded, int E, int64_t N, const uint8_t* g_codes,
+                                  const float* g_scales, int64_t K, int64_t npairs, int tile_tokens, float* y,
+                                  const Routing& r, cudaStream_t stream);
 // Token rows per routed tile for a MUL_MAT_ID problem (multiple of 32, <= 256).
 // Largest token tile of the routed product (the GEMM instance it launches).
 constexpr int kRoutedTileMax = 128;
@@ -90,8 +95,9 @@ int* device_error_word();
 // 2D tiled TMA descriptor over `rows` rows of `inner` elements.
 cudaError_t encode_2d_map(CUtensorMap* m, CUtensorMapDataType dtype, const void* base, uint64_t inner, uint64_t rows,
                           uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swizzle);
-cudaError_t launch_gemm_id(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums, int E, int64_t N,
-                           const uint8_t* a_codes, const float* a_scales, int64_t K, const int32_t* ids, int64_t M,
-                           int top_k, int act_per_slot, float* y, const Routing& r, cudaStream_t stream);
+cudaError_t launch_gemm_id(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums,
+                           const uint8_t* w_expanded, int E, int64_t N, const uint8_t* a_codes, const float* a_scales,
+                           int64_t K, const int32_t* ids, int64_t M, int top_k, int act_per_slot, float* y,
+                           const Routing& r, cudaStream_t stream);
 
 }  // namespace w4a4

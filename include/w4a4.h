@@ -87,6 +87,13 @@ typedef enum {
  *   sums  : device, [rows][K/32] int16, the block's code sum sum_j (q_j - 8).
  *           Derived data (no extra information): written by h32_q4_0_pack_weights
  *           and q4_0_import from the codes, read by the GEMMs.
+ *   expanded: device, [round_up(rows, 8)][K] bytes, or NULL.  Optional derived
+ *           data: byte k of row r is q_k - 8 as an fp8 e4m3 value times 2^9
+ *           (sign and magnitude: q - 8 >= 0 -> q - 8, else 0x80 | (8 - q)), in
+ *           element order; the pad rows are zero.  When the packers or the
+ *           import get it they fill it; w4a4_gemm then loads the weights straight
+ *           into the tensor-core operand layout instead of converting the codes
+ *           in every tile.  Twice the codes' memory (w4a4_q4_0_expanded_bytes).
  */
 typedef struct {
   uint8_t* codes;
@@ -95,6 +102,7 @@ typedef struct {
   int64_t rows;
   int64_t K;
   uint32_t tag; /* W4A4_TAG_Q4_0 | (W4A4_TAG_ROTATED if rotated) */
+  uint8_t* expanded;
 } w4a4_q4_0;
 
 /*
@@ -144,6 +152,7 @@ typedef struct {
 size_t w4a4_q4_0_codes_bytes(int64_t rows, int64_t K);
 size_t w4a4_q4_0_scales_bytes(int64_t rows, int64_t K);
 size_t w4a4_q4_0_sums_bytes(int64_t rows, int64_t K);
+size_t w4a4_q4_0_expanded_bytes(int64_t rows, int64_t K);
 size_t w4a4_act4_codes_bytes(int64_t rows, int64_t K);
 size_t w4a4_act4_scales_bytes(int64_t rows, int64_t K);
 size_t w4a4_act8_codes_bytes(int64_t rows, int64_t K);
