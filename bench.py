@@ -222,8 +222,9 @@ def profiled_traffic(summary: str, sources: tuple[str, ...]) -> tuple[float | No
         return None, f"profiles/{summary} has no traffic line"
 
 
-GEMM_SOURCES = ("gemm_tc.cu", "w4a4_device.cuh", "w4a4_kernels.cuh")
-ACT_SOURCES = ("act_quant.cu", "w4a4_device.cuh", "w4a4_kernels.cuh")
+# the files that define each kernel's device code (the internal host header is left out)
+GEMM_SOURCES = ("gemm_tc.cu", "w4a4_device.cuh")
+ACT_SOURCES = ("act_quant.cu", "w4a4_device.cuh")
 
 
 def graph_time(fn, n: int = 20, reps: int = 5) -> float:
@@ -570,7 +571,9 @@ def run_ours(args, shape) -> dict | None:
     act_traffic, act_traffic_src = profiled_traffic(f"act_rotate_quantize_{shape.name}.md", ACT_SOURCES)
     gemm_roof = {"bound": "alu", "achieved": fold_flops / (gemm_avg * 1e-3) / 1e12, "peak": fp32_peak,
                  "unit": "TFLOP/s", "frac": None, "traffic": gemm_traffic, "traffic_source": gemm_traffic_src,
-                 "algorithmic_bytes": float(N * K // 2 + N * B * 4 + M * K // 2 + M * B * 4 + M * N * 4),
+                 # weights read as the expanded operand (1 byte per weight) when present, else as codes
+                 "algorithmic_bytes": float((N * K if wq0.expanded is not None else N * K // 2) + N * B * 4
+                                            + M * K // 2 + M * B * 4 + M * N * 4),
                  "kernel": "w4a4_gemm_tc_kernel",
                  "peak_source": f"derived: {sm_count} SMs x 128 fp32 lanes x 2 flops x {peaks.get('sm_max_mhz', 2070.0)} MHz"}
     gemm_roof["frac"] = gemm_roof["achieved"] / gemm_roof["peak"]
