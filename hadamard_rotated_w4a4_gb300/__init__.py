@@ -52,7 +52,7 @@ TAG_ROTATED = 0x1
 EXPORTS = [
     "w4a4_q4_0_codes_bytes", "w4a4_q4_0_scales_bytes", "w4a4_q4_0_sums_bytes", "w4a4_q4_0_expanded_bytes",
     "w4a4_act4_codes_bytes",
-    "w4a4_act4_scales_bytes", "h32_q4_0_pack_weights", "q4_0_import", "w4a4_rotate_quantize_act", "w4a4_gemm", "w4a4_gemm_workspace_bytes",
+    "w4a4_act4_scales_bytes", "w4a4_act4_expanded_bytes", "h32_q4_0_pack_weights", "q4_0_import", "w4a4_rotate_quantize_act", "w4a4_gemm", "w4a4_gemm_workspace_bytes",
     "w4a4_gemm_partials", "w4a4_gemm_id", "w4a4_gemm_id_workspace_bytes", "w4a4_gemm_id_status", "w4a4_gemm_id_static", "w4a4_check", "w4a4_last_error",
     "w4a4_status_name", "w4a4_abi_version", "w4a4_act8_codes_bytes", "w4a4_act8_scales_bytes", "w4a4_gemm_small_m",
     "w4a8_rotate_quantize_act", "w4a8_gemm", "w4a8_gemm_partials", "w4a8_gemm_workspace_bytes",
@@ -76,7 +76,7 @@ class _Q4_0Desc(ctypes.Structure):
 
 class _Act4Desc(ctypes.Structure):
     _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("rows", ctypes.c_int64),
-                ("K", ctypes.c_int64), ("tag", ctypes.c_uint32)]
+                ("K", ctypes.c_int64), ("tag", ctypes.c_uint32), ("expanded", ctypes.c_void_p)]
 
 
 class _Act16Desc(ctypes.Structure):
@@ -105,7 +105,8 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
     i64, vp, i32, u = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
     for name in ("w4a4_q4_0_codes_bytes", "w4a4_q4_0_scales_bytes", "w4a4_q4_0_sums_bytes", "w4a4_q4_0_expanded_bytes",
                  "w4a4_act4_codes_bytes",
-                 "w4a4_act4_scales_bytes", "w4a4_act8_codes_bytes", "w4a4_act8_scales_bytes"):
+                 "w4a4_act4_scales_bytes", "w4a4_act4_expanded_bytes", "w4a4_act8_codes_bytes",
+                 "w4a4_act8_scales_bytes"):
         f = getattr(lib, name)
         f.argtypes, f.restype = [i64, i64], u
     lib.h32_q4_0_pack_weights.argtypes = [vp, i32, i64, i64, i64, i32, ctypes.POINTER(_Q4_0Desc), vp]
@@ -202,12 +203,15 @@ class Q4_0Weights:
 
 @dataclass
 class Act4:
-    """int4 activations: codes uint8 [rows][K/2] (two's complement nibbles), scales fp32 [rows][K/32]."""
+    """int4 activations: codes uint8 [rows][K/2] (two's complement nibbles), scales fp32 [rows][K/32]
+    and, optionally, the expanded operand (the offset codes a + 8 as bytes, [round_up(rows, 8)][K])
+    that lets the dense GEMM, with expanded weights, skip converting the activations."""
     codes: torch.Tensor
     scales_buf: torch.Tensor
     rows: int
     K: int
     rotated: bool
+    expanded: torch.Tensor | None = None  # uint8 buffer of w4a4_act4_expanded_bytes, or None
 
     @property
     def scales(self) -> torch.Tensor:
@@ -220,10 +224,15 @@ class Act4:
 
     def head(self, rows: int) -> "Act4":
         """The first `rows` rows (views of the same buffers)."""
-        return Act4(self.codes[:rows], self.scales_buf, rows, self.K, self.rotated)
+        return Act4(self.codes[:rows], self.scales_buf, rows, self.K, self.rotated, self.expanded)
+
+    def without_expanded(self) -> "Act4":
+        """The same activations without the expanded operand (the GEMM then converts the codes)."""
+        return Act4(self.codes, self.scales_buf, self.rows, self.K, self.rotated)
 
     def desc(self) -> _Act4Desc:
-        return _Act4Desc(self.codes.data_ptr(), self.scales_buf.data_ptr(), self.rows, self.K, self.tag)
+        return _Act4Desc(self.codes.data_ptr(), self.scales_buf.data_ptr(), self.rows, self.K, self.tag,
+                         self.expanded.data_ptr() if self.expanded is not None else None)
 
 
 def alloc_q4_0(rows: int, K: int, device, rotated: bool = True, expanded: bool = True) -> Q4_0Weights:
@@ -239,14 +248,19 @@ def alloc_q4_0(rows: int, K: int, device, rotated: bool = True, expanded: bool =
     return Q4_0Weights(codes, sbuf, ubuf, rows, K, rotated, ebuf)
 
 
-def alloc_act4(rows: int, K: int, device, rotated: bool = True) -> Act4:
+def alloc_act4(rows: int, K: int, device, rotated: bool = True, expanded: bool = True) -> Act4:
     lib = load_library()
     if K <= 0 or K % 32:
         raise W4A4Error(1, f"K={K} must be a positive multiple of 32")
     nc, ns = lib.w4a4_act4_codes_bytes(rows, K), lib.w4a4_act4_scales_bytes(rows, K)
     codes = torch.empty(max(nc, 16), dtype=torch.uint8, device=device)[:nc].view(rows, K // 2)
     sbuf = torch.empty(max(ns, 16), dtype=torch.uint8, device=device)
-    return Act4(codes, sbuf, rows, K, rotated)
+    ebuf = None
+    if expanded:
+        ne = lib.w4a4_act4_expanded_bytes(rows, K)
+        ebuf = torch.empty(max(ne, 16), dtype=torch.uint8, device=device)
+        ebuf[rows * K:].zero_()  # the pad rows are read into unused MMA columns only; keep them defined
+    return Act4(codes, sbuf, rows, K, rotated, ebuf)
 
 
 def h32_q4_0_pack_weights(w: torch.Tensor, rotate: bool = True, out: Q4_0Weights | None = None,

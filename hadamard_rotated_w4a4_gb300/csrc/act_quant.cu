@@ -51,7 +51,9 @@ __device__ __forceinline__ uint32_t nib(float y, float inv) {
 
 // One 32-element block held by this lane: rotate (optional), then
 //   BITS = 4: d_a = amax / 7, int4 codes (round half away, clamp -8..7), 16
-//             bytes in the Q4_0 nibble order;
+//             bytes in the Q4_0 nibble order; with `expanded`, also the 32
+//             offset codes a + 8 as bytes in element order (the e4m3 operand
+//             bytes of the dense GEMM);
 //   BITS = 8: d_a = amax / 127, int8 codes (round half away, clamp -127..127),
 //             32 bytes in element order (the exact path's activations);
 //   BITS = 16: no quantisation (the rotate-only route): the 32 rotated values
@@ -67,7 +69,8 @@ __device__ __forceinline__ void rotate_block(float (&y)[32]) {
 
 template <int BITS>
 __device__ __forceinline__ void quantize_block(float (&y)[32], int rotate, bool ok, uint8_t* __restrict__ codes,
-                                               float* __restrict__ scales, int64_t i) {
+                                               float* __restrict__ scales, uint8_t* __restrict__ expanded,
+                                               int64_t i) {
   if (rotate) rotate_block(y);
   if constexpr (BITS == 16) {
     uint32_t w[16];
@@ -127,6 +130,16 @@ __device__ __forceinline__ void quantize_block(float (&y)[32], int rotate, bool 
   if (ok) {
     reinterpret_cast<uint4*>(codes)[i] = make_uint4(w[0], w[1], w[2], w[3]);
     scales[i] = d;
+    if (expanded) {
+      // a + 8 = nibble ^ 8; low nibbles are elements 0..15, high nibbles 16..31
+      uint32_t u[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) u[t] = w[t] ^ 0x88888888u;
+      uint4* dst = reinterpret_cast<uint4*>(expanded) + 2 * i;
+      dst[0] = make_uint4(u[0] & 0x0F0F0F0Fu, u[1] & 0x0F0F0F0Fu, u[2] & 0x0F0F0F0Fu, u[3] & 0x0F0F0F0Fu);
+      dst[1] = make_uint4((u[0] >> 4) & 0x0F0F0F0Fu, (u[1] >> 4) & 0x0F0F0F0Fu, (u[2] >> 4) & 0x0F0F0F0Fu,
+                          (u[3] >> 4) & 0x0F0F0F0Fu);
+    }
   }
 }
 
@@ -134,7 +147,8 @@ template <int BITS>
 __global__ void __launch_bounds__(32 * kWarps) act_rotate_quantize_kernel(const float* __restrict__ x, int64_t M,
                                                                           int64_t K, int64_t ldx, int rotate,
                                                                           uint8_t* __restrict__ codes,
-                                                                          float* __restrict__ scales) {
+                                                                          float* __restrict__ scales,
+                                                                          uint8_t* __restrict__ expanded) {
   __shared__ __align__(16) float tile[kWarps][32 * kRow];
   const int lane = threadIdx.x & 31;
   const int wib = threadIdx.x >> 5;
@@ -174,7 +188,7 @@ __global__ void __launch_bounds__(32 * kWarps) act_rotate_quantize_kernel(const 
       y[4 * k + 3] = v.w;
     }
     __syncwarp();
-    quantize_block<BITS>(y, rotate, ok, codes, scales, i);
+    quantize_block<BITS>(y, rotate, ok, codes, scales, expanded, i);
   }
 }
 
@@ -240,7 +254,7 @@ __device__ __forceinline__ void tma_load_chunk(float* dst, const CUtensorMap* ma
 template <int BITS>
 __global__ void __launch_bounds__(32 * kTmaWarps) act_rotate_quantize_tma_kernel(
     const __grid_constant__ CUtensorMap xmap, int64_t nblk, int rotate, uint8_t* __restrict__ codes,
-    float* __restrict__ scales, int* err) {
+    float* __restrict__ scales, uint8_t* __restrict__ expanded, int* err) {
   extern __shared__ __align__(1024) uint8_t act_smem[];
   ActSmem& S = *reinterpret_cast<ActSmem*>(act_smem);
   const int lane = threadIdx.x & 31;
@@ -295,7 +309,7 @@ __global__ void __launch_bounds__(32 * kTmaWarps) act_rotate_quantize_tma_kernel
       ++issued;
     }
     const int64_t i = (gw + it * nw) * 32 + lane;
-    quantize_block<BITS>(y, 0, i < nblk, codes, scales, i);
+    quantize_block<BITS>(y, 0, i < nblk, codes, scales, expanded, i);
   }
   if (__any_sync(0xFFFFFFFFu, failed)) {
     // a load never completed: record it and wait (bounded) for the copies still
@@ -314,7 +328,7 @@ __global__ void __launch_bounds__(32 * kTmaWarps) act_rotate_quantize_tma_kernel
 namespace {
 template <int BITS>
 cudaError_t launch_act(const float* x, int64_t M, int64_t K, int64_t ldx, int rotate, uint8_t* codes, float* scales,
-                       cudaStream_t stream) {
+                       uint8_t* expanded, cudaStream_t stream) {
   const int64_t nblk = M * (K / 32);
   const int64_t nchunks = (nblk + 31) / 32;
   if (ldx == K && nblk < (int64_t(1) << 31) - 64) {
@@ -336,7 +350,7 @@ cudaError_t launch_act(const float* x, int64_t M, int64_t K, int64_t ldx, int ro
       if (ctas > cap) ctas = cap;
       if (ctas < 1) ctas = 1;
       act_rotate_quantize_tma_kernel<BITS><<<static_cast<unsigned>(ctas), 32 * kTmaWarps, sizeof(ActSmem), stream>>>(
-          xmap, nblk, rotate, codes, scales, device_error_word());
+          xmap, nblk, rotate, codes, scales, expanded, device_error_word());
       return cudaGetLastError();
     }
   }
@@ -345,24 +359,24 @@ cudaError_t launch_act(const float* x, int64_t M, int64_t K, int64_t ldx, int ro
   if (ctas > cap) ctas = cap;
   if (ctas < 1) ctas = 1;
   act_rotate_quantize_kernel<BITS><<<static_cast<unsigned>(ctas), 32 * kWarps, 0, stream>>>(x, M, K, ldx, rotate, codes,
-                                                                                       scales);
+                                                                                       scales, expanded);
   return cudaGetLastError();
 }
 }  // namespace
 
 cudaError_t launch_act_rotate_quantize(const float* x, int64_t M, int64_t K, int64_t ldx, int rotate,
-                                       uint8_t* codes, float* scales, cudaStream_t stream) {
-  return launch_act<4>(x, M, K, ldx, rotate, codes, scales, stream);
+                                       uint8_t* codes, float* scales, uint8_t* expanded, cudaStream_t stream) {
+  return launch_act<4>(x, M, K, ldx, rotate, codes, scales, expanded, stream);
 }
 
 cudaError_t launch_act_rotate_quantize8(const float* x, int64_t M, int64_t K, int64_t ldx, int rotate,
                                         int8_t* codes, float* scales, cudaStream_t stream) {
-  return launch_act<8>(x, M, K, ldx, rotate, reinterpret_cast<uint8_t*>(codes), scales, stream);
+  return launch_act<8>(x, M, K, ldx, rotate, reinterpret_cast<uint8_t*>(codes), scales, nullptr, stream);
 }
 
 cudaError_t launch_act_rotate_bf16(const float* x, int64_t M, int64_t K, int64_t ldx, int rotate, uint16_t* out,
                                    cudaStream_t stream) {
-  return launch_act<16>(x, M, K, ldx, rotate, reinterpret_cast<uint8_t*>(out), nullptr, stream);
+  return launch_act<16>(x, M, K, ldx, rotate, reinterpret_cast<uint8_t*>(out), nullptr, nullptr, stream);
 }
 
 }  // namespace w4a4

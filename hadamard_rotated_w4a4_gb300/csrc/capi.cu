@@ -78,8 +78,8 @@ w4a4_status check_act4(const w4a4_act4* a, const char* fn) {
   if (s != W4A4_OK) return s;
   if (a->rows > 0 && (!a->codes || !a->scales))
     return fail(W4A4_ERR_INVALID_ARG, "%s: activation pointers are NULL", fn);
-  if (!aligned16(a->codes) || !aligned16(a->scales))
-    return fail(W4A4_ERR_ALIGNMENT, "%s: activation codes/scales must be 16-byte aligned", fn);
+  if (!aligned16(a->codes) || !aligned16(a->scales) || !aligned16(a->expanded))
+    return fail(W4A4_ERR_ALIGNMENT, "%s: activation codes/scales/expanded must be 16-byte aligned", fn);
   return W4A4_OK;
 }
 
@@ -137,6 +137,7 @@ size_t w4a4_q4_0_expanded_bytes(int64_t rows, int64_t K) {
   return round16(static_cast<size_t>((rows + 7) / 8 * 8) * static_cast<size_t>(K));
 }
 size_t w4a4_act4_codes_bytes(int64_t rows, int64_t K) { return w4a4_q4_0_codes_bytes(rows, K); }
+size_t w4a4_act4_expanded_bytes(int64_t rows, int64_t K) { return w4a4_q4_0_expanded_bytes(rows, K); }
 size_t w4a4_act8_codes_bytes(int64_t rows, int64_t K) {
   if (!valid_k(K) || rows < 0) return 0;
   return round16(static_cast<size_t>(rows) * static_cast<size_t>(K));
@@ -233,13 +234,14 @@ w4a4_status w4a4_rotate_quantize_act(const float* x, int64_t M, int64_t K, int64
   if (rotate != 0 && rotate != 1) return fail(W4A4_ERR_INVALID_ARG, "%s: rotate must be 0 or 1", fn);
   if (ldx < K) return fail(W4A4_ERR_INVALID_ARG, "%s: ldx=%lld < K=%lld", fn, (long long)ldx, (long long)K);
   if (M > 0 && (!x || !out->codes || !out->scales)) return fail(W4A4_ERR_INVALID_ARG, "%s: NULL pointer", fn);
-  if (!aligned16(x) || !aligned16(out->codes) || !aligned16(out->scales) || (ldx % 4) != 0)
+  if (!aligned16(x) || !aligned16(out->codes) || !aligned16(out->scales) || !aligned16(out->expanded) ||
+      (ldx % 4) != 0)
     return fail(W4A4_ERR_ALIGNMENT, "%s: pointers and rows (ldx * 4 bytes) must be 16-byte aligned", fn);
   out->rows = M;
   out->K = K;
   out->tag = W4A4_TAG_ACT4 | (rotate ? W4A4_TAG_ROTATED : 0u);
   if (M == 0) return ok();
-  return cuda_status(w4a4::launch_act_rotate_quantize(x, M, K, ldx, rotate, out->codes, out->scales,
+  return cuda_status(w4a4::launch_act_rotate_quantize(x, M, K, ldx, rotate, out->codes, out->scales, out->expanded,
                                                       reinterpret_cast<cudaStream_t>(stream)), fn);
 }
 
@@ -266,8 +268,9 @@ w4a4_status w4a4_gemm(const w4a4_q4_0* w, const w4a4_act4* a, float* y, int64_t 
       return fail(W4A4_ERR_WORKSPACE, "%s: workspace %zu bytes < %zu needed", fn, ws_bytes, need);
     if (!aligned16(ws)) return fail(W4A4_ERR_ALIGNMENT, "%s: ws must be 16-byte aligned", fn);
   }
-  return cuda_status(w4a4::launch_gemm_tc(w->codes, w->scales, w->sums, w->expanded, N, a->codes, a->scales, M, a->K, y, ldy, nullptr,
-                                          ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream)), fn);
+  return cuda_status(w4a4::launch_gemm_tc(w->codes, w->scales, w->sums, w->expanded, N, a->codes, a->scales,
+                                          a->expanded, M, a->K, y, ldy, nullptr, ws, ws_bytes,
+                                          reinterpret_cast<cudaStream_t>(stream)), fn);
 }
 
 w4a4_status w4a4_gemm_small_m(const w4a4_q4_0* w, const w4a4_act4* a, float* y, int64_t ldy, w4a4_stream_t stream) {
@@ -295,8 +298,9 @@ w4a4_status w4a4_gemm_partials(const w4a4_q4_0* w, const w4a4_act4* a, int32_t* 
   if (a->rows == 0 || w->rows == 0) return ok();
   if (!P) return fail(W4A4_ERR_INVALID_ARG, "%s: P is NULL", fn);
   if (!aligned16(P)) return fail(W4A4_ERR_ALIGNMENT, "%s: P must be 16-byte aligned", fn);
-  return cuda_status(w4a4::launch_gemm_tc(w->codes, w->scales, w->sums, nullptr, w->rows, a->codes, a->scales, a->rows, a->K, nullptr,
-                                          0, P, nullptr, 0, reinterpret_cast<cudaStream_t>(stream)), fn);
+  return cuda_status(w4a4::launch_gemm_tc(w->codes, w->scales, w->sums, nullptr, w->rows, a->codes, a->scales, nullptr,
+                                          a->rows, a->K, nullptr, 0, P, nullptr, 0,
+                                          reinterpret_cast<cudaStream_t>(stream)), fn);
 }
 
 w4a4_status w4a8_rotate_quantize_act(const float* x, int64_t M, int64_t K, int64_t ldx, int rotate,
@@ -521,6 +525,6 @@ const char* w4a4_status_name(w4a4_status s) {
   return "W4A4_ERR_UNKNOWN";
 }
 
-int w4a4_abi_version(void) { return 100; }
+int w4a4_abi_version(void) { return 200; }
 
 }  // extern "C"

@@ -79,8 +79,9 @@ constexpr uint32_t kWaitHintNs = W4A4_WAIT_HINT_NS;
 // warps 4-11 fold.  The 256-column instance has two converter warps (2-3) and
 // 384 threads; the 128-column instance, whose workers need fewer registers,
 // adds warpgroup 3 as four more converter warps (512 threads) and a third fp8
-// stage.  Registers after setmaxnreg: 128 x 64 + 256 x 216 <= 168 x 384, and
-// 256 x 72 + 256 x 184 = 128 x 512.
+// stage.  Registers after setmaxnreg: 128 x 56 + 256 x 224 = 168 x 384 (the
+// workers' 224 leave the fold loop without spills), 128 x 72 + 256 x 208 <=
+// 168 x 384 with expanded activations, and 256 x 72 + 256 x 184 = 128 x 512.
 // AB: activation code width.  4 = the W4A4 product (int4 activations, e4m3
 // operands, one kind::f8f6f4 MMA per block); 8 = the exact path (int8
 // activations, f16 operands, two kind::f16 MMAs of K = 16 per block; int8 and
@@ -91,37 +92,49 @@ constexpr uint32_t kWaitHintNs = W4A4_WAIT_HINT_NS;
 // WEXP: the weights come pre-expanded (the e4m3 bytes of q - 8, loaded by a 4D
 // TMA straight into the K-major operand layout) and the MMA reads them from the
 // raw stage; the converters then handle only the activations.
-template <int TTM, int AB = 4, bool WEXP = false>
+// AEXP (with WEXP, W4A4 only): the activations come pre-expanded as well (the
+// offset codes a + 8 as e4m3 bytes, same 4D load); nothing is converted and the
+// converter warps only publish the per-stage scales.
+template <int TTM, int AB = 4, bool WEXP = false, bool AEXP = false>
 struct __align__(128) Smem {
+  static_assert(!AEXP || (WEXP && AB == 4), "expanded activations go with expanded weights, W4A4 only");
   static constexpr int TT = TTM;
   static constexpr int ABITS = AB;
   static constexpr bool WX = WEXP;
+  static constexpr bool AX = AEXP;
   static constexpr int WROW = KB * (WEXP ? 32 : 16);  // raw weight bytes per row and stage
-  static constexpr int ARAW_ROW = KB * 4 * AB;  // raw activation bytes per row and stage: 64 or 128
+  static constexpr int ARAW_ROW = AEXP ? KB * 32 : KB * 4 * AB;  // raw activation bytes per row and stage
   static constexpr int OPB = AB == 4 ? 1 : 2;   // operand bytes per element: e4m3 or f16
   static constexpr int WOP = TW * 32 * OPB + 32;   // operand buffer strides, padded by 32 bytes so that the
   static constexpr int AOP = TTM * 32 * OPB + 32;  // converters' stores to 4 buffers hit distinct banks
   static constexpr int NBUF = 512 / TTM;  // TMEM accumulator buffers
   static constexpr int CONV = TTM == 256 ? 2 : 6;                   // converter warps
   static constexpr int THREADS = TTM == 256 ? 384 : 512;
-  static constexpr int REGS_LOW = TTM == 256 ? 64 : 72;             // warpgroups 0 and 3
-  static constexpr int REGS_HIGH = TTM == 256 ? 216 : 184;          // warpgroups 1-2
+  // (the expanded-operand instance's workers publish nothing and need fewer
+  // registers; its converter warps publish the scales and take more)
+  static constexpr int REGS_LOW = TTM == 256 ? (AEXP ? 72 : 56) : 72;       // warpgroups 0 and 3
+  static constexpr int REGS_HIGH = TTM == 256 ? (AEXP ? 208 : 224) : 184;   // warpgroups 1-2
   static constexpr int F8 = AB == 16 ? 4 : AB == 8 ? 6 : (TTM == 256 ? W4A4_F8_BUFFERS : 12);  // operand buffers
   // Who writes the per-stage scale slots.  The 128-column instance has converter
   // warps to spare and lets them do it: stage s's scales go to slot s % 4 while
   // stage s is converted, after the converters waited for the MMA to release
   // stage s - F8/4 >= s - 3's operand buffers; those MMAs needed the workers to
   // release every block before them by NBUF = 4 blocks, so the workers are done
-  // with stage s - 4, the slot's previous user.  In the 256-column instance the
+  // with stage s - 4, the slot's previous user.  With expanded activations the
+  // converters publish stage s into slot s % (RAW + 1) once stage s's codes have
+  // landed: the producer refilled that raw slot only after the MMA of the last
+  // block of stage s - RAW completed, and that MMA (NBUF = 2) waited for every
+  // worker to release block 4(s - RAW) + 1, past the slot's previous user, stage
+  // s - RAW - 1.  In the 256-column instance the
   // workers publish stage s + 1's scales during block kb = 2 of stage s into slot
   // (s + 1) % 3, last read by stage s - 2; that block's MMA needed every warp to
   // release block 4s + 2 - NBUF = 4s, past stage s - 2.
-  static constexpr bool CONV_SCALES = TTM == 128;
-  static constexpr int NSC = CONV_SCALES ? 4 : 3;
+  static constexpr bool CONV_SCALES = TTM == 128 || AEXP;
+  static constexpr int NSC = AEXP ? RAW + 1 : CONV_SCALES ? 4 : 3;
   uint8_t wraw[RAW][TW * WROW];  // TMA box: 128 rows x 64 code bytes, or (WEXP) the operand layout of 4 blocks
   uint8_t araw[RAW][TTM * ARAW_ROW];  // TMA box: tt rows x 64 (int4) or 128 (int8) bytes
   uint8_t wf8[WEXP ? 1 : F8][WOP];
-  uint8_t af8[F8][AOP];
+  uint8_t af8[AEXP ? 1 : F8][AOP];
   float sda[NSC][KB][TTM];              // d_a per stage, block-major
   float sdw[NSC][KB][TW];              // d_w * 2^18
   float scorr[NSC][KB][TW];            // -d_w * 8 S_w (exact)
@@ -143,6 +156,7 @@ static_assert(sizeof(Smem<128, 8>) <= 227 * 1024, "shared memory per CTA is at m
 static_assert(sizeof(Smem<128, 16>) <= 227 * 1024, "shared memory per CTA is at most 227 KB");
 static_assert(sizeof(Smem<256, 4, true>) <= 227 * 1024, "shared memory per CTA is at most 227 KB");
 static_assert(sizeof(Smem<128, 4, true>) <= 227 * 1024, "shared memory per CTA is at most 227 KB");
+static_assert(sizeof(Smem<256, 4, true, true>) <= 227 * 1024, "shared memory per CTA is at most 227 KB");
 
 struct TcArgs {
   const uint16_t* w_scales;
@@ -217,6 +231,34 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, SM& S) {
       S.abort = 1;
       atomicOr(&g_w4a4_device_error, 1);
       return false;
+    }
+  }
+}
+__device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\nmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(su32(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded spinning wait for the MMA issuer, whose handoffs are on the critical
+// path: non-blocking tests, with the abort flag and the time bound checked every
+// 64 polls (about 1.5% faster end to end than the blocking wait).
+template <class SM>
+__device__ __forceinline__ bool mbar_spin(uint64_t* b, uint32_t parity, SM& S) {
+  if (mbar_test(b, parity)) return true;
+  const uint64_t t0 = gtime();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_test(b, parity)) return true;
+    if ((n & 63) == 0) {
+      if (S.abort) return false;
+      if (gtime() - t0 > kTimeoutNs) {
+        S.abort = 1;
+        atomicOr(&g_w4a4_device_error, 1);
+        return false;
+      }
     }
   }
 }
@@ -513,7 +555,13 @@ __device__ void producer(const TcArgs& p, SM& S, const CUtensorMap* wmap, const 
       } else {
         tma_2d(S.wraw[slot], wmap, static_cast<int32_t>(s * KB * 16), static_cast<int32_t>(T.wrow0), &S.full_raw[slot]);
       }
-      tma_2d(S.araw[slot], amap, static_cast<int32_t>(s * SM::ARAW_ROW), static_cast<int32_t>(T.m0), &S.full_raw[slot]);
+      if constexpr (SM::AX) {  // the activations' operand bytes, same 4D layout as the weights
+        tma_4d(S.araw[slot], amap, 0, 0, static_cast<int32_t>(s * KB * 2), static_cast<int32_t>(T.m0 / 8),
+               &S.full_raw[slot]);
+      } else {
+        tma_2d(S.araw[slot], amap, static_cast<int32_t>(s * SM::ARAW_ROW), static_cast<int32_t>(T.m0),
+               &S.full_raw[slot]);
+      }
       ++gstage;
     }
   }
@@ -542,11 +590,22 @@ __device__ void mma_issuer(const TcArgs& p, SM& S, uint32_t tmem) {
     for (int64_t b = static_cast<int64_t>(sg.s0) * KB; b < b_end; ++b, ++gblk) {
       const int f = gblk % SM::F8;
       const int tb = static_cast<int>(gblk % SM::NBUF);
-      if (!mbar_wait(&S.f8_full[f], (gblk / SM::F8) & 1, S)) goto done;
-      if (!mbar_wait(&S.tm_empty[tb], ((gblk / SM::NBUF) & 1) ^ 1, S)) goto done;
+      if constexpr (SM::AX) {  // both operands come straight from the raw stage: wait for its copies
+        const int s = static_cast<int>(b / KB);
+        const uint32_t g = gst + static_cast<uint32_t>(s - sg.s0);
+        if (b == static_cast<int64_t>(s) * KB && !mbar_spin(&S.full_raw[g % RAW], (g / RAW) & 1, S)) goto done;
+      } else {
+        if (!mbar_spin(&S.f8_full[f], (gblk / SM::F8) & 1, S)) goto done;
+      }
+      if (!mbar_spin(&S.tm_empty[tb], ((gblk / SM::NBUF) & 1) ^ 1, S)) goto done;
       tc_fence_after();
       const uint32_t dt = tmem + static_cast<uint32_t>(tb * SM::TT);
-      if constexpr (SM::ABITS == 4 && SM::WX) {
+      if constexpr (SM::AX) {
+        const int s = static_cast<int>(b / KB), kb = static_cast<int>(b - static_cast<int64_t>(s) * KB);
+        const uint32_t slot = (gst + static_cast<uint32_t>(s - sg.s0)) % RAW;
+        mma_f8(dt, kmajor_desc_sbo(S.wraw[slot] + kb * 256, KB * 2 * 128),
+               kmajor_desc_sbo(S.araw[slot] + kb * 256, KB * 2 * 128), idesc);
+      } else if constexpr (SM::ABITS == 4 && SM::WX) {
         // A straight from the raw stage: block kb's two 16-byte chunks of every
         // row are core matrices 128 bytes apart, 8-row groups 8 chunks apart
         const int s = static_cast<int>(b / KB), kb = static_cast<int>(b - static_cast<int64_t>(s) * KB);
@@ -560,7 +619,7 @@ __device__ void mma_issuer(const TcArgs& p, SM& S, uint32_t tmem) {
         mma_f16(dt, ad + (256 >> 4), bd + (256 >> 4), idesc, 1u);
       }
       mma_commit(&S.tm_full[tb]);
-      mma_commit(&S.f8_empty[f]);
+      if constexpr (!SM::AX) mma_commit(&S.f8_empty[f]);
       if constexpr (SM::WX) {  // the stage's weights are read once its last block's MMA completes
         const int64_t s = b / KB;
         const int64_t last = ((s + 1) * KB < B ? (s + 1) * KB : B) - 1;
@@ -671,7 +730,7 @@ __device__ void converters(const TcArgs& p, SM& S) {
       // stage's codes are converted (the loads' latency hides behind that)
       uint4 sa[AR];
       uint2 swd[WR], sws[WR];
-      if constexpr (SM::CONV_SCALES) {
+      auto load_stage_scales = [&]() {
       if constexpr (SM::ABITS != 16) {  // the rotate-only route has no activation scales
 #pragma unroll
       for (int i = 0; i < AR; ++i) {
@@ -687,8 +746,13 @@ __device__ void converters(const TcArgs& p, SM& S) {
         swd[i] = load_halves4(p.w_scales + row * B, s, static_cast<int>(B), vec);
         sws[i] = load_halves4(reinterpret_cast<const uint16_t*>(p.w_sums) + row * B, s, static_cast<int>(B), vec);
       }
-      }
+      };
+      // with nothing to convert the loads wait until the stage has landed (several
+      // stages of slack), so that they are not held across the wait
+      if constexpr (SM::CONV_SCALES && !SM::AX) load_stage_scales();
       if (!mbar_wait(&S.full_raw[slot], (gstage / RAW) & 1, S)) return;
+      if constexpr (SM::AX) load_stage_scales();
+      if constexpr (!SM::AX) {  // (expanded operands: nothing to convert, scales only)
       for (int kk = 0; kk < nbk; ++kk) {
         const uint32_t g = gblk + kk;
         if (!mbar_wait(&S.f8_empty[g % F8], ((g / F8) & 1) ^ 1, S)) return;
@@ -786,6 +850,7 @@ __device__ void converters(const TcArgs& p, SM& S) {
         }
         }
       }
+      }
       if constexpr (SM::CONV_SCALES) {
         const int sc = static_cast<int>(gstage % SM::NSC);
 #pragma unroll
@@ -829,8 +894,10 @@ __device__ void converters(const TcArgs& p, SM& S) {
       fence_async_smem();
       __syncwarp();
       if (lane == 0) {
-        for (int kk = 0; kk < nbk; ++kk) mbar_arrive(&S.f8_full[(gblk + kk) % F8]);
-        mbar_arrive(&S.empty_raw[slot]);
+        if constexpr (!SM::AX) {
+          for (int kk = 0; kk < nbk; ++kk) mbar_arrive(&S.f8_full[(gblk + kk) % F8]);
+          mbar_arrive(&S.empty_raw[slot]);
+        }
         if constexpr (SM::CONV_SCALES) mbar_arrive(&S.sc_ready[gstage % SM::NSC]);
       }
       gblk += nbk;
@@ -1109,11 +1176,11 @@ __device__ void workers(const TcArgs& p, SM& S, uint32_t tmem) {
   }
 }
 
-template <bool PARTIALS, int TTM, int AB, bool WEXP>
-__global__ void __launch_bounds__(Smem<TTM, AB, WEXP>::THREADS, 1)
+template <bool PARTIALS, int TTM, int AB, bool WEXP, bool AEXP>
+__global__ void __launch_bounds__(Smem<TTM, AB, WEXP, AEXP>::THREADS, 1)
     w4a4_gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap amap,
                         const TcArgs p) {
-  using SmemT = Smem<TTM, AB, WEXP>;
+  using SmemT = Smem<TTM, AB, WEXP, AEXP>;
   // Smem is taken straight from the __shared__ array (no integer round trip), so
   // the compiler keeps every access in the shared address space (LDS/STS).  The
   // operands need 16-byte alignment (no swizzle), the TMA boxes 128 bytes.
@@ -1128,7 +1195,8 @@ __global__ void __launch_bounds__(Smem<TTM, AB, WEXP>::THREADS, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < RAW; ++i) {
       mbar_init(&S.full_raw[i], 1);
-      mbar_init(&S.empty_raw[i], SmemT::CONV + (SmemT::WX ? 1 : 0));  // (WEXP: plus the MMA's commit)
+      // the converters' arrivals (unless nothing is converted), plus the MMA's commit when it reads the stage
+      mbar_init(&S.empty_raw[i], (SmemT::AX ? 0 : SmemT::CONV) + (SmemT::WX ? 1 : 0));
     }
     for (int i = 0; i < SmemT::F8; ++i) {
       mbar_init(&S.f8_full[i], SmemT::CONV);
@@ -1227,11 +1295,11 @@ cudaError_t expanded_map(CUtensorMap* m, const uint8_t* wexp, int64_t rows, int6
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <bool PARTIALS, int TTM, int AB = 4, bool WEXP = false>
+template <bool PARTIALS, int TTM, int AB = 4, bool WEXP = false, bool AEXP = false>
 cudaError_t launch_tc(const CUtensorMap& wmap, const CUtensorMap& amap, const TcArgs& a, int64_t max_tiles,
                       cudaStream_t stream) {
-  auto kern = w4a4_gemm_tc_kernel<PARTIALS, TTM, AB, WEXP>;
-  using SM = Smem<TTM, AB, WEXP>;
+  auto kern = w4a4_gemm_tc_kernel<PARTIALS, TTM, AB, WEXP, AEXP>;
+  using SM = Smem<TTM, AB, WEXP, AEXP>;
   constexpr size_t kSmemBytes = sizeof(SM);
   static bool configured[64] = {};
   static int regs_ok[64] = {};
@@ -1346,16 +1414,17 @@ int* device_error_word() {
 
 cudaError_t launch_gemm_tc(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums,
                            const uint8_t* w_expanded, int64_t N, const uint8_t* a_codes, const float* a_scales,
-                           int64_t M, int64_t K, float* y, int64_t ldy, int32_t* P, void* ws, size_t ws_bytes,
-                           cudaStream_t stream) {
+                           const uint8_t* a_expanded, int64_t M, int64_t K, float* y, int64_t ldy, int32_t* P,
+                           void* ws, size_t ws_bytes, cudaStream_t stream) {
   TcArgs a{};
   a.w_scales = w_scales; a.w_sums = w_sums; a.a_scales = a_scales;
   a.M = M; a.N = N; a.K = K; a.y = y; a.ldy = ldy; a.P = P;
   a.tt = token_tile(M, P ? 256 : kDenseTT);
   const bool wexp = w_expanded != nullptr && !P;
+  const bool aexp = wexp && a_expanded != nullptr;
   CUtensorMap wmap, amap;
   cudaError_t e = wexp ? expanded_map(&wmap, w_expanded, N, K, TW) : codes_map(&wmap, w_codes, N, K, TW);
-  if (e == cudaSuccess) e = codes_map(&amap, a_codes, M, K, a.tt);
+  if (e == cudaSuccess) e = aexp ? expanded_map(&amap, a_expanded, M, K, a.tt) : codes_map(&amap, a_codes, M, K, a.tt);
   if (e != cudaSuccess) return e;
   int64_t grid = ((N + TW - 1) / TW) * ((M + a.tt - 1) / a.tt);
   if (P) return launch_tc<true, 256>(wmap, amap, a, grid, stream);
@@ -1366,6 +1435,7 @@ cudaError_t launch_gemm_tc(const uint8_t* w_codes, const uint16_t* w_scales, con
     a.sk_part = reinterpret_cast<float4*>(static_cast<uint8_t*>(ws) + pl.count_bytes);
     grid = pl.grid;
   }
+  if (aexp) return launch_tc<false, kDenseTT, 4, true, true>(wmap, amap, a, grid, stream);
   if (wexp) return launch_tc<false, kDenseTT, 4, true>(wmap, amap, a, grid, stream);
   return launch_tc<false, kDenseTT>(wmap, amap, a, grid, stream);
 }

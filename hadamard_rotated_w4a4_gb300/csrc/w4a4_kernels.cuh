@@ -34,8 +34,10 @@ Routing routing_in(void* ws, int64_t npairs, int E, int64_t K);
 constexpr size_t kIdStaticScratchBytes = size_t(16) << 20;
 cudaError_t id_static_scratch(void** addr);
 
+// expanded (optional): the offset codes a + 8 as bytes in element order, [M][K]
+// (the e4m3 activation operand of the dense GEMM).
 cudaError_t launch_act_rotate_quantize(const float* x, int64_t M, int64_t K, int64_t ldx, int rotate,
-                                       uint8_t* codes, float* scales, cudaStream_t stream);
+                                       uint8_t* codes, float* scales, uint8_t* expanded, cudaStream_t stream);
 // The exact path's 8-bit activations: int8 codes [M][K] (element order), fp32 scales.
 cudaError_t launch_act_rotate_quantize8(const float* x, int64_t M, int64_t K, int64_t ldx, int rotate,
                                         int8_t* codes, float* scales, cudaStream_t stream);
@@ -55,11 +57,13 @@ cudaError_t launch_import_q4_0(const void* blocks, int64_t N, int64_t K, uint8_t
 // Dense product (P == nullptr) or exact partials (P != nullptr).  With a
 // workspace of at least gemm_workspace_bytes(M, N, K) bytes (16-byte aligned,
 // zero before its first use) the dense product may run a stream-K schedule.
-// w_expanded (optional, the dense product only): the pre-expanded weight operand.
+// w_expanded (optional, the dense product only): the pre-expanded weight operand;
+// a_expanded (optional, used together with w_expanded): the pre-expanded
+// activation operand ([round_up(M, 8)][K] offset-code bytes).
 cudaError_t launch_gemm_tc(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums,
                            const uint8_t* w_expanded, int64_t N, const uint8_t* a_codes, const float* a_scales,
-                           int64_t M, int64_t K, float* y, int64_t ldy, int32_t* P, void* ws, size_t ws_bytes,
-                           cudaStream_t stream);
+                           const uint8_t* a_expanded, int64_t M, int64_t K, float* y, int64_t ldy, int32_t* P,
+                           void* ws, size_t ws_bytes, cudaStream_t stream);
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
 // The exact path (rotated Q4_0 weights x int8 activations, f16 tensor-core
 // MMAs): dense product (P == nullptr) or exact partials; workspace as above.

@@ -110,6 +110,15 @@ typedef struct {
  *   codes : device, [rows][K/2] bytes, same nibble order as Q4_0; each nibble is
  *           a 4-bit two's complement integer in -8..7.
  *   scales: device, [rows][K/32] fp32, the block scale d_a.
+ *   expanded: device, [round_up(rows, 8)][K] bytes, or NULL.  Optional derived
+ *           data: byte k of row r is the offset code a_k + 8 (0..15), which is
+ *           also the fp8 e4m3 value (a_k + 8) * 2^-9, in element order.  When
+ *           w4a4_rotate_quantize_act gets it, it fills rows 0..rows-1 (the pad
+ *           rows are never read into a result and are left as they are);
+ *           w4a4_gemm, given expanded weights as well, then loads both operands
+ *           straight into the tensor-core layout and converts nothing.  Twice the
+ *           codes' memory (w4a4_act4_expanded_bytes).  The other entry points
+ *           ignore it.
  */
 typedef struct {
   uint8_t* codes;
@@ -117,6 +126,7 @@ typedef struct {
   int64_t rows;
   int64_t K;
   uint32_t tag; /* W4A4_TAG_ACT4 | (W4A4_TAG_ROTATED if rotated) */
+  uint8_t* expanded;
 } w4a4_act4;
 
 /*
@@ -155,6 +165,7 @@ size_t w4a4_q4_0_sums_bytes(int64_t rows, int64_t K);
 size_t w4a4_q4_0_expanded_bytes(int64_t rows, int64_t K);
 size_t w4a4_act4_codes_bytes(int64_t rows, int64_t K);
 size_t w4a4_act4_scales_bytes(int64_t rows, int64_t K);
+size_t w4a4_act4_expanded_bytes(int64_t rows, int64_t K);
 size_t w4a4_act8_codes_bytes(int64_t rows, int64_t K);
 size_t w4a4_act8_scales_bytes(int64_t rows, int64_t K);
 size_t w4a4_act16_values_bytes(int64_t rows, int64_t K);
@@ -409,7 +420,8 @@ w4a4_status w4a4_check(w4a4_stream_t stream);
 const char* w4a4_last_error(void);
 /* A fixed name for a status value. */
 const char* w4a4_status_name(w4a4_status s);
-/* ABI version of this library (major * 100 + minor). */
+/* ABI version of this library (major * 100 + minor).  2.00: w4a4_act4 gained the
+ * `expanded` field (a layout change; callers built against 1.xx must rebuild). */
 int w4a4_abi_version(void);
 
 #ifdef __cplusplus

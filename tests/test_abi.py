@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_names(lib):
-    assert lib.w4a4_abi_version() == 100
+    assert lib.w4a4_abi_version() == 200
     for code, name in w4.STATUS.items():
         assert lib.w4a4_status_name(code).decode() == name
 

@@ -1,10 +1,12 @@
-"""The expanded weight operand: the e4m3 bytes of q - 8 the packers and the
-import write beside the Q4_0 codes, which the dense GEMM loads straight into the
+"""The expanded operands: the e4m3 bytes of q - 8 the packers and the import
+write beside the Q4_0 codes, and the offset codes a + 8 the activation kernel
+writes beside the int4 codes, which the dense GEMM loads straight into the
 tensor-core operand layout.
 
 Bar: the expanded bytes bit-exact against the codes (the oracle's, through the
-sign-and-magnitude rule, pad rows zero); the GEMM with them bit-identical to the
-GEMM that converts the codes itself (same MMA operands, same fold)."""
+sign-and-magnitude rule for weights, pad rows zero; a + 8 for activations); the
+GEMM with them bit-identical to the GEMM that converts the codes itself (same
+MMA operands, same fold)."""
 import numpy as np
 import pytest
 import torch
@@ -117,6 +119,77 @@ def test_routed_gemm_with_expanded_weights_is_bit_identical(dev, name, act_per_s
     ids = torch.from_numpy(np.ascontiguousarray(mi["ids"], dtype=np.int32)).to(dev)
     y1 = w4.w4a4_gemm_id(wq, s.E, aq, ids, s.top_k, act_per_slot)
     y2 = w4.w4a4_gemm_id(wq.without_expanded(), s.E, aq, ids, s.top_k, act_per_slot)
+    torch.cuda.synchronize()
+    w4.w4a4_check()
+    assert torch.equal(y1, y2)
+
+
+# ---------------------------------------------------------------- expanded activations
+def _act_expanded_np(a: w4.Act4) -> np.ndarray:
+    torch.cuda.synchronize()
+    return a.expanded[: a.rows * a.K].view(a.rows, a.K).cpu().numpy()
+
+
+@pytest.mark.parametrize("rotate", [True, False])
+@pytest.mark.parametrize("M,K", [(1, 32), (7, 256), (65, 1024), (300, 160), (600, 8192)])
+def test_act_writes_expanded_bytes(dev, M, K, rotate):
+    d = si.random_dense(M, K, 1, seed=M + 7 * K)
+    a = w4.w4a4_rotate_quantize_act(f32_tensor(d["x"], dev), rotate=rotate)
+    ref = oracle.quantize_activations(d["x"], rotate)
+    assert np.array_equal(_act_expanded_np(a), (ref["q"].astype(np.int64) + 8).astype(np.uint8))
+
+
+def test_act_expanded_bytes_strided_rows(dev):
+    """Rows with a stride (ldx > K) take the other activation kernel; same bytes."""
+    d = si.random_dense(37, 512, 1, seed=11)
+    x = torch.zeros(37, 640, dtype=torch.float32, device=dev)
+    x[:, :512] = f32_tensor(d["x"], dev)
+    a = w4.w4a4_rotate_quantize_act(x[:, :512])
+    ref = oracle.quantize_activations(d["x"])
+    assert np.array_equal(_act_expanded_np(a), (ref["q"].astype(np.int64) + 8).astype(np.uint8))
+
+
+ACT_SHAPES = [(64, 256, 256), (1, 32, 1), (3, 64, 5), (129, 96, 130), (300, 1024, 520), (257, 160, 64),
+              (17, 5120, 33), (512, 512, 1000), (600, 8192, 64)]
+
+
+@pytest.mark.parametrize("M,K,N", ACT_SHAPES)
+@pytest.mark.parametrize("stream_k", [True, False])
+def test_gemm_with_expanded_activations_is_bit_identical(dev, M, K, N, stream_k):
+    d = si.random_dense(M, K, N, seed=5 * M + K + N)
+    wq = w4.h32_q4_0_pack_weights(bf16_tensor(d["w_bf16"], dev))
+    a = w4.w4a4_rotate_quantize_act(f32_tensor(d["x"], dev))
+    assert a.expanded is not None and wq.expanded is not None
+    ws = True if stream_k else None
+    y_ax = w4.w4a4_gemm(wq, a, ws=ws)                    # both operands expanded
+    y_wx = w4.w4a4_gemm(wq, a.without_expanded(), ws=ws)  # weights expanded, activations converted
+    torch.cuda.synchronize()
+    w4.w4a4_check()
+    assert torch.equal(y_ax, y_wx), float((y_ax - y_wx).abs().max())
+    R = oracle.w4a4_matmul(oracle.pack_weights(d["w_bf16"]), oracle.quantize_activations(d["x"]))
+    assert_close(y_ax.cpu().numpy(), R)
+
+
+def test_gemm_expanded_activations_on_a_row_slice(dev):
+    """Act4.head(): the slice keeps the expanded buffer; rows past it are valid memory and never stored."""
+    d = si.random_dense(300, 512, 96, seed=12)
+    wq = w4.h32_q4_0_pack_weights(bf16_tensor(d["w_bf16"], dev))
+    a = w4.w4a4_rotate_quantize_act(f32_tensor(d["x"], dev))
+    y = w4.w4a4_gemm(wq, a.head(131))
+    y_ref = w4.w4a4_gemm(wq, a)[:131]
+    torch.cuda.synchronize()
+    assert torch.equal(y, y_ref)
+
+
+@pytest.mark.parametrize("cfg", ["c1", "c2", "c3"])
+def test_gemm_expanded_activations_full_size(dev, cfg):
+    d = si.dense_inputs(cfg)
+    s = d["shape"]
+    wq = w4.h32_q4_0_pack_weights(bf16_tensor(d["w_bf16"], dev))
+    a = w4.w4a4_rotate_quantize_act(f32_tensor(d["x"], dev))
+    ws = torch.zeros(max(16, w4.w4a4_gemm_workspace_bytes(s.M, s.N, s.K)), dtype=torch.uint8, device=dev)
+    y1 = w4.w4a4_gemm(wq, a, ws=ws)
+    y2 = w4.w4a4_gemm(wq, a.without_expanded(), ws=ws)
     torch.cuda.synchronize()
     w4.w4a4_check()
     assert torch.equal(y1, y2)
