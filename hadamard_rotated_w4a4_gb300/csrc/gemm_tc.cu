@@ -493,42 +493,55 @@ __device__ __forceinline__ bool sk_arrive(const TcArgs& p, int64_t t, int nst, i
   return last != 0;
 }
 // Sum the partials of this warp's region and write them to Y (row m0 + col,
-// feature n).  Four float4 (16 columns) at a time: each contributor's four
-// loads are issued together, so one L2 round trip is paid per contributor and
-// group, not per value.
+// feature n).  Four groups of 16 columns (16 float4 per thread) per pass: each
+// contributor's 16 loads are issued together, so a pass pays one L2 round trip
+// per contributor -- the fix-up of a 256-column tile cut in two takes four round
+// trips, not sixteen.  The sum runs in CTA order for every value, as before.
 template <int CPW>
 __device__ __forceinline__ void sk_finish(const TcArgs& p, int64_t t, int nst, int w, int lane, int h, int64_t m0,
                                           int ntok, int64_t n, bool n_ok) {
+  constexpr int GB = 4;  // 16-column groups per pass
+  static_assert((2 * CPW) % GB == 0, "whole passes");
   const int64_t u_lo = t * nst;
   const int64_t c_lo = sk_cta_of_unit(p, u_lo), c_hi = sk_cta_of_unit(p, u_lo + nst - 1);
 #pragma unroll 1
-  for (int g = 0; g < 2 * CPW; ++g) {
-    float4 a[4];
+  for (int g0 = 0; g0 < 2 * CPW; g0 += GB) {
+    float4 a[GB][4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) a[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int gg = 0; gg < GB; ++gg)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) a[gg][k] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 1
     for (int64_t c = c_lo; c <= c_hi; ++c) {
-      const float4* src = sk_slot(p, c, sk_begin(p, c) >= u_lo, w, lane) + g * 4 * 32;
-      float4 v[4];
+      const float4* src = sk_slot(p, c, sk_begin(p, c) >= u_lo, w, lane) + g0 * 4 * 32;
+      float4 v[GB][4];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) v[k] = __ldcg(src + k * 32);
+      for (int gg = 0; gg < GB; ++gg)
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        a[k].x += v[k].x;
-        a[k].y += v[k].y;
-        a[k].z += v[k].z;
-        a[k].w += v[k].w;
-      }
+        for (int k = 0; k < 4; ++k) v[gg][k] = __ldcg(src + (gg * 4 + k) * 32);
+#pragma unroll
+      for (int gg = 0; gg < GB; ++gg)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          a[gg][k].x += v[gg][k].x;
+          a[gg][k].y += v[gg][k].y;
+          a[gg][k].z += v[gg][k].z;
+          a[gg][k].w += v[gg][k].w;
+        }
     }
     if (n_ok) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int col = (h + 2 * (g >> 1)) * 32 + 16 * (g & 1) + 4 * k;  // float4 q = 4 g + k
-        float* yc = p.y + (m0 + col) * p.ldy + n;
-        if (col + 0 < ntok) yc[0] = a[k].x;
-        if (col + 1 < ntok) yc[p.ldy] = a[k].y;
-        if (col + 2 < ntok) yc[2 * p.ldy] = a[k].z;
-        if (col + 3 < ntok) yc[3 * p.ldy] = a[k].w;
+      for (int gg = 0; gg < GB; ++gg) {
+        const int g = g0 + gg;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int col = (h + 2 * (g >> 1)) * 32 + 16 * (g & 1) + 4 * k;  // float4 q = 4 g + k
+          float* yc = p.y + (m0 + col) * p.ldy + n;
+          if (col + 0 < ntok) yc[0] = a[gg][k].x;
+          if (col + 1 < ntok) yc[p.ldy] = a[gg][k].y;
+          if (col + 2 < ntok) yc[2 * p.ldy] = a[gg][k].z;
+          if (col + 3 < ntok) yc[3 * p.ldy] = a[gg][k].w;
+        }
       }
     }
   }
@@ -1147,8 +1160,7 @@ __device__ void workers(const TcArgs& p, SM& S, uint32_t tmem) {
         }
         if (sk_arrive(p, sg.t, nst, warp - 4, lane))
           sk_finish<CPW>(p, sg.t, nst, warp - 4, lane, h, T.m0, T.ntok, T.n0 + n_in, n_in < T.rows_w);
-      }
-      if (!split && n_in < T.rows_w) {
+      } else if (n_in < T.rows_w) {  // (else: the accumulators are dead during the fix-up)
         const int64_t n = T.n0 + n_in;
 #pragma unroll
         for (int i = 0; i < CPW; ++i) {
