@@ -1033,6 +1033,15 @@ __device__ void workers(const TcArgs& p, SM& S, uint32_t tmem) {
       const float2 dw2 = make_float2(dw, dw);
       const float2 corr2 = make_float2(corr, corr);
       const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(tb * TT);
+      // The buffer goes back to the MMA as soon as this warp's last TMEM load has
+      // landed (the fast paths below), not after the folding that follows it.
+      bool released = false;
+      auto release = [&]() {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.tm_empty[tb]);
+        released = true;
+      };
       if (!PARTIALS && TT == 128) {
         // 128-column instance, any tile width: this warp's chunks h and h + 2
         // (those below nchunks) are loaded together, one TMEM round trip per
@@ -1045,6 +1054,7 @@ __device__ void workers(const TcArgs& p, SM& S, uint32_t tmem) {
         if (c0) tmem_ld32(tw, ra);
         if (c1) tmem_ld32(tw + 64u, rb);
         tmem_wait32x2(ra, rb);
+        release();
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
           if (i == 0 ? !c0 : !c1) continue;
@@ -1087,7 +1097,10 @@ __device__ void workers(const TcArgs& p, SM& S, uint32_t tmem) {
             acc[i][o + 0] = __ffma2_rn(t0, make_float2(d.x, d.y), acc[i][o + 0]);
             acc[i][o + 1] = __ffma2_rn(t1, make_float2(d.z, d.w), acc[i][o + 1]);
           }
-          if (k < 2 * CPW - 1) tmem_wait(nxt);
+          if (k < 2 * CPW - 1) {
+            tmem_wait(nxt);
+            if (k == 2 * CPW - 2) release();  // every piece of this block is in registers
+          }
         }
       } else {
         // This warp's 16-column pieces: k -> chunk h + 2 (k / 2), half k % 2.
@@ -1141,9 +1154,7 @@ __device__ void workers(const TcArgs& p, SM& S, uint32_t tmem) {
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.tm_empty[tb]);
+      if (!released) release();
       ++gfold;
     }
     gsc = gsc0 + static_cast<uint32_t>(sg.s1 - sg.s0);
