@@ -80,8 +80,8 @@ constexpr uint32_t kWaitHintNs = W4A4_WAIT_HINT_NS;
 // 384 threads; the 128-column instance, whose workers need fewer registers,
 // adds warpgroup 3 as four more converter warps (512 threads) and a third fp8
 // stage.  Registers after setmaxnreg: 128 x 56 + 256 x 224 = 168 x 384 (the
-// workers' 224 leave the fold loop without spills), 128 x 72 + 256 x 208 <=
-// 168 x 384 with expanded activations, and 256 x 72 + 256 x 184 = 128 x 512.
+// workers' 224 leave the fold loop without spills), and 256 x 72 + 256 x 184 =
+// 128 x 512.
 // AB: activation code width.  4 = the W4A4 product (int4 activations, e4m3
 // operands, one kind::f8f6f4 MMA per block); 8 = the exact path (int8
 // activations, f16 operands, two kind::f16 MMAs of K = 16 per block; int8 and
@@ -110,10 +110,11 @@ struct __align__(128) Smem {
   static constexpr int NBUF = 512 / TTM;  // TMEM accumulator buffers
   static constexpr int CONV = TTM == 256 ? 2 : 6;                   // converter warps
   static constexpr int THREADS = TTM == 256 ? 384 : 512;
-  // (the expanded-operand instance's workers publish nothing and need fewer
-  // registers; its converter warps publish the scales and take more)
-  static constexpr int REGS_LOW = TTM == 256 ? (AEXP ? 72 : 56) : 72;       // warpgroups 0 and 3
-  static constexpr int REGS_HIGH = TTM == 256 ? (AEXP ? 208 : 224) : 184;   // warpgroups 1-2
+  // (in the expanded-operand instance the converter warps' scale publishing
+  // spills a little at 56; it has stages of slack, while the workers' fold runs
+  // 2-4% faster at 224 than at 208 -- and 40 / 232 spills in the MMA issuer)
+  static constexpr int REGS_LOW = TTM == 256 ? 56 : 72;       // warpgroups 0 and 3
+  static constexpr int REGS_HIGH = TTM == 256 ? 224 : 184;    // warpgroups 1-2
   static constexpr int F8 = AB == 16 ? 4 : AB == 8 ? 6 : (TTM == 256 ? W4A4_F8_BUFFERS : 12);  // operand buffers
   // Who writes the per-stage scale slots.  The 128-column instance has converter
   // warps to spare and lets them do it: stage s's scales go to slot s % 4 while
