@@ -8,7 +8,7 @@ Sources (engine docs "The lean option: ROCmFP4, ROCmI4 and Hadamard Q4_0"):
   bits, after the same per-32-block rotation as the weights;
 * section "MoE: W4A4 on the experts": Q4_0 has one scale per 32 values.
 
-Readings where the pages are silent (all listed in the design doc):
+Readings where the pages are silent:
 
 * weight block: m = the rotated value of largest magnitude, the lowest index
   on ties; d = m / -8 in fp32; id = 1/d (0 when d == 0); code
