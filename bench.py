@@ -55,6 +55,20 @@ def max_over_ranks(ms: float, world: int, device=None) -> float:
     return float(t.item())
 
 
+def replay_steps(first: int, count: int, nsets: int, replay_cycle, replay_one) -> None:
+    """Run steps first .. first + count - 1, step i on input set i % nsets: a
+    whole cycle of sets (replay_cycle(), sets 0 .. nsets - 1 in order) where one
+    starts at set 0 and fits, else one step (replay_one(set index))."""
+    i = first
+    while count > 0:
+        if i % nsets == 0 and count >= nsets:
+            replay_cycle()
+            i, count = i + nsets, count - nsets
+        else:
+            replay_one(i % nsets)
+            i, count = i + 1, count - 1
+
+
 def whole_job_value(world: int, ops_per_replica: float, ms_per_step: float) -> float:
     """Throughput of the whole job: the work of all replicas over the slowest one's step time."""
     return world * ops_per_replica / (ms_per_step * 1e-3) / 1e12
@@ -455,14 +469,7 @@ def run_ours(args, shape) -> dict | None:
                 step(i, gstream)
 
     def run_steps(first, count):
-        i = first
-        while count > 0:
-            if i % nsets == 0 and count >= nsets:
-                cycle.replay()
-                i, count = i + nsets, count - nsets
-            else:
-                graphs[i % nsets].replay()
-                i, count = i + 1, count - 1
+        replay_steps(first, count, nsets, cycle.replay, lambda k: graphs[k].replay())
 
     with torch.cuda.stream(gstream):
         run_steps(0, args.warmup)

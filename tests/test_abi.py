@@ -176,3 +176,17 @@ def test_exact_path_validation(lib):
     assert s == "W4A4_ERR_MISMATCH"
     d = _Act4Desc(FAKE, FAKE, 0, 0, 0)
     assert status(lib, "w4a8_rotate_quantize_act", FAKE, 4, 100, 100, 1, ctypes.byref(d), None)[0] == "W4A4_ERR_INVALID_ARG"
+
+
+def test_expanded_activation_operand_size_and_alignment(lib):
+    # [round_up(rows, 8)][K] bytes, the buffer rounded to 16 bytes
+    assert lib.w4a4_act4_expanded_bytes(512, 5120) == 512 * 5120
+    assert lib.w4a4_act4_expanded_bytes(65, 256) == 72 * 256
+    assert lib.w4a4_act4_expanded_bytes(1, 32) == 8 * 32
+    assert lib.w4a4_act4_expanded_bytes(4, 33) == 0  # K not a multiple of 32
+    # a misaligned expanded buffer is refused before any launch, by the quantiser and by the GEMM
+    d = _Act4Desc(FAKE, FAKE, 0, 0, 0, FAKE + 8)
+    assert status(lib, "w4a4_rotate_quantize_act", FAKE, 4, 64, 64, 1, ctypes.byref(d), None)[0] == "W4A4_ERR_ALIGNMENT"
+    bad = _Act4Desc(FAKE, FAKE, 64, 256, w4.TAG_ACT4 | 1, FAKE + 4)
+    s, msg = status(lib, "w4a4_gemm", ctypes.byref(q4()), ctypes.byref(bad), FAKE, 64, None, 0, None)
+    assert s == "W4A4_ERR_ALIGNMENT" and "expanded" in msg
