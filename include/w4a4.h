@@ -233,6 +233,9 @@ w4a4_status q4_0_import(const void* blocks, int64_t N, int64_t K, int rotated, w
  *   rotate : 1 = rotate (for rotated weights); 0 = quantise unrotated values.
  *   out    : host struct; out->codes / out->scales point to caller buffers of
  *            w4a4_act4_codes_bytes / _scales_bytes; rows, K, tag are written.
+ *            out->expanded: NULL, or a 16-byte aligned buffer of
+ *            w4a4_act4_expanded_bytes, which then also receives the offset
+ *            codes a + 8 of rows 0..M-1 (see w4a4_act4).
  * Per block: y as for the weights; a = max |y|; d_a = a / 7 (fp32, stored);
  * q = clamp(round_half_away(y * (1/d_a)), -8, 7) (q = 0 when d_a = 0).
  */
@@ -247,7 +250,9 @@ w4a4_status w4a4_rotate_quantize_act(const float* x, int64_t M, int64_t K, int64
  *         the 16-byte rule); Y[m][n] = sum_b d_w d_a P (fp32).
  * w->K must equal a->K and both tags must agree on rotation, else
  * W4A4_ERR_MISMATCH.  The per-block integer partials are exact on the tensor
- * cores; the scale fold is fp32.
+ * cores; the scale fold is fp32.  When w->expanded and a->expanded are both set,
+ * the kernel reads them instead of the codes (same result, bit for bit); they
+ * must then hold the expanded form of the same codes.
  *   ws  : optional device workspace (NULL, or w4a4_gemm_workspace_bytes(M, N,
  *         K) bytes or more, 16-byte aligned, all zero before its first use).
  *         Its first MiB holds arrival counters that every call leaves at zero
