@@ -18,6 +18,7 @@ the max over ranks and ``value`` counts the work of all ranks.
 from __future__ import annotations
 
 import argparse
+import datetime
 import json
 import os
 import statistics
@@ -84,16 +85,19 @@ def emit(line: dict | None, rank: int) -> bool:
 
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
-    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+    """Samples nvidia-smi clocks and throttle reasons (every 100 ms) while kernels run.
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    Each sample carries nvidia-smi's own timestamp; ``summary(t0, t1)`` keeps the
+    samples taken between two host wall-clock times (the load window)."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.lines: list[str] = []
+        self.lines: list[tuple[float, str]] = []
         self._t = None
 
     def __enter__(self):
@@ -110,7 +114,7 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -122,25 +126,38 @@ class ClockSampler:
                 self.proc.kill()
         return False
 
-    def summary(self) -> dict:
-        sm, smax, reasons = [], [], set()
+    @staticmethod
+    def parse(lines, t0: float | None = None, t1: float | None = None) -> dict:
+        """Median SM clock, max clock and the throttle reasons seen in the samples
+        read between host times t0 and t1 (all samples when not given)."""
+        sm, smax, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for t_read, ln in lines:
             parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
+                continue
+            try:  # nvidia-smi's own time of the sample (local time); the read time if unparsable
+                t = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                t = t_read
+            if (t0 is not None and t < t0) or (t1 is not None and t > t1):
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
+                sm.append(float(parts[2]))
+                smax.append(float(parts[3]))
+                power.append(float(parts[4]))
             except ValueError:
                 continue
-            for nm, v in zip(names, parts[5:9]):
+            for nm, v in zip(names, parts[6:10]):
                 if v.lower().startswith("active"):
                     reasons.add(nm)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "power_w_median": statistics.median(power)}
+
+    def summary(self, t0: float | None = None, t1: float | None = None) -> dict:
+        return self.parse(self.lines, t0, t1)
 
 
 # ----------------------------------------------------------------------------- oracle arm
@@ -200,6 +217,44 @@ def read_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "sm_max_mhz": 2070.0, "fallback": True}
 
 
+def fold_peak_tflops(peaks: dict, sm_count: int) -> float:
+    """fp32-pipe peak in the FMA convention (2 flops per FMA): SMs x 128 lanes x 2 x max SM clock."""
+    return sm_count * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+
+
+def gemm_algorithmic_bytes(w_rows: int, K: int, a_rows: int, y_rows: int, N: int) -> int:
+    """The GEMM's algorithmic HBM bytes: weight codes + fp16 scales, activation codes + fp32
+    scales, fp32 output (the expanded operands and the block sums are derived copies, left out)."""
+    B = K // 32
+    return w_rows * K // 2 + w_rows * B * 2 + a_rows * K // 2 + a_rows * B * 4 + y_rows * N * 4
+
+
+def act_algorithmic_bytes(M: int, K: int) -> int:
+    """The activation kernel's algorithmic HBM bytes: fp32 in, int4 codes + fp32 scales out."""
+    return M * K * 4 + M * K // 2 + M * (K // 32) * 4
+
+
+def gemm_roofline(ms: float, pairs: int, K: int, hbm_bytes: int, peaks: dict, sm_count: int) -> dict:
+    """Both bounds of a GEMM launch: the scale fold on the fp32 pipe (2 FMAs = 4 flops per
+    output and block) and the algorithmic bytes against the measured copy bandwidth."""
+    fold_flops = 4.0 * pairs * (K // 32)
+    fpk = fold_peak_tflops(peaks, sm_count)
+    fold = fold_flops / (ms * 1e-3) / 1e12
+    gbs = hbm_bytes / (ms * 1e-3) / 1e9
+    return {"ms": ms, "effective_tops": 2.0 * pairs * K / (ms * 1e-3) / 1e12,
+            "fold": {"achieved": fold, "peak": fpk, "unit": "TFLOP/s", "frac": fold / fpk,
+                     "work": "2 fp32 FMAs (4 flops) per output and 32-block"},
+            "hbm": {"algorithmic_bytes": hbm_bytes, "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": gbs / peaks["hbm_gbs"]}}
+
+
+def act_roofline(ms: float, M: int, K: int, peaks: dict, expanded: bool) -> dict:
+    b = act_algorithmic_bytes(M, K)
+    gbs = b / (ms * 1e-3) / 1e9
+    return {"ms": ms, "algorithmic_bytes": b, "expanded_write_bytes": M * K if expanded else 0,
+            "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"]}
+
+
 def source_digest(*names: str) -> str:
     """sha256 over kernel sources, to tie an ncu traffic figure to the kernel it was taken on."""
     import hashlib
@@ -237,7 +292,7 @@ def profiled_traffic(summary: str, sources: tuple[str, ...]) -> tuple[float | No
 
 
 # the files that define each kernel's device code (the internal host header is left out)
-GEMM_SOURCES = ("gemm_tc.cu", "w4a4_device.cuh")
+GEMM_SOURCES = ("gemm_grp.cu", "tc_ptx.cuh", "w4a4_device.cuh")
 ACT_SOURCES = ("act_quant.cu", "w4a4_device.cuh")
 
 
@@ -272,7 +327,7 @@ def graph_time(fn, n: int = 20, reps: int = 5) -> float:
     return best
 
 
-def moe_extra(dev) -> dict:
+def moe_extra(dev, peaks: dict | None = None) -> dict:
     """The expert-routed workload (1024 tokens, 128 experts, top-8): activation
     quantisation and w4a4_gemm_id for gate/up (K2048 -> N768, activations per
     token) and down (K768 -> N2048, activations per token-slot), device time."""
@@ -280,33 +335,90 @@ def moe_extra(dev) -> dict:
     import hadamard_rotated_w4a4_gb300 as w4
     mi = si.moe_inputs("c4")
     s = mi["shape"]
+    peaks = peaks or read_peaks()
+    sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
     ids = torch.from_numpy(np.ascontiguousarray(mi["ids"], dtype=np.int32)).to(dev)
     out = {"workload": s.what}
     for name, wkey, xkey, N, per_slot in (("gate", "wg_bf16", "x_gate", s.N_gate, False),
                                           ("down", "wd_bf16", "x_down", s.N_down, True)):
         w = torch.from_numpy(mi[wkey].reshape(s.E * N, -1).view(np.int16)).to(dev).view(torch.bfloat16)
-        wq = w4.h32_q4_0_pack_weights(w)
+        wq0 = w4.h32_q4_0_pack_weights(w)
         del w
-        x = torch.from_numpy(mi[xkey]).to(dev)
-        K = x.shape[1]
-        aq = w4.alloc_act4(x.shape[0], K, dev)
+        x0 = torch.from_numpy(mi[xkey]).to(dev)
+        K = x0.shape[1]
+        # two input sets (weights, activations, output), each above 129 MB, rotated across calls
+        sets = []
+        for _ in range(2):
+            wq = w4.alloc_q4_0(s.E * N, K, dev)
+            wq.codes.copy_(wq0.codes)
+            wq.scales_buf.copy_(wq0.scales_buf)
+            wq.sums_buf.copy_(wq0.sums_buf)
+            # the routed product reads the int4 codes: no expanded activation operand
+            sets.append((wq, x0.clone(), w4.alloc_act4(x0.shape[0], K, dev, expanded=False),
+                         torch.empty(s.M, s.top_k, N, dtype=torch.float32, device=dev)))
+        del wq0, x0
         ws = torch.zeros(w4.w4a4_gemm_id_workspace_bytes(s.M, s.top_k, s.E, K), dtype=torch.uint8, device=dev)
-        y = torch.empty(s.M, s.top_k, N, dtype=torch.float32, device=dev)
-        act_ms = graph_time(lambda i, st: w4.w4a4_rotate_quantize_act(x, out=aq, stream=st))
-        gid_ms = graph_time(lambda i, st: w4.w4a4_gemm_id(wq, s.E, aq, ids, s.top_k, per_slot, y=y, ws=ws, stream=st))
+        act_ms = graph_time(lambda i, st: w4.w4a4_rotate_quantize_act(sets[i % 2][1], out=sets[i % 2][2], stream=st))
+        gid_ms = graph_time(lambda i, st: w4.w4a4_gemm_id(sets[i % 2][0], s.E, sets[i % 2][2], ids, s.top_k, per_slot,
+                                                          y=sets[i % 2][3], ws=ws, stream=st))
+        aq = sets[0][2]
         ops = 2.0 * s.M * s.top_k * N * K
+        a_rows = s.M * s.top_k if per_slot else s.M
         out[name] = {"K": K, "N": N, "act_ms": act_ms, "gemm_id_ms": gid_ms,
                      "gemm_id_effective_tops": ops / (gid_ms * 1e-3) / 1e12,
-                     "weight_mb": s.E * N * K * 0.5625 / 1e6}
+                     "weight_mb": s.E * N * K * 0.5625 / 1e6,
+                     "l2": "2 input sets rotated, each larger than L2",
+                     "roofline": gemm_roofline(gid_ms, s.M * s.top_k * N, K,
+                                               gemm_algorithmic_bytes(s.E * N, K, a_rows, s.M * s.top_k, N),
+                                               peaks, sm_count),
+                     "act_roofline": act_roofline(act_ms, a_rows, K, peaks, aq.expanded is not None)}
         w4.w4a4_gemm_id_status(ws)
-        del wq, x, aq, ws, y
+        del sets, aq, ws
     del mi
     torch.cuda.empty_cache()
     return out
 
 
-def prefill_proxy(dev, stream, nrep: int) -> dict:
-    """GEMM-only prefill proxy for one dense layer at 512 tokens.
+def time_dense(dev, name: str, rows: int, nrep: int) -> dict:
+    """Device times of the activation kernel and the GEMM on the first `rows` tokens of a
+    dense config, each replayed from a CUDA graph over input sets that together exceed L2."""
+    import torch
+    import hadamard_rotated_w4a4_gb300 as w4
+
+    d = si.dense_inputs(name)
+    w = torch.from_numpy(d["w_bf16"].view(np.int16)).to(dev).view(torch.bfloat16)
+    x = torch.from_numpy(np.ascontiguousarray(d["x"][:rows])).to(dev)
+    del d
+    N, K = w.shape
+    set_bytes = N * K // 2 + N * K // 8 + rows * K * 5.5 + rows * N * 4  # codes, scales/sums, activations, Y
+    nsets = max(2, int(np.ceil(2.2 * L2_BYTES / set_bytes)))
+    wq0 = w4.h32_q4_0_pack_weights(w)
+    del w
+    sets = []
+    for _ in range(nsets):
+        wq = w4.alloc_q4_0(N, K, dev)
+        wq.codes.copy_(wq0.codes)
+        wq.scales_buf.copy_(wq0.scales_buf)
+        wq.sums_buf.copy_(wq0.sums_buf)
+        sets.append((wq, x.clone(), w4.alloc_act4(rows, K, dev), torch.empty(rows, N, device=dev)))
+    del wq0
+    for s_ in sets:
+        w4.w4a4_rotate_quantize_act(s_[1], out=s_[2])
+    gws = torch.zeros(max(16, w4.w4a4_gemm_workspace_bytes(rows, N, K)), dtype=torch.uint8, device=dev)
+    out = {
+        "M": rows, "K": K, "N": N,
+        "act_ms": graph_time(lambda i, st: w4.w4a4_rotate_quantize_act(sets[i % nsets][1], out=sets[i % nsets][2],
+                                                                        stream=st), nrep),
+        "gemm_ms": graph_time(lambda i, st: w4.w4a4_gemm(sets[i % nsets][0], sets[i % nsets][2],
+                                                         y=sets[i % nsets][3], ws=gws, stream=st), nrep),
+    }
+    del gws, sets
+    torch.cuda.empty_cache()
+    return out
+
+
+def prefill_proxy(dev, nrep: int) -> tuple[dict, dict]:
+    """GEMM-only prefill proxy for one dense layer at 512 tokens, and the full-size c3 times.
 
     A dense layer of the pages' 27B model at hidden 5120 / FFN 17408 runs, per
     512-token micro-batch: 4 attention projections (taken at K5120 N5120),
@@ -316,48 +428,14 @@ def prefill_proxy(dev, stream, nrep: int) -> dict:
     out attention, norms and everything else in a layer: not comparable with
     whole-model prompt rates.
     """
-    import torch
-    import hadamard_rotated_w4a4_gb300 as w4
-
-    out = {}
-    for name, rows in (("c1", 512), ("c2", 512), ("c3", 512)):
-        d = si.dense_inputs(name)
-        w = torch.from_numpy(d["w_bf16"].view(np.int16)).to(dev).view(torch.bfloat16)
-        x = torch.from_numpy(np.ascontiguousarray(d["x"][:rows])).to(dev)
-        del d
-        N, K = w.shape
-        set_bytes = N * K * 1.5 + N * K // 8 + rows * K * 5.5 + rows * N * 4  # incl. both expanded operands
-        nsets = max(2, int(np.ceil(2.2 * L2_BYTES / set_bytes)))
-        wq0 = w4.h32_q4_0_pack_weights(w)
-        del w
-        sets = []
-        for i in range(nsets):
-            wq = w4.alloc_q4_0(N, K, dev)
-            wq.codes.copy_(wq0.codes)
-            wq.scales_buf.copy_(wq0.scales_buf)
-            wq.sums_buf.copy_(wq0.sums_buf)
-            if wq.expanded is not None:
-                wq.expanded.copy_(wq0.expanded)
-            sets.append((wq, x.clone(), w4.alloc_act4(rows, K, dev), torch.empty(rows, N, device=dev)))
-        del wq0
-        for s_ in sets:
-            w4.w4a4_rotate_quantize_act(s_[1], out=s_[2])
-        gws = torch.zeros(max(16, w4.w4a4_gemm_workspace_bytes(rows, N, K)), dtype=torch.uint8, device=dev)
-        out[name] = {
-            "act_ms": graph_time(lambda i, st: w4.w4a4_rotate_quantize_act(sets[i % nsets][1], out=sets[i % nsets][2],
-                                                                            stream=st), nrep),
-            "gemm_ms": graph_time(lambda i, st: w4.w4a4_gemm(sets[i % nsets][0], sets[i % nsets][2],
-                                                             y=sets[i % nsets][3], ws=gws, stream=st), nrep),
-        }
-        del gws
-        del sets
-        torch.cuda.empty_cache()
+    out = {name: time_dense(dev, name, 512, nrep) for name in ("c1", "c2", "c3")}
     layer_ms = (4 * out["c1"]["gemm_ms"] + 2 * out["c2"]["gemm_ms"] + out["c3"]["gemm_ms"]
                 + 3 * out["c1"]["act_ms"] + out["c3"]["act_ms"])
-    return {"value": 512.0 / (layer_ms * 1e-3), "unit": "tok/s per layer", "layer_ms": layer_ms,
-            "what": "512 / (4 GEMM K5120xN5120 + 2 GEMM K5120xN17408 + 1 GEMM K17408xN5120 + 3 act K5120 "
-                    "+ 1 act K17408), M=512; GEMM-only, not a whole-model rate",
-            "kernels_ms": out}
+    proxy = {"value": 512.0 / (layer_ms * 1e-3), "unit": "tok/s per layer", "layer_ms": layer_ms,
+             "what": "512 / (4 GEMM K5120xN5120 + 2 GEMM K5120xN17408 + 1 GEMM K17408xN5120 + 3 act K5120 "
+                     "+ 1 act K17408), M=512; GEMM-only, not a whole-model rate",
+             "kernels_ms": out}
+    return proxy, {"c2": out["c2"], "c3": time_dense(dev, "c3", si.DENSE["c3"].M, nrep)}
 
 
 def run_probes() -> dict:
@@ -435,7 +513,6 @@ def run_ours(args, shape) -> dict | None:
         aq = w4.alloc_act4(M, K, dev)
         y = torch.empty(M, N, dtype=torch.float32, device=dev)
         sets.append((wq, xs, aq, y))
-    del w_dev
     torch.cuda.synchronize()
 
     gws = torch.zeros(max(16, w4.w4a4_gemm_workspace_bytes(M, N, K)), dtype=torch.uint8, device=dev)
@@ -480,14 +557,34 @@ def run_ours(args, shape) -> dict | None:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with ClockSampler(dev.index or 0) as clk:
+        tr0 = time.time()
         with torch.cuda.stream(gstream):
             t0.record(gstream)
             run_steps(args.warmup, args.steps)
             t1.record(gstream)
         torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    total_ms = t0.elapsed_time(t1)
+        if world > 1:
+            torch.distributed.barrier()
+        total_ms = t0.elapsed_time(t1)
+        # Load window: the same steps (whole cycles of the input sets) replayed for at
+        # least 0.6 s right after the timed region, so that the clock samples (every
+        # 100 ms) see the kernels under load; its time per step cross-checks ms_per_step.
+        w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        nwin = 0
+        tw0 = time.time()
+        with torch.cuda.stream(gstream):
+            w0.record(gstream)
+            while True:
+                for _ in range(max(1, 256 // nsets)):
+                    cycle.replay()
+                    nwin += nsets
+                gstream.synchronize()
+                if time.time() - tw0 >= 0.6:
+                    break
+            w1.record(gstream)
+        torch.cuda.synchronize()
+        tw1 = time.time()
+    window_ms_per_step = w0.elapsed_time(w1) / nwin
 
     # per-kernel device time: each kernel back to back over the same rotating input sets,
     # events only around the loops (on the launching stream)
@@ -498,6 +595,17 @@ def run_ours(args, shape) -> dict | None:
                                                                     stream=st), nk)
     gemm_avg = graph_time(lambda i, st: w4.w4a4_gemm(sets[i % nsets][0], sets[i % nsets][2], y=sets[i % nsets][3],
                                                      ws=gws, stream=st), nk)
+    # the optional expanded weight copy (1 byte per weight beside the Q4_0 codes):
+    # the same GEMM when it loads that copy instead of converting the codes
+    expanded_w = None
+    if not args.no_exact and world == 1:
+        wxs = [w4.h32_q4_0_pack_weights(w_dev, expanded=True) for _ in range(nsets)]
+        gemm_wx = graph_time(lambda i, st: w4.w4a4_gemm(wxs[i % nsets], sets[i % nsets][2], y=sets[i % nsets][3],
+                                                        ws=gws, stream=st), nk)
+        expanded_w = {"what": "the same GEMM reading the optional expanded weight copy (2.9x the Q4_0 footprint) "
+                              "instead of converting the codes, over as many rotating weight sets",
+                      "gemm_ms": gemm_wx, "speedup_vs_codes": gemm_avg / gemm_wx}
+        del wxs
     # the exact path (int8 activations) on the same sets: the pages' comparison
     exact = None
     if not args.no_exact and world == 1:
@@ -540,6 +648,7 @@ def run_ours(args, shape) -> dict | None:
         verify = {"what": "8-token verification batch, same weights", "tensor_core_ms": tc_ms, "small_m_ms": sm_ms,
                   "small_m_weight_gbs": wbytes / (sm_ms * 1e-3) / 1e9}
         del x8, a4v, y8, wsv
+    del w_dev
     w4.w4a4_check()
     total_ms = max_over_ranks(total_ms, world, dev)
     ms_per_step = total_ms / args.steps
@@ -606,39 +715,44 @@ def run_ours(args, shape) -> dict | None:
 
     peaks = read_peaks()
     probes = run_probes() if not args.no_probes else {}
-    B = K // 32
-    a_exp = sets[0][2].expanded is not None and wq0.expanded is not None
-    # GEMM roofline: the per-block scale fold on the fp32 pipe.  Per (m, n, block) it
-    # takes two fp32-pipe operations (the product by d_w, with the offset correction
-    # folded in, and the fused multiply-add with d_a): 4 flops in the FMA convention.
-    fold_flops = 4.0 * M * N * B
     sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
-    fp32_peak = sm_count * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
-    gemm_traffic, gemm_traffic_src = profiled_traffic(f"gemm_tc_{shape.name}.md", GEMM_SOURCES)
+    a_exp = sets[0][2].expanded is not None
+    gemm_traffic, gemm_traffic_src = profiled_traffic(f"gemm_grp_{shape.name}.md", GEMM_SOURCES)
     act_traffic, act_traffic_src = profiled_traffic(f"act_rotate_quantize_{shape.name}.md", ACT_SOURCES)
-    gemm_roof = {"bound": "alu", "achieved": fold_flops / (gemm_avg * 1e-3) / 1e12, "peak": fp32_peak,
-                 "unit": "TFLOP/s", "frac": None, "traffic": gemm_traffic, "traffic_source": gemm_traffic_src,
-                 # each operand read as its expanded form (1 byte per element) when the GEMM uses it, else as codes
-                 "algorithmic_bytes": float((N * K if wq0.expanded is not None else N * K // 2) + N * B * 4
-                                            + (M * K if a_exp else M * K // 2) + M * B * 4 + M * N * 4),
-                 "kernel": "w4a4_gemm_tc_kernel",
-                 "peak_source": f"derived: {sm_count} SMs x 128 fp32 lanes x 2 flops x {peaks.get('sm_max_mhz', 2070.0)} MHz"}
-    gemm_roof["frac"] = gemm_roof["achieved"] / gemm_roof["peak"]
-    # fp32 in; codes, scales and (when allocated) the expanded operand out
-    act_bytes = M * K * 4 + M * K // 2 + M * B * 4 + (M * K if a_exp else 0)
-    act_roof = {"bound": "hbm", "achieved": act_bytes / (act_avg * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "kernel": "act_rotate_quantize_kernel", "traffic": act_traffic,
-                "traffic_source": act_traffic_src, "algorithmic_bytes": float(act_bytes),
+    # the dominant kernel (the GEMM): bound by the per-block scale fold on the fp32 pipe
+    g1 = gemm_roofline(gemm_avg, M * N, K, gemm_algorithmic_bytes(N, K, M, M, N), peaks, sm_count)
+    gemm_roof = {"bound": "alu", "achieved": g1["fold"]["achieved"], "peak": g1["fold"]["peak"], "unit": "TFLOP/s",
+                 "frac": g1["fold"]["frac"], "traffic": gemm_traffic, "traffic_source": gemm_traffic_src,
+                 "work": g1["fold"]["work"], "algorithmic_bytes": g1["hbm"]["algorithmic_bytes"],
+                 "hbm_frac": g1["hbm"]["frac"], "kernel": "w4a4_grp_kernel",
+                 "peak_source": f"derived: {sm_count} SMs x 128 fp32 lanes x 2 flops x "
+                                f"{peaks.get('sm_max_mhz', 2070.0)} MHz (the FMA-convention peak; the probe "
+                                f"measures fma.rn.f32x2 at 79.7 TFLOP/s)"}
+    a1 = act_roofline(act_avg, M, K, peaks, a_exp)
+    act_roof = {"bound": "hbm", **{k: a1[k] for k in ("achieved", "peak", "unit", "frac", "algorithmic_bytes",
+                                                      "expanded_write_bytes")},
+                "kernel": "act_rotate_quantize_tma_kernel", "traffic": act_traffic,
+                "traffic_source": act_traffic_src,
                 "peak_source": "MEASURED_PEAKS.json hbm_gbs (measured)" if not peaks.get("fallback") else "fallback"}
-    act_roof["frac"] = act_roof["achieved"] / act_roof["peak"]
     eff_tops_gemm = ops / (gemm_avg * 1e-3) / 1e12
     int8_peak = probes.get("int8_mma_sync_tops") if probes else None
-    proxy = None
+    proxy, dense_cfg = None, {}
     if not args.no_proxy and world == 1:
-        proxy = prefill_proxy(dev, stream, 16)
+        proxy, dense_cfg = prefill_proxy(dev, 16)
     moe = None
     if not args.no_moe and world == 1:
-        moe = moe_extra(dev)
+        moe = moe_extra(dev, peaks)
+    # every config's kernels against their bounds (algorithmic bytes; expanded writes apart)
+    rooflines = {"c1": {"gemm": g1, "act": a1}}
+    for name, t in dense_cfg.items():
+        rooflines[name] = {"M": t["M"], "K": t["K"], "N": t["N"],
+                           "gemm": gemm_roofline(t["gemm_ms"], t["M"] * t["N"], t["K"],
+                                                 gemm_algorithmic_bytes(t["N"], t["K"], t["M"], t["M"], t["N"]),
+                                                 peaks, sm_count),
+                           "act": act_roofline(t["act_ms"], t["M"], t["K"], peaks, True)}
+    if moe:
+        for part in ("gate", "down"):
+            rooflines[f"c4_{part}"] = {"gemm": moe[part]["roofline"], "act": moe[part]["act_roofline"]}
 
     cpu = None
     if not args.no_cpu_baseline:
@@ -650,7 +764,11 @@ def run_ours(args, shape) -> dict | None:
                "sample": f"{len(rows)} of {M} activation rows x all {N} weight rows, one pass "
                          f"(numpy; BLAS matmuls threaded, elementwise single-threaded)", "seconds": tc}
 
-    clocks = clk.summary()
+    clocks = clk.summary(tr0, tw1)
+    clocks["samples_under_load"] = clocks.pop("samples")
+    clocks["window"] = {"seconds": tw1 - tw0, "steps": nwin, "ms_per_step": window_ms_per_step,
+                        "what": "clock samples of the timed steps and of a load window right after them "
+                                "(the same steps replayed for >= 0.6 s)"}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -661,11 +779,13 @@ def run_ours(args, shape) -> dict | None:
                    "parallelism": "replicas" if world > 1 else "single"},
         "roofline": gemm_roof,
         "roofline_act": act_roof,
+        "rooflines": rooflines,
         "gemm_effective_tops": eff_tops_gemm,
-        "pct_int8_peak": (eff_tops_gemm / int8_peak) if int8_peak else None,
+        "int8_mma_sync_peak_ratio": (eff_tops_gemm / int8_peak) if int8_peak else None,
         "prefill_tok_s_proxy": proxy,
         "moe": moe,
         "exact_path": exact,
+        "expanded_weights": expanded_w,
         "rotate_only": rotate_only,
         "verification_batch": verify,
         "kernel_ms": {"act_rotate_quantize": act_avg, "gemm": gemm_avg},
@@ -699,9 +819,18 @@ def main():
     ap.add_argument("--no-moe", action="store_true", help="skip the expert-routed workload timing")
     ap.add_argument("--no-exact", action="store_true", help="skip the exact-path (int8 activations) timing")
     ap.add_argument("--no-verify", action="store_true", help="skip the 8-token verification-batch timing")
+    ap.add_argument("--moe-only", action="store_true",
+                    help="time only the expert-routed workload and print its figures (a profiling aid, "
+                         "not the benchmark line)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.moe_only:
+        import torch
+        import hadamard_rotated_w4a4_gb300 as w4
+        w4.load_library(build_if_missing=True)
+        print(json.dumps({"moe": moe_extra(torch.device("cuda", torch.cuda.current_device()))}), flush=True)
+        return
     shape = si.DENSE[args.config]
     line = run_reference(args, shape) if args.impl == "reference" else run_ours(args, shape)
     emit(line, env_rank()[0])

@@ -57,7 +57,7 @@ EXPORTS = [
     "w4a4_status_name", "w4a4_abi_version", "w4a4_act8_codes_bytes", "w4a4_act8_scales_bytes", "w4a4_gemm_small_m",
     "w4a8_rotate_quantize_act", "w4a8_gemm", "w4a8_gemm_partials", "w4a8_gemm_workspace_bytes",
     "w4a4_act16_values_bytes", "w4a16_rotate_act", "w4a16_gemm", "w4a16_gemm_workspace_bytes",
-    "h32_q4_0_pack_weights_imatrix",
+    "h32_q4_0_pack_weights_imatrix", "w4a4_debug_set_wait_limit",
 ]
 
 
@@ -131,6 +131,8 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.w4a4_gemm_id_static.argtypes = [ctypes.POINTER(_Q4_0Desc), i32, i64, ctypes.POINTER(_Act4Desc), vp, i64, i32,
                                          i32, vp, vp]
     lib.w4a4_check.argtypes = [vp]
+    lib.w4a4_debug_set_wait_limit.argtypes = [ctypes.c_uint64, ctypes.c_uint64]
+    lib.w4a4_debug_set_wait_limit.restype = None
     for name in ("h32_q4_0_pack_weights", "q4_0_import", "w4a4_rotate_quantize_act", "w4a4_gemm",
                  "w4a4_gemm_partials", "w4a4_gemm_id", "w4a4_gemm_id_status", "w4a4_check",
                  "w4a8_rotate_quantize_act", "w4a8_gemm", "w4a8_gemm_partials", "w4a4_gemm_small_m"):
@@ -235,7 +237,11 @@ class Act4:
                          self.expanded.data_ptr() if self.expanded is not None else None)
 
 
-def alloc_q4_0(rows: int, K: int, device, rotated: bool = True, expanded: bool = True) -> Q4_0Weights:
+def alloc_q4_0(rows: int, K: int, device, rotated: bool = True, expanded: bool = False) -> Q4_0Weights:
+    """Buffers for Q4_0 weights.  expanded=True also allocates the optional expanded
+    operand (1 byte per weight beside the 0.5-byte codes and the 0.125 bytes of
+    scales and sums: 2.9x the Q4_0 footprint); the dense GEMM then loads it instead
+    of converting the codes.  The codes stay the format of record either way."""
     lib = load_library()
     nc, ns = lib.w4a4_q4_0_codes_bytes(rows, K), lib.w4a4_q4_0_scales_bytes(rows, K)
     if K <= 0 or K % 32:
@@ -264,8 +270,9 @@ def alloc_act4(rows: int, K: int, device, rotated: bool = True, expanded: bool =
 
 
 def h32_q4_0_pack_weights(w: torch.Tensor, rotate: bool = True, out: Q4_0Weights | None = None,
-                          stream=None) -> Q4_0Weights:
-    """Rotate (H32 per 32-block along K) and Q4_0-pack weights w [N][K] (bf16 or fp32, CUDA)."""
+                          stream=None, expanded: bool = False) -> Q4_0Weights:
+    """Rotate (H32 per 32-block along K) and Q4_0-pack weights w [N][K] (bf16 or fp32, CUDA).
+    expanded=True also writes the optional expanded operand (see alloc_q4_0)."""
     _cuda(w, "w")
     if w.dim() != 2 or w.stride(1) != 1:
         raise ValueError("w must be a 2-D tensor with unit stride along K")
@@ -273,7 +280,7 @@ def h32_q4_0_pack_weights(w: torch.Tensor, rotate: bool = True, out: Q4_0Weights
     if dtype is None:
         raise ValueError("w must be bf16 or fp32")
     N, K = w.shape
-    out = out or alloc_q4_0(N, K, w.device, rotate)
+    out = out or alloc_q4_0(N, K, w.device, rotate, expanded)
     d = out.desc()
     ldw = w.stride(0) if N > 1 else K  # a single row's stride is meaningless (may be 0)
     _check(load_library().h32_q4_0_pack_weights(w.data_ptr(), dtype, N, K, ldw, int(rotate),
@@ -283,7 +290,7 @@ def h32_q4_0_pack_weights(w: torch.Tensor, rotate: bool = True, out: Q4_0Weights
 
 
 def h32_q4_0_pack_weights_imatrix(w: torch.Tensor, imatrix: torch.Tensor | None, rotate: bool = True,
-                                  out: Q4_0Weights | None = None, stream=None) -> Q4_0Weights:
+                                  out: Q4_0Weights | None = None, stream=None, expanded: bool = False) -> Q4_0Weights:
     """As h32_q4_0_pack_weights, with each block's scale chosen against the importance vector
     imatrix (fp32 [K], CUDA, the unrotated input channels' importance; None = uniform)."""
     _cuda(w, "w")
@@ -297,7 +304,7 @@ def h32_q4_0_pack_weights_imatrix(w: torch.Tensor, imatrix: torch.Tensor | None,
         _cuda(imatrix, "imatrix")
         if imatrix.dtype != torch.float32 or imatrix.numel() != K or not imatrix.is_contiguous():
             raise ValueError("imatrix must be a contiguous fp32 tensor of K values")
-    out = out or alloc_q4_0(N, K, w.device, rotate)
+    out = out or alloc_q4_0(N, K, w.device, rotate, expanded)
     d = out.desc()
     ldw = w.stride(0) if N > 1 else K
     _check(load_library().h32_q4_0_pack_weights_imatrix(
@@ -308,7 +315,7 @@ def h32_q4_0_pack_weights_imatrix(w: torch.Tensor, imatrix: torch.Tensor | None,
 
 
 def q4_0_import(blocks: torch.Tensor, K: int, rotated: bool = True, out: Q4_0Weights | None = None,
-                stream=None) -> Q4_0Weights:
+                stream=None, expanded: bool = False) -> Q4_0Weights:
     """Import canonical 18-byte Q4_0 blocks (uint8 CUDA tensor, N * K/32 * 18 bytes) bit for bit."""
     _cuda(blocks, "blocks")
     if blocks.dtype != torch.uint8 or not blocks.is_contiguous():
@@ -316,7 +323,7 @@ def q4_0_import(blocks: torch.Tensor, K: int, rotated: bool = True, out: Q4_0Wei
     if K <= 0 or K % 32 or blocks.numel() % (18 * (K // 32)):
         raise W4A4Error(1, "blocks size is not a multiple of a row of K/32 blocks")
     N = blocks.numel() // (18 * (K // 32))
-    out = out or alloc_q4_0(N, K, blocks.device, rotated)
+    out = out or alloc_q4_0(N, K, blocks.device, rotated, expanded)
     d = out.desc()
     _check(load_library().q4_0_import(blocks.data_ptr(), N, K, int(rotated), ctypes.byref(d), _stream(stream)))
     out.rotated = bool(rotated)
@@ -458,8 +465,23 @@ def w4a4_gemm_id_static(experts: Q4_0Weights, E: int, a: Act4, ids: torch.Tensor
 
 
 def w4a4_check(stream=None) -> None:
-    """Synchronise and raise W4A4Error(W4A4_ERR_TIMEOUT) if a GEMM kernel gave up on a bounded wait."""
-    _check(load_library().w4a4_check(_stream(stream)))
+    """Synchronise and raise W4A4Error(W4A4_ERR_TIMEOUT) if a GEMM kernel gave up on a bounded wait.
+
+    A kernel that gave up may leave stream-K arrival tickets standing in its
+    workspace, and a later call on that workspace would then finish its cut
+    tiles wrongly.  So on a timeout every cached per-stream workspace is dropped
+    (the next call allocates a zeroed one); a workspace the caller passed in
+    must be zeroed by the caller before it is used again.
+    """
+    status = load_library().w4a4_check(_stream(stream))
+    if status == 8:  # W4A4_ERR_TIMEOUT
+        _GEMM_WS.clear()
+    _check(status)
+
+
+def w4a4_debug_set_wait_limit(wait_ns: int = 0, producer_delay_ns: int = 0) -> None:
+    """Test hook: the super-tile GEMM's pipeline-wait bound and a producer delay ((0, 0): defaults)."""
+    load_library().w4a4_debug_set_wait_limit(int(wait_ns), int(producer_delay_ns))
 
 
 def w4a4_gemm_id_status(ws: torch.Tensor, stream=None) -> None:

@@ -22,7 +22,7 @@ ROOT = os.path.dirname(PKG)
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 
-LIB_SOURCES = ["act_quant.cu", "pack_weights.cu", "gemm_tc.cu", "gemm_id.cu", "gemm_small_m.cu", "capi.cu"]
+LIB_SOURCES = ["act_quant.cu", "pack_weights.cu", "gemm_tc.cu", "gemm_grp.cu", "gemm_id.cu", "gemm_small_m.cu", "capi.cu"]
 PROBE_SOURCES = ["probes.cu"]
 LIB = os.path.join(PKG, "libw4a4.so")
 PROBE_LIB = os.path.join(PKG, "libw4a4_probes.so")

@@ -263,6 +263,9 @@ __global__ void __launch_bounds__(32 * kTmaWarps) act_rotate_quantize_tma_kernel
     if (threadIdx.x == 0 && err) atomicOr(err, 16);
     return;
   }
+  // a GEMM launched after this kernel may start its set-up and weight loads now
+  // (it waits for this grid to finish before it reads the activations)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int64_t nchunks = (nblk + 31) / 32;
   const int64_t gw = static_cast<int64_t>(blockIdx.x) * kTmaWarps + wib;
   const int64_t nw = static_cast<int64_t>(gridDim.x) * kTmaWarps;

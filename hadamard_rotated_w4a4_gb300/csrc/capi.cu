@@ -246,8 +246,9 @@ w4a4_status w4a4_rotate_quantize_act(const float* x, int64_t M, int64_t K, int64
 }
 
 size_t w4a4_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-  if (M < 0 || N < 0 || !valid_k(K)) return 0;
-  return w4a4::gemm_workspace_bytes(M, N, K);
+  if (M <= 0 || N <= 0 || !valid_k(K)) return 0;
+  const size_t a = w4a4::gemm_workspace_bytes(M, N, K), b = w4a4::grp_workspace_bytes(M, N, K);
+  return a > b ? a : b;
 }
 
 w4a4_status w4a4_gemm(const w4a4_q4_0* w, const w4a4_act4* a, float* y, int64_t ldy, void* ws, size_t ws_bytes,
@@ -263,13 +264,19 @@ w4a4_status w4a4_gemm(const w4a4_q4_0* w, const w4a4_act4* a, float* y, int64_t 
   if (!y) return fail(W4A4_ERR_INVALID_ARG, "%s: y is NULL", fn);
   if ((reinterpret_cast<uintptr_t>(y) & 3u) != 0) return fail(W4A4_ERR_ALIGNMENT, "%s: y must be 4-byte aligned", fn);
   if (ws) {
-    const size_t need = w4a4::gemm_workspace_bytes(M, N, a->K);
+    const size_t need = w4a4_gemm_workspace_bytes(M, N, a->K);
     if (ws_bytes < need)
       return fail(W4A4_ERR_WORKSPACE, "%s: workspace %zu bytes < %zu needed", fn, ws_bytes, need);
     if (!aligned16(ws)) return fail(W4A4_ERR_ALIGNMENT, "%s: ws must be 16-byte aligned", fn);
   }
+  // with the expanded activation operand: the super-tile kernel; else the kernel that
+  // converts both operands' codes
+  if (a->expanded)
+    return cuda_status(w4a4::launch_gemm_grp(w->codes, w->scales, w->sums, w->expanded, N, a->expanded, a->scales,
+                                             M, a->K, y, ldy, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream)),
+                       fn);
   return cuda_status(w4a4::launch_gemm_tc(w->codes, w->scales, w->sums, w->expanded, N, a->codes, a->scales,
-                                          a->expanded, M, a->K, y, ldy, nullptr, ws, ws_bytes,
+                                          M, a->K, y, ldy, nullptr, ws, ws_bytes,
                                           reinterpret_cast<cudaStream_t>(stream)), fn);
 }
 
@@ -298,7 +305,7 @@ w4a4_status w4a4_gemm_partials(const w4a4_q4_0* w, const w4a4_act4* a, int32_t* 
   if (a->rows == 0 || w->rows == 0) return ok();
   if (!P) return fail(W4A4_ERR_INVALID_ARG, "%s: P is NULL", fn);
   if (!aligned16(P)) return fail(W4A4_ERR_ALIGNMENT, "%s: P must be 16-byte aligned", fn);
-  return cuda_status(w4a4::launch_gemm_tc(w->codes, w->scales, w->sums, nullptr, w->rows, a->codes, a->scales, nullptr,
+  return cuda_status(w4a4::launch_gemm_tc(w->codes, w->scales, w->sums, nullptr, w->rows, a->codes, a->scales,
                                           a->rows, a->K, nullptr, 0, P, nullptr, 0,
                                           reinterpret_cast<cudaStream_t>(stream)), fn);
 }
@@ -440,7 +447,7 @@ w4a4_status w4a4_gemm_id(const w4a4_q4_0* experts, int E, int64_t N, const w4a4_
   if (!aligned16(ws) || (reinterpret_cast<uintptr_t>(y) & 3u) != 0)
     return fail(W4A4_ERR_ALIGNMENT, "%s: ws must be 16-byte aligned and y 4-byte aligned", fn);
   const w4a4::Routing r = w4a4::routing_in(ws, M * top_k, E, a->K);
-  return cuda_status(w4a4::launch_gemm_id(experts->codes, experts->scales, experts->sums, experts->expanded, E, N, a->codes, a->scales, a->K, ids, M,
+  return cuda_status(w4a4::launch_gemm_id(experts->codes, experts->scales, experts->sums, E, N, a->codes, a->scales, a->K, ids, M,
                                           top_k, act_per_slot, y, r, reinterpret_cast<cudaStream_t>(stream)), fn);
 }
 
@@ -490,7 +497,7 @@ w4a4_status w4a4_gemm_id_static(const w4a4_q4_0* experts, int E, int64_t N, cons
   cudaError_t e = w4a4::id_static_scratch(&ws);
   if (e != cudaSuccess) return cuda_status(e, fn);
   const w4a4::Routing r = w4a4::routing_in(ws, M * top_k, E, a->K);
-  return cuda_status(w4a4::launch_gemm_id(experts->codes, experts->scales, experts->sums, experts->expanded, E, N, a->codes, a->scales,
+  return cuda_status(w4a4::launch_gemm_id(experts->codes, experts->scales, experts->sums, E, N, a->codes, a->scales,
                                           a->K, ids, M, top_k, act_per_slot, y, r,
                                           reinterpret_cast<cudaStream_t>(stream)),
                      fn);
@@ -506,6 +513,10 @@ w4a4_status w4a4_check(w4a4_stream_t stream) {
   if (flag != 0)
     return fail(W4A4_ERR_TIMEOUT, "%s: a bounded wait inside a GEMM kernel gave up; its output is incomplete", fn);
   return ok();
+}
+
+void w4a4_debug_set_wait_limit(uint64_t wait_ns, uint64_t producer_delay_ns) {
+  w4a4::grp_set_wait_limit(wait_ns, producer_delay_ns);
 }
 
 const char* w4a4_last_error(void) { return g_err; }

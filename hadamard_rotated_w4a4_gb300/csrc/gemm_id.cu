@@ -3,14 +3,17 @@
 // W4A4 kernel runs the expert matmuls too, where an MoE spends nearly all of its
 // prompt work.
 //
-// Three launches on the caller's stream:
-//   1. route_prep (one CTA): histogram of ids per expert, exclusive scans of the
-//      pair counts and of the row tiles per expert, the pair list grouped by
-//      expert, zeroed output rows and a device flag for ids outside [0, E);
-//   2. gather: each routed row's activation codes and scales, copied in expert
-//      order into the workspace, so that every expert's rows are contiguous;
-//   3. the grouped GEMM over (expert row tile, weight tile), loading both
-//      operands with 2D TMA and scattering each output row to (token, slot).
+// Three launches on the caller's stream, each of the later two allowed to start
+// while the one before finishes (programmatic dependent launch):
+//   1. route (one CTA): the (token, slot) pairs per expert, their exclusive scan,
+//      the pair list grouped by expert, and the GEMM's work list -- each expert's
+//      rows cut into segments of at most 256, each segment paired with groups of
+//      up to 4 weight tiles so that a tile fills up to 256 accumulator columns;
+//      ids outside [0, E) zero their output row and set a device flag;
+//   2. gather (every SM): each routed row's int4 codes and scales, copied in
+//      expert order so that every segment is contiguous;
+//   3. the super-tile GEMM (gemm_grp.cu) over the work list, scattering each
+//      output row to its (token, slot).
 #include <mutex>
 
 #include "w4a4_kernels.cuh"
@@ -19,15 +22,58 @@ namespace w4a4 {
 
 namespace {
 
-constexpr int kPrepThreads = 1024;
+constexpr int kRouteThreads = 1024;
+constexpr int kSegRows = 256;  // token rows per segment (the GEMM's accumulator columns)
+constexpr int kMaxG = 4;       // weight tiles per tile
 
-__global__ void __launch_bounds__(kPrepThreads) route_prep_kernel(const int32_t* __restrict__ ids, int64_t npairs,
-                                                                   int E, int64_t N, int tile_tokens,
-                                                                   float* __restrict__ y, Routing r) {
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Weight tiles per tile of a segment of `ntok` rows, balanced over the NT tiles.
+__device__ __forceinline__ int seg_group(int ntok, int NT) {
+  const int cw = (ntok + 31) & ~31;
+  const int gmax = min(min(kMaxG, kSegRows / cw), NT);
+  const int ng = (NT + gmax - 1) / gmax;
+  return (NT + ng - 1) / ng;
+}
+
+// Block-wide exclusive scan of one value per thread (kRouteThreads threads).
+__device__ __forceinline__ int block_excl_scan(int v, int* warp_tot, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_tot[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int t = lane < kRouteThreads / 32 ? warp_tot[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, t, o);
+      if (lane >= o) t += y;
+    }
+    warp_tot[lane] = t;  // inclusive over warps
+    if (lane == 31) *total = t;
+  }
+  __syncthreads();
+  const int before = (warp > 0 ? warp_tot[warp - 1] : 0) + x - v;
+  __syncthreads();  // warp_tot is reused by the next scan
+  return before;
+}
+
+__global__ void __launch_bounds__(kRouteThreads) route_kernel(const int32_t* __restrict__ ids, int64_t npairs,
+                                                               int E, int64_t N, int NT, float* __restrict__ y,
+                                                               Routing r) {
   extern __shared__ int32_t sh[];  // cnt[E], cursor[E]
   int32_t* cnt = sh;
   int32_t* cur = sh + E;
+  __shared__ int warp_tot[32];
+  __shared__ int tot[3];
   __shared__ int bad;
+  grid_dep_launch();
   const int tid = threadIdx.x;
   for (int e = tid; e < E; e += blockDim.x) cnt[e] = 0;
   if (tid == 0) bad = 0;
@@ -38,43 +84,67 @@ __global__ void __launch_bounds__(kPrepThreads) route_prep_kernel(const int32_t*
       atomicAdd(&cnt[e], 1);
     } else {
       bad = 1;
-      float* yr = y + i * N;  // an unused slot's output row is zero
-      for (int64_t n = 0; n < N; ++n) yr[n] = 0.f;
+      float4* yr = reinterpret_cast<float4*>(y + i * N);  // an unused slot's output row is zero
+      if ((N & 3) == 0 && (reinterpret_cast<uintptr_t>(y) & 15) == 0) {
+        for (int64_t n = 0; n < N / 4; ++n) yr[n] = make_float4(0.f, 0.f, 0.f, 0.f);
+      } else {
+        for (int64_t n = 0; n < N; ++n) y[i * N + n] = 0.f;
+      }
     }
   }
   __syncthreads();
-  if (tid == 0) {
-    int32_t off = 0, toff = 0;
-    for (int e = 0; e < E; ++e) {
-      r.offsets[e] = off;
-      r.tile_off[e] = toff;
-      r.counts[e] = cnt[e];
-      cur[e] = off;
-      off += cnt[e];
-      toff += (cnt[e] + tile_tokens - 1) / tile_tokens;
+  // each thread owns a run of consecutive experts: its rows, segments and tiles
+  const int per = (E + kRouteThreads - 1) / kRouteThreads;
+  const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
+  int rows = 0, segs = 0, tiles = 0;
+  for (int e = e0; e < e1; ++e) {
+    const int n = cnt[e];
+    rows += n;
+    for (int s = 0; s * kSegRows < n; ++s) {
+      const int g = seg_group(min(kSegRows, n - s * kSegRows), NT);
+      ++segs;
+      tiles += (NT + g - 1) / g;
     }
-    r.offsets[E] = off;
-    r.tile_off[E] = toff;
-    r.flag[0] = bad;
+  }
+  int row0 = block_excl_scan(rows, warp_tot, &tot[0]);
+  int seg0 = block_excl_scan(segs, warp_tot, &tot[1]);
+  int tile0 = block_excl_scan(tiles, warp_tot, &tot[2]);
+  for (int e = e0; e < e1; ++e) {
+    const int n = cnt[e];
+    r.offsets[e] = row0;
+    cur[e] = row0;
+    for (int s = 0; s * kSegRows < n; ++s) {
+      const int ntok = min(kSegRows, n - s * kSegRows);
+      const int g = seg_group(ntok, NT);
+      r.segs[seg0] = make_int4(row0 + s * kSegRows, e, ntok, g);
+      r.seg_tiles[seg0] = tile0;
+      ++seg0;
+      tile0 += (NT + g - 1) / g;
+    }
+    row0 += n;
+  }
+  if (tid == 0) {
+    r.offsets[E] = tot[0];
+    r.seg_tiles[tot[1]] = tot[2];
+    r.hdr[0] = bad;
+    r.hdr[1] = tot[1];  // segments
+    r.hdr[2] = tot[2];  // tiles
+    r.hdr[3] = tot[0];  // routed rows
   }
   __syncthreads();
   for (int64_t i = tid; i < npairs; i += blockDim.x) {
     const int e = ids[i];
-    if (e >= 0 && e < E) {
-      const int pos = atomicAdd(&cur[e], 1);
-      r.perm[pos] = static_cast<int32_t>(i);
-    }
+    if (e >= 0 && e < E) r.perm[atomicAdd(&cur[e], 1)] = static_cast<int32_t>(i);
   }
 }
 
-size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
-
-// One warp per gathered row: 16-byte code chunks and the row's scales.
-__global__ void __launch_bounds__(256) gather_rows_kernel(const uint8_t* __restrict__ codes,
-                                                          const float* __restrict__ scales, int64_t K,
-                                                          int top_k, int act_per_slot, Routing r, int E,
-                                                          uint8_t* __restrict__ gcodes, float* __restrict__ gscales) {
-  const int64_t rows = r.offsets[E];
+// One warp per routed row: its code bytes (16-byte chunks) and scales, in expert order.
+__global__ void __launch_bounds__(256) gather_kernel(const uint8_t* __restrict__ codes,
+                                                     const float* __restrict__ scales, int64_t K, int top_k,
+                                                     int act_per_slot, Routing r) {
+  grid_dep_wait();
+  grid_dep_launch();
+  const int64_t rows = r.hdr[3];
   const int64_t B = K / 32;
   const int lane = threadIdx.x & 31;
   const int64_t w0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -83,40 +153,29 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint8_t* __restr
     const int64_t pr = r.perm[i];
     const int64_t src = act_per_slot ? pr : pr / top_k;
     const uint4* s = reinterpret_cast<const uint4*>(codes + src * (K / 2));
-    uint4* d = reinterpret_cast<uint4*>(gcodes + i * (K / 2));
+    uint4* d = reinterpret_cast<uint4*>(r.gcodes + i * (K / 2));
     for (int64_t c = lane; c < B; c += 32) d[c] = s[c];
     const float* ss = scales + src * B;
-    float* ds = gscales + i * B;
+    float* ds = r.gscales + i * B;
     for (int64_t c = lane; c < B; c += 32) ds[c] = ss[c];
   }
 }
 
-}  // namespace
+size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
-#ifndef W4A4_ROUTED_TILE_MULT
-#define W4A4_ROUTED_TILE_MULT 2
-#endif
-int routed_tile_tokens(int64_t npairs, int E) {
-  // about one tile per expert: twice the mean number of rows an expert receives,
-  // in 32s, so that an expert a little above the mean still takes one tile (its
-  // weights are converted once per weight tile, not twice)
-  const int64_t mean = W4A4_ROUTED_TILE_MULT * ((npairs + E - 1) / E);
-  int64_t t = (mean + 31) & ~int64_t(31);
-  if (t < 32) t = 32;
-  if (t > kRoutedTileMax) t = kRoutedTileMax;
-  return static_cast<int>(t);
-}
+}  // namespace
 
 RoutingLayout routing_layout(int64_t npairs, int E, int64_t K) {
   RoutingLayout L{};
+  const int64_t max_seg = (npairs + kSegRows - 1) / kSegRows + E;
   size_t off = 0;
-  L.flag = off;     off += 16;  // first, so that a status query needs only the pointer
-  L.counts = off;   off += align16(sizeof(int32_t) * static_cast<size_t>(E));
-  L.offsets = off;  off += align16(sizeof(int32_t) * static_cast<size_t>(E + 1));
-  L.tile_off = off; off += align16(sizeof(int32_t) * static_cast<size_t>(E + 1));
-  L.perm = off;     off += align16(sizeof(int32_t) * static_cast<size_t>(npairs));
-  L.gcodes = off;   off += align16(static_cast<size_t>(npairs) * static_cast<size_t>(K / 2));
-  L.gscales = off;  off += align16(static_cast<size_t>(npairs) * static_cast<size_t>(K / 32) * sizeof(float));
+  L.hdr = off;       off += 16;  // flag first, so that a status query needs only the pointer
+  L.offsets = off;   off += align16(sizeof(int32_t) * static_cast<size_t>(E + 1));
+  L.segs = off;      off += align16(16 * static_cast<size_t>(max_seg));
+  L.seg_tiles = off; off += align16(sizeof(int32_t) * static_cast<size_t>(max_seg + 1));
+  L.perm = off;      off += align16(sizeof(int32_t) * static_cast<size_t>(npairs));
+  L.gcodes = off;    off += align16(static_cast<size_t>(npairs) * static_cast<size_t>(K / 2));
+  L.gscales = off;   off += align16(static_cast<size_t>(npairs) * static_cast<size_t>(K / 32) * sizeof(float));
   L.total = off;
   return L;
 }
@@ -125,13 +184,14 @@ Routing routing_in(void* ws, int64_t npairs, int E, int64_t K) {
   const RoutingLayout L = routing_layout(npairs, E, K);
   uint8_t* base = static_cast<uint8_t*>(ws);
   Routing r;
-  r.counts = reinterpret_cast<int32_t*>(base + L.counts);
+  r.hdr = reinterpret_cast<int32_t*>(base + L.hdr);
   r.offsets = reinterpret_cast<int32_t*>(base + L.offsets);
-  r.tile_off = reinterpret_cast<int32_t*>(base + L.tile_off);
+  r.segs = reinterpret_cast<int4*>(base + L.segs);
+  r.seg_tiles = reinterpret_cast<int32_t*>(base + L.seg_tiles);
   r.perm = reinterpret_cast<int32_t*>(base + L.perm);
-  r.flag = reinterpret_cast<int32_t*>(base + L.flag);
   r.gcodes = base + L.gcodes;
   r.gscales = reinterpret_cast<float*>(base + L.gscales);
+  r.rows = npairs;
   return r;
 }
 
@@ -158,24 +218,33 @@ cudaError_t id_static_scratch(void** addr) {
   return cudaSuccess;
 }
 
-cudaError_t launch_gemm_id(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums,
-                           const uint8_t* w_expanded, int E, int64_t N, const uint8_t* a_codes, const float* a_scales,
-                           int64_t K, const int32_t* ids, int64_t M, int top_k, int act_per_slot, float* y,
-                           const Routing& r, cudaStream_t stream) {
+cudaError_t launch_gemm_id(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums, int E,
+                           int64_t N, const uint8_t* a_codes, const float* a_scales, int64_t K, const int32_t* ids,
+                           int64_t M, int top_k, int act_per_slot, float* y, const Routing& r, cudaStream_t stream) {
   const int64_t npairs = M * top_k;
+  const int NT = static_cast<int>((N + 127) / 128);
   const size_t sh = sizeof(int32_t) * 2 * static_cast<size_t>(E);
-  const int tile = routed_tile_tokens(npairs, E);
-  route_prep_kernel<<<1, kPrepThreads, sh, stream>>>(ids, npairs, E, N, tile, y, r);
+  if (sh > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(sh));
+    if (e != cudaSuccess) return e;
+  }
+  route_kernel<<<1, kRouteThreads, sh, stream>>>(ids, npairs, E, N, NT, y, r);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int64_t gwarps = npairs < 4096 * 8 ? npairs : 4096 * 8;
-  gather_rows_kernel<<<static_cast<unsigned>((gwarps + 7) / 8), 256, 0, stream>>>(a_codes, a_scales, K, top_k,
-                                                                                 act_per_slot, r, E, r.gcodes,
-                                                                                 r.gscales);
-  e = cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  const int64_t gwarps = npairs < 8 * 1024 ? npairs : 8 * 1024;
+  cfg.gridDim = dim3(static_cast<unsigned>((gwarps + 7) / 8));
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, gather_kernel, a_codes, a_scales, K, top_k, act_per_slot, r);
   if (e != cudaSuccess) return e;
-  return launch_gemm_tc_routed(w_codes, w_scales, w_sums, w_expanded, E, N, r.gcodes, r.gscales, K, npairs, tile, y, r,
-                               stream);
+  return launch_gemm_grp_routed(w_codes, w_scales, w_sums, E, N, K, r, y, stream);
 }
 
 }  // namespace w4a4

@@ -1,10 +1,14 @@
-// Block-scaled W4A4 GEMM on the 5th-generation tensor cores (tcgen05, TMEM, TMA).
+// Block-scaled W4A4 GEMM on the 5th-generation tensor cores (tcgen05, TMEM, TMA),
+// the instance that converts both operands' codes in the kernel: the dense
+// product without the expanded activation operand, the exact integer partials,
+// and the two other routes (the exact path's int8 activations, the rotate-only
+// route's bf16 activations).  The dense product with the expanded activation
+// operand and the routed product run in the super-tile kernel (gemm_grp.cu).
 //
 // Engine docs "The lean option: ROCmFP4, ROCmI4 and Hadamard Q4_0", section
 // "Hadamard-rotated Q4_0: W4A4 prompt processing": int4 weights times int4
 // activations on the matrix units, weights read as plain Q4_0 (code q stands for
-// q - 8); section "MoE: W4A4 on the experts": the same product on the routed
-// expert matmuls (MUL_MAT_ID).
+// q - 8).
 //
 //   P[n][m][b] = sum_{j<32} (q_w - 8) q_a            exact, on the tensor cores
 //   Y[m][n]   += d_w[n][b] * d_a[m][b] * P[n][m][b]   fp32 fold on the CUDA cores
@@ -38,9 +42,12 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <mutex>
+
 
 #include <cuda_bf16.h>
 
+#include "tc_ptx.cuh"
 #include "w4a4_kernels.cuh"
 
 namespace w4a4 {
@@ -162,18 +169,14 @@ static_assert(sizeof(Smem<256, 4, true, true>) <= 227 * 1024, "shared memory per
 struct TcArgs {
   const uint16_t* w_scales;
   const int16_t* w_sums;  // per weight row and block: S_w = sum_j (q_w - 8)
-  const float* a_scales;  // dense: [M][B]; routed: gathered [npairs][B]
-  int64_t M;              // dense: token rows; routed: (token, slot) pairs
+  const float* a_scales;  // [M][B]
+  int64_t M;              // token rows
   int64_t N;              // output features (per expert)
   int64_t K;
   float* y;
   int64_t ldy;
   int32_t* P;
   int tt;                 // token tile (multiple of 32, <= the kernel's TTM): the A box height
-  const int32_t* perm;    // routed: gathered row -> pair index (the Y row)
-  const int32_t* offsets;
-  const int32_t* tile_off;
-  int E;
   // Stream-K schedule (dense product only): the tiles' K stages form one list of
   // sk_units units, cut into gridDim.x equal contiguous ranges.  0 = each CTA
   // takes whole tiles blockIdx.x, blockIdx.x + gridDim.x, ...
@@ -182,44 +185,7 @@ struct TcArgs {
   float4* sk_part;               // [2 * gridDim.x][8 warps][32][32 lanes] fp32 partials
 };
 
-// ------------------------------------------------------------------ PTX helpers
-__device__ __forceinline__ uint32_t su32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ uint64_t gtime() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(count));
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(su32(b)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// As mbar_try, but the thread may sleep (up to `ns` nanoseconds) until the phase
-// completes instead of spinning through issue slots.
-__device__ __forceinline__ bool mbar_try_sleep(uint64_t* b, uint32_t parity, uint32_t ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\nselp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(su32(b)), "r"(parity), "r"(ns)
-      : "memory");
-  return ok != 0;
-}
+// ------------------------------------------------------------------ bounded waits
 // Bounded wait on phase `parity`; false if it (or another role) gave up.
 template <class SM>
 __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, SM& S) {
@@ -234,15 +200,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, SM& S) {
       return false;
     }
   }
-}
-__device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n.reg .pred p;\nmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(su32(b)), "r"(parity)
-      : "memory");
-  return ok != 0;
 }
 // Bounded spinning wait for the MMA issuer, whose handoffs are on the critical
 // path: non-blocking tests, with the abort flag and the time bound checked every
@@ -263,116 +220,11 @@ __device__ __forceinline__ bool mbar_spin(uint64_t* b, uint32_t parity, SM& S) {
     }
   }
 }
-__device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* map, int32_t x, int32_t y, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-      ::"r"(su32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(su32(bar))
-      : "memory");
-}
-// 4D box (the expanded weights' map): coordinates {byte in chunk, row in group, chunk, group}.
-__device__ __forceinline__ void tma_4d(void* dst, const CUtensorMap* map, int32_t c0, int32_t c1, int32_t c2,
-                                       int32_t c3, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
-      "[%6];" ::"r"(su32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(su32(bar))
-      : "memory");
-}
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// K-major operand without swizzle: 8-row x 16-byte core matrices, the two
-// 16-byte halves of a 32-byte row 128 bytes apart (LBO), 8-row groups 256 bytes
-// apart (SBO); descriptor version 1 (bits 46-47).
-__device__ __forceinline__ uint64_t kmajor_desc(const void* smem) {
-  const uint32_t a = su32(smem);
-  return static_cast<uint64_t>((a >> 4) & 0x3FFFu) | (static_cast<uint64_t>(128 >> 4) << 16) |
-         (static_cast<uint64_t>(256 >> 4) << 32) | (static_cast<uint64_t>(1) << 46);
-}
-// kind::f8f6f4 instruction descriptor: D f32, A and B e4m3, both K-major, M = 128.
-__device__ __forceinline__ uint32_t f8_idesc(int n) {
-  return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(128 >> 4) << 24);
-}
-// kind::f16 with bf16 A and B (format code 1 in the A and B type fields).
-__device__ __forceinline__ uint32_t bf16_idesc(int n) { return f8_idesc(n) | (1u << 7) | (1u << 10); }
-__device__ __forceinline__ void mma_f8(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc) {
-  asm volatile(
-      "{\n.reg .pred p;\nsetp.ne.b32 p, 0, 0;\n"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
-      "l"(a), "l"(b), "r"(idesc));
-}
-// K-major operand of 16-bit elements: 8-row x 16-byte core matrices, K-adjacent
-// core matrices 128 bytes apart, 8-row groups `sbo` bytes apart.
-__device__ __forceinline__ uint64_t kmajor_desc_sbo(const void* smem, uint32_t sbo) {
-  const uint32_t a = su32(smem);
-  return static_cast<uint64_t>((a >> 4) & 0x3FFFu) | (static_cast<uint64_t>(128 >> 4) << 16) |
-         (static_cast<uint64_t>(sbo >> 4) << 32) | (static_cast<uint64_t>(1) << 46);
-}
-// kind::f16 MMA, f16 x f16 -> f32 (same instruction-descriptor layout as above:
-// format code 0 is f16 for this kind); accumulate into D when acc != 0.
-__device__ __forceinline__ void mma_f16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc));
-}
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(bar))
-               : "memory");
-}
-// 16 consecutive TMEM columns of this thread's lane; asynchronous until tmem_wait.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-}
-// Wait for this thread's outstanding TMEM loads.  The registers of the load in
-// flight are in/out operands, so no use of them can be scheduled above the wait.
-__device__ __forceinline__ void tmem_wait(uint32_t (&r)[16]) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;"
-               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
-                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
-                 "+r"(r[15])
-               :
-               : "memory");
-}
-// 32 consecutive TMEM columns of this thread's lane; asynchronous until a wait.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
-      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-}
-// Ties 16 registers to a preceding wait (an empty volatile statement: volatile
-// statements keep their order, so no use of them moves above the wait).
-__device__ __forceinline__ void tie16(uint32_t* r) {
-  asm volatile(""
-               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
-                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
-                 "+r"(r[15])
-               :
-               : "memory");
-}
-// Wait for this thread's TMEM loads into two 32-register buffers.
-__device__ __forceinline__ void tmem_wait32x2(uint32_t (&a)[32], uint32_t (&b)[32]) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-  tie16(a);
-  tie16(a + 16);
-  tie16(b);
-  tie16(b + 16);
-}
 // ------------------------------------------------------------------ tiles
 struct Tile {
   int64_t n0;     // first weight row of the tile within its expert
   int64_t wrow0;  // first weight row in the (stacked) weight tensor
-  int64_t m0;     // first token row (dense) or gathered row (routed)
+  int64_t m0;     // first token row
   int rows_w;     // valid weight rows (<= 128)
   int ntok;       // valid token rows (<= tt)
   int nmma;       // MMA N: ntok rounded up to 32
@@ -380,37 +232,20 @@ struct Tile {
 
 __device__ __forceinline__ int64_t num_tiles(const TcArgs& p) {
   const int64_t ntw = (p.N + TW - 1) / TW;
-  if (p.tile_off) return static_cast<int64_t>(p.tile_off[p.E]) * ntw;
   return ntw * ((p.M + p.tt - 1) / p.tt);
 }
 
+// Weight-tile major, so that consecutive CTAs share a weight tile in L2.
 __device__ __forceinline__ Tile decode_tile(const TcArgs& p, int64_t t) {
   Tile T;
-  const int64_t ntw = (p.N + TW - 1) / TW;
-  int64_t wt;
-  if (p.tile_off) {  // expert segments of the gathered rows, tt rows per tile
-    const int64_t mt = t / ntw;
-    wt = t - mt * ntw;
-    int lo = 0, hi = p.E - 1;  // last expert whose first tile is <= mt
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (p.tile_off[mid] <= mt) lo = mid; else hi = mid - 1;
-    }
-    T.m0 = p.offsets[lo] + (mt - p.tile_off[lo]) * p.tt;
-    const int64_t left = p.offsets[lo + 1] - T.m0;
-    T.ntok = static_cast<int>(left < p.tt ? left : p.tt);
-    T.wrow0 = static_cast<int64_t>(lo) * p.N;
-  } else {  // weight tile major, so consecutive CTAs share a weight tile in L2
-    const int64_t ntt = (p.M + p.tt - 1) / p.tt;
-    wt = t / ntt;
-    const int64_t tt = t - wt * ntt;
-    T.m0 = tt * p.tt;
-    const int64_t left = p.M - T.m0;
-    T.ntok = static_cast<int>(left < p.tt ? left : p.tt);
-    T.wrow0 = 0;
-  }
+  const int64_t ntt = (p.M + p.tt - 1) / p.tt;
+  const int64_t wt = t / ntt;
+  const int64_t tt = t - wt * ntt;
+  T.m0 = tt * p.tt;
+  const int64_t left = p.M - T.m0;
+  T.ntok = static_cast<int>(left < p.tt ? left : p.tt);
   T.n0 = wt * TW;
-  T.wrow0 += T.n0;
+  T.wrow0 = T.n0;
   const int64_t lw = p.N - T.n0;
   T.rows_w = static_cast<int>(lw < TW ? lw : TW);
   T.nmma = (T.ntok + 31) & ~31;
@@ -1183,12 +1018,10 @@ __device__ void workers(const TcArgs& p, SM& S, uint32_t tmem) {
               const float v0 = acc[i][j].x, v1 = acc[i][j].y;
               const int col = c * 32 + 2 * j;
               if (col < T.ntok) {
-                const int64_t row = p.perm ? static_cast<int64_t>(p.perm[T.m0 + col]) : T.m0 + col;
-                p.y[row * p.ldy + n] = v0;
+                p.y[(T.m0 + col) * p.ldy + n] = v0;
               }
               if (col + 1 < T.ntok) {
-                const int64_t row = p.perm ? static_cast<int64_t>(p.perm[T.m0 + col + 1]) : T.m0 + col + 1;
-                p.y[row * p.ldy + n] = v1;
+                p.y[(T.m0 + col + 1) * p.ldy + n] = v1;
               }
             }
           }
@@ -1425,9 +1258,11 @@ cudaError_t encode_2d_map(CUtensorMap* m, CUtensorMapDataType dtype, const void*
 }
 
 int* device_error_word() {
+  static std::mutex mu;
   static int* cached[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
   if (!cached[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_w4a4_device_error) != cudaSuccess) return nullptr;
@@ -1438,17 +1273,16 @@ int* device_error_word() {
 
 cudaError_t launch_gemm_tc(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums,
                            const uint8_t* w_expanded, int64_t N, const uint8_t* a_codes, const float* a_scales,
-                           const uint8_t* a_expanded, int64_t M, int64_t K, float* y, int64_t ldy, int32_t* P,
-                           void* ws, size_t ws_bytes, cudaStream_t stream) {
+                           int64_t M, int64_t K, float* y, int64_t ldy, int32_t* P, void* ws, size_t ws_bytes,
+                           cudaStream_t stream) {
   TcArgs a{};
   a.w_scales = w_scales; a.w_sums = w_sums; a.a_scales = a_scales;
   a.M = M; a.N = N; a.K = K; a.y = y; a.ldy = ldy; a.P = P;
   a.tt = token_tile(M, P ? 256 : kDenseTT);
   const bool wexp = w_expanded != nullptr && !P;
-  const bool aexp = wexp && a_expanded != nullptr;
   CUtensorMap wmap, amap;
   cudaError_t e = wexp ? expanded_map(&wmap, w_expanded, N, K, TW) : codes_map(&wmap, w_codes, N, K, TW);
-  if (e == cudaSuccess) e = aexp ? expanded_map(&amap, a_expanded, M, K, a.tt) : codes_map(&amap, a_codes, M, K, a.tt);
+  if (e == cudaSuccess) e = codes_map(&amap, a_codes, M, K, a.tt);
   if (e != cudaSuccess) return e;
   int64_t grid = ((N + TW - 1) / TW) * ((M + a.tt - 1) / a.tt);
   if (P) return launch_tc<true, 256>(wmap, amap, a, grid, stream);
@@ -1459,7 +1293,6 @@ cudaError_t launch_gemm_tc(const uint8_t* w_codes, const uint16_t* w_scales, con
     a.sk_part = reinterpret_cast<float4*>(static_cast<uint8_t*>(ws) + pl.count_bytes);
     grid = pl.grid;
   }
-  if (aexp) return launch_tc<false, kDenseTT, 4, true, true>(wmap, amap, a, grid, stream);
   if (wexp) return launch_tc<false, kDenseTT, 4, true>(wmap, amap, a, grid, stream);
   return launch_tc<false, kDenseTT>(wmap, amap, a, grid, stream);
 }
@@ -1514,27 +1347,6 @@ cudaError_t launch_gemm_w4a16(const uint8_t* w_codes, const uint16_t* w_scales, 
     grid = pl.grid;
   }
   return launch_tc<false, kW4A8TT, 16>(wmap, amap, a, grid, stream);
-}
-
-cudaError_t launch_gemm_tc_routed(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums,
-                                  const uint8_t* w_expanded, int E, int64_t N, const uint8_t* g_codes,
-                                  const float* g_scales, int64_t K, int64_t npairs, int tile_tokens, float* y,
-                                  const Routing& r, cudaStream_t stream) {
-  TcArgs a{};
-  a.w_scales = w_scales; a.w_sums = w_sums; a.a_scales = g_scales;
-  a.M = npairs; a.N = N; a.K = K; a.y = y; a.ldy = N;
-  a.tt = tile_tokens;
-  a.perm = r.perm; a.offsets = r.offsets; a.tile_off = r.tile_off; a.E = E;
-  // the expanded weights' 8-row groups must not straddle experts
-  const bool wexp = w_expanded != nullptr && N % 8 == 0;
-  CUtensorMap wmap, amap;
-  cudaError_t e = wexp ? expanded_map(&wmap, w_expanded, static_cast<int64_t>(E) * N, K, TW)
-                       : codes_map(&wmap, w_codes, static_cast<int64_t>(E) * N, K, TW);
-  if (e == cudaSuccess) e = codes_map(&amap, g_codes, npairs, K, a.tt);
-  if (e != cudaSuccess) return e;
-  const int64_t max_tiles = (npairs / tile_tokens + E) * ((N + TW - 1) / TW);
-  if (wexp) return launch_tc<false, kRoutedTileMax, 4, true>(wmap, amap, a, max_tiles, stream);
-  return launch_tc<false, kRoutedTileMax>(wmap, amap, a, max_tiles, stream);
 }
 
 cudaError_t read_and_clear_device_error(int* value) {

@@ -149,6 +149,48 @@ __global__ void __launch_bounds__(128) tcgen05_f8_probe(int iters, int* status) 
   if (tid < 32) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 256;" ::"r"(tmem));
 }
 
+
+// Lane layout of the 16x256b TMEM load, read back from a known pattern.  One CTA
+// of 4 warps allocates 32 columns; warp w writes its lane quarter with the
+// 32x32b store (thread t <-> lane 32w + t, register j <-> column j), the value
+// lane * 256 + column, then loads lanes 32w..32w+15 and 32w+16..32w+31 with
+// 16x256b.x1 and records the 4 + 4 registers of every thread: out[128][8].
+__global__ void __launch_bounds__(128) tmem_layout_probe(uint32_t* out) {
+  __shared__ uint32_t tmem_base;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 32;" ::"r"(smem_u32(&tmem_base)));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::);
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::);
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::);
+  const uint32_t tmem = tmem_base;
+  const uint32_t row = static_cast<uint32_t>(32 * warp + lane);
+  const uint32_t quarter = tmem + (static_cast<uint32_t>(32 * warp) << 16);
+  uint32_t v[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) v[j] = row * 256u + static_cast<uint32_t>(j);
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(quarter), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]));
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+  uint32_t a[4], b[4];
+  asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]) : "r"(quarter));
+  asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]) : "r"(quarter + (16u << 16)));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    out[tid * 8 + j] = a[j];
+    out[tid * 8 + 4 + j] = b[j];
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::);
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::);
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 32;" ::"r"(tmem));
+}
+
 template <typename F>
 double time_kernel(F launch) {
   cudaEvent_t e0, e1;
@@ -224,6 +266,20 @@ double w4a4_probe_tcgen05_f8(int iters) {
   if (s <= 0 || h != 0) return 0.0;
   const double flops = 2.0 * 128 * 256 * 32 * static_cast<double>(iters) * blocks;
   return flops / s;
+}
+
+
+// The 16x256b TMEM load's register layout: out (host, 128 x 8 words) receives,
+// per thread of 4 warps, the lane * 256 + column values of its 4 + 4 registers
+// (lanes 32w.. and 32w + 16.. of its warp's quarter).  0 on success.
+int w4a4_probe_tmem_layout(uint32_t* out) {
+  uint32_t* d = nullptr;
+  if (cudaMalloc(&d, 128 * 8 * sizeof(uint32_t)) != cudaSuccess) return 1;
+  tmem_layout_probe<<<1, 128>>>(d);
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(out, d, 128 * 8 * sizeof(uint32_t), cudaMemcpyDeviceToHost);
+  cudaFree(d);
+  return e == cudaSuccess ? 0 : 2;
 }
 
 }  // extern "C"

@@ -14,17 +14,18 @@ int num_sms();
 
 // Routing tables of one MUL_MAT_ID call, carved out of the caller's workspace.
 struct Routing {
-  int32_t* counts;    // [E]     (token, slot) pairs per expert
-  int32_t* offsets;   // [E + 1] exclusive prefix of counts
-  int32_t* tile_off;  // [E + 1] exclusive prefix of row tiles per expert
-  int32_t* perm;      // [M * top_k] pair indices p = t * top_k + s, grouped by expert
-  int32_t* flag;      // [1]     nonzero: some id was outside [0, E)
-  uint8_t* gcodes;    // [M * top_k][K/2] activation codes gathered in expert order
-  float* gscales;     // [M * top_k][K/32] their scales
+  int32_t* hdr;        // [4]: nonzero if some id was outside [0, E); segments; tiles; routed rows
+  int32_t* offsets;    // [E + 1] first gathered row of each expert
+  int4* segs;          // [segments] {first gathered row, expert, rows (<= 256), weight tiles per tile}
+  int32_t* seg_tiles;  // [segments + 1] first tile of each segment
+  int32_t* perm;       // [M * top_k] gathered row -> pair index t * top_k + s
+  uint8_t* gcodes;     // [M * top_k][K/2] activation codes gathered in expert order
+  float* gscales;      // [M * top_k][K/32] their scales
+  int64_t rows;        // capacity of the gathered arrays (M * top_k)
 };
 
 struct RoutingLayout {
-  size_t counts, offsets, tile_off, perm, flag, gcodes, gscales, total;
+  size_t hdr, offsets, segs, seg_tiles, perm, gcodes, gscales, total;
 };
 RoutingLayout routing_layout(int64_t npairs, int E, int64_t K);
 Routing routing_in(void* ws, int64_t npairs, int E, int64_t K);
@@ -54,16 +55,15 @@ cudaError_t launch_pack_q4_0_weighted(const void* w, int w_dtype, int64_t N, int
                                       uint8_t* expanded, cudaStream_t stream);
 cudaError_t launch_import_q4_0(const void* blocks, int64_t N, int64_t K, uint8_t* codes, uint16_t* scales,
                                int16_t* sums, uint8_t* expanded, cudaStream_t stream);
-// Dense product (P == nullptr) or exact partials (P != nullptr).  With a
-// workspace of at least gemm_workspace_bytes(M, N, K) bytes (16-byte aligned,
-// zero before its first use) the dense product may run a stream-K schedule.
-// w_expanded (optional, the dense product only): the pre-expanded weight operand;
-// a_expanded (optional, used together with w_expanded): the pre-expanded
-// activation operand ([round_up(M, 8)][K] offset-code bytes).
+// Dense product (P == nullptr) or exact partials (P != nullptr), both operands
+// from their codes.  With a workspace of at least gemm_workspace_bytes(M, N, K)
+// bytes (16-byte aligned, zero before its first use) the dense product may run a
+// stream-K schedule.  w_expanded (optional, the dense product only): the
+// pre-expanded weight operand.
 cudaError_t launch_gemm_tc(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums,
                            const uint8_t* w_expanded, int64_t N, const uint8_t* a_codes, const float* a_scales,
-                           const uint8_t* a_expanded, int64_t M, int64_t K, float* y, int64_t ldy, int32_t* P,
-                           void* ws, size_t ws_bytes, cudaStream_t stream);
+                           int64_t M, int64_t K, float* y, int64_t ldy, int32_t* P, void* ws, size_t ws_bytes,
+                           cudaStream_t stream);
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
 // The exact path (rotated Q4_0 weights x int8 activations, f16 tensor-core
 // MMAs): dense product (P == nullptr) or exact partials; workspace as above.
@@ -83,14 +83,20 @@ cudaError_t launch_gemm_w4a16(const uint8_t* w_codes, const uint16_t* w_scales, 
 // tensor-core kernel's whole-tile schedule.
 cudaError_t launch_gemm_small_m(const uint8_t* w_codes, const uint16_t* w_scales, int64_t N, const uint8_t* a_codes,
                                 const float* a_scales, int M, int64_t K, float* y, int64_t ldy, cudaStream_t stream);
-cudaError_t launch_gemm_tc_routed(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums,
-                                  const uint8_t* w_expanded, int E, int64_t N, const uint8_t* g_codes,
-                                  const float* g_scales, int64_t K, int64_t npairs, int tile_tokens, float* y,
-                                  const Routing& r, cudaStream_t stream);
-// Token rows per routed tile for a MUL_MAT_ID problem (multiple of 32, <= 256).
-// Largest token tile of the routed product (the GEMM instance it launches).
-constexpr int kRoutedTileMax = 128;
-int routed_tile_tokens(int64_t npairs, int E);
+// The super-tile GEMM (gemm_grp.cu).  Dense: expanded activations [round_up(M, 8)][K]
+// (offset-code bytes), optional expanded weights; workspace as for launch_gemm_tc,
+// of grp_workspace_bytes(M, N, K) bytes.  Routed: the gathered codes and work list
+// of `r`, weights as Q4_0 codes.
+cudaError_t launch_gemm_grp(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums,
+                            const uint8_t* w_expanded, int64_t N, const uint8_t* a_expanded, const float* a_scales,
+                            int64_t M, int64_t K, float* y, int64_t ldy, void* ws, size_t ws_bytes,
+                            cudaStream_t stream);
+size_t grp_workspace_bytes(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_gemm_grp_routed(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums,
+                                   int E, int64_t N, int64_t K, const Routing& r, float* y, cudaStream_t stream);
+// Test hook: the bound of the super-tile GEMM's pipeline waits (0 = the default
+// second) and a delay before its producer's first copy.
+void grp_set_wait_limit(uint64_t wait_ns, uint64_t producer_delay_ns);
 // Reads the GEMM kernels' device error word (bounded waits that gave up) and clears it.
 cudaError_t read_and_clear_device_error(int* value);
 // Device address of the error word the GEMM and activation kernels set when a
@@ -99,9 +105,8 @@ int* device_error_word();
 // 2D tiled TMA descriptor over `rows` rows of `inner` elements.
 cudaError_t encode_2d_map(CUtensorMap* m, CUtensorMapDataType dtype, const void* base, uint64_t inner, uint64_t rows,
                           uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swizzle);
-cudaError_t launch_gemm_id(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums,
-                           const uint8_t* w_expanded, int E, int64_t N, const uint8_t* a_codes, const float* a_scales,
-                           int64_t K, const int32_t* ids, int64_t M, int top_k, int act_per_slot, float* y,
-                           const Routing& r, cudaStream_t stream);
+cudaError_t launch_gemm_id(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums, int E,
+                           int64_t N, const uint8_t* a_codes, const float* a_scales, int64_t K, const int32_t* ids,
+                           int64_t M, int top_k, int act_per_slot, float* y, const Routing& r, cudaStream_t stream);
 
 }  // namespace w4a4

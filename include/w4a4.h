@@ -421,6 +421,19 @@ w4a4_status w4a4_gemm_id_static(const w4a4_q4_0* experts, int E, int64_t N, cons
  */
 w4a4_status w4a4_check(w4a4_stream_t stream);
 
+/*
+ * w4a4_debug_set_wait_limit -- a test hook for the bounded waits.  Later launches
+ * of the super-tile GEMM kernel (w4a4_gemm with the expanded activation operand,
+ * and w4a4_gemm_id) give up on a pipeline wait after wait_ns nanoseconds instead
+ * of one second, and their producer holds its first copy back for
+ * producer_delay_ns.  With a delay longer than the limit every CTA gives up: the
+ * kernel returns by itself, with its output incomplete, and w4a4_check reports
+ * W4A4_ERR_TIMEOUT.  (0, 0) restores the defaults.  Not synchronised with other
+ * host threads; for tests only.  The wind-down waits (copies in flight, MMAs in
+ * flight before TMEM is released) keep their one-second bound.
+ */
+void w4a4_debug_set_wait_limit(uint64_t wait_ns, uint64_t producer_delay_ns);
+
 /* The message of the last failed call on this thread ("" if none). */
 const char* w4a4_last_error(void);
 /* A fixed name for a status value. */

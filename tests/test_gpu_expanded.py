@@ -44,7 +44,7 @@ def _expanded_np(wq: w4.Q4_0Weights) -> np.ndarray:
 @pytest.mark.parametrize("N,K", [(8, 32), (13, 256), (130, 1024), (5, 5120)])
 def test_pack_writes_expanded_bytes(dev, N, K, rotate):
     d = si.random_dense(4, K, N, seed=N + K)
-    wq = w4.h32_q4_0_pack_weights(bf16_tensor(d["w_bf16"], dev), rotate=rotate)
+    wq = w4.h32_q4_0_pack_weights(bf16_tensor(d["w_bf16"], dev), rotate=rotate, expanded=True)
     ref = oracle.pack_weights(d["w_bf16"], rotate)
     assert np.array_equal(_expanded_np(wq), _expected_bytes(ref["q"].astype(np.int64)))
 
@@ -52,13 +52,13 @@ def test_pack_writes_expanded_bytes(dev, N, K, rotate):
 def test_weighted_pack_and_import_write_expanded_bytes(dev):
     d = si.random_dense(4, 512, 37, seed=5)
     imp = np.random.default_rng(6).uniform(0, 2, 512).astype(np.float32)
-    wq = w4.h32_q4_0_pack_weights_imatrix(bf16_tensor(d["w_bf16"], dev), f32_tensor(imp, dev))
+    wq = w4.h32_q4_0_pack_weights_imatrix(bf16_tensor(d["w_bf16"], dev), f32_tensor(imp, dev), expanded=True)
     torch.cuda.synchronize()
     q = oracle.unpack_nibbles(wq.codes.cpu().numpy()).astype(np.int64)
     assert np.array_equal(_expanded_np(wq), _expected_bytes(q))
     # import: canonical 18-byte blocks of the same weights
     blocks = oracle.q4_0_to_aos(wq.codes.cpu().numpy(), wq.scales.cpu().numpy())
-    wi = w4.q4_0_import(torch.from_numpy(np.ascontiguousarray(blocks).reshape(-1)).to(dev), 512)
+    wi = w4.q4_0_import(torch.from_numpy(np.ascontiguousarray(blocks).reshape(-1)).to(dev), 512, expanded=True)
     assert np.array_equal(_expanded_np(wi), _expected_bytes(q))
 
 
@@ -70,7 +70,7 @@ SHAPES = [(64, 256, 256), (1, 32, 1), (3, 64, 5), (129, 96, 130), (300, 1024, 52
 @pytest.mark.parametrize("stream_k", [True, False])
 def test_gemm_with_expanded_weights_is_bit_identical(dev, M, K, N, stream_k):
     d = si.random_dense(M, K, N, seed=3 * M + K + N)
-    wq = w4.h32_q4_0_pack_weights(bf16_tensor(d["w_bf16"], dev))
+    wq = w4.h32_q4_0_pack_weights(bf16_tensor(d["w_bf16"], dev), expanded=True)
     assert wq.expanded is not None
     a = w4.w4a4_rotate_quantize_act(f32_tensor(d["x"], dev))
     ws = True if stream_k else None
@@ -87,7 +87,7 @@ def test_gemm_expanded_on_a_row_slice(dev):
     """head(): a slice of the rows keeps the same expanded buffer (the 8-row groups
     past the slice are valid memory, their rows never stored)."""
     d = si.random_dense(40, 512, 300, seed=9)
-    wq = w4.h32_q4_0_pack_weights(bf16_tensor(d["w_bf16"], dev))
+    wq = w4.h32_q4_0_pack_weights(bf16_tensor(d["w_bf16"], dev), expanded=True)
     a = w4.w4a4_rotate_quantize_act(f32_tensor(d["x"], dev))
     y = w4.w4a4_gemm(wq.head(131), a)
     y_ref = w4.w4a4_gemm(wq, a)[:, :131]
@@ -99,7 +99,7 @@ def test_gemm_expanded_on_a_row_slice(dev):
 def test_gemm_expanded_full_size(dev, cfg):
     d = si.dense_inputs(cfg)
     s = d["shape"]
-    wq = w4.h32_q4_0_pack_weights(bf16_tensor(d["w_bf16"], dev))
+    wq = w4.h32_q4_0_pack_weights(bf16_tensor(d["w_bf16"], dev), expanded=True)
     a = w4.w4a4_rotate_quantize_act(f32_tensor(d["x"], dev))
     ws = torch.zeros(max(16, w4.w4a4_gemm_workspace_bytes(s.M, s.N, s.K)), dtype=torch.uint8, device=dev)
     y1 = w4.w4a4_gemm(wq, a, ws=ws)
@@ -114,7 +114,7 @@ def test_routed_gemm_with_expanded_weights_is_bit_identical(dev, name, act_per_s
     mi = si.moe_inputs(name, seed=4)
     s = mi["shape"]
     w, x, N = (mi["wd_bf16"], mi["x_down"], s.N_down) if act_per_slot else (mi["wg_bf16"], mi["x_gate"], s.N_gate)
-    wq = w4.h32_q4_0_pack_weights(bf16_tensor(w.reshape(s.E * N, -1), dev))
+    wq = w4.h32_q4_0_pack_weights(bf16_tensor(w.reshape(s.E * N, -1), dev), expanded=True)
     aq = w4.w4a4_rotate_quantize_act(f32_tensor(x, dev))
     ids = torch.from_numpy(np.ascontiguousarray(mi["ids"], dtype=np.int32)).to(dev)
     y1 = w4.w4a4_gemm_id(wq, s.E, aq, ids, s.top_k, act_per_slot)
@@ -157,7 +157,7 @@ ACT_SHAPES = [(64, 256, 256), (1, 32, 1), (3, 64, 5), (129, 96, 130), (300, 1024
 @pytest.mark.parametrize("stream_k", [True, False])
 def test_gemm_with_expanded_activations_is_bit_identical(dev, M, K, N, stream_k):
     d = si.random_dense(M, K, N, seed=5 * M + K + N)
-    wq = w4.h32_q4_0_pack_weights(bf16_tensor(d["w_bf16"], dev))
+    wq = w4.h32_q4_0_pack_weights(bf16_tensor(d["w_bf16"], dev), expanded=True)
     a = w4.w4a4_rotate_quantize_act(f32_tensor(d["x"], dev))
     assert a.expanded is not None and wq.expanded is not None
     ws = True if stream_k else None
@@ -173,7 +173,7 @@ def test_gemm_with_expanded_activations_is_bit_identical(dev, M, K, N, stream_k)
 def test_gemm_expanded_activations_on_a_row_slice(dev):
     """Act4.head(): the slice keeps the expanded buffer; rows past it are valid memory and never stored."""
     d = si.random_dense(300, 512, 96, seed=12)
-    wq = w4.h32_q4_0_pack_weights(bf16_tensor(d["w_bf16"], dev))
+    wq = w4.h32_q4_0_pack_weights(bf16_tensor(d["w_bf16"], dev), expanded=True)
     a = w4.w4a4_rotate_quantize_act(f32_tensor(d["x"], dev))
     y = w4.w4a4_gemm(wq, a.head(131))
     y_ref = w4.w4a4_gemm(wq, a)[:131]
@@ -185,7 +185,7 @@ def test_gemm_expanded_activations_on_a_row_slice(dev):
 def test_gemm_expanded_activations_full_size(dev, cfg):
     d = si.dense_inputs(cfg)
     s = d["shape"]
-    wq = w4.h32_q4_0_pack_weights(bf16_tensor(d["w_bf16"], dev))
+    wq = w4.h32_q4_0_pack_weights(bf16_tensor(d["w_bf16"], dev), expanded=True)
     a = w4.w4a4_rotate_quantize_act(f32_tensor(d["x"], dev))
     ws = torch.zeros(max(16, w4.w4a4_gemm_workspace_bytes(s.M, s.N, s.K)), dtype=torch.uint8, device=dev)
     y1 = w4.w4a4_gemm(wq, a, ws=ws)

@@ -62,6 +62,43 @@ def test_static_scratch_matches_workspace_variant(dev, name, act_per_slot):
     w4.w4a4_gemm_id_static(wq, s.E, aq, ids, s.top_k, act_per_slot, y1)
     w4.w4a4_gemm_id_static(wq, s.E, aq, ids, s.top_k, act_per_slot, y2)
     w4.w4a4_check()
-    ref = want.cpu().numpy()
-    assert_close(y1.cpu().numpy(), ref)
-    assert_close(y2.cpu().numpy(), ref)
+    # the same kernels on the same inputs: the results agree bit for bit
+    assert torch.equal(y1, want)
+    assert torch.equal(y2, want)
+
+
+@pytest.mark.gpu
+def test_static_scratch_zeroes_rows_of_bad_ids(dev):
+    """Ids outside [0, E) zero their output rows through the fixed scratch too, and
+    every other row is the workspace variant's, bit for bit; the call after it,
+    with good ids, is unaffected by what the bad call left in the scratch."""
+    import torch
+    from w4a4_testutil import bf16_tensor, f32_tensor
+
+    mi = si.moe_inputs("moe_tiny", seed=2)
+    s = mi["shape"]
+    wq = w4.h32_q4_0_pack_weights(bf16_tensor(mi["wg_bf16"].reshape(s.E * s.N_gate, -1), dev))
+    aq = w4.w4a4_rotate_quantize_act(f32_tensor(mi["x_gate"], dev))
+    bad = mi["ids"].astype(np.int32).copy()
+    bad[3, 1] = -1
+    bad[7, 0] = s.E
+    bad[0, s.top_k - 1] = 1 << 20
+    ids_bad = torch.from_numpy(bad).to(dev)
+    ids_good = torch.from_numpy(np.ascontiguousarray(mi["ids"], dtype=np.int32)).to(dev)
+
+    ws = torch.empty(w4.w4a4_gemm_id_workspace_bytes(s.M, s.top_k, s.E, s.K_gate), dtype=torch.uint8, device=dev)
+    want = w4.w4a4_gemm_id(wq, s.E, aq, ids_bad, s.top_k, False, ws=ws)
+    with pytest.raises(w4.W4A4Error):
+        w4.w4a4_gemm_id_status(ws)
+    y = torch.full((s.M, s.top_k, s.N_gate), float("nan"), device=dev)
+    w4.w4a4_gemm_id_static(wq, s.E, aq, ids_bad, s.top_k, False, y)
+    w4.w4a4_check()
+    mask = torch.from_numpy((bad < 0) | (bad >= s.E)).to(dev)
+    assert int(mask.sum()) == 3
+    assert torch.all(y[mask] == 0)
+    assert torch.equal(y, want)
+
+    y_good = torch.full((s.M, s.top_k, s.N_gate), float("nan"), device=dev)
+    w4.w4a4_gemm_id_static(wq, s.E, aq, ids_good, s.top_k, False, y_good)
+    w4.w4a4_check()
+    assert torch.equal(y_good, w4.w4a4_gemm_id(wq, s.E, aq, ids_good, s.top_k, False))
