@@ -30,12 +30,12 @@
 // token columns (2 of every 8).  A d_a value in shared memory then serves 4 rows
 // instead of 1, and a warp's d_a loads are 32 contiguous bytes (one wavefront).
 //
-// Warp roles (G = 1: 384 threads; G = 4: 512 threads):
+// Warp roles (512 threads; 384 with pre-expanded weights, which need no warps 12-15):
 //   warp 0         producer: TMA loads of each stage (4 blocks) into a 3-deep ring;
 //   warp 1         TMEM allocator and MMA issuer;
-//   warps 2-3      each stage's scales (d_a, d_w 2^18, -d_w 8 S_w) into a scale slot,
-//                  and (G = 1) the conversion of its operand codes;
-//   warps 12-15    (G = 4) the conversion of the operand codes, block by block;
+//   warps 2-3      publishers: each stage's scales (d_a, d_w 2^18, -d_w 8 S_w) into a
+//                  scale slot;
+//   warps 12-15    converters: the operand codes into the fp8 operand, block by block;
 //   warps 4-11     workers: the fold of each block, the epilogue.
 // Every pipeline wait is bounded; a wait that gives up sets the device error
 // word (read by w4a4_check) and the CTA winds down.
@@ -72,12 +72,14 @@ struct __align__(1024) GSmem {
   static_assert(AEXP || G == 4, "converted activations in the multi-tile instance only");
   static constexpr bool WX = WEXP;
   static constexpr bool AX = AEXP;
-  // helper warps (each publishes scales and converts operands): warps 2-3, and
-  // warps 12-15 in the multi-tile instance
-  static constexpr int HELP = G == 1 ? 2 : 6;
-  static constexpr int THREADS = G == 1 ? 384 : 512;
-  static constexpr int REGS_LOW = G == 1 ? 56 : 48;     // warpgroups 0 and 3
-  static constexpr int REGS_HIGH = G == 1 ? 224 : 208;  // warpgroups 1-2 (workers)
+  // helper warps (each publishes scales and converts operands): warps 2-3 and
+  // 12-15 (the pre-expanded-weight instance converts nothing: warps 2-3 only)
+  static constexpr int HELP = WEXP ? 2 : 6;
+  static constexpr int PUB = 2;            // publishers: warps 2-3
+  static constexpr int CONV = HELP - PUB;  // converters: warps 12-15
+  static constexpr int THREADS = WEXP ? 384 : 512;
+  static constexpr int REGS_LOW = WEXP ? 56 : 48;     // warpgroups 0 and 3
+  static constexpr int REGS_HIGH = WEXP ? 224 : 208;  // warpgroups 1-2 (workers)
   static constexpr int WSUB = WEXP ? 16384 : 8192;      // raw weight bytes per sub-tile and stage
   static constexpr int AROW = AEXP ? 128 : 64;          // raw activation bytes per row and stage
   // a stage holds cw activation rows then g weight sub-tiles, g * cw <= 256, g <= G
@@ -88,7 +90,9 @@ struct __align__(1024) GSmem {
   // scale slots (the workers free a slot after the stage's last block): the converters
   // may publish this many stages ahead of the fold
   static constexpr int NSC = G == 1 ? 4 : 2;
-  uint8_t raw[RAW][STAGE];   // [activation rows: cw x AROW bytes in 32-row TMA boxes][weights: g x WSUB]
+  // [activation rows: cw x AROW bytes in 32-row TMA boxes][weights: g x WSUB]; the
+  // expanded operands in the 128-byte swizzle, 1024-byte aligned atoms
+  uint8_t raw[RAW][STAGE];
   uint8_t f8[F8][F8B];
   float sda[NSC][KB][TCOLS];    // d_a per column, permuted (see col_slot)
   float sdw[NSC][KB][G][TW];    // d_w 2^18 per weight row, permuted (see row_slot)
@@ -279,8 +283,8 @@ __device__ __forceinline__ void load_weights(const GArgs& p, SM& S, const CUtens
                                              int slot) {
   uint8_t* wst = S.raw[slot] + T.cw * SM::AROW;
   for (int i = 0; i < T.g; ++i) {
-    if constexpr (SM::WX) {  // pre-expanded weights: the operand layout directly
-      tma_4d(wst, wmap, 0, 0, s * KB * 2, static_cast<int32_t>((T.wrow0 + i * TW) / 8), &S.full_raw[slot]);
+    if constexpr (SM::WX) {  // pre-expanded weights: 128 rows x 128 bytes, 128-byte swizzle
+      tma_2d(wst, wmap, s * KB * 32, static_cast<int32_t>(T.wrow0 + i * TW), &S.full_raw[slot]);
     } else {  // codes: 128 rows x 64 bytes, 64-byte swizzle
       tma_2d(wst + i * SM::WSUB, wmap, s * KB * 16, static_cast<int32_t>(T.wrow0 + i * TW), &S.full_raw[slot]);
     }
@@ -291,8 +295,8 @@ __device__ __forceinline__ void load_acts(const GArgs& p, SM& S, const CUtensorM
                                           int slot) {
   uint8_t* st = S.raw[slot];
   for (int j = 0; j < T.cw / 32; ++j) {
-    if constexpr (SM::AX) {  // expanded: 32-row boxes {16 B, 8 rows, 8 chunks, 4 groups} = [group][chunk][row][16 B]
-      tma_4d(st + j * 4096, amap, 0, 0, s * KB * 2, static_cast<int32_t>(T.a_row0 / 8) + 4 * j, &S.full_raw[slot]);
+    if constexpr (SM::AX) {  // expanded: 32 rows x 128 bytes, 128-byte swizzle
+      tma_2d(st + j * 4096, amap, s * KB * 32, static_cast<int32_t>(T.a_row0) + 32 * j, &S.full_raw[slot]);
     } else {  // codes: 32 rows x 64 bytes
       tma_2d(st + j * 2048, amap, s * KB * 16, static_cast<int32_t>(T.a_row0) + 32 * j, &S.full_raw[slot]);
     }
@@ -392,11 +396,11 @@ __device__ void mma_issuer(const GArgs& p, SM& S, uint32_t tmem) {
         if (!WX && !bspin(&S.f8_full[f], (gblk / SM::F8) & 1, S, p)) goto done;
         if (!bspin(&S.tm_empty[tb], ((gblk / NBUF) & 1) ^ 1, S, p)) goto done;
         tc_fence_after();
-        // activations: block kb of the raw stage (chunks 2kb, 2kb + 1; 8-row groups 1024 bytes
-        // apart) or the converted operand next to the weights (groups 256 bytes apart)
-        const uint64_t bdesc = SM::AX ? kmajor_desc_sbo(st + kb * 256, 1024) : kmajor_desc(S.f8[f] + SM::F8W);
+        // activations: block kb of the raw stage (bytes 32kb.. of each swizzled 128-byte
+        // row) or the converted operand next to the weights (8-row groups 256 bytes apart)
+        const uint64_t bdesc = SM::AX ? kmajor_desc_sw128(st + kb * 32) : kmajor_desc(S.f8[f] + SM::F8W);
         for (int i = 0; i < T.g; ++i) {
-          const uint64_t adesc = WX ? kmajor_desc_sbo(st + T.cw * SM::AROW + kb * 256, 1024)
+          const uint64_t adesc = WX ? kmajor_desc_sw128(st + T.cw * SM::AROW + kb * 32)
                                     : kmajor_desc(S.f8[f] + i * 4096);
           mma_f8(tmem + static_cast<uint32_t>(tb * TCOLS + i * T.cw), adesc, bdesc, idesc);
         }
@@ -429,43 +433,27 @@ __device__ __forceinline__ uint2 ld_h4(const uint16_t* row, int s, int B, bool v
   return make_uint2(v[0] | (v[1] << 16), v[2] | (v[3] << 16));
 }
 
-// One stage's scales (threads t of HT): loaded together (one round trip to L2
-// per stage) into registers, then stored into scale slot sc in the orders the
-// workers read -- d_a per column, d_w 2^18 and -d_w 8 S_w per weight row.
-template <class SM>
-struct StageScales {
-  static constexpr int HT = 32 * SM::HELP;
-  static constexpr int AR = (TCOLS + HT - 1) / HT;          // columns per helper thread
-  static constexpr int WR = (SM::F8W / 32 + HT - 1) / HT;   // weight rows per helper thread
-  uint4 av[AR];
-  uint2 dh[WR], sw[WR];
-
-  __device__ __forceinline__ void load(const GArgs& p, const Tile& T, int s, int t, bool vec) {
-    const int64_t B64 = p.K / 32;
-    const int B = static_cast<int>(B64);
-    const int cols = T.g * T.cw;
+// One stage's scales into scale slot sc, by the helper threads (t of HT), in two
+// phases of loads issued together (one round trip to L2 each): d_a per column,
+// then d_w 2^18 and -d_w 8 S_w per weight row, stored in the orders the workers
+// read.
+template <class SM, int HT>
+__device__ __forceinline__ void publish_scales(const GArgs& p, SM& S, const Tile& T, int s, int sc, int t, bool vec) {
+  constexpr int AR = (TCOLS + HT - 1) / HT;          // columns per helper thread
+  constexpr int WR = (SM::F8W / 32 + HT - 1) / HT;   // weight rows per helper thread
+  const int64_t B64 = p.K / 32;
+  const int B = static_cast<int>(B64);
+  const int nbk = min(KB, B - s * KB);
+  const int cols = T.g * T.cw;
+  {
+    uint4 av[AR];
 #pragma unroll
     for (int i = 0; i < AR; ++i) {
-      const int c = t + HT * i;
+      const int c = min(t + HT * i, TCOLS - 1);
       const int si = SM::G == 1 ? 0 : c / T.cw, jt = c - si * T.cw;
       const bool ok = c < cols && jt < T.ntok;
       av[i] = ld_f4(p.a_scales + (T.a_row0 + (ok ? jt : 0)) * B64, s, B, vec);
     }
-#pragma unroll
-    for (int i = 0; i < WR; ++i) {
-      const int r = min(t + HT * i, SM::F8W / 32 - 1);
-      const int si = r / TW, rr = r - si * TW;
-      const bool ok = si < T.g && T.n0 + si * TW + rr < p.N;
-      const int64_t row = T.wrow0 + (ok ? si * TW + rr : 0);
-      dh[i] = ld_h4(p.w_scales + row * B64, s, B, vec);
-      sw[i] = ld_h4(reinterpret_cast<const uint16_t*>(p.w_sums) + row * B64, s, B, vec);
-    }
-  }
-
-  __device__ __forceinline__ void store(const GArgs& p, SM& S, const Tile& T, int s, int sc, int t) const {
-    const int B = static_cast<int>(p.K / 32);
-    const int nbk = min(KB, B - s * KB);
-    const int cols = T.g * T.cw;
 #pragma unroll
     for (int i = 0; i < AR; ++i) {
       const int c = t + HT * i;
@@ -478,10 +466,25 @@ struct StageScales {
         for (int kk = 0; kk < KB; ++kk) S.sda[sc][kk][cs] = (ok && kk < nbk) ? __uint_as_float(w4[kk]) : 0.f;
       }
     }
+  }
+  // weight rows in batches of at most 4 per thread (the loads of a batch go out together)
+  constexpr int RB = WR < 4 ? WR : 4;
 #pragma unroll
-    for (int i = 0; i < WR; ++i) {
-      const int r = t + HT * i;
-      if (r < SM::F8W / 32) {
+  for (int i0 = 0; i0 < WR; i0 += RB) {
+    uint2 dh[RB], sw[RB];
+#pragma unroll
+    for (int i = 0; i < RB; ++i) {
+      const int r = min(t + HT * (i0 + i), SM::F8W / 32 - 1);
+      const int si = r / TW, rr = r - si * TW;
+      const bool ok = si < T.g && T.n0 + si * TW + rr < p.N;
+      const int64_t row = T.wrow0 + (ok ? si * TW + rr : 0);
+      dh[i] = ld_h4(p.w_scales + row * B64, s, B, vec);
+      sw[i] = ld_h4(reinterpret_cast<const uint16_t*>(p.w_sums) + row * B64, s, B, vec);
+    }
+#pragma unroll
+    for (int i = 0; i < RB; ++i) {
+      const int r = t + HT * (i0 + i);
+      if (i0 + i < WR && r < SM::F8W / 32) {
         const int si = r / TW, rr = r - si * TW;
         const bool ok = si < T.g && T.n0 + si * TW + rr < p.N;
         const int rs = row_slot(rr);
@@ -500,20 +503,18 @@ struct StageScales {
       }
     }
   }
-};
+}
 
-// The helper warps (2-3, and 12-15 in the G = 4 instance), stage by stage: the
-// stage's scale loads go out first; the scales are published (once the workers
-// have freed the slot) before the conversion in the G = 1 instance, whose 8
-// operand slots and 4 scale slots let the helpers run ahead, and after the
-// stage's third block is converted in the G = 4 instance, whose 3 operand slots
-// keep the helpers less than a stage ahead (the load latency then hides behind
-// the conversion, and the fold of the stage's first block does not wait for the
-// rest of the stage).
+// The helper warps, in two roles that run side by side.  Publishers (warps 2-3),
+// stage by stage: once the workers have freed the scale slot, the stage's scale
+// loads go out together (one round trip to L2) and the scales are published; the
+// scale slots (4, or 2 in the G = 4 instance) let them run ahead of the fold.
+// Converters (warps 12-15; none with pre-expanded weights), block by block: the
+// stage's operand codes into an operand slot (8, or 3) ahead of the MMA.  Apart,
+// the publishers' load latency does not hold up the conversion.
 template <class SM>
-__device__ void helpers(const GArgs& p, SM& S, int t) {
-  constexpr int HT = 32 * SM::HELP;
-  constexpr int PUB_AFTER = SM::G == 1 ? -1 : 2;  // publish after converting this block (-1: before)
+__device__ void publishers(const GArgs& p, SM& S, int t) {
+  constexpr int HT = 32 * SM::PUB;
   const int lane = threadIdx.x & 31;
   const int B = static_cast<int>(p.K / 32);
   const int nst = (B + KB - 1) / KB;
@@ -522,72 +523,79 @@ __device__ void helpers(const GArgs& p, SM& S, int t) {
                    (reinterpret_cast<uintptr_t>(p.w_sums) & 7) == 0;
   grid_dep_wait();
   const int64_t ntiles = num_tiles(p);
-  uint32_t gst = 0, gblk = 0;
+  uint32_t gst = 0;
   int64_t next = seg_start(p);
   Seg sg;
   while (seg_next(p, nst, ntiles, next, sg)) {
     const Tile T = tile_at(p, sg.t);
     for (int s = sg.s0; s < sg.s1; ++s, ++gst) {
       const int sc = gst % SM::NSC;
+      if (!bwait(&S.sc_free[sc], ((gst / SM::NSC) & 1) ^ 1, S, p)) return;
+      publish_scales<SM, HT>(p, S, T, s, sc, t, vec);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.sc_ready[sc]);
+    }
+  }
+}
+
+template <class SM>
+__device__ void converters(const GArgs& p, SM& S, int t) {
+  constexpr int HT = 32 * SM::CONV;
+  const int lane = threadIdx.x & 31;
+  const int B = static_cast<int>(p.K / 32);
+  const int nst = (B + KB - 1) / KB;
+  grid_dep_wait();
+  const int64_t ntiles = num_tiles(p);
+  uint32_t gst = 0, gblk = 0;
+  int64_t next = seg_start(p);
+  Seg sg;
+  while (seg_next(p, nst, ntiles, next, sg)) {
+    const Tile T = tile_at(p, sg.t);
+    for (int s = sg.s0; s < sg.s1; ++s, ++gst) {
       const int nbk = min(KB, B - s * KB);
-      StageScales<SM> sv;
-      sv.load(p, T, s, t, vec);
-      auto publish = [&]() -> bool {
-        if (!bwait(&S.sc_free[sc], ((gst / SM::NSC) & 1) ^ 1, S, p)) return false;
-        sv.store(p, S, T, s, sc, t);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&S.sc_ready[sc]);
-        return true;
-      };
-      if (PUB_AFTER < 0 || SM::WX) {
-        if (!publish()) return;
-      }
-      if constexpr (!SM::WX) {
-        const int slot = gst % RAW;
-        if (!bwait(&S.full_raw[slot], (gst / RAW) & 1, S, p)) return;
-        const uint8_t* ast = S.raw[slot];
-        const uint8_t* wst = ast + T.cw * SM::AROW;
-        const int rows = T.g * TW;
-        for (int kb = 0; kb < nbk; ++kb, ++gblk) {
-          const int f = gblk % SM::F8;
-          if (!bwait(&S.f8_empty[f], ((gblk / SM::F8) & 1) ^ 1, S, p)) return;
+      const int slot = gst % RAW;
+      if (!bwait(&S.full_raw[slot], (gst / RAW) & 1, S, p)) return;
+      const uint8_t* ast = S.raw[slot];
+      const uint8_t* wst = ast + T.cw * SM::AROW;
+      const int rows = T.g * TW;
+      for (int kb = 0; kb < nbk; ++kb, ++gblk) {
+        const int f = gblk % SM::F8;
+        if (!bwait(&S.f8_empty[f], ((gblk / SM::F8) & 1) ^ 1, S, p)) return;
 #pragma unroll 1
-          for (int r = t; r < rows; r += HT) {
-            const int si = r >> 7, rr = r & (TW - 1);
-            // 64-byte swizzle of the TMA box: 16-byte chunk kb of row rr sits at kb ^ ((rr >> 1) & 3)
-            const uint4 raw =
-                *reinterpret_cast<const uint4*>(wst + si * SM::WSUB + rr * 64 + 16 * (kb ^ ((rr >> 1) & 3)));
-            uint32_t l0, h0, l1, h1, l2, h2, l3, h3;
-            q4_0_word_to_e4m3(raw.x, l0, h0);
-            q4_0_word_to_e4m3(raw.y, l1, h1);
-            q4_0_word_to_e4m3(raw.z, l2, h2);
-            q4_0_word_to_e4m3(raw.w, l3, h3);
-            uint8_t* d = S.f8[f] + si * 4096 + (rr >> 3) * 256 + (rr & 7) * 16;
-            *reinterpret_cast<uint4*>(d) = make_uint4(l0, l1, l2, l3);        // elements 0-15
-            *reinterpret_cast<uint4*>(d + 128) = make_uint4(h0, h1, h2, h3);  // elements 16-31
-          }
-          if constexpr (!SM::AX) {
-            // activations: the offset codes a + 8 (nibble ^ 8) spread to bytes, the e4m3 operand
-#pragma unroll 1
-            for (int r = t; r < T.cw; r += HT) {
-              const uint4 raw = *reinterpret_cast<const uint4*>(ast + r * 64 + 16 * kb);
-              const uint32_t x0 = raw.x ^ 0x88888888u, x1 = raw.y ^ 0x88888888u;
-              const uint32_t x2 = raw.z ^ 0x88888888u, x3 = raw.w ^ 0x88888888u;
-              uint8_t* d = S.f8[f] + SM::F8W + (r >> 3) * 256 + (r & 7) * 16;
-              *reinterpret_cast<uint4*>(d) =
-                  make_uint4(x0 & 0x0F0F0F0Fu, x1 & 0x0F0F0F0Fu, x2 & 0x0F0F0F0Fu, x3 & 0x0F0F0F0Fu);
-              *reinterpret_cast<uint4*>(d + 128) = make_uint4((x0 >> 4) & 0x0F0F0F0Fu, (x1 >> 4) & 0x0F0F0F0Fu,
-                                                              (x2 >> 4) & 0x0F0F0F0Fu, (x3 >> 4) & 0x0F0F0F0Fu);
-            }
-          }
-          fence_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&S.f8_full[f]);
-          if (PUB_AFTER >= 0 && kb == min(PUB_AFTER, nbk - 1) && !publish()) return;
+        for (int r = t; r < rows; r += HT) {
+          const int si = r >> 7, rr = r & (TW - 1);
+          // 64-byte swizzle of the TMA box: 16-byte chunk kb of row rr sits at kb ^ ((rr >> 1) & 3)
+          const uint4 raw =
+              *reinterpret_cast<const uint4*>(wst + si * SM::WSUB + rr * 64 + 16 * (kb ^ ((rr >> 1) & 3)));
+          uint32_t l0, h0, l1, h1, l2, h2, l3, h3;
+          q4_0_word_to_e4m3(raw.x, l0, h0);
+          q4_0_word_to_e4m3(raw.y, l1, h1);
+          q4_0_word_to_e4m3(raw.z, l2, h2);
+          q4_0_word_to_e4m3(raw.w, l3, h3);
+          uint8_t* d = S.f8[f] + si * 4096 + (rr >> 3) * 256 + (rr & 7) * 16;
+          *reinterpret_cast<uint4*>(d) = make_uint4(l0, l1, l2, l3);        // elements 0-15
+          *reinterpret_cast<uint4*>(d + 128) = make_uint4(h0, h1, h2, h3);  // elements 16-31
         }
+        if constexpr (!SM::AX) {
+          // activations: the offset codes a + 8 (nibble ^ 8) spread to bytes, the e4m3 operand
+#pragma unroll 1
+          for (int r = t; r < T.cw; r += HT) {
+            const uint4 raw = *reinterpret_cast<const uint4*>(ast + r * 64 + 16 * kb);
+            const uint32_t x0 = raw.x ^ 0x88888888u, x1 = raw.y ^ 0x88888888u;
+            const uint32_t x2 = raw.z ^ 0x88888888u, x3 = raw.w ^ 0x88888888u;
+            uint8_t* d = S.f8[f] + SM::F8W + (r >> 3) * 256 + (r & 7) * 16;
+            *reinterpret_cast<uint4*>(d) =
+                make_uint4(x0 & 0x0F0F0F0Fu, x1 & 0x0F0F0F0Fu, x2 & 0x0F0F0F0Fu, x3 & 0x0F0F0F0Fu);
+            *reinterpret_cast<uint4*>(d + 128) = make_uint4((x0 >> 4) & 0x0F0F0F0Fu, (x1 >> 4) & 0x0F0F0F0Fu,
+                                                            (x2 >> 4) & 0x0F0F0F0Fu, (x3 >> 4) & 0x0F0F0F0Fu);
+          }
+        }
+        fence_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&S.empty_raw[slot]);  // the raw codes are converted
+        if (lane == 0) mbar_arrive(&S.f8_full[f]);
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.empty_raw[slot]);  // the raw codes are converted
     }
   }
 }
@@ -824,11 +832,11 @@ __global__ void __launch_bounds__(GSmem<G, WEXP, AEXP>::THREADS, 1)
     for (int i = 0; i < RAW; ++i) {
       mbar_init(&S.full_raw[i], 1);
       // the converters' arrivals once the codes are converted, and the MMA's commit
-      mbar_init(&S.empty_raw[i], (WEXP ? 0 : SM::HELP) + 1);
+      mbar_init(&S.empty_raw[i], SM::CONV + 1);
     }
     if constexpr (!WEXP) {  // (pre-expanded weights: no operand slots in use)
       for (int i = 0; i < SM::F8; ++i) {
-        mbar_init(&S.f8_full[i], SM::HELP);
+        mbar_init(&S.f8_full[i], SM::CONV);
         mbar_init(&S.f8_empty[i], 1);
       }
     }
@@ -837,7 +845,7 @@ __global__ void __launch_bounds__(GSmem<G, WEXP, AEXP>::THREADS, 1)
       mbar_init(&S.tm_empty[i], kWorkers);
     }
     for (int i = 0; i < SM::NSC; ++i) {
-      mbar_init(&S.sc_ready[i], SM::HELP);
+      mbar_init(&S.sc_ready[i], SM::PUB);
       mbar_init(&S.sc_free[i], kWorkers);
     }
     mbar_init(&S.mma_done, 1);
@@ -865,8 +873,10 @@ __global__ void __launch_bounds__(GSmem<G, WEXP, AEXP>::THREADS, 1)
     } else if (warp == 1) {
       if ((threadIdx.x & 31) == 0) mma_issuer(p, S, tmem);
       __syncwarp();
-    } else {  // helpers: warps 2-3 (threads 0-63), and warps 12-15 (threads 64-191)
-      helpers(p, S, warp < 4 ? threadIdx.x - 64 : 64 + threadIdx.x - 384);
+    } else if (warp < 4) {  // publishers: warps 2-3
+      publishers(p, S, threadIdx.x - 64);
+    } else {  // converters: warps 12-15
+      converters(p, S, threadIdx.x - 384);
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(SM::REGS_HIGH));
@@ -910,18 +920,18 @@ cudaError_t codes_map_sw64(CUtensorMap* m, const uint8_t* codes, int64_t rows, i
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// Expanded operand bytes [rows8][K] as {16 B, 8 rows, K/16 chunks, row groups}:
-// a box of 8 chunks x box_groups groups lands as [group][chunk][row][16 B].
-cudaError_t expanded_map4(CUtensorMap* m, const uint8_t* x, int64_t rows, int64_t K, int box_groups) {
+// Expanded operand bytes [rows][K]: box 128 bytes (one stage of 4 blocks) x
+// box_rows rows, 128-byte swizzle (the MMA's K-major swizzled layout).  Rows past
+// `rows` read as zero.
+cudaError_t expanded_map_sw128(CUtensorMap* m, const uint8_t* x, int64_t rows, int64_t K, int box_rows) {
   auto fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
-  const int64_t groups = (rows + 7) / 8;
-  const cuuint64_t dims[4] = {16, 8, static_cast<cuuint64_t>(K / 16), static_cast<cuuint64_t>(groups)};
-  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(K), 16, static_cast<cuuint64_t>(8 * K)};
-  const cuuint32_t box[4] = {16, 8, static_cast<cuuint32_t>(KB * 2), static_cast<cuuint32_t>(box_groups)};
-  const cuuint32_t estr[4] = {1, 1, 1, 1};
-  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<uint8_t*>(x), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(KB * 32), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(x), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
@@ -1054,8 +1064,8 @@ cudaError_t launch_gemm_grp(const uint8_t* w_codes, const uint16_t* w_scales, co
   }
   const bool wexp = w_expanded != nullptr && pl.g == 1;
   CUtensorMap wmap, amap;
-  cudaError_t e = wexp ? expanded_map4(&wmap, w_expanded, N, K, TW / 8) : codes_map_sw64(&wmap, w_codes, N, K);
-  if (e == cudaSuccess) e = expanded_map4(&amap, a_expanded, M, K, 4);
+  cudaError_t e = wexp ? expanded_map_sw128(&wmap, w_expanded, N, K, TW) : codes_map_sw64(&wmap, w_codes, N, K);
+  if (e == cudaSuccess) e = expanded_map_sw128(&amap, a_expanded, M, K, 32);
   if (e != cudaSuccess) return e;
   if (pl.g > 1) return launch_grp<4, false, true>(wmap, amap, a, grid, stream);
   if (wexp) return launch_grp<1, true, true>(wmap, amap, a, grid, stream);

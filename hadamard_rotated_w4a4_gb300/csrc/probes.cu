@@ -9,6 +9,8 @@
 #include <cstdio>
 #include <cuda_runtime.h>
 
+#include "tc_ptx.cuh"
+
 namespace {
 
 constexpr int kChains = 8;
@@ -191,6 +193,335 @@ __global__ void __launch_bounds__(128) tmem_layout_probe(uint32_t* out) {
   if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 32;" ::"r"(tmem));
 }
 
+
+// Latency of one tcgen05.mma kind::f8f6f4 (M = 128, K = 32), issue to the
+// completion its commit signals, in clock64 cycles: thread 0 issues it on zero
+// operands (K-major, no swizzle, 8-row groups `sbo` bytes apart) and spins on the
+// mbarrier.  Meanwhile warps 1-8 (`loaders` bit 0) stream 16x256b TMEM loads from
+// the other 256 columns, as a fold would, and (bit 1) 16-byte shared-memory loads.
+// out[rep] for 32 repetitions.
+__global__ void __launch_bounds__(288) mma_latency_probe(int n, int sbo, int loaders, unsigned long long* out,
+                                                         int* status, const uint8_t* gsrc, int64_t gbytes) {
+  extern __shared__ __align__(1024) uint8_t dyn[];
+  uint8_t* a_s = dyn;                // 16 groups x sbo bytes
+  uint8_t* b_s = dyn + 16 * 1024;    // 32 groups x sbo bytes
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ __align__(8) uint64_t cbar;
+  __shared__ __align__(8) uint64_t bar2;
+  __shared__ uint32_t tmem_base;
+  __shared__ volatile int stop;
+  __shared__ volatile int ack;
+  __shared__ volatile unsigned long long t_obs;
+  uint8_t* c_s = dyn + 48 * 1024;  // bulk-copy destination, 48 KB
+  const int tid = threadIdx.x, warp = tid >> 5;
+  // operands: zero (fill 0) or a pattern of nonzero e4m3 values (fill 1: bytes 0x01..0x0F and 0x81..0x8F)
+  for (int i = tid; i < (16 + 32) * 1024 / 4; i += blockDim.x) {
+    const uint32_t h = static_cast<uint32_t>(i) * 2654435761u;
+    reinterpret_cast<uint32_t*>(dyn)[i] = (loaders & 4) ? ((h & 0x0F0F0F0Fu) | 0x01010101u) | (h & 0x80808080u) : 0u;
+  }
+  if (tid == 0) {
+    stop = 0;
+    ack = 0;
+    t_obs = 0;
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar)));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&cbar)));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar2)));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::);
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::);
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(&tmem_base)));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::);
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::);
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::);
+  const uint32_t tmem = tmem_base;
+  const uint32_t idesc = (1u << 4) | ((static_cast<uint32_t>(n) >> 3) << 17) | ((128u >> 4) << 24);
+  const uint64_t adesc = desc_kmajor_noswizzle(smem_u32(a_s), 128, sbo);
+  const uint64_t bdesc = desc_kmajor_noswizzle(smem_u32(b_s), 128, sbo);
+  if (warp == 0) {
+    if (tid == 0) {
+      int bad = 0;
+      for (int rep = 0; rep < 32; ++rep) {
+        unsigned long long t0, t1;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        asm volatile("mov.u64 %0, %%clock64;" : "=l"(t0));
+        asm volatile(
+            "{\n.reg .pred p;\nsetp.ne.b32 p, 0, 0;\n"
+            "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc));
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(&bar)));
+        uint32_t done = 0;
+        const uint32_t parity = rep & 1;
+        if (loaders & 16) {  // warp 1 observes the completion; this thread waits for its word
+          if (loaders & 32) {  // first 3000 cycles of plain busy work
+            unsigned long long tb;
+            do {
+              asm volatile("mov.u64 %0, %%clock64;" : "=l"(tb));
+            } while (tb - t0 < 3000);
+          }
+          if (loaders & 64) {  // wait on a second barrier that the observer arrives on
+            for (long spin = 0; !done && spin < 100000000L; ++spin) {
+              if (loaders & 128)
+                asm volatile(
+                    "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, "
+                    "p;\n}\n"
+                    : "=r"(done) : "r"(smem_u32(&bar2)), "r"(parity) : "memory");
+              else
+                asm volatile(
+                    "{\n.reg .pred p;\nmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, "
+                    "p;\n}\n"
+                    : "=r"(done) : "r"(smem_u32(&bar2)), "r"(parity) : "memory");
+            }
+          } else {
+            for (long spin = 0; !done && spin < 100000000L; ++spin) done = ack == rep + 1;
+          }
+          t1 = t_obs;
+        } else {
+          for (long spin = 0; !done && spin < 100000000L; ++spin) {
+            asm volatile(
+                "{\n.reg .pred p;\nmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+                : "=r"(done) : "r"(smem_u32(&bar)), "r"(parity));
+          }
+          asm volatile("mov.u64 %0, %%clock64;" : "=l"(t1));
+        }
+        if (!done) bad = 1;
+        out[rep] = t1 - t0;
+        if (bad) break;
+      }
+      if (bad) atomicExch(status, 1);
+      stop = 1;
+    }
+    __syncwarp();
+  } else if ((loaders & 16) && warp == 1) {  // the completion observer
+    if ((tid & 31) == 0) {
+      for (int rep = 0; rep < 32 && !stop; ++rep) {
+        uint32_t done = 0;
+        for (long spin = 0; !done && spin < 100000000L; ++spin)
+          asm volatile(
+              "{\n.reg .pred p;\nmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+              : "=r"(done) : "r"(smem_u32(&bar)), "r"(static_cast<uint32_t>(rep & 1)));
+        unsigned long long t;
+        asm volatile("mov.u64 %0, %%clock64;" : "=l"(t));
+        t_obs = t;
+        __threadfence_block();
+        if (loaders & 64)
+          asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&bar2)) : "memory");
+        else
+          ack = rep + 1;
+        if (!done) break;
+      }
+    }
+    __syncwarp();
+  } else if ((loaders & 8) && warp == 8) {  // warp 8: 48 KB bulk copies from global memory, back to back
+    if ((tid & 31) == 0) {
+      int64_t off = 0;
+      for (long it = 0; !stop && it < 1000000L; ++it) {
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(&cbar)), "r"(48 * 1024)
+                     : "memory");
+        for (int c = 0; c < 3; ++c)
+          asm volatile(
+              "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                  smem_u32(c_s + c * 16384)),
+              "l"(gsrc + off + c * 16384), "r"(16384), "r"(smem_u32(&cbar))
+              : "memory");
+        off = (off + 48 * 1024) % (gbytes - 48 * 1024);
+        uint32_t done = 0;
+        for (long spin = 0; !done && spin < 100000000L; ++spin)
+          asm volatile(
+              "{\n.reg .pred p;\nmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+              : "=r"(done) : "r"(smem_u32(&cbar)), "r"(static_cast<uint32_t>(it & 1)));
+      }
+    }
+    __syncwarp();
+  } else if (loaders & 3) {  // warps 1-8: TMEM loads from columns 256.. of their lane quarter, and/or shared loads
+    const uint32_t quarter = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + 256u;
+    uint32_t acc = 0;
+    for (long it = 0; !stop && it < 100000000L; ++it) {
+      if (loaders & 1) {
+        uint32_t r[16];
+        const uint32_t col = static_cast<uint32_t>((it & 7) * 32);
+        asm volatile(
+            "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+              "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+            : "r"(quarter + col));
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        for (int j = 0; j < 16; ++j) acc += r[j];
+      }
+      if (loaders & 2) {
+        uint32_t v0, v1, v2, v3;
+        asm volatile("ld.volatile.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(v0), "=r"(v1), "=r"(v2), "=r"(v3)
+                     : "r"(smem_u32(dyn + ((tid * 16 + it * 512) & (48 * 1024 - 1)))));
+        acc += v0 + v3;
+      }
+    }
+    if (acc == 12345u) out[40] = acc;
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::);
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::);
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem));
+}
+
+
+// Issue rate of back-to-back fp8 MMAs from one thread: `iters` MMAs of M 128, N n,
+// K 32, a commit after every `per_commit` of them; the clock after each issue.
+// flags bit 0: alternate two 256-column TMEM buffers; bit 1: warps 1-8 run a
+// fused multiply-add loop meanwhile (paired fp32, as the fold does); bit 2:
+// accumulate into D (from the third MMA on); bit 3: no clock reads between issues;
+// bit 4: zero operands; bit 5: every operand byte 0x01; bit 6: one CTA per SM
+// (block 0 timed); bit 7: 256 TMEM columns (the two buffers 128 apart); bit 8:
+// 128-byte swizzled operands; bit 9: unswizzled, 8-row groups 1024 bytes apart.
+__global__ void __launch_bounds__(288) mma_rate_probe(int n, int per_commit, int iters, int flags,
+                                                      unsigned long long* out, int* status) {
+  extern __shared__ __align__(1024) uint8_t dyn[];
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t tmem_base;
+  __shared__ volatile int stop;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  for (int i = tid; i < 48 * 1024 / 4; i += blockDim.x)
+    reinterpret_cast<uint32_t*>(dyn)[i] = (flags & 16) ? 0u : (flags & 32) ? 0x01010101u : 0x01020304u;
+  if (tid == 0) {
+    stop = 0;
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar)));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::);
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::);
+  if (warp == 0) {
+    if (flags & 128)
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 256;" ::"r"(smem_u32(&tmem_base)));
+    else
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(&tmem_base)));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::);
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::);
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::);
+  const uint32_t tmem = tmem_base;
+  const uint32_t idesc = (1u << 4) | ((static_cast<uint32_t>(n) >> 3) << 17) | ((128u >> 4) << 24);
+  // operands: bit 8, the 128-byte swizzle (A 16 KB at 0, B 32 KB at 16 KB, 128-byte
+  // rows), K step k at byte 32k of the row; bit 9, no swizzle with 8-row groups 1024
+  // bytes apart; else no swizzle, groups 256 bytes apart
+  const uint64_t adesc = (flags & 256) ? w4a4::kmajor_desc_sw128(dyn)
+                         : (flags & 512) ? desc_kmajor_noswizzle(smem_u32(dyn), 128, 1024)
+                                         : desc_kmajor_noswizzle(smem_u32(dyn), 128, 256);
+  const uint64_t bdesc = (flags & 256) ? w4a4::kmajor_desc_sw128(dyn + 16384)
+                         : (flags & 512) ? desc_kmajor_noswizzle(smem_u32(dyn + 16384), 128, 1024)
+                                         : desc_kmajor_noswizzle(smem_u32(dyn + 16384), 128, 256);
+  if (warp == 0) {
+    if (tid == 0) {
+      unsigned long long t;
+      int commits = 0;
+      asm volatile("mov.u64 %0, %%clock64;" : "=l"(t));
+      if (blockIdx.x == 0) out[0] = t;
+      int cnt = 0;
+      const uint32_t alt = (flags & 1) ? 128u : 0u;
+      const int acc_from = (flags & 4) ? 2 : iters;
+      for (int i = 0; i < iters; ++i) {
+        const uint32_t d = tmem + ((i & 1) ? alt : 0u);
+        const uint32_t acc = static_cast<uint32_t>(i >= acc_from);
+        const uint64_t koff = (flags & 768) ? static_cast<uint64_t>(2 * (i & 3)) : 0u;  // 32 bytes >> 4
+        asm volatile(
+            "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+            "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+            "l"(adesc + koff), "l"(bdesc + koff), "r"(idesc), "r"(acc));
+        if (++cnt == per_commit || i + 1 == iters) {
+          cnt = 0;
+          asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+              smem_u32(&bar)));
+          ++commits;
+        }
+        if (!(flags & 8)) {
+          asm volatile("mov.u64 %0, %%clock64;" : "=l"(t));
+          if (i < 60 && blockIdx.x == 0) out[1 + i] = t;
+        }
+      }
+      // every commit's phase: wait for the last one (count 1: one phase per commit)
+      uint32_t done = 0;
+      for (long spin = 0; !done && spin < 100000000L; ++spin)
+        asm volatile(
+            "{\n.reg .pred p;\nmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(done) : "r"(smem_u32(&bar)), "r"(static_cast<uint32_t>((commits - 1) & 1)));
+      asm volatile("mov.u64 %0, %%clock64;" : "=l"(t));
+      if (blockIdx.x == 0) out[61] = t;
+      if (!done) atomicExch(status, 1);
+      stop = 1;
+    }
+    __syncwarp();
+  } else if (flags & 2) {
+    float2 a = make_float2(tid, 1.f), b = make_float2(0.5f, 0.25f), c0 = make_float2(0.f, 0.f), c1 = c0, c2 = c0,
+           c3 = c0;
+    for (long it = 0; !stop && it < 10000000L; ++it) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        c0 = __ffma2_rn(a, b, c0);
+        c1 = __ffma2_rn(a, c0, c1);
+        c2 = __ffma2_rn(b, c1, c2);
+        c3 = __ffma2_rn(a, c2, c3);
+      }
+    }
+    if (c3.x == 12345.f) out[62] = 1;
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::);
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::);
+  if (warp == 0) {
+    if (flags & 128)
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 256;" ::"r"(tmem));
+    else
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem));
+  }
+}
+
+
+// TMEM load latency: warps 0..nwarps-1 each time `reps` back-to-back
+// (tcgen05.ld + tcgen05.wait::ld) of the 16x256b shape, .x4 (x8 = 0) or .x8
+// (x8 = 1), from their lane quarter of a 512-column allocation.
+__global__ void __launch_bounds__(256) tmem_ld_probe(int x8, int nwarps, int reps, unsigned long long* out) {
+  __shared__ uint32_t tmem_base;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(&tmem_base)));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::);
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::);
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::);
+  const uint32_t tmem = tmem_base + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+  uint32_t acc = 0;
+  if (warp < nwarps) {
+    unsigned long long t0, t1;
+    asm volatile("mov.u64 %0, %%clock64;" : "=l"(t0));
+    for (int it = 0; it < reps; ++it) {
+      const uint32_t col = static_cast<uint32_t>((it & 3) * 128);
+      if (x8) {
+        uint32_t r[32];
+        w4a4::tmem_ld16x256_x8(tmem + col, r);
+        w4a4::tmem_wait32(r);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc += r[j];
+      } else {
+        uint32_t r[16];
+        w4a4::tmem_ld16x256_x4(tmem + col, r);
+        w4a4::tmem_wait(r);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) acc += r[j];
+      }
+    }
+    asm volatile("mov.u64 %0, %%clock64;" : "=l"(t1));
+    if ((tid & 31) == 0) out[warp] = t1 - t0;
+  }
+  if (acc == 0x12345678u) out[63] = acc;
+  asm volatile("tcgen05.fence::before_thread_sync;" ::);
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::);
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem_base));
+}
+
 template <typename F>
 double time_kernel(F launch) {
   cudaEvent_t e0, e1;
@@ -280,6 +611,110 @@ int w4a4_probe_tmem_layout(uint32_t* out) {
   if (e == cudaSuccess) e = cudaMemcpy(out, d, 128 * 8 * sizeof(uint32_t), cudaMemcpyDeviceToHost);
   cudaFree(d);
   return e == cudaSuccess ? 0 : 2;
+}
+
+
+// One tcgen05 MMA's latency (clock64 cycles, median of 32 repetitions after 4) for
+// M = 128, N = n, K = 32 fp8, K-major operands with 8-row groups sbo bytes apart;
+// loaders: bit 0, eight other warps stream TMEM loads meanwhile; bit 1, shared-memory
+// loads; bit 2, nonzero operands; bit 3, a warp streaming 48 KB bulk copies from
+// global memory into shared memory; bit 4, the completion observed by another
+// warp (the issuing thread waits for that warp's word); bit 5, with bit 4, the
+// issuing thread busy for 3000 cycles first; bit 6, with bit 4, the issuing
+// thread waits on a second mbarrier that the observer arrives on (test_wait
+// polls; bit 7: try_wait).  -1 on failure.
+double w4a4_probe_mma_latency(int n, int sbo, int loaders) {
+  if (n < 16 || n > 256 || n % 16 || (sbo != 256 && sbo != 1024) || loaders < 0 || loaders > 255) return -1.0;
+  unsigned long long* d = nullptr;
+  int* status = nullptr;
+  if (cudaMalloc(&d, 64 * sizeof(unsigned long long)) != cudaSuccess) return -1.0;
+  if (cudaMalloc(&status, sizeof(int)) != cudaSuccess) { cudaFree(d); return -1.0; }
+  cudaMemset(status, 0, sizeof(int));
+  const size_t smem = (16 + 32 + 48) * 1024;
+  const int64_t gbytes = int64_t(64) << 20;
+  uint8_t* gsrc = nullptr;
+  if (cudaMalloc(&gsrc, gbytes) != cudaSuccess) { cudaFree(d); cudaFree(status); return -1.0; }
+  cudaMemset(gsrc, 0x11, gbytes);
+  cudaFuncSetAttribute(mma_latency_probe, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  mma_latency_probe<<<1, 288, smem>>>(n, sbo, loaders, d, status, gsrc, gbytes);
+  unsigned long long h[64] = {};
+  int hs = 1;
+  const cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) {
+    cudaMemcpy(h, d, sizeof(h), cudaMemcpyDeviceToHost);
+    cudaMemcpy(&hs, status, sizeof(int), cudaMemcpyDeviceToHost);
+  }
+  cudaFree(d);
+  cudaFree(status);
+  cudaFree(gsrc);
+  if (e != cudaSuccess || hs != 0) return -1.0;
+  unsigned long long v[28];
+  for (int i = 0; i < 28; ++i) v[i] = h[4 + i];
+  for (int i = 1; i < 28; ++i)
+    for (int j = i; j > 0 && v[j - 1] > v[j]; --j) {
+      const unsigned long long t = v[j];
+      v[j] = v[j - 1];
+      v[j - 1] = t;
+    }
+  return static_cast<double>(v[14]);
+}
+
+
+// Back-to-back MMA issue (mma_rate_probe): out2[0] = median cycles between issues
+// 10..59, out2[1] = cycles from the first issue to the last commit's completion
+// divided by iters.  0 on success.
+int w4a4_probe_mma_rate(int n, int per_commit, int iters, int flags, double* out2) {
+  if (n < 16 || n > 256 || n % 16 || per_commit < 1 || iters < 61 || iters > 100000 || flags < 0 || flags > 1023 || (flags & 768) == 768)
+    return -1;
+  if ((flags & 1) && n > ((flags & 128) ? 128 : 256)) return -1;  // the second buffer must fit
+  unsigned long long* d = nullptr;
+  int* status = nullptr;
+  if (cudaMalloc(&d, 64 * sizeof(unsigned long long)) != cudaSuccess) return -1;
+  if (cudaMalloc(&status, sizeof(int)) != cudaSuccess) { cudaFree(d); return -1; }
+  cudaMemset(d, 0, 64 * sizeof(unsigned long long));
+  cudaMemset(status, 0, sizeof(int));
+  const size_t smem = 48 * 1024;
+  cudaFuncSetAttribute(mma_rate_probe, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  mma_rate_probe<<<(flags & 64) ? sms() : 1, 288, smem>>>(n, per_commit, iters, flags, d, status);
+  unsigned long long h[64] = {};
+  int hs = 1;
+  const cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) {
+    cudaMemcpy(h, d, sizeof(h), cudaMemcpyDeviceToHost);
+    cudaMemcpy(&hs, status, sizeof(int), cudaMemcpyDeviceToHost);
+  }
+  cudaFree(d);
+  cudaFree(status);
+  if (e != cudaSuccess || hs != 0) return -1;
+  unsigned long long v[49];
+  for (int i = 0; i < 49; ++i) v[i] = h[12 + i] - h[11 + i];
+  for (int i = 1; i < 49; ++i)
+    for (int j = i; j > 0 && v[j - 1] > v[j]; --j) {
+      const unsigned long long t = v[j];
+      v[j] = v[j - 1];
+      v[j - 1] = t;
+    }
+  out2[0] = static_cast<double>(v[24]);
+  out2[1] = static_cast<double>(h[61] - h[0]) / iters;
+  return 0;
+}
+
+
+// Cycles per TMEM load + wait (tmem_ld_probe), averaged over the timed warps.
+double w4a4_probe_tmem_ld(int x8, int nwarps, int reps) {
+  if (nwarps < 1 || nwarps > 8 || reps < 1 || reps > 100000 || (x8 != 0 && x8 != 1)) return -1.0;
+  unsigned long long* d = nullptr;
+  if (cudaMalloc(&d, 64 * sizeof(unsigned long long)) != cudaSuccess) return -1.0;
+  cudaMemset(d, 0, 64 * sizeof(unsigned long long));
+  tmem_ld_probe<<<1, 256>>>(x8, nwarps, reps, d);
+  unsigned long long h[64] = {};
+  const cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) cudaMemcpy(h, d, sizeof(h), cudaMemcpyDeviceToHost);
+  cudaFree(d);
+  if (e != cudaSuccess) return -1.0;
+  double sum = 0;
+  for (int w = 0; w < nwarps; ++w) sum += static_cast<double>(h[w]);
+  return sum / nwarps / reps;
 }
 
 }  // extern "C"

@@ -100,6 +100,16 @@ __device__ __forceinline__ uint64_t kmajor_desc_sbo(const void* smem, uint32_t s
   return static_cast<uint64_t>((a >> 4) & 0x3FFFu) | (static_cast<uint64_t>(128 >> 4) << 16) |
          (static_cast<uint64_t>(sbo >> 4) << 32) | (static_cast<uint64_t>(1) << 46);
 }
+// K-major operand in the 128-byte swizzle (what a TMA copy with SWIZZLE_128B
+// writes): rows of 128 bytes, 8-row atoms 1024 bytes apart, 16-byte chunk c of row
+// r stored at chunk c ^ (r % 8).  The atoms are 1024-byte aligned; the start
+// address may sit 32 * k bytes into the row (the k-th 32-byte K step), which the
+// hardware swizzles along with the rest of the address.  Layout type 2 (bits 61-63).
+__device__ __forceinline__ uint64_t kmajor_desc_sw128(const void* smem) {
+  const uint32_t a = su32(smem);
+  return static_cast<uint64_t>((a >> 4) & 0x3FFFu) | (static_cast<uint64_t>(1) << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) | (static_cast<uint64_t>(2) << 61);
+}
 // kind::f16 MMA, f16 x f16 -> f32 (same instruction-descriptor layout as above:
 // format code 0 is f16 for this kind); accumulate into D when acc != 0.
 __device__ __forceinline__ void mma_f16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
@@ -170,6 +180,28 @@ __device__ __forceinline__ void tmem_ld16x256_x4(uint32_t taddr, uint32_t (&r)[1
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
         "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
+}
+
+// 16x256b TMEM load, eight 8-column repeats (64 columns): thread t receives rows
+// t/4 and t/4 + 8 of the 16 lanes starting at taddr's lane, columns 2(t%4) and
+// 2(t%4) + 1 of every 8-column group: r[4g + 2i + e] = (row t/4 + 8i, column
+// 8g + 2(t%4) + e), g < 8.  Asynchronous until a tcgen05.wait::ld.
+__device__ __forceinline__ void tmem_ld16x256_x8(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+// Wait for this thread's TMEM loads, the 32 registers of the one in flight tied
+// to the wait (no use of them is scheduled above it).
+__device__ __forceinline__ void tmem_wait32(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+  tie16(r);
+  tie16(r + 16);
 }
 
 }  // namespace w4a4
