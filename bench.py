@@ -327,6 +327,22 @@ def graph_time(fn, n: int = 20, reps: int = 5) -> float:
     return best
 
 
+def act_time(dev, x0, expanded: bool, nrep: int = 20) -> float:
+    """Device milliseconds per activation-kernel call on x0's shape, over input and
+    output sets that together exceed L2 by 2.2x (the kernel touches nothing else)."""
+    import torch
+    import hadamard_rotated_w4a4_gb300 as w4
+    M, K = x0.shape
+    touched = M * K * 4 + M * K // 2 + M * (K // 32) * 4 + (M * K if expanded else 0)
+    nsets = max(2, int(np.ceil(2.2 * L2_BYTES / touched)))
+    xs = [x0.clone() for _ in range(nsets)]
+    outs = [w4.alloc_act4(M, K, dev, expanded=expanded) for _ in range(nsets)]
+    ms = graph_time(lambda i, st: w4.w4a4_rotate_quantize_act(xs[i % nsets], out=outs[i % nsets], stream=st), nrep)
+    del xs, outs
+    torch.cuda.empty_cache()
+    return ms
+
+
 def moe_extra(dev, peaks: dict | None = None) -> dict:
     """The expert-routed workload (1024 tokens, 128 experts, top-8): activation
     quantisation and w4a4_gemm_id for gate/up (K2048 -> N768, activations per
@@ -358,7 +374,7 @@ def moe_extra(dev, peaks: dict | None = None) -> dict:
                          torch.empty(s.M, s.top_k, N, dtype=torch.float32, device=dev)))
         del wq0, x0
         ws = torch.zeros(w4.w4a4_gemm_id_workspace_bytes(s.M, s.top_k, s.E, K), dtype=torch.uint8, device=dev)
-        act_ms = graph_time(lambda i, st: w4.w4a4_rotate_quantize_act(sets[i % 2][1], out=sets[i % 2][2], stream=st))
+        act_ms = act_time(dev, sets[0][1], expanded=False)
         gid_ms = graph_time(lambda i, st: w4.w4a4_gemm_id(sets[i % 2][0], s.E, sets[i % 2][2], ids, s.top_k, per_slot,
                                                           y=sets[i % 2][3], ws=ws, stream=st))
         aq = sets[0][2]
@@ -367,7 +383,8 @@ def moe_extra(dev, peaks: dict | None = None) -> dict:
         out[name] = {"K": K, "N": N, "act_ms": act_ms, "gemm_id_ms": gid_ms,
                      "gemm_id_effective_tops": ops / (gid_ms * 1e-3) / 1e12,
                      "weight_mb": s.E * N * K * 0.5625 / 1e6,
-                     "l2": "2 input sets rotated, each larger than L2",
+                     "l2": "GEMM: 2 input sets rotated, each larger than L2; activation kernel: its own "
+                           "input/output sets, together 2.2x L2",
                      "roofline": gemm_roofline(gid_ms, s.M * s.top_k * N, K,
                                                gemm_algorithmic_bytes(s.E * N, K, a_rows, s.M * s.top_k, N),
                                                peaks, sm_count),
@@ -407,8 +424,7 @@ def time_dense(dev, name: str, rows: int, nrep: int) -> dict:
     gws = torch.zeros(max(16, w4.w4a4_gemm_workspace_bytes(rows, N, K)), dtype=torch.uint8, device=dev)
     out = {
         "M": rows, "K": K, "N": N,
-        "act_ms": graph_time(lambda i, st: w4.w4a4_rotate_quantize_act(sets[i % nsets][1], out=sets[i % nsets][2],
-                                                                        stream=st), nrep),
+        "act_ms": act_time(dev, x, expanded=True, nrep=nrep),
         "gemm_ms": graph_time(lambda i, st: w4.w4a4_gemm(sets[i % nsets][0], sets[i % nsets][2],
                                                          y=sets[i % nsets][3], ws=gws, stream=st), nrep),
     }

@@ -28,23 +28,34 @@ namespace {
 constexpr int kWarps = 8;
 constexpr int kRow = 36;  // floats per padded block row in shared memory
 
+// Stage h = 1 pairs the two halves of each register pair (scalar adds); stages
+// h >= 2 pair whole register pairs, so each runs as paired fp32 adds -- the same
+// IEEE additions in the same order, half the instructions.
 __device__ __forceinline__ void fwht32(float (&v)[32]) {
 #pragma unroll
-  for (int h = 1; h < 32; h <<= 1) {
+  for (int i = 0; i < 32; i += 2) {
+    const float a = v[i], b = v[i + 1];
+    v[i] = __fadd_rn(a, b);
+    v[i + 1] = __fsub_rn(a, b);
+  }
+  float2 (&w)[16] = *reinterpret_cast<float2 (*)[16]>(&v);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      if ((i & h) == 0) {
-        const float a = v[i], b = v[i + h];
-        v[i] = __fadd_rn(a, b);
-        v[i + h] = __fsub_rn(a, b);
+  for (int h2 = 1; h2 < 16; h2 <<= 1) {  // h = 2 h2
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      if ((j & h2) == 0) {
+        const float2 a = w[j], b = w[j + h2];
+        w[j] = __fadd2_rn(a, b);
+        w[j + h2] = __fadd2_rn(a, make_float2(-b.x, -b.y));  // a - b, exactly
       }
     }
   }
 }
 
-// round half away from zero, then to a 4-bit two's complement nibble
-__device__ __forceinline__ uint32_t nib(float y, float inv) {
-  float r = round_half_away(__fmul_rn(y, inv));
+// an already scaled value y * (1 / d): round half away from zero, clamp, and the
+// 4-bit two's complement nibble
+__device__ __forceinline__ uint32_t nib_scaled(float v) {
+  float r = round_half_away(v);
   r = fminf(fmaxf(r, -8.0f), 7.0f);
   return static_cast<uint32_t>(static_cast<int>(r)) & 0xFu;
 }
@@ -62,9 +73,10 @@ __device__ __forceinline__ uint32_t nib(float y, float inv) {
 // stored at block index i if ok.
 __device__ __forceinline__ void rotate_block(float (&y)[32]) {
   fwht32(y);
-  const float cst = c_h32();
+  const float2 cst = make_float2(c_h32(), c_h32());
+  float2 (&w)[16] = *reinterpret_cast<float2 (*)[16]>(&y);
 #pragma unroll
-  for (int k = 0; k < 32; ++k) y[k] = __fmul_rn(y[k], cst);
+  for (int k = 0; k < 16; ++k) w[k] = __fmul2_rn(w[k], cst);
 }
 
 template <int BITS>
@@ -114,6 +126,12 @@ __device__ __forceinline__ void quantize_block(float (&y)[32], int rotate, bool 
   }
   const float d = __fdiv_rn(a, 7.0f);
   const float inv = (d != 0.0f) ? __frcp_rn(d) : 0.0f;
+  {  // y * inv, paired (the same products)
+    float2 (&yw)[16] = *reinterpret_cast<float2 (*)[16]>(&y);
+    const float2 inv2 = make_float2(inv, inv);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) yw[k] = __fmul2_rn(yw[k], inv2);
+  }
   // byte t of the 16 = element t (low nibble) | element t + 16 (high nibble)
   uint32_t w[4];
 #pragma unroll
@@ -121,8 +139,8 @@ __device__ __forceinline__ void quantize_block(float (&y)[32], int rotate, bool 
     uint32_t word = 0;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const uint32_t lo = nib(y[4 * t + k], inv);
-      const uint32_t hi = nib(y[16 + 4 * t + k], inv);
+      const uint32_t lo = nib_scaled(y[4 * t + k]);
+      const uint32_t hi = nib_scaled(y[16 + 4 * t + k]);
       word |= (lo | (hi << 4)) << (8 * k);
     }
     w[t] = word;

@@ -522,6 +522,222 @@ __global__ void __launch_bounds__(256) tmem_ld_probe(int x8, int nwarps, int rep
   if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem_base));
 }
 
+
+// The bare MMA -> fold handshake: warp 0 lane 0 issues one M 128, N 256, K 32
+// fp8 MMA per block into TMEM buffer b % 2 (after the buffer's release) and
+// commits it; warps 1-8 wait for each block and hand its buffer back.  flags bit
+// 0: the consumers wait with try_wait (else test_wait polls); bit 1: each
+// consumer warp loads one 16x256b.x4 piece of the block first; bit 2: the
+// issuer waits with try_wait.  out[0] = cycles per block seen by warp 1.
+__global__ void __launch_bounds__(288) pipe_probe(int nblocks, int flags, unsigned long long* out, int* status) {
+  extern __shared__ __align__(1024) uint8_t dyn[];
+  __shared__ __align__(8) uint64_t full[2], empty[2];
+  __shared__ uint32_t tmem_base;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int i = tid; i < 48 * 1024 / 4; i += blockDim.x) reinterpret_cast<uint32_t*>(dyn)[i] = 0x01020304u;
+  if (tid == 0) {
+    for (int i = 0; i < 2; ++i) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&full[i])));
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 8;" ::"r"(smem_u32(&empty[i])));
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::);
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::);
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(&tmem_base)));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::);
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::);
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::);
+  const uint32_t tmem = tmem_base;
+  const uint32_t idesc = (1u << 4) | ((256u >> 3) << 17) | ((128u >> 4) << 24);
+  const uint64_t adesc = desc_kmajor_noswizzle(smem_u32(dyn), 128, 256);
+  const uint64_t bdesc = desc_kmajor_noswizzle(smem_u32(dyn + 16384), 128, 256);
+  const long kSpin = 20000000L;
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int b = 0; b < nblocks; ++b) {
+        const int tb = b & 1;
+        uint32_t ok = 0;
+        const uint32_t par = ((b >> 1) & 1) ^ 1;
+        for (long n = 0; !ok && n < kSpin; ++n) {
+          if (flags & 4)
+            asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+                         : "=r"(ok) : "r"(smem_u32(&empty[tb])), "r"(par) : "memory");
+          else
+            asm volatile("{\n.reg .pred p;\nmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+                         : "=r"(ok) : "r"(smem_u32(&empty[tb])), "r"(par) : "memory");
+        }
+        if (!ok) { atomicExch(status, 1); break; }
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, 0, 0;\ntcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n"
+                     ::"r"(tmem + static_cast<uint32_t>(tb * 256)), "l"(adesc), "l"(bdesc), "r"(idesc));
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(&full[tb])) : "memory");
+      }
+    }
+    __syncwarp();
+  } else if (warp <= 8) {
+    unsigned long long t0 = 0, t1;
+    uint32_t acc = 0;
+    const uint32_t q = static_cast<uint32_t>(warp & 3);
+    for (int b = 0; b < nblocks; ++b) {
+      const int tb = b & 1;
+      uint32_t ok = 0;
+      const uint32_t par = (b >> 1) & 1;
+      for (long n = 0; !ok && n < kSpin; ++n) {
+        if (flags & 1)
+          asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+                       : "=r"(ok) : "r"(smem_u32(&full[tb])), "r"(par) : "memory");
+        else
+          asm volatile("{\n.reg .pred p;\nmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+                       : "=r"(ok) : "r"(smem_u32(&full[tb])), "r"(par) : "memory");
+      }
+      if (!ok) { atomicExch(status, 2); break; }
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      if (b == 16 && warp == 1 && lane == 0) asm volatile("mov.u64 %0, %%clock64;" : "=l"(t0));
+      if (flags & 2) {
+        uint32_t r[16];
+        w4a4::tmem_ld16x256_x4(tmem + (q << 21) + static_cast<uint32_t>(tb * 256 + 32 * (warp >> 2)), r);
+        w4a4::tmem_wait(r);
+        acc += r[0] ^ r[15];
+      }
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&empty[tb])) : "memory");
+    }
+    asm volatile("mov.u64 %0, %%clock64;" : "=l"(t1));
+    if (warp == 1 && lane == 0 && nblocks > 16) out[0] = (t1 - t0) / static_cast<unsigned long long>(nblocks - 16);
+    if (acc == 0x12345u) out[1] = acc;
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::);
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::);
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem));
+}
+
+
+// The fold alone: warps fold `nblocks` 128 x 256 accumulator blocks read from
+// TMEM (two 256-column buffers, alternating) with the GEMM's per-piece loop --
+// 16x256b.x4 loads one piece ahead, paired FMAs t = fma(D, dw, c), acc = fma(t,
+// da, acc) with scales from shared memory -- and no barrier.  out[w] = cycles per
+// block of warp w.
+template <int NW, int mode>
+__global__ void __launch_bounds__(32 * NW) fold_probe(int nblocks, unsigned long long* out) {
+  // mode bit 0: no TMEM loads (registers from the loop index); bit 1: scales from
+  // registers (no shared loads); bit 2: 16 warps, each with half the columns
+  // (chunks hq and hq + 4 of the 8), else 8 warps with four chunks each.
+  __shared__ uint32_t tmem_base;
+  __shared__ __align__(16) float sc[4096];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  constexpr int nw = NW;
+  constexpr int NKK = NW == 16 ? 2 : 4;  // chunks per warp
+  for (int i = tid; i < 4096; i += blockDim.x) sc[i] = 1.0f + 0.001f * (i & 63);
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(&tmem_base)));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::);
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::);
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::);
+  const int q = warp & 3, h = warp >> 2, jr = lane >> 2, u = lane & 3;
+  float2 acc[NKK][2][4][2];
+#pragma unroll
+  for (int a = 0; a < NKK; ++a)
+#pragma unroll
+    for (int b = 0; b < 2; ++b)
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        acc[a][b][x][0] = make_float2(0.f, 0.f);
+        acc[a][b][x][1] = make_float2(0.f, 0.f);
+      }
+  unsigned long long t0, t1;
+  asm volatile("mov.u64 %0, %%clock64;" : "=l"(t0));
+  {
+    for (int bk = 0; bk < nblocks; ++bk) {
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>((bk & 1) * 256);
+      const float* sb = sc + (bk & 7) * 512;
+      float4 dwv, crv;
+      if constexpr ((mode & 2) != 0) {
+        dwv = make_float4(1.f + bk, 2.f, 3.f, 4.f);
+        crv = make_float4(0.5f, 0.25f + bk, 0.125f, 1.f);
+      } else {
+        dwv = *reinterpret_cast<const float4*>(sb + 32 * q + 4 * jr);
+        crv = *reinterpret_cast<const float4*>(sb + 128 + 32 * q + 4 * jr);
+      }
+      uint32_t ra[16], rb[16];
+      constexpr int np = 2 * NKK;
+      if constexpr ((mode & 1) == 0) {
+        w4a4::tmem_ld16x256_x4(tbase + static_cast<uint32_t>(32 * h), ra);
+        w4a4::tmem_wait(ra);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) ra[i] = __float_as_uint(1.0f + i + bk);
+      }
+      float4 da0 = make_float4(0.f, 0.f, 0.f, 0.f), da1 = da0;
+#pragma unroll
+      for (int pc = 0; pc < np; ++pc) {
+        const int kk = pc >> 1, hf = pc & 1;
+        const int kcol = NW == 16 ? h + 4 * kk : h + 2 * kk;
+        uint32_t(&cur)[16] = (pc & 1) ? rb : ra;
+        uint32_t(&nxt)[16] = (pc & 1) ? ra : rb;
+        if (pc + 1 < np) {
+          const int k1 = NW == 16 ? h + 4 * ((pc + 1) >> 1) : h + 2 * ((pc + 1) >> 1), hf1 = (pc + 1) & 1;
+          if constexpr ((mode & 1) == 0) {
+            w4a4::tmem_ld16x256_x4(tbase + (static_cast<uint32_t>(16 * hf1) << 16) + static_cast<uint32_t>(32 * k1),
+                                   nxt);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) nxt[i] = __float_as_uint(2.0f + i + pc + bk);
+          }
+        }
+        if (hf == 0) {
+          if constexpr ((mode & 2) != 0) {
+            da0 = make_float4(0.1f * kk, 0.2f, 0.3f, 0.4f + bk);
+            da1 = make_float4(0.5f, 0.6f + bk, 0.7f, 0.8f);
+          } else {
+            const float4* dap = reinterpret_cast<const float4*>(sb + 256 + (32 * kcol) % 256 + 8 * u);
+            da0 = dap[0];
+            da1 = dap[1];
+          }
+        }
+        const float dA = hf ? dwv.z : dwv.x, dB = hf ? dwv.w : dwv.y;
+        const float cA = hf ? crv.z : crv.x, cB = hf ? crv.w : crv.y;
+        const float2 dw0 = make_float2(dA, dA), dw1 = make_float2(dB, dB);
+        const float2 c0 = make_float2(cA, cA), c1 = make_float2(cB, cB);
+        const float2 dav[4] = {make_float2(da0.x, da0.y), make_float2(da0.z, da0.w), make_float2(da1.x, da1.y),
+                               make_float2(da1.z, da1.w)};
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          const float2 a0 =
+              __ffma2_rn(make_float2(__uint_as_float(cur[4 * x]), __uint_as_float(cur[4 * x + 1])), dw0, c0);
+          const float2 a1 =
+              __ffma2_rn(make_float2(__uint_as_float(cur[4 * x + 2]), __uint_as_float(cur[4 * x + 3])), dw1, c1);
+          acc[kk][hf][x][0] = __ffma2_rn(a0, dav[x], acc[kk][hf][x][0]);
+          acc[kk][hf][x][1] = __ffma2_rn(a1, dav[x], acc[kk][hf][x][1]);
+        }
+        if constexpr ((mode & 1) == 0) {
+          if (pc + 1 < np) w4a4::tmem_wait(nxt);
+        }
+      }
+    }
+  }
+  asm volatile("mov.u64 %0, %%clock64;" : "=l"(t1));
+  float sum = 0.f;
+#pragma unroll
+  for (int a = 0; a < NKK; ++a)
+#pragma unroll
+    for (int b = 0; b < 2; ++b)
+#pragma unroll
+      for (int x = 0; x < 4; ++x) sum += acc[a][b][x][0].x + acc[a][b][x][1].y;
+  if (lane == 0) out[warp] = (t1 - t0) / static_cast<unsigned long long>(nblocks);
+  if (sum == 1234.5f) out[63] = 1;
+  asm volatile("tcgen05.fence::before_thread_sync;" ::);
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::);
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem_base));
+}
+
 template <typename F>
 double time_kernel(F launch) {
   cudaEvent_t e0, e1;
@@ -715,6 +931,61 @@ double w4a4_probe_tmem_ld(int x8, int nwarps, int reps) {
   double sum = 0;
   for (int w = 0; w < nwarps; ++w) sum += static_cast<double>(h[w]);
   return sum / nwarps / reps;
+}
+
+
+// Cycles per block of the bare MMA -> fold handshake (pipe_probe), -1 on failure.
+double w4a4_probe_pipe(int nblocks, int flags) {
+  if (nblocks < 32 || nblocks > 100000 || flags < 0 || flags > 7) return -1.0;
+  unsigned long long* d = nullptr;
+  int* status = nullptr;
+  if (cudaMalloc(&d, 4 * sizeof(unsigned long long)) != cudaSuccess) return -1.0;
+  if (cudaMalloc(&status, sizeof(int)) != cudaSuccess) { cudaFree(d); return -1.0; }
+  cudaMemset(d, 0, 4 * sizeof(unsigned long long));
+  cudaMemset(status, 0, sizeof(int));
+  const size_t smem = 48 * 1024;
+  cudaFuncSetAttribute(pipe_probe, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  pipe_probe<<<1, 288, smem>>>(nblocks, flags, d, status);
+  unsigned long long h[4] = {};
+  int hs = 1;
+  const cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) {
+    cudaMemcpy(h, d, sizeof(h), cudaMemcpyDeviceToHost);
+    cudaMemcpy(&hs, status, sizeof(int), cudaMemcpyDeviceToHost);
+  }
+  cudaFree(d);
+  cudaFree(status);
+  if (e != cudaSuccess || hs != 0) return -1.0;
+  return static_cast<double>(h[0]);
+}
+
+
+// Cycles per 128 x 256 block of the fold alone (fold_probe, see its modes), mean
+// over the warps.
+double w4a4_probe_fold(int nblocks, int mode) {
+  if (nblocks < 1 || nblocks > 100000 || mode < 0 || mode > 7) return -1.0;
+  unsigned long long* d = nullptr;
+  if (cudaMalloc(&d, 64 * sizeof(unsigned long long)) != cudaSuccess) return -1.0;
+  cudaMemset(d, 0, 64 * sizeof(unsigned long long));
+  const int nw = (mode & 4) ? 16 : 8;
+  switch (mode) {
+    case 0: fold_probe<8, 0><<<1, 256>>>(nblocks, d); break;
+    case 1: fold_probe<8, 1><<<1, 256>>>(nblocks, d); break;
+    case 2: fold_probe<8, 2><<<1, 256>>>(nblocks, d); break;
+    case 3: fold_probe<8, 3><<<1, 256>>>(nblocks, d); break;
+    case 4: fold_probe<16, 4><<<1, 512>>>(nblocks, d); break;
+    case 5: fold_probe<16, 5><<<1, 512>>>(nblocks, d); break;
+    case 6: fold_probe<16, 6><<<1, 512>>>(nblocks, d); break;
+    default: fold_probe<16, 7><<<1, 512>>>(nblocks, d); break;
+  }
+  unsigned long long h[64] = {};
+  const cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) cudaMemcpy(h, d, sizeof(h), cudaMemcpyDeviceToHost);
+  cudaFree(d);
+  if (e != cudaSuccess) return -1.0;
+  double sum = 0;
+  for (int w = 0; w < nw; ++w) sum += static_cast<double>(h[w]);
+  return sum / nw;
 }
 
 }  // extern "C"

@@ -161,6 +161,12 @@ __device__ __forceinline__ void tie16(uint32_t* r) {
                :
                : "memory");
 }
+// Wait for this thread's TMEM loads into two 16-register buffers.
+__device__ __forceinline__ void tmem_wait2(uint32_t (&a)[16], uint32_t (&b)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+  tie16(a);
+  tie16(b);
+}
 // Wait for this thread's TMEM loads into two 32-register buffers.
 __device__ __forceinline__ void tmem_wait32x2(uint32_t (&a)[32], uint32_t (&b)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
