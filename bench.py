@@ -343,6 +343,46 @@ def act_time(dev, x0, expanded: bool, nrep: int = 20) -> float:
     return ms
 
 
+def verify_extra(dev, name: str, peaks: dict | None = None, nrep: int = 20) -> dict:
+    """A drafter's 8-token verification batch on a dense config's weights: the
+    general GEMM (whole-tile schedule) and the small-M kernel, each replayed from a
+    CUDA graph over weight sets that together exceed L2."""
+    import torch
+    import hadamard_rotated_w4a4_gb300 as w4
+    peaks = peaks or read_peaks()
+    d = si.dense_inputs(name)
+    w = torch.from_numpy(d["w_bf16"].view(np.int16)).to(dev).view(torch.bfloat16)
+    x8 = torch.from_numpy(np.ascontiguousarray(d["x"][:8])).to(dev)
+    del d
+    N, K = w.shape
+    wq0 = w4.h32_q4_0_pack_weights(w)
+    del w
+    wbytes = N * K // 2 + N * (K // 32) * 2
+    nsets = max(2, int(np.ceil(2.2 * L2_BYTES / wbytes)))
+    sets = []
+    for _ in range(nsets):
+        wq = w4.alloc_q4_0(N, K, dev)
+        wq.codes.copy_(wq0.codes)
+        wq.scales_buf.copy_(wq0.scales_buf)
+        wq.sums_buf.copy_(wq0.sums_buf)
+        sets.append(wq)
+    del wq0
+    a4v = w4.w4a4_rotate_quantize_act(x8)
+    y8 = torch.empty(8, N, dtype=torch.float32, device=dev)
+    wsv = torch.zeros(max(16, w4.w4a4_gemm_workspace_bytes(8, N, K)), dtype=torch.uint8, device=dev)
+    tc_ms = graph_time(lambda i, st: w4.w4a4_gemm(sets[i % nsets], a4v, y=y8, ws=wsv, stream=st), nrep)
+    sm_ms = graph_time(lambda i, st: w4.w4a4_gemm_small_m(sets[i % nsets], a4v, y=y8, stream=st), nrep)
+    gbs = wbytes / (sm_ms * 1e-3) / 1e9
+    out = {"what": f"8-token verification batch on the {name} weights (K{K} N{N})", "tensor_core_ms": tc_ms,
+           "small_m_ms": sm_ms, "small_m_weight_gbs": gbs,
+           "roofline": {"bound": "hbm", "algorithmic_bytes": wbytes, "achieved": gbs, "peak": peaks["hbm_gbs"],
+                        "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"]},
+           "l2": f"{nsets} weight sets rotated"}
+    del sets, a4v, y8, wsv
+    torch.cuda.empty_cache()
+    return out
+
+
 def moe_extra(dev, peaks: dict | None = None) -> dict:
     """The expert-routed workload (1024 tokens, 128 experts, top-8): activation
     quantisation and w4a4_gemm_id for gate/up (K2048 -> N768, activations per
@@ -474,6 +514,33 @@ def run_probes() -> dict:
         "fp32_ffma2_tflops": lib.w4a4_probe_ffma(1, 20000) / 1e12,
         "fp8_tcgen05_tflops": lib.w4a4_probe_tcgen05_f8(20000) / 1e12,
     }
+    return out
+
+
+def run_pipeline_probes() -> dict:
+    """Latency and rate probes behind the super-tile GEMM's design (single CTA, clock64
+    cycles): back-to-back tcgen05 MMA issue, TMEM load + wait, the bare MMA-to-fold
+    barrier handshake, and the fold loop alone.  A profiling aid, not in the bench line."""
+    import ctypes
+    from hadamard_rotated_w4a4_gb300 import build as b
+    b.build(probes=True)
+    lib = ctypes.CDLL(b.PROBE_LIB)
+    lib.w4a4_probe_mma_rate.argtypes = [ctypes.c_int] * 4 + [ctypes.POINTER(ctypes.c_double)]
+    lib.w4a4_probe_tmem_ld.argtypes, lib.w4a4_probe_tmem_ld.restype = [ctypes.c_int] * 3, ctypes.c_double
+    lib.w4a4_probe_pipe.argtypes, lib.w4a4_probe_pipe.restype = [ctypes.c_int] * 2, ctypes.c_double
+    lib.w4a4_probe_fold.argtypes, lib.w4a4_probe_fold.restype = [ctypes.c_int] * 2, ctypes.c_double
+    out = {}
+    for n in (64, 128, 256):
+        for name, flags in (("no_swizzle", 8), ("sw128", 8 | 256)):
+            o = (ctypes.c_double * 2)()
+            rc = lib.w4a4_probe_mma_rate(n, 1, 2000, flags, o)
+            out[f"mma_issue_cycles_n{n}_{name}"] = o[1] if rc == 0 else None
+    for x8, nm in ((0, "x4"), (1, "x8")):
+        out[f"tmem_ld_wait_cycles_16x256b_{nm}_8warps"] = lib.w4a4_probe_tmem_ld(x8, 8, 2000)
+    out["handshake_cycles_per_block_n256_2buf"] = lib.w4a4_probe_pipe(2000, 1)
+    for mode, nm in ((0, "8warps"), (1, "8warps_no_tmem_loads"), (2, "8warps_no_scale_loads"),
+                     (3, "8warps_fma_only"), (4, "16warps")):
+        out[f"fold_cycles_per_128x256_block_{nm}"] = lib.w4a4_probe_fold(2000, mode)
     return out
 
 
@@ -758,6 +825,9 @@ def run_ours(args, shape) -> dict | None:
     moe = None
     if not args.no_moe and world == 1:
         moe = moe_extra(dev, peaks)
+    verify_c3 = None
+    if not args.no_verify and world == 1 and shape.name != "c3":
+        verify_c3 = verify_extra(dev, "c3", peaks)
     # every config's kernels against their bounds (algorithmic bytes; expanded writes apart)
     rooflines = {"c1": {"gemm": g1, "act": a1}}
     for name, t in dense_cfg.items():
@@ -804,6 +874,7 @@ def run_ours(args, shape) -> dict | None:
         "expanded_weights": expanded_w,
         "rotate_only": rotate_only,
         "verification_batch": verify,
+        "verification_batch_c3": verify_c3,
         "kernel_ms": {"act_rotate_quantize": act_avg, "gemm": gemm_avg},
         "pack_weights_ms": pack_ms,
         "pack_weights_imatrix_ms": imx_ms,
@@ -838,6 +909,9 @@ def main():
     ap.add_argument("--moe-only", action="store_true",
                     help="time only the expert-routed workload and print its figures (a profiling aid, "
                          "not the benchmark line)")
+    ap.add_argument("--verify-only", action="store_true",
+                    help="time only the 8-token verification batch on --config's weights and print its "
+                         "figures (a profiling aid, not the benchmark line)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -846,6 +920,13 @@ def main():
         import hadamard_rotated_w4a4_gb300 as w4
         w4.load_library(build_if_missing=True)
         print(json.dumps({"moe": moe_extra(torch.device("cuda", torch.cuda.current_device()))}), flush=True)
+        return
+    if args.verify_only:
+        import torch
+        import hadamard_rotated_w4a4_gb300 as w4
+        w4.load_library(build_if_missing=True)
+        dev = torch.device("cuda", torch.cuda.current_device())
+        print(json.dumps({"verification_batch": verify_extra(dev, args.config)}), flush=True)
         return
     shape = si.DENSE[args.config]
     line = run_reference(args, shape) if args.impl == "reference" else run_ours(args, shape)
