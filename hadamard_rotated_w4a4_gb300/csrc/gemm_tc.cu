@@ -1257,6 +1257,8 @@ cudaError_t encode_2d_map(CUtensorMap* m, CUtensorMapDataType dtype, const void*
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Cached per device for the process's life; cudaDeviceReset invalidates the
+// cached address (the header tells callers not to use a reset device again).
 int* device_error_word() {
   static std::mutex mu;
   static int* cached[64] = {};

@@ -250,9 +250,11 @@ w4a4_status w4a4_rotate_quantize_act(const float* x, int64_t M, int64_t K, int64
  *         the 16-byte rule); Y[m][n] = sum_b d_w d_a P (fp32).
  * w->K must equal a->K and both tags must agree on rotation, else
  * W4A4_ERR_MISMATCH.  The per-block integer partials are exact on the tensor
- * cores; the scale fold is fp32.  When w->expanded and a->expanded are both set,
- * the kernel reads them instead of the codes (same result, bit for bit); they
- * must then hold the expanded form of the same codes.
+ * cores; the scale fold is fp32.  When a->expanded is set, the super-tile kernel
+ * loads it instead of converting the activation codes, and reads w->expanded,
+ * if set, instead of converting the weight codes (same result, bit for bit); an
+ * expanded buffer must then hold the expanded form of the same codes.  Without
+ * a->expanded, a kernel that converts both operands' codes runs.
  *   ws  : optional device workspace (NULL, or w4a4_gemm_workspace_bytes(M, N,
  *         K) bytes or more, 16-byte aligned, all zero before its first use).
  *         Its first MiB holds arrival counters that every call leaves at zero
@@ -418,6 +420,11 @@ w4a4_status w4a4_gemm_id_static(const w4a4_q4_0* experts, int E, int64_t N, cons
  * that stopped making progress for a second).  Such a kernel stops early, so
  * its output is incomplete: W4A4_ERR_TIMEOUT.  Clears the condition.  Returns
  * W4A4_ERR_CUDA for an error already pending on the stream.
+ *
+ * The library caches, per device, the addresses of its device-side state (this
+ * error word, the static routing scratch of w4a4_gemm_id_static) and each
+ * kernel's launch attributes.  cudaDeviceReset invalidates them: a process that
+ * resets a device must not call the library on that device again.
  */
 w4a4_status w4a4_check(w4a4_stream_t stream);
 
