@@ -541,6 +541,11 @@ def run_pipeline_probes() -> dict:
     for mode, nm in ((0, "8warps"), (1, "8warps_no_tmem_loads"), (2, "8warps_no_scale_loads"),
                      (3, "8warps_fma_only"), (4, "16warps")):
         out[f"fold_cycles_per_128x256_block_{nm}"] = lib.w4a4_probe_fold(2000, mode)
+    lib.w4a4_probe_fold_mma.argtypes = [ctypes.c_int] * 3 + [ctypes.POINTER(ctypes.c_double)]
+    for mp, tp in ((0, 0), (1, 0), (0, 2)):
+        o = (ctypes.c_double * 2)()
+        if lib.w4a4_probe_fold_mma(2000, mp, tp, o) == 0:
+            out[f"fold_beside_issuers_mma{mp}_copies{tp}"] = {"beside_issuers": o[0], "other_warps": o[1]}
     return out
 
 

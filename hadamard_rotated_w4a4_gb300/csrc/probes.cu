@@ -738,6 +738,157 @@ __global__ void __launch_bounds__(32 * NW) fold_probe(int nblocks, unsigned long
   if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem_base));
 }
 
+
+// The fold loop (8 warps, warps 4-11, as fold_probe mode 0 on TMEM columns
+// 256..511) with warp 1 issuing `mma_per` back-to-back M 128 N 256 K 32 fp8 MMAs
+// into columns 0..255 for every block the fold warps do (mma_per = 0: idle) and
+// warp 0 issuing `tma_per` 4 KB bulk copies per block (0: idle).  out[w] = fold
+// cycles per block of warp w (4..11), so the warps beside the issuers (SM
+// sub-partitions 0 and 1) can be compared with the others.
+__global__ void __launch_bounds__(384) fold_mma_probe(int nblocks, int mma_per, int tma_per, const uint8_t* gsrc,
+                                                      unsigned long long* out, int* status) {
+  extern __shared__ __align__(1024) uint8_t dyn[];
+  __shared__ uint32_t tmem_base;
+  __shared__ __align__(16) float sc[4096];
+  __shared__ __align__(8) uint64_t mbar, cbar;
+  __shared__ volatile int stop;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int i = tid; i < 4096; i += blockDim.x) sc[i] = 1.0f + 0.001f * (i & 63);
+  for (int i = tid; i < 48 * 1024 / 4; i += blockDim.x) reinterpret_cast<uint32_t*>(dyn)[i] = 0x01020304u;
+  if (tid == 0) {
+    stop = 0;
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&mbar)));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&cbar)));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::);
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::);
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(&tmem_base)));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::);
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::);
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::);
+  const uint32_t tmem = tmem_base;
+  if (warp == 1) {
+    if (lane == 0 && mma_per > 0) {
+      const uint32_t idesc = (1u << 4) | ((256u >> 3) << 17) | ((128u >> 4) << 24);
+      const uint64_t adesc = desc_kmajor_noswizzle(smem_u32(dyn), 128, 256);
+      const uint64_t bdesc = desc_kmajor_noswizzle(smem_u32(dyn + 16384), 128, 256);
+      uint32_t ph = 0;
+      for (long it = 0; !stop && it < 4000000L; ++it) {
+        for (int k = 0; k < mma_per; ++k)
+          asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, 0, 0;\ntcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n"
+                       ::"r"(tmem), "l"(adesc), "l"(bdesc), "r"(idesc));
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(&mbar)) : "memory");
+        uint32_t done = 0;
+        for (long n = 0; !done && n < 20000000L; ++n)
+          asm volatile("{\n.reg .pred p;\nmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+                       : "=r"(done) : "r"(smem_u32(&mbar)), "r"(ph) : "memory");
+        if (!done) { atomicExch(status, 1); break; }
+        ph ^= 1;
+        // pace: about one group of MMAs per 700 cycles (a fold block)
+        unsigned long long t0, t1;
+        asm volatile("mov.u64 %0, %%clock64;" : "=l"(t0));
+        do { asm volatile("mov.u64 %0, %%clock64;" : "=l"(t1)); } while (t1 - t0 < 500 && !stop);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 0) {
+    if (lane == 0 && tma_per > 0) {
+      uint32_t ph = 0;
+      for (long it = 0; !stop && it < 4000000L; ++it) {
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(&cbar)), "r"(4096 * tma_per) : "memory");
+        for (int k = 0; k < tma_per; ++k)
+          asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], 4096, [%2];"
+                       ::"r"(smem_u32(dyn + 32768 + 4096 * (k & 3))), "l"(gsrc + (static_cast<int64_t>(it * tma_per + k) % 4096) * 4096),
+                         "r"(smem_u32(&cbar)) : "memory");
+        uint32_t done = 0;
+        for (long n = 0; !done && n < 20000000L; ++n)
+          asm volatile("{\n.reg .pred p;\nmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+                       : "=r"(done) : "r"(smem_u32(&cbar)), "r"(ph) : "memory");
+        if (!done) { atomicExch(status, 2); break; }
+        ph ^= 1;
+      }
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    const int q = warp & 3, h = (warp - 4) >> 2, jr = lane >> 2, u = lane & 3;
+    float2 acc[4][2][4][2];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 2; ++b)
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          acc[a][b][x][0] = make_float2(0.f, 0.f);
+          acc[a][b][x][1] = make_float2(0.f, 0.f);
+        }
+    unsigned long long t0, t1;
+    asm volatile("mov.u64 %0, %%clock64;" : "=l"(t0));
+    for (int bk = 0; bk < nblocks; ++bk) {
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + 256u;
+      const float* sb = sc + (bk & 7) * 512;
+      const float4 dwv = *reinterpret_cast<const float4*>(sb + 32 * q + 4 * jr);
+      const float4 crv = *reinterpret_cast<const float4*>(sb + 128 + 32 * q + 4 * jr);
+      uint32_t ra[16], rb[16];
+      w4a4::tmem_ld16x256_x4(tbase + static_cast<uint32_t>(32 * h), ra);
+      w4a4::tmem_wait(ra);
+      float4 da0, da1;
+#pragma unroll
+      for (int pc = 0; pc < 8; ++pc) {
+        const int kk = pc >> 1, hf = pc & 1;
+        uint32_t(&cur)[16] = (pc & 1) ? rb : ra;
+        uint32_t(&nxt)[16] = (pc & 1) ? ra : rb;
+        if (pc + 1 < 8) {
+          const int k1 = h + 2 * ((pc + 1) >> 1), hf1 = (pc + 1) & 1;
+          w4a4::tmem_ld16x256_x4(tbase + (static_cast<uint32_t>(16 * hf1) << 16) + static_cast<uint32_t>(32 * k1), nxt);
+        }
+        if (hf == 0) {
+          const float4* dap = reinterpret_cast<const float4*>(sb + 256 + (32 * (h + 2 * kk)) % 256 + 8 * u);
+          da0 = dap[0];
+          da1 = dap[1];
+        }
+        const float dA = hf ? dwv.z : dwv.x, dB = hf ? dwv.w : dwv.y;
+        const float cA = hf ? crv.z : crv.x, cB = hf ? crv.w : crv.y;
+        const float2 dw0 = make_float2(dA, dA), dw1 = make_float2(dB, dB);
+        const float2 c0 = make_float2(cA, cA), c1 = make_float2(cB, cB);
+        const float2 dav[4] = {make_float2(da0.x, da0.y), make_float2(da0.z, da0.w), make_float2(da1.x, da1.y),
+                               make_float2(da1.z, da1.w)};
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          const float2 a0 = __ffma2_rn(make_float2(__uint_as_float(cur[4 * x]), __uint_as_float(cur[4 * x + 1])), dw0, c0);
+          const float2 a1 =
+              __ffma2_rn(make_float2(__uint_as_float(cur[4 * x + 2]), __uint_as_float(cur[4 * x + 3])), dw1, c1);
+          acc[kk][hf][x][0] = __ffma2_rn(a0, dav[x], acc[kk][hf][x][0]);
+          acc[kk][hf][x][1] = __ffma2_rn(a1, dav[x], acc[kk][hf][x][1]);
+        }
+        if (pc + 1 < 8) w4a4::tmem_wait(nxt);
+      }
+    }
+    asm volatile("mov.u64 %0, %%clock64;" : "=l"(t1));
+    float sum = 0.f;
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 2; ++b)
+#pragma unroll
+        for (int x = 0; x < 4; ++x) sum += acc[a][b][x][0].x + acc[a][b][x][1].y;
+    if (lane == 0) out[warp] = (t1 - t0) / static_cast<unsigned long long>(nblocks);
+    if (sum == 1234.5f) out[63] = 1;
+  }
+  // warps 4-11 meet at a named barrier (256 threads) once their fold is done; one of
+  // them then tells the issuers to stop.  Warps 0-3 skip it.
+  if (warp >= 4) {
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    if (tid == 128) stop = 1;
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::);
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::);
+  if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem));
+}
+
 template <typename F>
 double time_kernel(F launch) {
   cudaEvent_t e0, e1;
@@ -986,6 +1137,39 @@ double w4a4_probe_fold(int nblocks, int mode) {
   double sum = 0;
   for (int w = 0; w < nw; ++w) sum += static_cast<double>(h[w]);
   return sum / nw;
+}
+
+
+// Fold cycles per block of the warps beside the MMA issuer and the copy issuer
+// (SM sub-partitions 0 and 1) and of the others (fold_mma_probe): out2[0] = mean
+// of warps 4, 5, 8, 9; out2[1] = mean of warps 6, 7, 10, 11.  0 on success.
+int w4a4_probe_fold_mma(int nblocks, int mma_per, int tma_per, double* out2) {
+  if (nblocks < 1 || nblocks > 100000 || mma_per < 0 || mma_per > 8 || tma_per < 0 || tma_per > 4) return -1;
+  unsigned long long* d = nullptr;
+  int* status = nullptr;
+  uint8_t* g = nullptr;
+  if (cudaMalloc(&d, 64 * sizeof(unsigned long long)) != cudaSuccess) return -1;
+  if (cudaMalloc(&status, sizeof(int)) != cudaSuccess) { cudaFree(d); return -1; }
+  if (cudaMalloc(&g, size_t(4096) * 4096 + 4096) != cudaSuccess) { cudaFree(d); cudaFree(status); return -1; }
+  cudaMemset(d, 0, 64 * sizeof(unsigned long long));
+  cudaMemset(status, 0, sizeof(int));
+  const size_t smem = 48 * 1024;
+  cudaFuncSetAttribute(fold_mma_probe, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  fold_mma_probe<<<1, 384, smem>>>(nblocks, mma_per, tma_per, g, d, status);
+  unsigned long long h[64] = {};
+  int hs = 1;
+  const cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) {
+    cudaMemcpy(h, d, sizeof(h), cudaMemcpyDeviceToHost);
+    cudaMemcpy(&hs, status, sizeof(int), cudaMemcpyDeviceToHost);
+  }
+  cudaFree(d);
+  cudaFree(status);
+  cudaFree(g);
+  if (e != cudaSuccess || hs != 0) return -1;
+  out2[0] = (h[4] + h[5] + h[8] + h[9]) / 4.0;
+  out2[1] = (h[6] + h[7] + h[10] + h[11]) / 4.0;
+  return 0;
 }
 
 }  // extern "C"
