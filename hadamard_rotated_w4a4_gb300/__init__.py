@@ -442,7 +442,7 @@ def w4a4_gemm_id(experts: Q4_0Weights, E: int, a: Act4, ids: torch.Tensor, top_k
 
 
 #: bytes of the library's fixed routing scratch, per device
-GEMM_ID_STATIC_SCRATCH_BYTES = 16 << 20
+GEMM_ID_STATIC_SCRATCH_BYTES = 64 << 20
 
 
 def w4a4_gemm_id_static(experts: Q4_0Weights, E: int, a: Act4, ids: torch.Tensor, top_k: int, act_per_slot: bool,

@@ -146,6 +146,7 @@ struct GArgs {
   int64_t sk_units;
   uint32_t* sk_count;
   float4* sk_part;
+  int sk_dyn;                // routed: stream-K over the routing kernel's tiles (units counted on the device)
   int* err;                  // device error word
   uint64_t wait_ns;          // bound of a pipeline wait
   uint64_t producer_delay_ns;  // test hook: the producer starts this late
@@ -232,13 +233,34 @@ struct Seg {
   int s0, s1;
   bool first;
 };
-__device__ __forceinline__ int64_t sk_begin(const GArgs& p, int64_t c) { return c * p.sk_units / gridDim.x; }
-__device__ __forceinline__ int64_t seg_start(const GArgs& p) {
-  return p.sk_units ? sk_begin(p, blockIdx.x) : static_cast<int64_t>(blockIdx.x);
+// The schedule: U stream-K units (tile x stage) cut into gridDim.x equal ranges,
+// or whole tiles blockIdx.x, blockIdx.x + gridDim.x, ... (U = 0).  Dense: U from
+// the host; routed with stream-K: ntiles x stages, once the routing kernel has
+// written the tile count.
+struct Sched {
+  int64_t U;
+  int64_t ntiles;
+};
+__device__ __forceinline__ Sched make_sched(const GArgs& p, int nst) {
+  Sched r;
+  r.ntiles = num_tiles(p);
+  r.U = p.sk_units;
+  if (p.sk_dyn) {  // the dense plan's rule: only where it shortens the longest CTA by more
+                   // than 10%, a fix-up counted as two stages (every role decides alike)
+    const int64_t G = gridDim.x, U = r.ntiles * nst;
+    const int64_t dp_span = ((r.ntiles + G - 1) / G) * nst, sk_span = (U + G - 1) / G + 2;
+    r.U = (U >= 2 && 10 * sk_span < 9 * dp_span) ? U : 0;
+  }
+  return r;
 }
-__device__ __forceinline__ bool seg_next(const GArgs& p, int nst, int64_t ntiles, int64_t& next, Seg& g) {
-  if (p.sk_units) {
-    const int64_t start = sk_begin(p, blockIdx.x), end = sk_begin(p, blockIdx.x + 1);
+__device__ __forceinline__ int64_t sk_begin(int64_t U, int64_t c) { return c * U / gridDim.x; }
+__device__ __forceinline__ int64_t seg_start(int64_t U) {
+  return U ? sk_begin(U, blockIdx.x) : static_cast<int64_t>(blockIdx.x);
+}
+__device__ __forceinline__ bool seg_next(const Sched& sch, int nst, int64_t& next, Seg& g) {
+  const int64_t U = sch.U, ntiles = sch.ntiles;
+  if (U) {
+    const int64_t start = sk_begin(U, blockIdx.x), end = sk_begin(U, blockIdx.x + 1);
     if (next >= end) return false;
     g.first = next == start;
     g.t = next / nst;
@@ -256,12 +278,12 @@ __device__ __forceinline__ bool seg_next(const GArgs& p, int nst, int64_t ntiles
   }
   return true;
 }
-__device__ __forceinline__ int64_t sk_cta_of_unit(const GArgs& p, int64_t u) {
+__device__ __forceinline__ int64_t sk_cta_of_unit(int64_t U, int64_t u) {
   const int64_t G = gridDim.x;
-  int64_t c = u * G / p.sk_units;
+  int64_t c = u * G / U;
   if (c >= G) c = G - 1;
-  for (int i = 0; i < 4 && c > 0 && sk_begin(p, c) > u; ++i) --c;
-  for (int i = 0; i < 4 && c + 1 < G && sk_begin(p, c + 1) <= u; ++i) ++c;
+  for (int i = 0; i < 4 && c > 0 && sk_begin(U, c) > u; ++i) --c;
+  for (int i = 0; i < 4 && c + 1 < G && sk_begin(U, c + 1) <= u; ++i) ++c;
   return c;
 }
 // One arrival on a (tile, warp) ticket: true for the last of `nparts`, which
@@ -313,17 +335,18 @@ __device__ void producer(const GArgs& p, SM& S, const CUtensorMap* wmap, const C
     }
   }
   uint32_t gstage = 0;
-  int64_t next = seg_start(p);
+  int64_t next = 0;
   Seg sg;
   bool have = false;
-  int64_t ntiles = 0;
+  Sched sch{};
   // The dense work list needs nothing from the previous kernel: the first stages'
   // weight copies go out before waiting for it (their slots are free on entry),
   // so that they overlap the kernel that writes the activations.
   int pre = 0;
   if (!p.segs) {
-    ntiles = num_tiles(p);
-    have = seg_next(p, nst, ntiles, next, sg);
+    sch = make_sched(p, nst);
+    next = seg_start(sch.U);
+    have = seg_next(sch, nst, next, sg);
     if (have && !S.abort) {
       const Tile T = tile_at(p, sg.t);
       const uint32_t bytes = static_cast<uint32_t>(T.cw * SM::AROW + T.g * SM::WSUB);
@@ -342,8 +365,9 @@ __device__ void producer(const GArgs& p, SM& S, const CUtensorMap* wmap, const C
     skip = pre;
   }
   if (p.segs) {
-    ntiles = num_tiles(p);
-    have = seg_next(p, nst, ntiles, next, sg);
+    sch = make_sched(p, nst);
+    next = seg_start(sch.U);
+    have = seg_next(sch, nst, next, sg);
   }
   bool stop = false;
   while (have && !stop && !S.abort) {
@@ -361,7 +385,7 @@ __device__ void producer(const GArgs& p, SM& S, const CUtensorMap* wmap, const C
       ++gstage;
     }
     skip = 0;
-    if (!stop) have = seg_next(p, nst, ntiles, next, sg);
+    if (!stop) have = seg_next(sch, nst, next, sg);
   }
   // the copies in flight must land before the CTA exits
   const uint32_t first = gstage > RAW ? gstage - RAW : 0;
@@ -378,11 +402,11 @@ __device__ void mma_issuer(const GArgs& p, SM& S, uint32_t tmem) {
   const int64_t B = p.K / 32;
   const int nst = static_cast<int>((B + KB - 1) / KB);
   grid_dep_wait();
-  const int64_t ntiles = num_tiles(p);
+  const Sched sch = make_sched(p, nst);
   uint32_t gblk = 0, gst = 0;
-  int64_t next = seg_start(p);
+  int64_t next = seg_start(sch.U);
   Seg sg;
-  while (seg_next(p, nst, ntiles, next, sg)) {
+  while (seg_next(sch, nst, next, sg)) {
     const Tile T = tile_at(p, sg.t);
     const uint32_t idesc = f8_idesc(T.cw);
     for (int s = sg.s0; s < sg.s1; ++s, ++gst) {
@@ -522,11 +546,11 @@ __device__ void publishers(const GArgs& p, SM& S, int t) {
                    (reinterpret_cast<uintptr_t>(p.w_scales) & 7) == 0 &&
                    (reinterpret_cast<uintptr_t>(p.w_sums) & 7) == 0;
   grid_dep_wait();
-  const int64_t ntiles = num_tiles(p);
+  const Sched sch = make_sched(p, nst);
   uint32_t gst = 0;
-  int64_t next = seg_start(p);
+  int64_t next = seg_start(sch.U);
   Seg sg;
-  while (seg_next(p, nst, ntiles, next, sg)) {
+  while (seg_next(sch, nst, next, sg)) {
     const Tile T = tile_at(p, sg.t);
     for (int s = sg.s0; s < sg.s1; ++s, ++gst) {
       const int sc = gst % SM::NSC;
@@ -545,11 +569,11 @@ __device__ void converters(const GArgs& p, SM& S, int t) {
   const int B = static_cast<int>(p.K / 32);
   const int nst = (B + KB - 1) / KB;
   grid_dep_wait();
-  const int64_t ntiles = num_tiles(p);
+  const Sched sch = make_sched(p, nst);
   uint32_t gst = 0, gblk = 0;
-  int64_t next = seg_start(p);
+  int64_t next = seg_start(sch.U);
   Seg sg;
-  while (seg_next(p, nst, ntiles, next, sg)) {
+  while (seg_next(sch, nst, next, sg)) {
     const Tile T = tile_at(p, sg.t);
     for (int s = sg.s0; s < sg.s1; ++s, ++gst) {
       const int nbk = min(KB, B - s * KB);
@@ -702,11 +726,11 @@ __device__ void workers(const GArgs& p, SM& S, uint32_t tmem) {
   const int B = static_cast<int>(B64);
   const int nst = (B + KB - 1) / KB;
   grid_dep_wait();
-  const int64_t ntiles = num_tiles(p);
+  const Sched sch = make_sched(p, nst);
   uint32_t gfold = 0, gst = 0;
-  int64_t next = seg_start(p);
+  int64_t next = seg_start(sch.U);
   Seg sg;
-  while (seg_next(p, nst, ntiles, next, sg)) {
+  while (seg_next(sch, nst, next, sg)) {
     const Tile T = tile_at(p, sg.t);
     const int nch = T.g * T.cw / 32;                  // 32-column chunks in the tile
     const int nk = nch > h ? (nch - h + 1) / 2 : 0;   // this warp's chunks
@@ -736,7 +760,7 @@ __device__ void workers(const GArgs& p, SM& S, uint32_t tmem) {
     gst += static_cast<uint32_t>(sg.s1 - sg.s0);
 
     // ---- epilogue
-    const bool split = p.sk_units && (sg.s0 > 0 || sg.s1 < nst);
+    const bool split = sch.U && (sg.s0 > 0 || sg.s1 < nst);
     if (split) {
       float4* mine = sk_slot(p, blockIdx.x, sg.first, warp - 4, lane);
 #pragma unroll
@@ -751,10 +775,13 @@ __device__ void workers(const GArgs& p, SM& S, uint32_t tmem) {
       __threadfence();
       __syncwarp();
       const int64_t u_lo = sg.t * nst;
-      const int64_t c_lo = sk_cta_of_unit(p, u_lo), c_hi = sk_cta_of_unit(p, u_lo + nst - 1);
+      const int64_t c_lo = sk_cta_of_unit(sch.U, u_lo), c_hi = sk_cta_of_unit(sch.U, u_lo + nst - 1);
+      // ticket of this (tile, warp) region: per tile (dense), or per the tile's first
+      // CTA (routed: a CTA's range ends inside at most one tile that starts in it)
+      const int64_t key = p.sk_dyn ? c_lo : sg.t;
       int last = 0;
       if (lane == 0)
-        last = sk_ticket(p.sk_count + sg.t * 8 + (warp - 4), static_cast<uint32_t>(c_hi - c_lo + 1)) ? 1 : 0;
+        last = sk_ticket(p.sk_count + key * 8 + (warp - 4), static_cast<uint32_t>(c_hi - c_lo + 1)) ? 1 : 0;
       last = __shfl_sync(0xFFFFFFFFu, last, 0);
       if (!last) continue;
       __threadfence();
@@ -768,7 +795,7 @@ __device__ void workers(const GArgs& p, SM& S, uint32_t tmem) {
             acc[kk][hf][x][1] = make_float2(0.f, 0.f);
           }
       for (int64_t c = c_lo; c <= c_hi; ++c) {
-        const float4* src = sk_slot(p, c, sk_begin(p, c) >= u_lo, warp - 4, lane);
+        const float4* src = sk_slot(p, c, sk_begin(sch.U, c) >= u_lo, warp - 4, lane);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           float4 v[2][4];
@@ -1033,6 +1060,8 @@ void grp_set_wait_limit(uint64_t wait_ns, uint64_t producer_delay_ns) {
   g_delay_ns = producer_delay_ns;
 }
 
+size_t grp_sk_part_bytes() { return kSkPartBytes; }
+
 size_t grp_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   const GPlan pl = plan_dense(M, N, K, M <= TCOLS);
   return pl.sk ? pl.ws_bytes : 0;
@@ -1088,6 +1117,14 @@ cudaError_t launch_gemm_grp_routed(const uint8_t* w_codes, const uint16_t* w_sca
   if (!a.err) return cudaErrorInvalidSymbol;
   a.wait_ns = g_wait_ns;
   a.producer_delay_ns = g_delay_ns;
+  // stream-K over the routing kernel's tiles: the units are counted on the device
+  int grid = num_sms();
+  if (r.sk_part && r.sk_count && r.sk_ctas > 0) {
+    a.sk_dyn = 1;
+    a.sk_count = r.sk_count;
+    a.sk_part = r.sk_part;
+    grid = r.sk_ctas;
+  }
   CUtensorMap wmap, amap;
   cudaError_t e = codes_map_sw64(&wmap, w_codes, static_cast<int64_t>(E) * N, K);
   if (e == cudaSuccess)
@@ -1095,7 +1132,7 @@ cudaError_t launch_gemm_grp_routed(const uint8_t* w_codes, const uint16_t* w_sca
                       static_cast<uint64_t>(r.rows), static_cast<uint64_t>(K / 2), KB * 16, 32,
                       CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e != cudaSuccess) return e;
-  return launch_grp<4, false, false>(wmap, amap, a, num_sms(), stream);
+  return launch_grp<4, false, false>(wmap, amap, a, grid, stream);
 }
 
 }  // namespace w4a4

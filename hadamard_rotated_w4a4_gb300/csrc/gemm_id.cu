@@ -136,6 +136,10 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const int32_t* __r
     const int e = ids[i];
     if (e >= 0 && e < E) r.perm[atomicAdd(&cur[e], 1)] = static_cast<int32_t>(i);
   }
+  // the GEMM's stream-K tickets start at zero (they return to zero after each use;
+  // clearing them here also recovers from a launch that gave up)
+  if (r.sk_count)
+    for (int i = tid; i < r.sk_ctas * 8; i += blockDim.x) r.sk_count[i] = 0u;
 }
 
 // One warp per routed row: its code bytes (16-byte chunks) and scales, in expert order.
@@ -176,6 +180,12 @@ RoutingLayout routing_layout(int64_t npairs, int E, int64_t K) {
   L.perm = off;      off += align16(sizeof(int32_t) * static_cast<size_t>(npairs));
   L.gcodes = off;    off += align16(static_cast<size_t>(npairs) * static_cast<size_t>(K / 2));
   L.gscales = off;   off += align16(static_cast<size_t>(npairs) * static_cast<size_t>(K / 32) * sizeof(float));
+  // stream-K over the routed tiles: one ticket per (tile's first CTA, worker warp),
+  // two partial tiles per CTA
+  L.sk_ctas = num_sms();
+  L.sk_count = off;  off += align16(sizeof(uint32_t) * 8 * static_cast<size_t>(L.sk_ctas));
+  off = (off + 255) & ~size_t(255);
+  L.sk_part = off;   off += 2 * static_cast<size_t>(L.sk_ctas) * grp_sk_part_bytes();
   L.total = off;
   return L;
 }
@@ -192,6 +202,9 @@ Routing routing_in(void* ws, int64_t npairs, int E, int64_t K) {
   r.gcodes = base + L.gcodes;
   r.gscales = reinterpret_cast<float*>(base + L.gscales);
   r.rows = npairs;
+  r.sk_count = reinterpret_cast<uint32_t*>(base + L.sk_count);
+  r.sk_part = reinterpret_cast<float4*>(base + L.sk_part);
+  r.sk_ctas = L.sk_ctas;
   return r;
 }
 

@@ -22,17 +22,21 @@ struct Routing {
   uint8_t* gcodes;     // [M * top_k][K/2] activation codes gathered in expert order
   float* gscales;      // [M * top_k][K/32] their scales
   int64_t rows;        // capacity of the gathered arrays (M * top_k)
+  uint32_t* sk_count;  // [sk_ctas * 8] stream-K tickets (zeroed by the routing kernel)
+  float4* sk_part;     // [2 * sk_ctas] stream-K partial tiles (grp_sk_part_bytes each)
+  int sk_ctas;         // the routed GEMM's grid: one CTA per SM of the current device
 };
 
 struct RoutingLayout {
-  size_t hdr, offsets, segs, seg_tiles, perm, gcodes, gscales, total;
+  size_t hdr, offsets, segs, seg_tiles, perm, gcodes, gscales, sk_count, sk_part, total;
+  int sk_ctas;
 };
 RoutingLayout routing_layout(int64_t npairs, int E, int64_t K);
 Routing routing_in(void* ws, int64_t npairs, int E, int64_t K);
 
 // Fixed routing scratch (for the no-workspace variant of the routed product):
 // its size, and the device address of the current device's copy.
-constexpr size_t kIdStaticScratchBytes = size_t(16) << 20;
+constexpr size_t kIdStaticScratchBytes = size_t(64) << 20;
 cudaError_t id_static_scratch(void** addr);
 
 // expanded (optional): the offset codes a + 8 as bytes in element order, [M][K]
@@ -92,6 +96,9 @@ cudaError_t launch_gemm_grp(const uint8_t* w_codes, const uint16_t* w_scales, co
                             int64_t M, int64_t K, float* y, int64_t ldy, void* ws, size_t ws_bytes,
                             cudaStream_t stream);
 size_t grp_workspace_bytes(int64_t M, int64_t N, int64_t K);
+// Bytes of one stream-K partial tile of the super-tile kernel (8 warps x 32 lanes x
+// 128 accumulators); a CTA needs two.
+size_t grp_sk_part_bytes();
 cudaError_t launch_gemm_grp_routed(const uint8_t* w_codes, const uint16_t* w_scales, const int16_t* w_sums,
                                    int E, int64_t N, int64_t K, const Routing& r, float* y, cudaStream_t stream);
 // Test hook: the bound of the super-tile GEMM's pipeline waits (0 = the default

@@ -355,10 +355,14 @@ w4a4_status w4a4_gemm_partials(const w4a4_q4_0* w, const w4a4_act4* a, int32_t* 
  *   y       : device, fp32 [M][top_k][N] (row t*top_k + s), contiguous,
  *             4-byte aligned.
  *   ws      : device workspace of at least w4a4_gemm_id_workspace_bytes(M,
- *             top_k, E, K) bytes, 16-byte aligned; its contents on entry do not
- *             matter.  It holds the routing (counts, offsets, pair list), the
- *             routed activation rows gathered in expert order, and a device
- *             error flag (its first word).
+ *             top_k, E, K) bytes (sized on the current device), 16-byte aligned;
+ *             its contents on entry do not matter.  It holds the routing
+ *             (counts, offsets, pair list), the routed activation rows gathered
+ *             in expert order, a device error flag (its first word), and the
+ *             slots of the GEMM's stream-K schedule: the (tile x K-stage) units
+ *             of all routed tiles are cut into one equal range per SM, and a
+ *             tile cut between CTAs is summed in CTA order (a fixed order: the
+ *             result does not depend on timing).
  * An id outside [0, E) is not used: its output row is zeroed, the device flag in
  * ws is set, and w4a4_gemm_id_status() on the same ws returns
  * W4A4_ERR_DEVICE_FLAG.  Each call clears the flag first.
@@ -393,7 +397,9 @@ w4a4_status w4a4_gemm_id_status(const void* ws, w4a4_stream_t stream);
  * ws_bytes.  The output is the same as w4a4_gemm_id's on the same inputs.
  *   - Size limit: a problem with w4a4_gemm_id_workspace_bytes(M, top_k, E, K)
  *     greater than W4A4_GEMM_ID_STATIC_SCRATCH_BYTES is refused with
- *     W4A4_ERR_WORKSPACE before anything runs; use w4a4_gemm_id for it.
+ *     W4A4_ERR_WORKSPACE before anything runs; use w4a4_gemm_id for it.  (The
+ *     MoE workload of 1024 tokens, top-8, K 2048 on 152 SMs needs about 49 MiB,
+ *     most of it the stream-K slots.)
  *   - Set-up: the first call on a device, with that device current, looks up
  *     the array's device address once (cudaGetSymbolAddress) and keeps it.
  *     Make that first call before any stream capture.
@@ -408,7 +414,7 @@ w4a4_status w4a4_gemm_id_status(const void* ws, w4a4_stream_t stream);
  *     The flag that records it stays inside the library, so no status query
  *     reports it.  Callers that need the check use w4a4_gemm_id.
  */
-#define W4A4_GEMM_ID_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+#define W4A4_GEMM_ID_STATIC_SCRATCH_BYTES ((size_t)64 << 20)
 
 w4a4_status w4a4_gemm_id_static(const w4a4_q4_0* experts, int E, int64_t N, const w4a4_act4* a,
                                 const int32_t* ids, int64_t M, int top_k, int act_per_slot, float* y,

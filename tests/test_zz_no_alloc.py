@@ -20,7 +20,7 @@ FAKE = 0x10000  # aligned, never dereferenced: the call below fails validation f
 
 def test_oversized_problem_refused_before_launch():
     lib = w4.load_library(build_if_missing=True)
-    E, N, K, M, k = 8, 64, 4096, 4096, 2  # 8192 routed rows x 2048 code bytes: > 16 MiB of scratch
+    E, N, K, M, k = 8, 64, 4096, 16384, 2  # 32768 routed rows x 2048 code bytes: > 64 MiB of scratch
     assert w4.w4a4_gemm_id_workspace_bytes(M, k, E, K) > w4.GEMM_ID_STATIC_SCRATCH_BYTES
     wd = _Q4_0Desc(FAKE, FAKE, FAKE, E * N, K, w4.TAG_Q4_0 | 1)
     ad = _Act4Desc(FAKE, FAKE, M, K, w4.TAG_ACT4 | 1)
