@@ -233,13 +233,16 @@ struct Seg {
   int s0, s1;
   bool first;
 };
-// The schedule: U stream-K units (tile x stage) cut into gridDim.x equal ranges,
+// The schedule: U stream-K units (tile x stage) cut into G = min(U, gridDim.x)
+// equal ranges, one per CTA below G (the others idle: every range is non-empty,
+// so a cut tile's contributors are exactly the CTAs from its first to its last),
 // or whole tiles blockIdx.x, blockIdx.x + gridDim.x, ... (U = 0).  Dense: U from
-// the host; routed with stream-K: ntiles x stages, once the routing kernel has
-// written the tile count.
+// the host (which launches at most U CTAs); routed with stream-K: ntiles x
+// stages, once the routing kernel has written the tile count.
 struct Sched {
   int64_t U;
   int64_t ntiles;
+  int64_t G;
 };
 __device__ __forceinline__ Sched make_sched(const GArgs& p, int nst) {
   Sched r;
@@ -251,16 +254,19 @@ __device__ __forceinline__ Sched make_sched(const GArgs& p, int nst) {
     const int64_t dp_span = ((r.ntiles + G - 1) / G) * nst, sk_span = (U + G - 1) / G + 2;
     r.U = (U >= 2 && 10 * sk_span < 9 * dp_span) ? U : 0;
   }
+  r.G = (r.U && r.U < static_cast<int64_t>(gridDim.x)) ? r.U : static_cast<int64_t>(gridDim.x);
   return r;
 }
-__device__ __forceinline__ int64_t sk_begin(int64_t U, int64_t c) { return c * U / gridDim.x; }
-__device__ __forceinline__ int64_t seg_start(int64_t U) {
-  return U ? sk_begin(U, blockIdx.x) : static_cast<int64_t>(blockIdx.x);
+__device__ __forceinline__ int64_t sk_begin(const Sched& sch, int64_t c) {
+  return c >= sch.G ? sch.U : c * sch.U / sch.G;
+}
+__device__ __forceinline__ int64_t seg_start(const Sched& sch) {
+  return sch.U ? sk_begin(sch, blockIdx.x) : static_cast<int64_t>(blockIdx.x);
 }
 __device__ __forceinline__ bool seg_next(const Sched& sch, int nst, int64_t& next, Seg& g) {
   const int64_t U = sch.U, ntiles = sch.ntiles;
   if (U) {
-    const int64_t start = sk_begin(U, blockIdx.x), end = sk_begin(U, blockIdx.x + 1);
+    const int64_t start = sk_begin(sch, blockIdx.x), end = sk_begin(sch, blockIdx.x + 1);
     if (next >= end) return false;
     g.first = next == start;
     g.t = next / nst;
@@ -278,12 +284,12 @@ __device__ __forceinline__ bool seg_next(const Sched& sch, int nst, int64_t& nex
   }
   return true;
 }
-__device__ __forceinline__ int64_t sk_cta_of_unit(int64_t U, int64_t u) {
-  const int64_t G = gridDim.x;
-  int64_t c = u * G / U;
+__device__ __forceinline__ int64_t sk_cta_of_unit(const Sched& sch, int64_t u) {
+  const int64_t G = sch.G;
+  int64_t c = u * G / sch.U;
   if (c >= G) c = G - 1;
-  for (int i = 0; i < 4 && c > 0 && sk_begin(U, c) > u; ++i) --c;
-  for (int i = 0; i < 4 && c + 1 < G && sk_begin(U, c + 1) <= u; ++i) ++c;
+  for (int i = 0; i < 4 && c > 0 && sk_begin(sch, c) > u; ++i) --c;
+  for (int i = 0; i < 4 && c + 1 < G && sk_begin(sch, c + 1) <= u; ++i) ++c;
   return c;
 }
 // One arrival on a (tile, warp) ticket: true for the last of `nparts`, which
@@ -345,7 +351,7 @@ __device__ void producer(const GArgs& p, SM& S, const CUtensorMap* wmap, const C
   int pre = 0;
   if (!p.segs) {
     sch = make_sched(p, nst);
-    next = seg_start(sch.U);
+    next = seg_start(sch);
     have = seg_next(sch, nst, next, sg);
     if (have && !S.abort) {
       const Tile T = tile_at(p, sg.t);
@@ -366,7 +372,7 @@ __device__ void producer(const GArgs& p, SM& S, const CUtensorMap* wmap, const C
   }
   if (p.segs) {
     sch = make_sched(p, nst);
-    next = seg_start(sch.U);
+    next = seg_start(sch);
     have = seg_next(sch, nst, next, sg);
   }
   bool stop = false;
@@ -404,7 +410,7 @@ __device__ void mma_issuer(const GArgs& p, SM& S, uint32_t tmem) {
   grid_dep_wait();
   const Sched sch = make_sched(p, nst);
   uint32_t gblk = 0, gst = 0;
-  int64_t next = seg_start(sch.U);
+  int64_t next = seg_start(sch);
   Seg sg;
   while (seg_next(sch, nst, next, sg)) {
     const Tile T = tile_at(p, sg.t);
@@ -548,7 +554,7 @@ __device__ void publishers(const GArgs& p, SM& S, int t) {
   grid_dep_wait();
   const Sched sch = make_sched(p, nst);
   uint32_t gst = 0;
-  int64_t next = seg_start(sch.U);
+  int64_t next = seg_start(sch);
   Seg sg;
   while (seg_next(sch, nst, next, sg)) {
     const Tile T = tile_at(p, sg.t);
@@ -571,7 +577,7 @@ __device__ void converters(const GArgs& p, SM& S, int t) {
   grid_dep_wait();
   const Sched sch = make_sched(p, nst);
   uint32_t gst = 0, gblk = 0;
-  int64_t next = seg_start(sch.U);
+  int64_t next = seg_start(sch);
   Seg sg;
   while (seg_next(sch, nst, next, sg)) {
     const Tile T = tile_at(p, sg.t);
@@ -728,7 +734,7 @@ __device__ void workers(const GArgs& p, SM& S, uint32_t tmem) {
   grid_dep_wait();
   const Sched sch = make_sched(p, nst);
   uint32_t gfold = 0, gst = 0;
-  int64_t next = seg_start(sch.U);
+  int64_t next = seg_start(sch);
   Seg sg;
   while (seg_next(sch, nst, next, sg)) {
     const Tile T = tile_at(p, sg.t);
@@ -775,7 +781,7 @@ __device__ void workers(const GArgs& p, SM& S, uint32_t tmem) {
       __threadfence();
       __syncwarp();
       const int64_t u_lo = sg.t * nst;
-      const int64_t c_lo = sk_cta_of_unit(sch.U, u_lo), c_hi = sk_cta_of_unit(sch.U, u_lo + nst - 1);
+      const int64_t c_lo = sk_cta_of_unit(sch, u_lo), c_hi = sk_cta_of_unit(sch, u_lo + nst - 1);
       // ticket of this (tile, warp) region: per tile (dense), or per the tile's first
       // CTA (routed: a CTA's range ends inside at most one tile that starts in it)
       const int64_t key = p.sk_dyn ? c_lo : sg.t;
@@ -795,7 +801,7 @@ __device__ void workers(const GArgs& p, SM& S, uint32_t tmem) {
             acc[kk][hf][x][1] = make_float2(0.f, 0.f);
           }
       for (int64_t c = c_lo; c <= c_hi; ++c) {
-        const float4* src = sk_slot(p, c, sk_begin(sch.U, c) >= u_lo, warp - 4, lane);
+        const float4* src = sk_slot(p, c, sk_begin(sch, c) >= u_lo, warp - 4, lane);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           float4 v[2][4];

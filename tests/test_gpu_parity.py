@@ -371,6 +371,22 @@ def test_moe_skewed_routing(dev):
     assert_close(y.cpu().numpy(), R)
 
 
+@pytest.mark.parametrize("act_per_slot", [False, True])
+def test_moe_few_tiles_long_k(dev, act_per_slot):
+    # 4 experts x 1 tile of 2 weight sub-tiles, K 4096 (32 stages): 128 stream-K units,
+    # fewer than the SMs, so the routed schedule cuts them over 128 CTAs and the rest idle
+    E, N, K, M, k = 4, 256, 4096, 16, 2
+    rng = np.random.default_rng(21)
+    ids = np.stack([rng.choice(E, k, replace=False) for _ in range(M)]).astype(np.int32)
+    w = si.round_to_bf16(rng.standard_normal((E, N, K)).astype(np.float32) * np.float32(0.02))[0]
+    x = rng.standard_normal((M * k if act_per_slot else M, K)).astype(np.float32)
+    y, ws = _moe_gpu(dev, w, E, N, x, ids, k, act_per_slot)
+    w4.w4a4_gemm_id_status(ws)
+    R = oracle.w4a4_matmul_id(oracle.pack_weights(w.reshape(E * N, K)), E, oracle.quantize_activations(x), ids,
+                              act_per_slot)
+    assert_close(y.cpu().numpy(), R)
+
+
 def test_moe_bad_ids_flagged_and_zeroed(dev):
     mi = si.moe_inputs("moe_tiny", seed=2)
     s = mi["shape"]
