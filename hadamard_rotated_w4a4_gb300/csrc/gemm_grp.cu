@@ -97,6 +97,9 @@ struct __align__(1024) GSmem {
   float sda[NSC][KB][TCOLS];    // d_a per column, permuted (see col_slot)
   float sdw[NSC][KB][G][TW];    // d_w 2^18 per weight row, permuted (see row_slot)
   float scorr[NSC][KB][G][TW];  // -d_w 8 S_w
+  // output staging of the single-weight-tile instance: per worker warp, 8 tokens x 32
+  // features, 16-byte groups XOR-swizzled by token (see store_rows)
+  float ystage[G == 1 ? kWorkers : 1][G == 1 ? 256 : 1];
   // (NSC is declared above its use in the arrays)
   uint64_t full_raw[RAW];
   uint64_t empty_raw[RAW];
@@ -243,7 +246,12 @@ struct Sched {
   int64_t U;
   int64_t ntiles;
   int64_t G;
+  bool narrow;  // U x G < 2^32: the plan's products and quotients fit 32-bit arithmetic
 };
+// a / b for 0 <= a < 2^32 when the plan is narrow (a 64-bit division costs ~10x more)
+__device__ __forceinline__ int64_t sk_div(const Sched& sch, int64_t a, int64_t b) {
+  return sch.narrow ? static_cast<int64_t>(static_cast<uint32_t>(a) / static_cast<uint32_t>(b)) : a / b;
+}
 __device__ __forceinline__ Sched make_sched(const GArgs& p, int nst) {
   Sched r;
   r.ntiles = num_tiles(p);
@@ -255,10 +263,11 @@ __device__ __forceinline__ Sched make_sched(const GArgs& p, int nst) {
     r.U = (U >= 2 && 10 * sk_span < 9 * dp_span) ? U : 0;
   }
   r.G = (r.U && r.U < static_cast<int64_t>(gridDim.x)) ? r.U : static_cast<int64_t>(gridDim.x);
+  r.narrow = r.U * r.G < (static_cast<int64_t>(1) << 32);
   return r;
 }
 __device__ __forceinline__ int64_t sk_begin(const Sched& sch, int64_t c) {
-  return c >= sch.G ? sch.U : c * sch.U / sch.G;
+  return c >= sch.G ? sch.U : sk_div(sch, c * sch.U, sch.G);
 }
 __device__ __forceinline__ int64_t seg_start(const Sched& sch) {
   return sch.U ? sk_begin(sch, blockIdx.x) : static_cast<int64_t>(blockIdx.x);
@@ -269,7 +278,7 @@ __device__ __forceinline__ bool seg_next(const Sched& sch, int nst, int64_t& nex
     const int64_t start = sk_begin(sch, blockIdx.x), end = sk_begin(sch, blockIdx.x + 1);
     if (next >= end) return false;
     g.first = next == start;
-    g.t = next / nst;
+    g.t = sk_div(sch, next, nst);
     g.s0 = static_cast<int>(next - g.t * nst);
     const int64_t left = end - next;
     g.s1 = (nst - g.s0 <= left) ? nst : g.s0 + static_cast<int>(left);
@@ -286,7 +295,7 @@ __device__ __forceinline__ bool seg_next(const Sched& sch, int nst, int64_t& nex
 }
 __device__ __forceinline__ int64_t sk_cta_of_unit(const Sched& sch, int64_t u) {
   const int64_t G = sch.G;
-  int64_t c = u * G / sch.U;
+  int64_t c = sk_div(sch, u * G, sch.U);
   if (c >= G) c = G - 1;
   for (int i = 0; i < 4 && c > 0 && sk_begin(sch, c) > u; ++i) --c;
   for (int i = 0; i < 4 && c + 1 < G && sk_begin(sch, c + 1) <= u; ++i) ++c;
@@ -303,6 +312,112 @@ __device__ __forceinline__ bool sk_ticket(uint32_t* ctr, uint32_t nparts) {
 }
 __device__ __forceinline__ float4* sk_slot(const GArgs& p, int64_t cta, bool first, int w, int lane) {
   return p.sk_part + ((2 * cta + (first ? 0 : 1)) * 8 + w) * 1024 + lane;
+}
+
+// Loads and adds of stream-K partial tiles (a warp's region: 32 float4 per lane).
+__device__ __forceinline__ void sk_load8(const float4* src, int kk, float4 (&v)[2][4]) {
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+    for (int x = 0; x < 4; ++x) v[hf][x] = __ldcg(src + ((kk * 2 + hf) * 4 + x) * 32);
+}
+__device__ __forceinline__ void sk_add8(float2 (&a)[2][4][2], const float4 (&v)[2][4]) {
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      a[hf][x][0].x += v[hf][x].x;
+      a[hf][x][0].y += v[hf][x].y;
+      a[hf][x][1].x += v[hf][x].z;
+      a[hf][x][1].y += v[hf][x].w;
+    }
+}
+// A relaxed read of a ticket; the fence the reader issues before reading the
+// partials it counts completes the acquire.
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Stream-K epilogue of a warp's part of a tile cut between CTAs.  Each
+// contributor but the last deposits its part in its partial slot and arrives on
+// the tile's ticket; the last sums every part in CTA order, (((p_lo + p_lo+1) +
+// ...) + p_hi), taking its own part from its registers where that order allows,
+// so the result does not depend on which CTA comes last.  A contributor that
+// finds every other part already deposited, and whose own part can be added from
+// registers (two parts, or the first of several), is the last without arriving
+// and writes no partial.  True if acc now holds the tile's sum (this warp writes
+// Y), false if the part was deposited.
+__device__ __forceinline__ bool sk_epilogue(const GArgs& p, const Sched& sch, const Seg& sg, int nst, int w, int lane,
+                                            float2 (&acc)[4][2][4][2]) {
+  const int64_t u_lo = sg.t * nst;
+  const int64_t c_lo = sk_cta_of_unit(sch, u_lo), c_hi = sk_cta_of_unit(sch, u_lo + nst - 1);
+  const uint32_t nparts = static_cast<uint32_t>(c_hi - c_lo + 1);
+  // ticket of this (tile, warp) region: per tile (dense), or per the tile's first
+  // CTA (routed: a CTA's range ends inside at most one tile that starts in it)
+  uint32_t* ctr = p.sk_count + (p.sk_dyn ? c_lo : sg.t) * 8 + w;
+  const int64_t me = blockIdx.x;
+  int last = 0;
+  // every other part is in and this one can stay in registers: no arrival, reset
+  if (lane == 0 && (nparts == 2 || me == c_lo) && ld_relaxed_u32(ctr) + 1 == nparts) {
+    atomicExch(ctr, 0u);
+    last = 1;
+  }
+  last = __shfl_sync(0xFFFFFFFFu, last, 0);
+  if (!last) {
+    float4* mine = sk_slot(p, me, sg.first, w, lane);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+        for (int x = 0; x < 4; ++x)
+          __stcg(mine + ((kk * 2 + hf) * 4 + x) * 32,
+                 make_float4(acc[kk][hf][x][0].x, acc[kk][hf][x][0].y, acc[kk][hf][x][1].x, acc[kk][hf][x][1].y));
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) last = sk_ticket(ctr, nparts) ? 1 : 0;
+    last = __shfl_sync(0xFFFFFFFFu, last, 0);
+    if (!last) return false;
+  }
+  __syncwarp();
+  __threadfence();
+  if (nparts == 2) {  // one other part: p_lo + p_hi in either order, two chunks per batch of loads
+    const int64_t c = me == c_lo ? c_hi : c_lo;
+    const float4* src = sk_slot(p, c, sk_begin(sch, c) >= u_lo, w, lane);
+#pragma unroll
+    for (int kk = 0; kk < 4; kk += 2) {
+      float4 v0[2][4], v1[2][4];
+      sk_load8(src, kk, v0);
+      sk_load8(src, kk + 1, v1);
+      sk_add8(acc[kk], v0);
+      sk_add8(acc[kk + 1], v1);
+    }
+    return true;
+  }
+  // three or more parts: this CTA's own in registers when it comes first, else
+  // re-read with the rest (it was deposited: the shortcut above is taken only when
+  // the own part can stay in registers)
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+    float4 v0[2][4];
+    if (me != c_lo) {
+      sk_load8(sk_slot(p, c_lo, sk_begin(sch, c_lo) >= u_lo, w, lane), kk, v0);
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          acc[kk][hf][x][0] = make_float2(v0[hf][x].x, v0[hf][x].y);
+          acc[kk][hf][x][1] = make_float2(v0[hf][x].z, v0[hf][x].w);
+        }
+    }
+    for (int64_t c = c_lo + 1; c <= c_hi; ++c) {
+      sk_load8(sk_slot(p, c, sk_begin(sch, c) >= u_lo, w, lane), kk, v0);
+      sk_add8(acc[kk], v0);
+    }
+  }
+  return true;
 }
 
 // ------------------------------------------------------------------ roles
@@ -717,6 +832,55 @@ __device__ __forceinline__ bool fold_segment(const GArgs& p, SM& S, uint32_t tme
   return true;
 }
 
+// The single-weight-tile instance's output: per chunk kk and 8-token group x, the
+// warp's 8 tokens x 32 features go through shared memory (a 1 KB staging buffer
+// per warp) so that each lane stores two 16-byte runs of 4 features of one token
+// row instead of eight 4-byte values; 16-byte groups are XOR-swizzled by token so
+// that neither side conflicts on banks.  Rows past the segment's tokens and
+// features past N are not written; unaligned Y falls back to 4-byte stores.
+__device__ __forceinline__ void store_rows(const GArgs& p, float* ys, const Tile& T, const float2 (&acc)[4][2][4][2],
+                                           int nk, int h, int q, int jr, int u, int lane) {
+  const bool vec = (reinterpret_cast<uintptr_t>(p.y) & 15) == 0 && (p.ldy & 3) == 0;
+  const int tr = lane >> 2;  // the token this lane stores
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+    if (kk >= nk) continue;
+    const int k = h + 2 * kk;
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {  // token 2u + e, feature 8r + jr of the warp's 32
+          const int t = 2 * u + e, f = 8 * r + jr;
+          const float2 a2 = acc[kk][r >> 1][x][r & 1];
+          ys[t * 32 + 4 * ((f >> 2) ^ t) + (f & 3)] = e ? a2.y : a2.x;
+        }
+      __syncwarp();
+      const int jt = 32 * k + 8 * x + tr;  // token within the segment
+      if (jt < T.ntok) {
+        const int64_t orow = p.perm ? static_cast<int64_t>(p.perm[T.a_row0 + jt]) : T.a_row0 + jt;
+        float* yr = p.y + orow * p.ldy;
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          const int f4 = 2 * (lane & 3) + g;
+          const float4 v = *reinterpret_cast<const float4*>(&ys[tr * 32 + 4 * (f4 ^ tr)]);
+          const int64_t n = T.n0 + 32 * q + 4 * f4;
+          if (vec && n + 3 < p.N) {
+            *reinterpret_cast<float4*>(yr + n) = v;
+          } else {
+            if (n < p.N) yr[n] = v.x;
+            if (n + 1 < p.N) yr[n + 1] = v.y;
+            if (n + 2 < p.N) yr[n + 2] = v.z;
+            if (n + 3 < p.N) yr[n + 3] = v.w;
+          }
+        }
+      }
+      __syncwarp();
+    }
+  }
+}
+
 template <class SM>
 __device__ void workers(const GArgs& p, SM& S, uint32_t tmem) {
   const int lane = threadIdx.x & 31;
@@ -767,59 +931,10 @@ __device__ void workers(const GArgs& p, SM& S, uint32_t tmem) {
 
     // ---- epilogue
     const bool split = sch.U && (sg.s0 > 0 || sg.s1 < nst);
-    if (split) {
-      float4* mine = sk_slot(p, blockIdx.x, sg.first, warp - 4, lane);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-          for (int x = 0; x < 4; ++x)
-            __stcg(mine + ((kk * 2 + hf) * 4 + x) * 32,
-                   make_float4(acc[kk][hf][x][0].x, acc[kk][hf][x][0].y, acc[kk][hf][x][1].x, acc[kk][hf][x][1].y));
-      // ticket: the last contributor of this (tile, warp) region sums every partial in CTA order
-      __threadfence();
-      __syncwarp();
-      const int64_t u_lo = sg.t * nst;
-      const int64_t c_lo = sk_cta_of_unit(sch, u_lo), c_hi = sk_cta_of_unit(sch, u_lo + nst - 1);
-      // ticket of this (tile, warp) region: per tile (dense), or per the tile's first
-      // CTA (routed: a CTA's range ends inside at most one tile that starts in it)
-      const int64_t key = p.sk_dyn ? c_lo : sg.t;
-      int last = 0;
-      if (lane == 0)
-        last = sk_ticket(p.sk_count + key * 8 + (warp - 4), static_cast<uint32_t>(c_hi - c_lo + 1)) ? 1 : 0;
-      last = __shfl_sync(0xFFFFFFFFu, last, 0);
-      if (!last) continue;
-      __threadfence();
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-          for (int x = 0; x < 4; ++x) {
-            acc[kk][hf][x][0] = make_float2(0.f, 0.f);
-            acc[kk][hf][x][1] = make_float2(0.f, 0.f);
-          }
-      for (int64_t c = c_lo; c <= c_hi; ++c) {
-        const float4* src = sk_slot(p, c, sk_begin(sch, c) >= u_lo, warp - 4, lane);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          float4 v[2][4];
-#pragma unroll
-          for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-            for (int x = 0; x < 4; ++x) v[hf][x] = __ldcg(src + ((kk * 2 + hf) * 4 + x) * 32);
-#pragma unroll
-          for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-            for (int x = 0; x < 4; ++x) {
-              acc[kk][hf][x][0].x += v[hf][x].x;
-              acc[kk][hf][x][0].y += v[hf][x].y;
-              acc[kk][hf][x][1].x += v[hf][x].z;
-              acc[kk][hf][x][1].y += v[hf][x].w;
-            }
-        }
-      }
+    if (split && !sk_epilogue(p, sch, sg, nst, warp - 4, lane, acc)) continue;
+    if constexpr (SM::G == 1) {
+      store_rows(p, S.ystage[warp - 4], T, acc, nk, h, q, jr, u, lane);
+      continue;
     }
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
