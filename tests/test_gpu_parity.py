@@ -240,6 +240,28 @@ def test_stream_k_matches_oracle_and_is_deterministic(dev, M, K, N):
     assert_close(y_whole[ridx].cpu().numpy(), R)
 
 
+def test_stream_k_order_does_not_depend_on_timing(dev):
+    """Which CTA of a cut tile arrives last (and so sums the parts, its own from
+    registers, with or without depositing it) varies with timing; the sum is always
+    taken in CTA order, so every launch gives the same bits.  Launches run beside
+    a concurrent matmul on another stream to vary the arrival order."""
+    M, K, N = 512, 5120, 5120
+    d = si.dense_inputs("c1")
+    wq, aq = _gpu_pair(dev, d)
+    ws = torch.zeros(w4.w4a4_gemm_workspace_bytes(M, N, K), dtype=torch.uint8, device=dev)
+    ref = w4.w4a4_gemm(wq, aq, ws=ws)
+    side = torch.cuda.Stream()
+    big = torch.randn(4096, 4096, device=dev)
+    for i in range(10):
+        if i % 2:
+            with torch.cuda.stream(side):
+                big = (big @ big).clamp_(-1, 1)
+        y = w4.w4a4_gemm(wq, aq, ws=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(y, ref), f"launch {i} differs"
+    w4.w4a4_check()
+
+
 def test_stream_k_under_cuda_graph_replay(dev):
     """A captured split-schedule GEMM replays correctly: the tickets return to zero after every launch."""
     M, K, N = 300, 1024, 640
