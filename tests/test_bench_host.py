@@ -32,7 +32,7 @@ def test_replay_steps_uses_whole_cycles_when_aligned():
     assert calls == [3, 4, "cycle", 0, 1]
 
 
-def test_algorithmic_bytes_match_the_survey_figures():
+def test_algorithmic_bytes_match_the_per_unit_figures():
     # dense c1: 14.75 MB of weight codes + fp16 scales, 1.64 MB of activation codes + scales, 10.49 MB of Y
     assert abs(bench.gemm_algorithmic_bytes(5120, 5120, 512, 512, 5120) / 1e6 - 26.9) < 0.05
     # MoE gate: 128 experts x 768 rows of K2048, activations per token, Y per (token, slot)
